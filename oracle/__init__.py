@@ -1,0 +1,146 @@
+"""Float64 CPU oracle for multi-head scaled dot-product attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline leg may import this package.  It shares no code
+with the CUDA library (``transformer_head_scaled_sdpa_gb300``) and imports
+nothing from it; the product path never calls it.
+
+The arithmetic lives in ``mha_oracle.c`` (plain C, float64, one query row at a
+time): score s_j = scale * q.k_j, weights a_j = e^{s_j} / sum_i e^{s_i},
+output o = sum_j a_j v_j ("Attention Is All You Need", Section 3.2.1,
+Equation (1); formula page transformer-attention, section 証明), with the
+causal and key-padding masks removing keys before the softmax.  This module
+only compiles that file with gcc, loads it with ctypes and marshals arrays.
+
+Parity status: every function here is pinned by ``tests/test_oracle_*.py``
+(the pages' worked examples, closed-form invariants, brute force on tiny
+inputs and a library cross-check).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+MASK_NONE = 0
+MASK_CAUSAL = 1
+MASK_KEY_PADDING = 2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "mha_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_default = None
+
+
+def compile_source(src: str, out_path: str) -> str:
+    """gcc a C source of the oracle into a shared library at ``out_path``."""
+    os.makedirs(os.path.dirname(out_path), exist_ok=True)
+    tmp = out_path + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-std=c11", "-Wall", "-shared", "-fPIC",
+           src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out_path)
+    return out_path
+
+
+def build(force: bool = False) -> str:
+    """Compile ``mha_oracle.c`` into ``oracle/_build/liboracle.so`` (gcc, OpenMP)."""
+    fresh = (os.path.exists(_LIB_PATH)
+             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(SOURCE))
+    if force or not fresh:
+        compile_source(SOURCE, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _as_f64(x) -> np.ndarray:
+    """Exact float64 image of a numpy array or a (CPU) torch tensor."""
+    if hasattr(x, "detach"):  # torch tensor: widen on the torch side (exact)
+        import torch
+        x = x.detach().to("cpu", torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+class Oracle:
+    """ctypes handle on one build of the oracle library."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        lib.oracle_mha_f64.restype = ctypes.c_int
+        lib.oracle_mha_f64.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_double,
+            ctypes.c_int]
+        lib.oracle_default_threads.restype = ctypes.c_int
+        lib.oracle_default_threads.argtypes = []
+        self.lib = lib
+
+    def default_threads(self) -> int:
+        return int(self.lib.oracle_default_threads())
+
+    def mha(self, q, k, v, mask_kind: int = MASK_NONE, key_lens=None, scale=None,
+            threads: int | None = None, return_lse: bool = False):
+        """Attention over all heads: q [B,Lq,H,d], k and v [B,Lk,H,d] -> o [B,Lq,H,d].
+
+        ``scale`` None means 1/sqrt(d).  ``key_lens`` ([B] integers) is read
+        only under ``MASK_KEY_PADDING``.  With ``return_lse`` also returns the
+        row log-sum-exp of the scaled scores, shape [B, H, Lq].
+        """
+        q = _as_f64(q)
+        k = _as_f64(k)
+        v = _as_f64(v)
+        if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
+            raise ValueError("q, k, v must be [B, L, H, d]")
+        B, Lq, H, d = q.shape
+        Lk = k.shape[1]
+        if k.shape != (B, Lk, H, d) or v.shape != (B, Lk, H, d):
+            raise ValueError("k and v must be [B, Lk, H, d] matching q")
+        if scale is None:
+            scale = 1.0 / math.sqrt(d)
+        lens = None
+        if mask_kind == MASK_KEY_PADDING:
+            if key_lens is None:
+                raise ValueError("key padding needs key_lens")
+            if hasattr(key_lens, "detach"):
+                key_lens = key_lens.detach().cpu().numpy()
+            lens = np.ascontiguousarray(np.asarray(key_lens, dtype=np.int32))
+            if lens.shape != (B,):
+                raise ValueError("key_lens must have shape [B]")
+        out = np.empty((B, Lq, H, d), dtype=np.float64)
+        lse = np.empty((B, H, Lq), dtype=np.float64) if return_lse else None
+        rc = self.lib.oracle_mha_f64(
+            q.ctypes.data, k.ctypes.data, v.ctypes.data, out.ctypes.data,
+            lse.ctypes.data if lse is not None else None,
+            B, H, Lq, Lk, d, int(mask_kind),
+            lens.ctypes.data if lens is not None else None,
+            float(scale), int(threads) if threads else 0)
+        if rc != 0:
+            raise ValueError(f"oracle_mha_f64 rejected its arguments (code {rc})")
+        return (out, lse) if return_lse else out
+
+
+def _get() -> Oracle:
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def default_threads() -> int:
+    """Threads the oracle uses when ``threads`` is not given."""
+    return _get().default_threads()
+
+
+def mha(q, k, v, mask_kind: int = MASK_NONE, key_lens=None, scale=None,
+        threads: int | None = None, return_lse: bool = False):
+    """Attention over all heads with the default build (see ``Oracle.mha``)."""
+    return _get().mha(q, k, v, mask_kind=mask_kind, key_lens=key_lens, scale=scale,
+                      threads=threads, return_lse=return_lse)

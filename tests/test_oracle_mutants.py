@@ -1,0 +1,58 @@
+"""Plausible mistakes planted in copies of the oracle (on the CPU) must each
+fail at least one pin, which shows the pins can tell a wrong oracle apart."""
+import math
+import os
+
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+# (name, text in mha_oracle.c, replacement)
+C_MUTANTS = [
+    ("scale_dropped", "s[j] = scale * dot;", "s[j] = dot;"),
+    ("values_read_from_keys", "const double* v_row = v + j * kv_row_stride;",
+     "const double* v_row = k + j * kv_row_stride;"),
+    ("diagonal_masked", "n = i + 1 < Lk ? i + 1 : Lk;", "n = i < Lk ? i : Lk;"),
+    ("causal_ignored", "n = i + 1 < Lk ? i + 1 : Lk;", "n = Lk;"),
+    ("no_normalisation", "for (int64_t j = 0; j < n; ++j) s[j] /= sum;", ""),
+    ("max_not_subtracted", "s[j] = exp(s[j] - m);", "s[j] = exp(s[j]);"),
+    ("head_offset_dropped", "k + (b * Lk * H + h) * d", "k + (b * Lk * H) * d"),
+    ("row_order_wrong", "const int64_t h = (r / Lq) % H;", "const int64_t h = r % H;"),
+    ("padding_length_off_by_one", "n = len;", "n = len > 0 ? len - 1 : 0;"),
+    ("query_row_stride_wrong", "q + ((b * Lq + i) * H + h) * d", "q + ((b * Lq + h) * H + i) * d"),
+]
+
+
+def _run_checks(mha):
+    failed = []
+    for check in oracle_pins.ALL_CHECKS:
+        try:
+            check(mha)
+        except (AssertionError, ValueError, IndexError):
+            failed.append(check.__name__)
+    return failed
+
+
+@pytest.mark.parametrize("name,old,new", C_MUTANTS, ids=[m[0] for m in C_MUTANTS])
+def test_c_mutant_is_caught(tmp_path, name, old, new):
+    src = open(oracle.SOURCE, encoding="utf-8").read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    mutated = tmp_path / f"{name}.c"
+    mutated.write_text(src.replace(old, new), encoding="utf-8")
+    lib = oracle.compile_source(str(mutated), str(tmp_path / f"lib{name}.so"))
+    failed = _run_checks(oracle.Oracle(lib).mha)
+    assert failed, f"mutant {name} passed every pin"
+
+
+def test_default_scale_mutant_is_caught():
+    """Reading the formula page's rendering literally (divide by d_k, not sqrt)."""
+    base = oracle.Oracle(oracle.build())
+
+    def mha_over_dk(q, k, v, mask_kind=0, key_lens=None, scale=None, threads=None,
+                    return_lse=False):
+        if scale is None:
+            scale = 1.0 / q.shape[-1]
+        return base.mha(q, k, v, mask_kind, key_lens, scale, threads, return_lse)
+
+    assert _run_checks(mha_over_dk)

@@ -1,0 +1,129 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+This module is shared by the CUDA path's tests and benchmark and by the oracle
+checks.  It holds no attention arithmetic: it only draws random numbers and
+casts them, so both sides of a parity test receive the same bits.
+
+Recipe (one CPU ``torch.Generator`` per workload, seed = 1000 + the
+workload's index in ``WORKLOADS``): draw Q, then K, then V as float32 N(0, 1)
+samples of shape [B, L, H, d_k], multiply by the workload's input scale
+(1.0, or 0.5 for the GPT-3-like workload: exact in float32), and cast with
+round-to-nearest-even to the workload's dtype; under key padding then draw
+``key_lens`` uniformly from [len_lo, len_hi] as int32.
+
+The shapes stand in for the pages' models, whose data (WMT14, GPT-3's corpus)
+are not available: the base Transformer (d_model 512, 8 heads of d_k = 64;
+"Attention Is All You Need", Sections 3.1 and 3.2.2, and the cookipedia
+article's encoder/decoder sections), the big model's 16 heads, GPT-3's
+96 heads of d_k = 128 at a 2048-token context (formula page
+transformer-attention, section 起源 and 応用), and the cookipedia toy model
+(d_model 6, 2 heads, source length 8, target length 4; section トイモデル).
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+MASK_NONE = 0
+MASK_CAUSAL = 1
+MASK_KEY_PADDING = 2
+
+MASK_NAMES = {MASK_NONE: "none", MASK_CAUSAL: "causal", MASK_KEY_PADDING: "key_padding"}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    d_k: int
+    Lq: int
+    Lk: int
+    mask_kind: int
+    dtype: torch.dtype
+    input_scale: float = 1.0
+    len_lo: int = 0          # key padding: key_lens ~ U[len_lo, len_hi]
+    len_hi: int = 0
+    note: str = ""
+
+    @property
+    def seed(self) -> int:
+        return 1000 + WORKLOAD_INDEX[self.name]
+
+    def flops(self, key_lens=None) -> float:
+        """Nominal 4*B*H*Lq*Lk*d_k, halved under the causal mask."""
+        f = 4.0 * self.B * self.H * self.Lq * self.Lk * self.d_k
+        return f / 2 if self.mask_kind == MASK_CAUSAL else f
+
+
+WORKLOADS = [
+    Workload("toy_cross_f32", 1, 2, 3, 4, 8, MASK_NONE, torch.float32,
+             note="cookipedia toy model: d_model 6, 2 heads, target 4, source 8"),
+    Workload("base_encoder_self", 32, 8, 64, 128, 128, MASK_NONE, torch.bfloat16,
+             note="base model encoder self-attention"),
+    Workload("base_decoder_causal", 32, 8, 64, 512, 512, MASK_CAUSAL, torch.bfloat16,
+             note="base model decoder masked self-attention"),
+    Workload("base_cross_keypad", 64, 8, 64, 256, 512, MASK_KEY_PADDING, torch.bfloat16,
+             len_lo=256, len_hi=512,
+             note="base model cross-attention, encoder key padding"),
+    Workload("gpt3_causal", 4, 96, 128, 2048, 2048, MASK_CAUSAL, torch.bfloat16,
+             input_scale=0.5, note="GPT-3-like: 96 heads, d_k 128, 2048 context"),
+    # supplementary long-sequence rows at d_k = 64
+    Workload("big16_L2048", 8, 16, 64, 2048, 2048, MASK_NONE, torch.bfloat16,
+             note="big model head count, L 2048"),
+    Workload("big16_L2048_causal", 8, 16, 64, 2048, 2048, MASK_CAUSAL, torch.bfloat16),
+    Workload("base8_L4096", 16, 8, 64, 4096, 4096, MASK_NONE, torch.bfloat16),
+    Workload("base8_L4096_causal", 16, 8, 64, 4096, 4096, MASK_CAUSAL, torch.bfloat16),
+]
+WORKLOAD_INDEX = {w.name: i for i, w in enumerate(WORKLOADS)}
+BY_NAME = {w.name: w for w in WORKLOADS}
+
+
+def generate(w: Workload, seed: int | None = None, batch: slice | None = None):
+    """Return dict(q, k, v, key_lens) on the CPU for workload ``w``.
+
+    ``batch`` selects sequences after drawing (so a slice sees exactly the
+    values the full draw has).  ``key_lens`` is None unless key padding.
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed if seed is None else seed)
+    shape_q = (w.B, w.Lq, w.H, w.d_k)
+    shape_kv = (w.B, w.Lk, w.H, w.d_k)
+    out = {}
+    for name, shape in (("q", shape_q), ("k", shape_kv), ("v", shape_kv)):
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        if w.input_scale != 1.0:
+            x.mul_(w.input_scale)
+        out[name] = x.to(w.dtype)
+    key_lens = None
+    if w.mask_kind == MASK_KEY_PADDING:
+        key_lens = torch.randint(w.len_lo, w.len_hi + 1, (w.B,), generator=g,
+                                 dtype=torch.int64).to(torch.int32)
+    out["key_lens"] = key_lens
+    if batch is not None:
+        for name in ("q", "k", "v"):
+            out[name] = out[name][batch].contiguous()
+        if key_lens is not None:
+            out["key_lens"] = key_lens[batch].contiguous()
+    return out
+
+
+def random_case(seed: int, B: int, H: int, Lq: int, Lk: int, d_k: int,
+                dtype=torch.bfloat16, input_scale: float = 1.0,
+                key_lens_range: tuple[int, int] | None = None):
+    """Ad-hoc seeded case with the same recipe (for parity sweeps)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    out = {}
+    for name, L in (("q", Lq), ("k", Lk), ("v", Lk)):
+        x = torch.randn((B, L, H, d_k), generator=g, dtype=torch.float32)
+        if input_scale != 1.0:
+            x.mul_(input_scale)
+        out[name] = x.to(dtype)
+    out["key_lens"] = None
+    if key_lens_range is not None:
+        lo, hi = key_lens_range
+        out["key_lens"] = torch.randint(lo, hi + 1, (B,), generator=g,
+                                        dtype=torch.int64).to(torch.int32)
+    return out
