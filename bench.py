@@ -1,0 +1,419 @@
+"""Benchmark of the multi-head attention forward on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one mha_fwd call over the whole workload (every sequence, head and
+query tile), inputs resident in HBM.  Prints ONE JSON line (rank 0).
+
+Metric: attention forward TFLOP/s, FLOPs = 4*B*H*Lq*Lk*d_k (halved under the
+causal mask), bf16 inputs, float32 accumulation; also reported as a fraction
+of the measured dense bf16 tensor peak.  The default workload is the GPT-3-like
+causal self-attention (B 4, H 96, d_k 128, L 2048): the only L >= 2048 shape of
+the five the pages suggest, and the one the throughput target is quoted on.
+
+N > 1 (torchrun, one rank per GPU): weak scaling; every rank runs its own
+replica of the workload (rank-specific seed), no data-path collective.
+``--impl reference`` times the float64 CPU oracle on the host cores on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from transformer_head_scaled_sdpa_gb300 import dist as mdist  # noqa: E402
+from transformer_head_scaled_sdpa_gb300 import inputs  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (bf16, 1 GB300) and % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def visible_pairs(w, key_lens) -> float:
+    """(query, visible key) pairs: the algorithmic work unit."""
+    if w.mask_kind == inputs.MASK_CAUSAL:
+        L = w.Lq
+        return w.B * w.H * L * (L + 1) / 2
+    if w.mask_kind == inputs.MASK_KEY_PADDING:
+        lens = key_lens.clamp(0, w.Lk).to(torch.int64).sum().item()
+        return w.H * w.Lq * float(lens)
+    return float(w.B * w.H * w.Lq * w.Lk)
+
+
+def workload_config(w, extra=None):
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d_k": w.d_k,
+           "mask": inputs.MASK_NAMES[w.mask_kind], "input_scale": w.input_scale,
+           "seed": w.seed, "layout": "[B, L, H, d_k]"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# clocks: nvidia-smi sampled during the timed region
+# ---------------------------------------------------------------------------
+def gpu_id(dev) -> str:
+    """nvidia-smi --id of this device (its UUID: independent of CUDA_VISIBLE_DEVICES)."""
+    uuid = str(getattr(torch.cuda.get_device_properties(dev), "uuid", "") or "")
+    if uuid:
+        return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    return str(dev.index)
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: str):
+        self.gpu = gpu
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, name):
+        self.marks.append((name, time.time()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        used = inside if inside else rows
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in used:
+            for name, val in zip(names, r[3][5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[1] for r in used),
+                "sm_max_mhz": max(r[2] for r in used),
+                "reasons": sorted(reasons),
+                "samples": len(used),
+                "samples_in_timed_region": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def traffic_record(kernel_fp: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (null otherwise)."""
+    path = os.path.join(ROOT, "profiles", f"fwd_bf16_kernel_{workload}.traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_source_sha256") != kernel_fp:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def kernel_fingerprint() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "transformer_head_scaled_sdpa_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def cpu_baseline(w, case, budget_s=12.0):
+    """The oracle, as it stands, on a bounded sample of whole heads of the
+    workload; returns TFLOP/s of algorithmic work and the sample description."""
+    import oracle
+    cores = oracle.default_threads()
+    done_pairs = 0.0
+    heads = 0
+    t0 = time.perf_counter()
+    b_h = [(b, h) for b in range(w.B) for h in range(w.H)]
+    while heads < len(b_h):
+        b, h = b_h[heads]
+        sub = {n: case[n][b:b + 1, :, h:h + 1] for n in ("q", "k", "v")}
+        lens = case["key_lens"][b:b + 1] if case["key_lens"] is not None else None
+        oracle.mha(sub["q"], sub["k"], sub["v"], w.mask_kind,
+                   key_lens=lens.numpy() if lens is not None else None)
+        heads += 1
+        one = inputs.Workload(w.name, 1, 1, w.d_k, w.Lq, w.Lk, w.mask_kind, w.dtype)
+        done_pairs += visible_pairs(one, lens)
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    flops = 4.0 * w.d_k * done_pairs
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{heads} whole (b, h) heads of {w.name} ({w.Lq}x{w.Lk}, d_k {w.d_k}, "
+                      f"{inputs.MASK_NAMES[w.mask_kind]}) in float64, {dt:.1f} s wall",
+            "seconds": dt}
+
+
+def run_ours(args):
+    rank, world = mdist.init("nccl")
+    _, _, local_rank = mdist.env_rank_world()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from transformer_head_scaled_sdpa_gb300 import binding, build
+    if rank == 0:
+        build.build()
+    mdist.barrier(dev)
+    build.build()  # no-op once built; loads on every rank
+    w = inputs.BY_NAME[args.workload]
+    case = inputs.generate(w, seed=mdist.rank_seed(w.seed, rank))
+    q, k, v = (case[n].to(dev) for n in ("q", "k", "v"))
+    lens = case["key_lens"].to(dev) if case["key_lens"] is not None else None
+    out = torch.empty_like(q)
+    stream = torch.cuda.Stream(device=dev)
+    pairs = visible_pairs(w, case["key_lens"])
+    flops_alg = 4.0 * w.d_k * pairs                 # per launch, this rank
+    flops_nominal = w.flops()
+    bytes_in = sum(t.numel() * t.element_size() for t in (q, k, v))
+    bytes_alg = bytes_in + out.numel() * out.element_size()
+    inputs_exceed_l2 = bytes_in > L2_BYTES
+    flush = None
+    if not inputs_exceed_l2:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        binding.mha_fwd(q, k, v, out=out, mask_kind=w.mask_kind, key_lens=lens, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    rc = binding.mha_sync_status(stream)
+    if rc != 0:
+        raise binding.MhaError(rc, "warm-up")
+    launches_per_step = binding.last_launch_info()["kernels"]
+
+    sampler = ClockSampler(gpu_id(dev))
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    all_start = torch.cuda.Event(enable_timing=True)
+    all_end = torch.cuda.Event(enable_timing=True)
+    mdist.barrier(dev)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        all_start.record(stream)
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        all_end.record(stream)
+    torch.cuda.synchronize(dev)
+    mdist.barrier(dev)
+    t_wall1 = time.time()
+    rc = binding.mha_sync_status(stream)
+    if rc != 0:
+        raise binding.MhaError(rc, "timed region")
+    per_launch_ms = [a.elapsed_time(b) for a, b in ev]
+    kernel_ms = sum(per_launch_ms) / len(per_launch_ms)
+    total_ms = all_start.elapsed_time(all_end)
+    max_total_ms = mdist.max_over_ranks(total_ms, dev)
+    total_flops = mdist.sum_over_ranks(flops_alg * args.steps, dev)
+    if rank == 0:
+        time.sleep(0.3)
+        sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1) if rank == 0 else None
+
+    # end to end: pinned host buffers through the C ABI's host entry
+    e2e = None
+    if rank == 0 or world > 1:
+        hq, hk, hv = (case[n].pin_memory() for n in ("q", "k", "v"))
+        hout = torch.empty_like(hq).pin_memory()
+        hlens = case["key_lens"].pin_memory() if case["key_lens"] is not None else None
+        ws = torch.empty(binding.host_workspace_bytes(w.B, w.H, w.Lq, w.Lk, w.d_k, 2),
+                         dtype=torch.uint8, device=dev)
+        n_e2e = max(3, min(args.steps, 10))
+        for _ in range(2):
+            binding.mha_fwd_host(hq, hk, hv, hout, ws, mask_kind=w.mask_kind, key_lens=hlens,
+                                 stream=stream)
+        mdist.barrier(dev)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            binding.mha_fwd_host(hq, hk, hv, hout, ws, mask_kind=w.mask_kind, key_lens=hlens,
+                                 stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = mdist.max_over_ranks(e0.elapsed_time(e1) / n_e2e, dev)
+        e2e_flops = mdist.sum_over_ranks(flops_alg, dev)
+        h2d = bytes_in + (hlens.numel() * 4 if hlens is not None else 0)
+        e2e = {"value": e2e_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * 2),
+               "steps": n_e2e, "ms_per_step": e2e_ms,
+               "path": "mha_fwd_host (C ABI): pinned host q,k,v -> device, kernel, out -> host"}
+
+    if rank != 0:
+        mdist.finish()
+        return
+    peaks, peak_src = load_peaks()
+    value = total_flops / (max_total_ms * 1e-3) / 1e12
+    achieved = flops_alg / (kernel_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    traffic = traffic_record(kernel_fingerprint(), w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, no dataset)",
+        "config": workload_config(w, {
+            "parallelism": f"replicas x{world} (no collective)",
+            "inputs_exceed_l2": inputs_exceed_l2, "l2_flush": flush is not None,
+            "flops_per_step_per_gpu": flops_alg, "flops_nominal_per_step_per_gpu": flops_nominal}),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "pct_of_sustained_peak": 100.0 * value / world / float(
+            peaks.get("bf16_tflops_sustained", peak)),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} dense bf16 (burst)",
+                     "kernel": "fwd_bf16_kernel", "kernel_ms": kernel_ms,
+                     "algorithmic_bytes": bytes_alg,
+                     "achieved_gbs": bytes_alg / (kernel_ms * 1e-3) / 1e9},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": int(launches_per_step * args.steps),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, case)
+    print(json.dumps(line), flush=True)
+    mdist.finish()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the float64 oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = mdist.env_rank_world()
+    if rank != 0:
+        return
+    import oracle
+    w = inputs.BY_NAME[args.workload]
+    case = inputs.generate(w)
+    cores = oracle.default_threads()
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    one = inputs.Workload(w.name, 1, 1, w.d_k, w.Lq, w.Lk, w.mask_kind, w.dtype)
+
+    def run_heads(n, start):
+        pairs = 0.0
+        for i in range(n):
+            b, h = heads[(start + i) % len(heads)]
+            sub = {x: case[x][b:b + 1, :, h:h + 1] for x in ("q", "k", "v")}
+            lens = case["key_lens"][b:b + 1] if case["key_lens"] is not None else None
+            oracle.mha(sub["q"], sub["k"], sub["v"], w.mask_kind,
+                       key_lens=lens.numpy() if lens is not None else None)
+            pairs += visible_pairs(one, lens)
+        return 4.0 * w.d_k * pairs
+
+    t0 = time.perf_counter()
+    run_heads(1, 0)
+    t_head = time.perf_counter() - t0
+    budget = 150.0 / max(1, args.steps + args.warmup)   # whole run within a few minutes
+    per_step = max(1, int(budget / max(t_head, 1e-6)))
+    for i in range(args.warmup):
+        run_heads(per_step, i * per_step)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for i in range(args.steps):
+        flops += run_heads(per_step, (args.warmup + i) * per_step)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = (f"{per_step} whole (b, h) head(s) of {w.name} per step ({w.Lq}x{w.Lk}, d_k {w.d_k}, "
+              f"{inputs.MASK_NAMES[w.mask_kind]}), float64 oracle, {cores} threads")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) inputs, no dataset)",
+        "config": workload_config(w, {"parallelism": "host cores (OpenMP)"}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="gpt3_causal", choices=sorted(inputs.BY_NAME))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+/*
+ * mha.h -- C ABI of libmha.so: multi-head scaled dot-product attention forward
+ * on one GB300 (sm_103a).
+ *
+ * Operation ("Attention Is All You Need", Section 3.2.1, Equation (1)):
+ *     Attention(Q, K, V) = softmax(Q K^T / sqrt(d_k)) V
+ * computed independently for every sequence b in [0, B) and head h in [0, H),
+ * i.e. all heads in parallel (Section 3.2.2; cookipedia article, section
+ * "Transformer の構造": the n_head x d_k vector of each step is split into
+ * heads, attention runs on every head, and the head outputs are concatenated).
+ * For query row i of (b, h) and its visible keys j:
+ *     s_j = scale * (q_i . k_j),   a_j = exp(s_j) / sum_j' exp(s_j'),
+ *     o_i = sum_j a_j v_j
+ * (formula page transformer-attention, section 証明).
+ *
+ * Masks (mask_kind):
+ *   MHA_MASK_NONE         every key 0 .. Lk-1 is visible (encoder
+ *                         self-attention, and cross-attention without padding).
+ *   MHA_MASK_CAUSAL       key j is visible to query i only if j <= i: the
+ *                         strictly-upper triangle of Q K^T is set to -inf
+ *                         before the softmax, the diagonal is kept (cookipedia
+ *                         article, decoder section; "Attention Is All You
+ *                         Need", Section 3.1).  Requires Lq == Lk.
+ *   MHA_MASK_KEY_PADDING  key j of sequence b is visible only if
+ *                         j < key_lens[b] (clamped to [0, Lk]); for
+ *                         cross-attention over padded encoder outputs (the
+ *                         decoder's second attention layer, cookipedia
+ *                         decoder section).  Not on the pages: its meaning
+ *                         is this library's definition.
+ * A row with no visible key (Lk == 0, or key_lens[b] <= 0) gets output 0.
+ *
+ * Layout: q and out are [B, Lq, H, d_k], k and v are [B, Lk, H, d_k], dense
+ * row-major (d_k fastest, then H, then L, then B).  The output therefore comes
+ * out already concatenated over heads: row (b, i) holds H*d_k contiguous
+ * values, ready for the output projection W^O.  d_v = d_k.
+ *
+ * Ownership: the caller owns every buffer and the stream.  No entry point
+ * allocates device memory, and the device entry points never synchronise.
+ * All K and V rows 0 .. Lk-1 must hold finite values: rows past a key length
+ * are read (their weight is zero, but 0 * inf would still be NaN).
+ *
+ * Errors: argument errors are returned at once and nothing is launched.
+ * Errors found on the device (a pipeline wait that timed out) are recorded in
+ * a per-device status word and returned by mha_sync_status().
+ */
+#ifndef MHA_H
+#define MHA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MHA_OK = 0,
+    MHA_ERR_NULL = 1,        /* a required pointer is NULL */
+    MHA_ERR_SHAPE = 2,       /* negative size, causal with Lq != Lk, size overflow */
+    MHA_ERR_UNSUPPORTED = 3, /* d_k not supported for this dtype, misaligned pointer, no sm_103a device */
+    MHA_ERR_MASK = 4,        /* unknown mask_kind, or key_lens NULL under key padding */
+    MHA_ERR_SCALE = 5,       /* scale is NaN, infinite or negative */
+    MHA_ERR_LAUNCH = 6,      /* a CUDA call failed (launch, copy, synchronise) */
+    MHA_ERR_TIMEOUT = 7,     /* a bounded pipeline wait on the device gave up */
+    MHA_ERR_ALIAS = 8,       /* out overlaps q, k or v */
+    MHA_ERR_WORKSPACE = 9    /* workspace NULL or smaller than required */
+} mha_status;
+
+typedef enum {
+    MHA_MASK_NONE = 0,
+    MHA_MASK_CAUSAL = 1,
+    MHA_MASK_KEY_PADDING = 2
+} mha_mask_kind;
+
+/*
+ * mha_fwd -- bf16 attention forward on the device.
+ *   q, k, v   device pointers, bf16, layouts above; 16-byte aligned.
+ *   out       device pointer, bf16 [B, Lq, H, d_k]; must not overlap q, k, v.
+ *             Written with the softmax-normalised output rounded to nearest
+ *             even from float32 accumulators.
+ *   B, H, Lq, Lk   sizes >= 0.  B*H*Lq == 0 is a no-op returning MHA_OK;
+ *             Lk == 0 writes zeros.  k and v may be NULL when Lk == 0.
+ *   d_k       64 or 128.
+ *   mask_kind one of mha_mask_kind.
+ *   key_lens  device pointer to B int32 values, read only under
+ *             MHA_MASK_KEY_PADDING (may be NULL otherwise).
+ *   scale     multiplier of q.k (the inverse temperature; the formula page
+ *             transformer-attention, section 証明, takes the divisor tau > 0);
+ *             0 selects 1/sqrt(d_k).  NaN, infinite or negative values are
+ *             rejected with MHA_ERR_SCALE.
+ *   stream    a cudaStream_t (NULL = the legacy default stream).
+ * Products are accumulated in float32 on the tensor cores; the softmax runs in
+ * float32 with exp2 and the row maximum subtracted; the probabilities are
+ * rounded to bf16 before the product with V.
+ * Returns MHA_OK once the work is enqueued, or an error code.
+ */
+int mha_fwd(const void* q, const void* k, const void* v, void* out,
+            int B, int H, int Lq, int Lk, int d_k, int mask_kind,
+            const int32_t* key_lens, float scale, void* stream);
+
+/*
+ * mha_fwd_f32 -- float32 attention forward on the device (all float32
+ * arithmetic, CUDA cores).  Same arguments and layout as mha_fwd with float32
+ * tensors (4-byte aligned); d_k from 1 to 256.
+ */
+int mha_fwd_f32(const void* q, const void* k, const void* v, void* out,
+                int B, int H, int Lq, int Lk, int d_k, int mask_kind,
+                const int32_t* key_lens, float scale, void* stream);
+
+/*
+ * mha_fwd_host_workspace_bytes -- device workspace mha_fwd_host needs for
+ * these sizes (elem_bytes 2 for bf16, 4 for float32).  0 on bad sizes.
+ */
+size_t mha_fwd_host_workspace_bytes(int B, int H, int Lq, int Lk, int d_k,
+                                    int elem_bytes);
+
+/*
+ * mha_fwd_host -- the same operation on HOST buffers: copies q, k, v (and
+ * key_lens) into the caller's device workspace, runs mha_fwd (elem_bytes 2)
+ * or mha_fwd_f32 (elem_bytes 4) there, copies the output back into out and
+ * waits for the stream.  Host buffers should be page-locked for the copies to
+ * be asynchronous.  Returns the argument check's code, MHA_ERR_WORKSPACE,
+ * MHA_ERR_LAUNCH, or the device status (as mha_sync_status).
+ */
+int mha_fwd_host(const void* q, const void* k, const void* v, void* out,
+                 int B, int H, int Lq, int Lk, int d_k, int mask_kind,
+                 const int32_t* key_lens, float scale, int elem_bytes,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * mha_sync_status -- waits for the stream, then returns and clears the
+ * current device's status word: MHA_OK, MHA_ERR_TIMEOUT (a kernel's bounded
+ * wait gave up after about a second; its outputs are undefined), or
+ * MHA_ERR_LAUNCH (the stream reported a CUDA error).
+ */
+int mha_sync_status(void* stream);
+
+/*
+ * mha_selftest_timeout -- launches one CTA that waits on a shared-memory
+ * barrier nothing ever arrives on, using the same bounded wait as the
+ * attention kernels.  The wait gives up after about a second and records
+ * MHA_ERR_TIMEOUT, which the next mha_sync_status(stream) returns; the CUDA
+ * context stays usable.  Exercises the device-side failure reporting without
+ * a fault.  Returns MHA_OK once launched.
+ */
+int mha_selftest_timeout(void* stream);
+
+/* mha_status_string -- static English text for a status code. */
+const char* mha_status_string(int status);
+
+/*
+ * mha_last_launch_info -- diagnostics of the last mha_fwd / mha_fwd_f32 call
+ * on this thread: kernels launched, grid size (CTAs), threads per CTA and
+ * dynamic shared memory bytes.  Any pointer may be NULL.
+ */
+void mha_last_launch_info(int* kernels, int* grid, int* block, int* smem_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHA_H */

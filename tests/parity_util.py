@@ -1,0 +1,64 @@
+"""Helpers for GPU-vs-oracle parity tests.
+
+Tolerances (fixed by the target specification of this library):
+  - float32 inputs, float32 arithmetic: max |O - O_ref| <= 1e-5;
+  - bf16 inputs, float32 accumulation, bf16 output: max |O - O_ref| <= 1e-2
+    and ||O - O_ref||_F / ||O_ref||_F <= 5e-3,
+where O_ref is the float64 oracle evaluated on the exact float64 images of the
+values the GPU received.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+BF16_MAX_ABS = 1e-2
+BF16_REL_FRO = 5e-3
+F32_MAX_ABS = 1e-5
+
+
+def to_cuda(case):
+    out = {}
+    for name in ("q", "k", "v"):
+        out[name] = case[name].cuda()
+    out["key_lens"] = case["key_lens"].cuda() if case.get("key_lens") is not None else None
+    return out
+
+
+def gpu_run(binding, case, mask_kind, scale=0.0):
+    g = to_cuda(case)
+    fn = binding.mha_fwd if case["q"].dtype == torch.bfloat16 else binding.mha_fwd_f32
+    o = fn(g["q"], g["k"], g["v"], mask_kind=mask_kind, key_lens=g["key_lens"], scale=scale)
+    assert binding.mha_sync_status() == 0
+    return o
+
+
+def oracle_run(case, mask_kind, scale=None):
+    lens = case.get("key_lens")
+    return oracle.mha(case["q"], case["k"], case["v"], mask_kind,
+                      key_lens=lens.numpy() if lens is not None else None, scale=scale)
+
+
+def errors(out, ref):
+    o = out.detach().to("cpu", torch.float64).numpy()
+    diff = o - ref
+    max_abs = float(np.abs(diff).max()) if diff.size else 0.0
+    ref_norm = float(np.linalg.norm(ref))
+    rel_fro = float(np.linalg.norm(diff) / ref_norm) if ref_norm > 0 else float(np.linalg.norm(diff))
+    return max_abs, rel_fro
+
+
+def assert_bf16_close(out, ref, what=""):
+    assert torch.isfinite(out.float()).all(), f"{what}: non-finite output"
+    max_abs, rel = errors(out, ref)
+    assert max_abs <= BF16_MAX_ABS and rel <= BF16_REL_FRO, \
+        f"{what}: max_abs {max_abs:.3e} (<= {BF16_MAX_ABS}), rel_fro {rel:.3e} (<= {BF16_REL_FRO})"
+    return max_abs, rel
+
+
+def assert_f32_close(out, ref, what=""):
+    max_abs, rel = errors(out, ref)
+    assert max_abs <= F32_MAX_ABS, f"{what}: max_abs {max_abs:.3e} (<= {F32_MAX_ABS})"
+    return max_abs, rel

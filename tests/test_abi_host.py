@@ -1,0 +1,91 @@
+"""The C ABI on the host: libmha.so builds, loads, exports every function
+include/mha.h declares, and rejects bad arguments with the documented codes.
+The argument checks run before any CUDA call, so no GPU is needed; pointers
+below are never dereferenced."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from transformer_head_scaled_sdpa_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mha.h")
+
+OK, NULL, SHAPE, UNSUP, MASK, SCALE, LAUNCH, TIMEOUT, ALIAS, WORKSPACE = range(10)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mha_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "mha_fwd" in names and "mha_fwd_f32" in names and "mha_sync_status" in names
+    raw = ctypes.CDLL(binding.library_path())
+    for n in names:
+        assert hasattr(raw, n), f"libmha.so does not export {n}"
+
+
+def test_status_strings(lib):
+    for code in range(10):
+        s = binding.mha_status_string(code)
+        assert s and s != "unknown status"
+    assert binding.mha_status_string(99) == "unknown status"
+
+
+# fake, 256-aligned, non-overlapping device addresses
+Q, K, V, O, LENS = 0x10000000, 0x20000000, 0x30000000, 0x40000000, 0x50000000
+
+
+def fwd(lib, fn="mha_fwd", q=Q, k=K, v=V, o=O, B=2, H=3, Lq=64, Lk=64, d=64, mask=0,
+        lens=None, scale=0.0):
+    return getattr(lib, fn)(q, k, v, o, B, H, Lq, Lk, d, mask, lens, scale, None)
+
+
+@pytest.mark.parametrize("fn", ["mha_fwd", "mha_fwd_f32"])
+def test_argument_errors(lib, fn):
+    assert fwd(lib, fn, B=-1) == SHAPE
+    assert fwd(lib, fn, Lk=-5) == SHAPE
+    assert fwd(lib, fn, d=0) == SHAPE
+    assert fwd(lib, fn, mask=1, Lq=64, Lk=65) == SHAPE          # causal needs Lq == Lk
+    assert fwd(lib, fn, mask=3) == MASK
+    assert fwd(lib, fn, mask=2, lens=None) == MASK               # key padding needs key_lens
+    assert fwd(lib, fn, scale=math.nan) == SCALE
+    assert fwd(lib, fn, scale=math.inf) == SCALE
+    assert fwd(lib, fn, scale=-0.5) == SCALE
+    assert fwd(lib, fn, q=None) == NULL
+    assert fwd(lib, fn, o=None) == NULL
+    assert fwd(lib, fn, k=None) == NULL
+    assert fwd(lib, fn, o=Q + 64) == ALIAS                        # out overlaps q
+    assert fwd(lib, fn, o=K) == ALIAS
+    assert fwd(lib, fn, B=1 << 20, H=1 << 10, Lq=1 << 20) == SHAPE  # row count overflow
+    # empty query side: nothing to do, no device touched
+    assert fwd(lib, fn, B=0) == OK
+    assert fwd(lib, fn, Lq=0, mask=0) == OK
+    assert fwd(lib, fn, H=0, q=None, o=None) == OK
+
+
+def test_bf16_specific_errors(lib):
+    assert fwd(lib, d=96) == UNSUP          # bf16 path: d_k in {64, 128}
+    assert fwd(lib, d=32) == UNSUP
+    assert fwd(lib, q=Q + 8) == UNSUP       # TMA needs 16-byte aligned bases
+    assert fwd(lib, fn="mha_fwd_f32", d=257) == UNSUP
+    assert fwd(lib, fn="mha_fwd_f32", q=Q + 2) == UNSUP
+
+
+def test_host_entry_errors(lib):
+    assert lib.mha_fwd_host_workspace_bytes(2, 3, 64, 64, 64, 2) > 0
+    assert lib.mha_fwd_host_workspace_bytes(2, 3, 64, 64, 64, 3) == 0
+    assert lib.mha_fwd_host(Q, K, V, O, 2, 3, 64, 64, 64, 0, None, 0.0, 2, None, 0, None) == WORKSPACE
+    assert lib.mha_fwd_host(Q, K, V, O, 2, 3, 64, 64, 64, 0, None, 0.0, 3, None, 0, None) == UNSUP

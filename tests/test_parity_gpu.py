@@ -1,0 +1,237 @@
+"""CUDA path vs the float64 oracle, element by element, through the C ABI.
+
+Covers every workload (in full where the oracle finishes in seconds, else on
+sampled heads computed in full by the oracle), ragged and sub-tile shapes,
+the three masks, key lengths at 0, 1 and Lk, guard bands around the output,
+determinism, causal locality, and the empty cases.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from tests import parity_util as pu
+from transformer_head_scaled_sdpa_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+NONE, CAUSAL, KEYPAD = inputs.MASK_NONE, inputs.MASK_CAUSAL, inputs.MASK_KEY_PADDING
+
+
+@pytest.fixture(scope="module")
+def mha():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for gpu tests")
+    from transformer_head_scaled_sdpa_gb300 import binding, build
+    build.build()
+    return binding
+
+
+# --------------------------------------------------------------------------
+# the workloads
+# --------------------------------------------------------------------------
+SMALL_WORKLOADS = ["toy_cross_f32", "base_encoder_self", "base_decoder_causal",
+                   "base_cross_keypad"]
+LARGE_WORKLOADS = ["gpt3_causal", "big16_L2048", "big16_L2048_causal", "base8_L4096",
+                   "base8_L4096_causal"]
+
+
+@pytest.mark.parametrize("name", SMALL_WORKLOADS)
+def test_workload_full(mha, name):
+    w = inputs.BY_NAME[name]
+    case = inputs.generate(w)
+    out = pu.gpu_run(mha, case, w.mask_kind)
+    ref = pu.oracle_run(case, w.mask_kind)
+    if w.dtype == torch.float32:
+        pu.assert_f32_close(out, ref, name)
+        # the toy's heads concatenate to the model width: [1, 4, 2, 3] -> [1, 4, 6]
+        assert out.reshape(w.B, w.Lq, w.H * w.d_k).shape == (1, 4, 6)
+    else:
+        pu.assert_bf16_close(out, ref, name)
+
+
+@pytest.mark.parametrize("name", LARGE_WORKLOADS)
+def test_workload_sampled_heads(mha, name):
+    """Full-size launch; the oracle recomputes whole (b, h) heads, sampled."""
+    w = inputs.BY_NAME[name]
+    case = inputs.generate(w)
+    out = pu.gpu_run(mha, case, w.mask_kind).cpu()
+    assert torch.isfinite(out.float()).all()
+    rng = np.random.default_rng(w.seed)
+    picks = {(0, 0), (w.B - 1, w.H - 1)}
+    while len(picks) < 4:
+        picks.add((int(rng.integers(w.B)), int(rng.integers(w.H))))
+    for b, h in sorted(picks):
+        sub = {n: case[n][b:b + 1, :, h:h + 1].contiguous() for n in ("q", "k", "v")}
+        sub["key_lens"] = case["key_lens"][b:b + 1] if case["key_lens"] is not None else None
+        ref = pu.oracle_run(sub, w.mask_kind)
+        pu.assert_bf16_close(out[b:b + 1, :, h:h + 1], ref, f"{name} b={b} h={h}")
+
+
+# --------------------------------------------------------------------------
+# shapes: ragged tails, sub-tile, several tiles, both head sizes
+# --------------------------------------------------------------------------
+SHAPES = [
+    # B, H, Lq, Lk, d, mask, key_lens
+    (2, 3, 200, 333, 64, NONE, None),
+    (2, 3, 200, 333, 128, NONE, None),
+    (1, 2, 5, 7, 64, NONE, None),
+    (1, 2, 5, 7, 128, NONE, None),
+    (2, 2, 256, 1, 64, NONE, None),
+    (3, 2, 300, 300, 64, CAUSAL, None),
+    (3, 2, 300, 300, 128, CAUSAL, None),
+    (2, 4, 129, 129, 64, CAUSAL, None),
+    (1, 1, 1, 1, 64, CAUSAL, None),
+    (4, 2, 100, 400, 64, KEYPAD, [1, 400, 0, 129]),
+    (4, 2, 130, 257, 128, KEYPAD, [257, 128, 127, 1]),
+    (2, 3, 384, 640, 64, KEYPAD, [640, 300]),
+    (1, 8, 640, 640, 128, NONE, None),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s[:5])) + f"-m{s[5]}")
+def test_shapes(mha, shape):
+    B, H, Lq, Lk, d, mask, lens = shape
+    case = inputs.random_case(zlib.crc32(repr(shape).encode()) & 0xFFFF, B, H, Lq, Lk, d)
+    if lens is not None:
+        case["key_lens"] = torch.tensor(lens, dtype=torch.int32)
+    out = pu.gpu_run(mha, case, mask)
+    ref = pu.oracle_run(case, mask)
+    pu.assert_bf16_close(out, ref, str(shape))
+    if mask == KEYPAD:
+        for b, n in enumerate(lens):
+            if n <= 0:
+                assert torch.count_nonzero(out[b]) == 0
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.02, 0.5])
+def test_explicit_scale_and_peaked_scores(mha, scale):
+    """Scale 1 (unscaled, Luong) on inputs x4 makes the softmax nearly one-hot."""
+    case = inputs.random_case(77, 2, 2, 256, 256, 64, input_scale=2.0)
+    out = pu.gpu_run(mha, case, NONE, scale=scale)
+    ref = pu.oracle_run(case, NONE, scale=scale)
+    pu.assert_bf16_close(out, ref, f"scale {scale}")
+
+
+# --------------------------------------------------------------------------
+# properties
+# --------------------------------------------------------------------------
+def test_guard_bands_untouched(mha):
+    B, H, Lq, Lk, d = 2, 3, 200, 333, 64
+    case = pu.to_cuda(inputs.random_case(5, B, H, Lq, Lk, d))
+    n = B * Lq * H * d
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), 7.25, dtype=torch.bfloat16, device="cuda")
+    out = buf[guard:guard + n].view(B, Lq, H, d)
+    for mask, lens in ((NONE, None), (KEYPAD, torch.tensor([5, 333], dtype=torch.int32).cuda())):
+        mha.mha_fwd(case["q"], case["k"], case["v"], out=out, mask_kind=mask, key_lens=lens)
+        assert mha.mha_sync_status() == 0
+        assert torch.all(buf[:guard] == 7.25) and torch.all(buf[guard + n:] == 7.25)
+
+
+def test_deterministic(mha):
+    case = pu.to_cuda(inputs.random_case(6, 2, 4, 384, 384, 128))
+    a = mha.mha_fwd(case["q"], case["k"], case["v"], mask_kind=CAUSAL)
+    b = mha.mha_fwd(case["q"], case["k"], case["v"], mask_kind=CAUSAL)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_causal_locality(mha):
+    """Output rows <= t do not change when keys/values after t change."""
+    case = pu.to_cuda(inputs.random_case(8, 2, 2, 300, 300, 64))
+    o = mha.mha_fwd(case["q"], case["k"], case["v"], mask_kind=CAUSAL)
+    for t in (0, 127, 128, 200):
+        k2 = case["k"].clone()
+        v2 = case["v"].clone()
+        k2[:, t + 1:] = -3.0
+        v2[:, t + 1:] = 5.0
+        o2 = mha.mha_fwd(case["q"], k2, v2, mask_kind=CAUSAL)
+        torch.cuda.synchronize()
+        assert torch.equal(o2[:, :t + 1], o[:, :t + 1]), t
+
+
+def test_key_padding_ignores_padded_rows(mha):
+    case = pu.to_cuda(inputs.random_case(9, 3, 2, 128, 300, 64))
+    lens = torch.tensor([300, 77, 129], dtype=torch.int32, device="cuda")
+    o = mha.mha_fwd(case["q"], case["k"], case["v"], mask_kind=KEYPAD, key_lens=lens)
+    k2 = case["k"].clone()
+    v2 = case["v"].clone()
+    for b, n in enumerate(lens.tolist()):
+        k2[b, n:] = 9.0
+        v2[b, n:] = -4.0
+    o2 = mha.mha_fwd(case["q"], k2, v2, mask_kind=KEYPAD, key_lens=lens)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2)
+
+
+def test_empty_and_keyless(mha):
+    q = torch.zeros((0, 16, 2, 64), dtype=torch.bfloat16, device="cuda")
+    out = mha.mha_fwd(q, q, q)
+    assert out.shape == q.shape
+    q = torch.randn((2, 16, 2, 64), device="cuda").to(torch.bfloat16)
+    kv = torch.zeros((2, 0, 2, 64), dtype=torch.bfloat16, device="cuda")
+    out = torch.full_like(q, 3.0)
+    mha.mha_fwd(q, kv, kv, out=out)
+    assert mha.mha_sync_status() == 0
+    assert torch.count_nonzero(out) == 0
+
+
+def test_launch_shape(mha):
+    case = pu.to_cuda(inputs.random_case(10, 3, 5, 300, 300, 64))
+    mha.mha_fwd(case["q"], case["k"], case["v"])
+    info = mha.last_launch_info()
+    assert info["kernels"] == 1 and info["grid"] == 3 * 3 * 5
+    assert mha.mha_sync_status() == 0
+
+
+# --------------------------------------------------------------------------
+# float32 path
+# --------------------------------------------------------------------------
+F32_SHAPES = [
+    (1, 2, 4, 8, 3, NONE, None),
+    (2, 3, 17, 50, 1, NONE, None),
+    (2, 2, 70, 70, 17, CAUSAL, None),
+    (3, 2, 33, 90, 64, KEYPAD, [90, 1, 0]),
+    (1, 2, 40, 40, 100, CAUSAL, None),
+    (2, 1, 20, 65, 256, NONE, None),
+]
+
+
+@pytest.mark.parametrize("shape", F32_SHAPES, ids=lambda s: "x".join(map(str, s[:5])) + f"-m{s[5]}")
+def test_f32_shapes(mha, shape):
+    B, H, Lq, Lk, d, mask, lens = shape
+    case = inputs.random_case(d * 31 + Lk, B, H, Lq, Lk, d, dtype=torch.float32)
+    if lens is not None:
+        case["key_lens"] = torch.tensor(lens, dtype=torch.int32)
+    out = pu.gpu_run(mha, case, mask)
+    ref = pu.oracle_run(case, mask)
+    pu.assert_f32_close(out, ref, str(shape))
+
+
+# --------------------------------------------------------------------------
+# host-buffer entry and device-side failure reporting
+# --------------------------------------------------------------------------
+def test_host_entry_matches_device_entry(mha):
+    w = inputs.BY_NAME["base_cross_keypad"]
+    case = inputs.generate(w)
+    dev = pu.gpu_run(mha, case, w.mask_kind).cpu()
+    host = {n: case[n].pin_memory() for n in ("q", "k", "v")}
+    out = torch.empty_like(host["q"]).pin_memory()
+    ws = torch.empty(mha.host_workspace_bytes(w.B, w.H, w.Lq, w.Lk, w.d_k, 2),
+                     dtype=torch.uint8, device="cuda")
+    mha.mha_fwd_host(host["q"], host["k"], host["v"], out, ws, mask_kind=w.mask_kind,
+                     key_lens=case["key_lens"])
+    assert torch.equal(out, dev)
+
+
+def test_bounded_wait_reports_timeout(mha):
+    """A wait nothing completes gives up (~1 s), reports MHA_ERR_TIMEOUT, and
+    the context stays usable."""
+    mha.mha_selftest_timeout()
+    assert mha.mha_sync_status() == 7
+    assert mha.mha_sync_status() == 0  # cleared
+    case = inputs.random_case(11, 1, 2, 128, 128, 64)
+    out = pu.gpu_run(mha, case, NONE)
+    pu.assert_bf16_close(out, pu.oracle_run(case, NONE), "after timeout")

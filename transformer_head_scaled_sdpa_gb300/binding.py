@@ -1,0 +1,191 @@
+"""ctypes binding of libmha.so (C ABI in ``include/mha.h``).
+
+Argument marshalling only: every step of the attention forward runs in the
+library's CUDA kernels.  Tensors are torch tensors (device memory and streams
+come from PyTorch); their shapes are [B, L, H, d_k].  If the library has not
+been built, or cannot be loaded, every call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+MHA_OK = 0
+STATUS_NAMES = {
+    0: "MHA_OK", 1: "MHA_ERR_NULL", 2: "MHA_ERR_SHAPE", 3: "MHA_ERR_UNSUPPORTED",
+    4: "MHA_ERR_MASK", 5: "MHA_ERR_SCALE", 6: "MHA_ERR_LAUNCH", 7: "MHA_ERR_TIMEOUT",
+    8: "MHA_ERR_ALIAS", 9: "MHA_ERR_WORKSPACE",
+}
+
+_lock = threading.Lock()
+_lib = None
+
+_c_p = ctypes.c_void_p
+_c_i = ctypes.c_int
+_FWD_ARGS = [_c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_p,
+             ctypes.c_float, _c_p]
+
+
+class MhaError(RuntimeError):
+    """A non-zero mha_status from the library."""
+
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {STATUS_NAMES.get(self.code, self.code)} "
+                         f"({mha_status_string(self.code)})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """The loaded libmha.so (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it first "
+                    "(python -m transformer_head_scaled_sdpa_gb300.build)")
+            h = ctypes.CDLL(path)
+            h.mha_fwd.restype = _c_i
+            h.mha_fwd.argtypes = _FWD_ARGS
+            h.mha_fwd_f32.restype = _c_i
+            h.mha_fwd_f32.argtypes = _FWD_ARGS
+            h.mha_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+            h.mha_fwd_host_workspace_bytes.argtypes = [_c_i] * 6
+            h.mha_fwd_host.restype = _c_i
+            h.mha_fwd_host.argtypes = _FWD_ARGS[:-1] + [_c_i, _c_p, ctypes.c_size_t, _c_p]
+            h.mha_selftest_timeout.restype = _c_i
+            h.mha_selftest_timeout.argtypes = [_c_p]
+            h.mha_sync_status.restype = _c_i
+            h.mha_sync_status.argtypes = [_c_p]
+            h.mha_status_string.restype = ctypes.c_char_p
+            h.mha_status_string.argtypes = [_c_i]
+            h.mha_last_launch_info.restype = None
+            h.mha_last_launch_info.argtypes = [ctypes.POINTER(_c_i)] * 4
+            _lib = h
+    return _lib
+
+
+def mha_status_string(code: int) -> str:
+    return lib().mha_status_string(int(code)).decode()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _shape(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, L, H, d_k]")
+    B, Lq, H, d = q.shape
+    Lk = k.shape[1]
+    if tuple(k.shape) != (B, Lk, H, d) or tuple(v.shape) != (B, Lk, H, d):
+        raise ValueError(f"k {tuple(k.shape)} / v {tuple(v.shape)} do not match q {tuple(q.shape)}")
+    return B, H, Lq, Lk, d
+
+
+def _check_tensor(t, name, dtype, device_kind):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device.type != device_kind:
+        raise ValueError(f"{name} must be on {device_kind}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _call_fwd(fn_name, dtype, q, k, v, out, mask_kind, key_lens, scale, stream):
+    B, H, Lq, Lk, d = _shape(q, k, v)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n, dtype, "cuda")
+    if out is None:
+        out = torch.empty_like(q)
+    _check_tensor(out, "out", dtype, "cuda")
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have q's shape")
+    lens_ptr = None
+    if key_lens is not None:
+        _check_tensor(key_lens, "key_lens", torch.int32, "cuda")
+        if tuple(key_lens.shape) != (B,):
+            raise ValueError("key_lens must be [B]")
+        lens_ptr = key_lens.data_ptr()
+    rc = getattr(lib(), fn_name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 B, H, Lq, Lk, d, int(mask_kind), lens_ptr, float(scale),
+                                 _stream_handle(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, fn_name)
+    return out
+
+
+def mha_fwd(q, k, v, out=None, mask_kind: int = 0, key_lens=None, scale: float = 0.0,
+            stream=None):
+    """bf16 attention forward on the GPU (tcgen05 kernel); returns ``out``."""
+    return _call_fwd("mha_fwd", torch.bfloat16, q, k, v, out, mask_kind, key_lens, scale,
+                     stream)
+
+
+def mha_fwd_f32(q, k, v, out=None, mask_kind: int = 0, key_lens=None, scale: float = 0.0,
+                stream=None):
+    """float32 attention forward on the GPU (SIMT kernel); returns ``out``."""
+    return _call_fwd("mha_fwd_f32", torch.float32, q, k, v, out, mask_kind, key_lens, scale,
+                     stream)
+
+
+def host_workspace_bytes(B, H, Lq, Lk, d_k, elem_bytes) -> int:
+    return int(lib().mha_fwd_host_workspace_bytes(B, H, Lq, Lk, d_k, elem_bytes))
+
+
+def mha_fwd_host(q, k, v, out, workspace, mask_kind: int = 0, key_lens=None,
+                 scale: float = 0.0, stream=None) -> int:
+    """Attention on HOST tensors (pinned for async copies) through the C ABI's
+    host-buffer entry: H2D copies, the kernel and the D2H copy of ``out`` all
+    run on ``stream``; returns once ``out`` holds the result."""
+    B, H, Lq, Lk, d = _shape(q, k, v)
+    dtype = q.dtype
+    if dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("host tensors must be bf16 or float32")
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _check_tensor(t, n, dtype, "cpu")
+    lens_ptr = None
+    if key_lens is not None:
+        _check_tensor(key_lens, "key_lens", torch.int32, "cpu")
+        lens_ptr = key_lens.data_ptr()
+    _check_tensor(workspace, "workspace", torch.uint8, "cuda")
+    rc = lib().mha_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            B, H, Lq, Lk, d, int(mask_kind), lens_ptr, float(scale),
+                            2 if dtype == torch.bfloat16 else 4, workspace.data_ptr(),
+                            workspace.numel(), _stream_handle(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "mha_fwd_host")
+    return rc
+
+
+def mha_sync_status(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the device status code."""
+    return int(lib().mha_sync_status(_stream_handle(stream)))
+
+
+def mha_selftest_timeout(stream=None) -> int:
+    """Launch the bounded-wait self-test kernel (see include/mha.h)."""
+    rc = lib().mha_selftest_timeout(_stream_handle(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "mha_selftest_timeout")
+    return rc
+
+
+def last_launch_info() -> dict:
+    vals = [ctypes.c_int(0) for _ in range(4)]
+    lib().mha_last_launch_info(*[ctypes.byref(x) for x in vals])
+    return dict(zip(("kernels", "grid", "block", "smem"), (x.value for x in vals)))

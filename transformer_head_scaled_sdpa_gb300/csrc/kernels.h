@@ -1,0 +1,57 @@
+// kernels.h -- internal launch interface between the C ABI (mha_abi.cu) and
+// the kernels.  Not installed; no torch or Python types.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace mha {
+
+enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskKeyPadding = 2 };
+
+// Queries per CTA tile (M of the tcgen05 MMA) and keys per K/V tile.
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+
+struct Bf16Params {
+  CUtensorMap tm_q;  // [B, Lq, H, d] bf16, box {64, 1, 128, 1}, 128-byte swizzle
+  CUtensorMap tm_k;  // [B, Lk, H, d]
+  CUtensorMap tm_v;  // [B, Lk, H, d]
+  void* out;         // [B, Lq, H, d] bf16
+  const int32_t* key_lens;
+  DeviceStatus* status;
+  int B, H, Lq, Lk;
+  int mask_kind;
+  int n_qtiles;      // ceil(Lq / 128)
+  float scale_log2;  // scale * log2(e)
+};
+
+struct F32Params {
+  const float* q;
+  const float* k;
+  const float* v;
+  float* out;
+  const int32_t* key_lens;
+  int B, H, Lq, Lk, d;
+  int mask_kind;
+  float scale_log2;
+};
+
+struct LaunchInfo {
+  int kernels = 0;
+  int grid = 0;
+  int block = 0;
+  int smem = 0;
+};
+
+// Launches the bf16 tcgen05 forward for d in {64, 128}.
+cudaError_t launch_fwd_bf16(const Bf16Params& p, int d, cudaStream_t stream, LaunchInfo* info);
+
+// Launches the float32 SIMT forward (1 <= d <= 256).
+cudaError_t launch_fwd_f32(const F32Params& p, cudaStream_t stream, LaunchInfo* info);
+
+}  // namespace mha

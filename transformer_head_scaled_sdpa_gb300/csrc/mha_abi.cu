@@ -1,0 +1,346 @@
+// mha_abi.cu -- the C ABI of libmha.so (declared in include/mha.h): argument
+// checks, TMA tensor-map encoding, kernel dispatch, the host-buffer entry and
+// the per-device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mha.h"
+#include "kernels.h"
+
+namespace {
+
+using mha::DeviceStatus;
+
+// One status word per device: kernels record a bounded wait that gave up.
+__device__ DeviceStatus g_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int supported = 0;  // MHA_OK or MHA_ERR_UNSUPPORTED
+  DeviceStatus* status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+thread_local mha::LaunchInfo t_info;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Device set-up, once per device with that device current: capability check
+// and the device address of the status word.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_LAUNCH;
+  if (dev < 0 || dev >= kMaxDevices) return MHA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return MHA_ERR_LAUNCH;
+    st.supported = (major == 10 && minor == 3) ? MHA_OK : MHA_ERR_UNSUPPORTED;
+    if (st.supported == MHA_OK) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_status) != cudaSuccess) return MHA_ERR_LAUNCH;
+      st.status = static_cast<DeviceStatus*>(addr);
+      if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+          return MHA_ERR_LAUNCH;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+      }
+    }
+    st.ready = true;
+  }
+  *out = &st;
+  return st.supported;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a);
+  const uintptr_t y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+struct Sizes {
+  size_t q_elems = 0, kv_elems = 0;
+};
+
+// Checks shared by the device entries.  Returns MHA_OK and sets *empty when
+// there is nothing to compute.
+int check_args(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq,
+               int Lk, int d_k, int mask_kind, const int32_t* key_lens, float scale,
+               int elem_bytes, size_t align, bool* empty, Sizes* sz) {
+  *empty = false;
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || d_k < 0) return MHA_ERR_SHAPE;
+  if (mask_kind != MHA_MASK_NONE && mask_kind != MHA_MASK_CAUSAL &&
+      mask_kind != MHA_MASK_KEY_PADDING)
+    return MHA_ERR_MASK;
+  if (mask_kind == MHA_MASK_CAUSAL && Lq != Lk) return MHA_ERR_SHAPE;
+  if (!std::isfinite(scale) || scale < 0.f) return MHA_ERR_SCALE;
+  if (d_k == 0) return MHA_ERR_SHAPE;
+  // every element index must fit comfortably in 64 bits and every row count in 31
+  const long long rows_q = static_cast<long long>(B) * H * Lq;
+  const long long rows_k = static_cast<long long>(B) * H * Lk;
+  if (rows_q > (1ll << 40) || rows_k > (1ll << 40)) return MHA_ERR_SHAPE;
+  sz->q_elems = static_cast<size_t>(rows_q) * d_k;
+  sz->kv_elems = static_cast<size_t>(rows_k) * d_k;
+  if (rows_q == 0) {
+    *empty = true;
+    return MHA_OK;
+  }
+  if (!q || !out) return MHA_ERR_NULL;
+  if (Lk > 0 && (!k || !v)) return MHA_ERR_NULL;
+  if (mask_kind == MHA_MASK_KEY_PADDING && !key_lens) return MHA_ERR_MASK;
+  const uintptr_t mis = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out) |
+                         (Lk > 0 ? (reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v))
+                                 : 0)) &
+                        (align - 1);
+  if (mis) return MHA_ERR_UNSUPPORTED;
+  const size_t ob = sz->q_elems * elem_bytes;
+  const size_t kb = sz->kv_elems * elem_bytes;
+  if (overlaps(out, ob, q, ob) || overlaps(out, ob, k, kb) || overlaps(out, ob, v, kb))
+    return MHA_ERR_ALIAS;
+  return MHA_OK;
+}
+
+// 4-D map over a [B, L, H, d] bf16 tensor; box = 64 features x 1 head x 128
+// rows x 1 sequence, 128-byte swizzle (the tcgen05 operand layout).
+bool encode_map(CUtensorMap* m, const void* base, int B, int L, int H, int d) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(H) * d * 2,
+                                 static_cast<cuuint64_t>(L) * H * d * 2};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// One CTA waits on an mbarrier that nothing ever arrives on, with the same
+// bounded wait the pipelines use: after the limit it records
+// MHA_ERR_TIMEOUT in the status word and returns.
+__global__ void selftest_wait_kernel(DeviceStatus* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mha::mbar_init(mha::smem_u32(&bar), 1);
+    abort_flag = 0;
+    mha::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mha::mbar_wait(mha::smem_u32(&bar), 0, &abort_flag, status, 0xFF);
+  __syncthreads();
+}
+
+float effective_scale(float scale, int d_k) {
+  return scale == 0.f ? 1.f / std::sqrt(static_cast<float>(d_k)) : scale;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mha_fwd(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq, int Lk,
+            int d_k, int mask_kind, const int32_t* key_lens, float scale, void* stream) {
+  t_info = mha::LaunchInfo{};
+  bool empty = false;
+  Sizes sz;
+  int rc = check_args(q, k, v, out, B, H, Lq, Lk, d_k, mask_kind, key_lens, scale, 2, 16, &empty,
+                      &sz);
+  if (rc != MHA_OK) return rc;
+  if (d_k != 64 && d_k != 128) return MHA_ERR_UNSUPPORTED;
+  if (empty) return MHA_OK;
+  DeviceState* dev = nullptr;
+  rc = device_state(&dev);
+  if (rc != MHA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (Lk == 0) {
+    // no key anywhere: every row is 0 (bf16 zero is the all-zero pattern)
+    return cudaMemsetAsync(out, 0, sz.q_elems * 2, s) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
+  }
+  const long long n_qtiles = (Lq + mha::kBlockM - 1) / mha::kBlockM;
+  if (n_qtiles * B * H > 0x7fffffffll) return MHA_ERR_SHAPE;
+  mha::Bf16Params p;
+  std::memset(&p, 0, sizeof(p));
+  if (!encode_map(&p.tm_q, q, B, Lq, H, d_k) || !encode_map(&p.tm_k, k, B, Lk, H, d_k) ||
+      !encode_map(&p.tm_v, v, B, Lk, H, d_k))
+    return MHA_ERR_UNSUPPORTED;
+  p.out = out;
+  p.key_lens = key_lens;
+  p.status = dev->status;
+  p.B = B;
+  p.H = H;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.mask_kind = mask_kind;
+  p.n_qtiles = static_cast<int>(n_qtiles);
+  p.scale_log2 = effective_scale(scale, d_k) * kLog2e;
+  return mha::launch_fwd_bf16(p, d_k, s, &t_info) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
+}
+
+int mha_fwd_f32(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq,
+                int Lk, int d_k, int mask_kind, const int32_t* key_lens, float scale,
+                void* stream) {
+  t_info = mha::LaunchInfo{};
+  bool empty = false;
+  Sizes sz;
+  int rc = check_args(q, k, v, out, B, H, Lq, Lk, d_k, mask_kind, key_lens, scale, 4, 4, &empty,
+                      &sz);
+  if (rc != MHA_OK) return rc;
+  if (d_k > 256) return MHA_ERR_UNSUPPORTED;
+  if (empty) return MHA_OK;
+  DeviceState* dev = nullptr;
+  rc = device_state(&dev);
+  if (rc != MHA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (Lk == 0)
+    return cudaMemsetAsync(out, 0, sz.q_elems * 4, s) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
+  if ((static_cast<long long>(B) * H * Lq + 7) / 8 > 0x7fffffffll) return MHA_ERR_SHAPE;
+  mha::F32Params p;
+  p.q = static_cast<const float*>(q);
+  p.k = static_cast<const float*>(k);
+  p.v = static_cast<const float*>(v);
+  p.out = static_cast<float*>(out);
+  p.key_lens = key_lens;
+  p.B = B;
+  p.H = H;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.d = d_k;
+  p.mask_kind = mask_kind;
+  p.scale_log2 = effective_scale(scale, d_k) * kLog2e;
+  return mha::launch_fwd_f32(p, s, &t_info) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+size_t mha_fwd_host_workspace_bytes(int B, int H, int Lq, int Lk, int d_k, int elem_bytes) {
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || d_k < 1) return 0;
+  if (elem_bytes != 2 && elem_bytes != 4) return 0;
+  const size_t qb = static_cast<size_t>(B) * Lq * H * d_k * elem_bytes;
+  const size_t kb = static_cast<size_t>(B) * Lk * H * d_k * elem_bytes;
+  return align256(qb) * 2 + align256(kb) * 2 + align256(static_cast<size_t>(B) * 4);
+}
+
+int mha_fwd_host(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq,
+                 int Lk, int d_k, int mask_kind, const int32_t* key_lens, float scale,
+                 int elem_bytes, void* workspace, size_t workspace_bytes, void* stream) {
+  if (elem_bytes != 2 && elem_bytes != 4) return MHA_ERR_UNSUPPORTED;
+  const size_t need = mha_fwd_host_workspace_bytes(B, H, Lq, Lk, d_k, elem_bytes);
+  if (need == 0) return MHA_ERR_SHAPE;
+  const size_t qb = static_cast<size_t>(B) * Lq * H * d_k * elem_bytes;
+  const size_t kb = static_cast<size_t>(B) * Lk * H * d_k * elem_bytes;
+  if (qb == 0) return MHA_OK;
+  if (!workspace || workspace_bytes < need) return MHA_ERR_WORKSPACE;
+  if (!q || !out || (kb > 0 && (!k || !v))) return MHA_ERR_NULL;
+  if (mask_kind == MHA_MASK_KEY_PADDING && !key_lens) return MHA_ERR_MASK;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  uint8_t* dq = w;
+  uint8_t* dk = dq + align256(qb);
+  uint8_t* dv = dk + align256(kb);
+  uint8_t* dout = dv + align256(kb);
+  int32_t* dlens = reinterpret_cast<int32_t*>(dout + align256(qb));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(dq, q, qb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MHA_ERR_LAUNCH;
+  if (kb > 0) {
+    if (cudaMemcpyAsync(dk, k, kb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(dv, v, kb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return MHA_ERR_LAUNCH;
+  }
+  const int32_t* lens = nullptr;
+  if (mask_kind == MHA_MASK_KEY_PADDING) {
+    if (cudaMemcpyAsync(dlens, key_lens, static_cast<size_t>(B) * 4, cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+      return MHA_ERR_LAUNCH;
+    lens = dlens;
+  }
+  const int rc = (elem_bytes == 2)
+                     ? mha_fwd(dq, kb ? dk : nullptr, kb ? dv : nullptr, dout, B, H, Lq, Lk, d_k,
+                               mask_kind, lens, scale, stream)
+                     : mha_fwd_f32(dq, kb ? dk : nullptr, kb ? dv : nullptr, dout, B, H, Lq, Lk,
+                                   d_k, mask_kind, lens, scale, stream);
+  if (rc != MHA_OK) {
+    cudaStreamSynchronize(s);
+    return rc;
+  }
+  if (cudaMemcpyAsync(out, dout, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MHA_ERR_LAUNCH;
+  return mha_sync_status(stream);
+}
+
+int mha_selftest_timeout(void* stream) {
+  t_info = mha::LaunchInfo{};
+  DeviceState* dev = nullptr;
+  const int rc = device_state(&dev);
+  if (rc != MHA_OK) return rc;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev->status);
+  t_info.kernels = 1;
+  t_info.grid = 1;
+  t_info.block = 32;
+  return cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
+}
+
+int mha_sync_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MHA_ERR_LAUNCH;
+  DeviceState* dev = nullptr;
+  const int rc = device_state(&dev);
+  if (rc != MHA_OK) return rc;
+  DeviceStatus st;
+  if (cudaMemcpy(&st, dev->status, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MHA_ERR_LAUNCH;
+  if (st.code != 0) {
+    const DeviceStatus zero = {0, 0, 0, 0};
+    if (cudaMemcpy(dev->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return MHA_ERR_LAUNCH;
+  }
+  return st.code;
+}
+
+const char* mha_status_string(int status) {
+  switch (status) {
+    case MHA_OK: return "ok";
+    case MHA_ERR_NULL: return "a required pointer is NULL";
+    case MHA_ERR_SHAPE: return "bad sizes (negative, causal with Lq != Lk, or too large)";
+    case MHA_ERR_UNSUPPORTED:
+      return "unsupported (d_k for this dtype, pointer alignment, or device is not sm_103)";
+    case MHA_ERR_MASK: return "unknown mask kind, or key_lens missing under key padding";
+    case MHA_ERR_SCALE: return "scale must be finite and >= 0 (0 selects 1/sqrt(d_k))";
+    case MHA_ERR_LAUNCH: return "a CUDA call failed";
+    case MHA_ERR_TIMEOUT: return "a pipeline wait on the device timed out";
+    case MHA_ERR_ALIAS: return "out overlaps q, k or v";
+    case MHA_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+void mha_last_launch_info(int* kernels, int* grid, int* block, int* smem_bytes) {
+  if (kernels) *kernels = t_info.kernels;
+  if (grid) *grid = t_info.grid;
+  if (block) *block = t_info.block;
+  if (smem_bytes) *smem_bytes = t_info.smem;
+}
+
+}  // extern "C"
