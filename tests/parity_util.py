@@ -6,6 +6,14 @@ Tolerances (fixed by the target specification of this library):
     and ||O - O_ref||_F / ||O_ref||_F <= 5e-3,
 where O_ref is the float64 oracle evaluated on the exact float64 images of the
 values the GPU received.
+
+Outside the workloads' input distribution (nearly one-hot softmax rows with
+|O| of several units) the bf16 rounding floor alone exceeds 1e-2: the kernel
+rounds every probability p and every output to bf16 (unit roundoff 2^-8), so
+an output row close to one value row carries up to 2^-8|O| from P and 2^-8|O|
+from the final rounding.  Such cases use, element by element,
+    |O - O_ref| <= 1e-2 + 2^-7 |O_ref|
+together with the same relative Frobenius bound.
 """
 from __future__ import annotations
 
@@ -56,6 +64,16 @@ def assert_bf16_close(out, ref, what=""):
     assert max_abs <= BF16_MAX_ABS and rel <= BF16_REL_FRO, \
         f"{what}: max_abs {max_abs:.3e} (<= {BF16_MAX_ABS}), rel_fro {rel:.3e} (<= {BF16_REL_FRO})"
     return max_abs, rel
+
+
+def assert_bf16_close_rounding_aware(out, ref, what=""):
+    assert torch.isfinite(out.float()).all(), f"{what}: non-finite output"
+    o = out.detach().to("cpu", torch.float64).numpy()
+    excess = np.abs(o - ref) - (BF16_MAX_ABS + 2.0 ** -7 * np.abs(ref))
+    _, rel = errors(out, ref)
+    assert excess.max() <= 0 and rel <= BF16_REL_FRO, \
+        f"{what}: worst excess over 1e-2 + 2^-7|ref| is {excess.max():.3e}, rel_fro {rel:.3e}"
+    return float(excess.max()), rel
 
 
 def assert_f32_close(out, ref, what=""):

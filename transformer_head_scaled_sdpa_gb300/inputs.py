@@ -75,6 +75,10 @@ WORKLOADS = [
     Workload("big16_L2048_causal", 8, 16, 64, 2048, 2048, MASK_CAUSAL, torch.bfloat16),
     Workload("base8_L4096", 16, 8, 64, 4096, 4096, MASK_NONE, torch.bfloat16),
     Workload("base8_L4096_causal", 16, 8, 64, 4096, 4096, MASK_CAUSAL, torch.bfloat16),
+    # one sequence of the GPT-3-like shape (150 MB of inputs, still above L2):
+    # the small case for detailed profiler captures
+    Workload("gpt3_causal_b1", 1, 96, 128, 2048, 2048, MASK_CAUSAL, torch.bfloat16,
+             input_scale=0.5, note="GPT-3-like, one sequence"),
 ]
 WORKLOAD_INDEX = {w.name: i for i, w in enumerate(WORKLOADS)}
 BY_NAME = {w.name: w for w in WORKLOADS}
