@@ -192,7 +192,8 @@ def test_launch_shape(mha):
     case = pu.to_cuda(inputs.random_case(10, 3, 5, 300, 300, 64))
     mha.mha_fwd(case["q"], case["k"], case["v"])
     info = mha.last_launch_info()
-    assert info["kernels"] == 1 and info["grid"] == 3 * 3 * 5
+    # one CTA per (b, h, block of 256 query rows)
+    assert info["kernels"] == 1 and info["grid"] == 3 * 5 * 2
     assert mha.mha_sync_status() == 0
 
 

@@ -13,9 +13,11 @@ namespace mha {
 
 enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskKeyPadding = 2 };
 
-// Queries per CTA tile (M of the tcgen05 MMA) and keys per K/V tile.
+// Queries per tile (M of the tcgen05 MMA), keys per K/V tile, and query rows
+// per work unit of the bf16 kernel (two tiles share every K/V tile).
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
+constexpr int kUnitRows = 2 * kBlockM;
 
 struct Bf16Params {
   CUtensorMap tm_q;  // [B, Lq, H, d] bf16, box {64, 1, 128, 1}, 128-byte swizzle
@@ -26,7 +28,7 @@ struct Bf16Params {
   DeviceStatus* status;
   int B, H, Lq, Lk;
   int mask_kind;
-  int n_qtiles;      // ceil(Lq / 128)
+  int n_qtiles;      // query blocks per head: ceil(Lq / kUnitRows)
   float scale_log2;  // scale * log2(e)
 };
 

@@ -180,7 +180,7 @@ int mha_fwd(const void* q, const void* k, const void* v, void* out, int B, int H
     // no key anywhere: every row is 0 (bf16 zero is the all-zero pattern)
     return cudaMemsetAsync(out, 0, sz.q_elems * 2, s) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
   }
-  const long long n_qtiles = (Lq + mha::kBlockM - 1) / mha::kBlockM;
+  const long long n_qtiles = (Lq + mha::kUnitRows - 1) / mha::kUnitRows;
   if (n_qtiles * B * H > 0x7fffffffll) return MHA_ERR_SHAPE;
   mha::Bf16Params p;
   std::memset(&p, 0, sizeof(p));
