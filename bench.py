@@ -226,13 +226,18 @@ def run_ours(args):
     flops_nominal = w.flops()
     bytes_in = sum(t.numel() * t.element_size() for t in (q, k, v))
     bytes_alg = bytes_in + out.numel() * out.element_size()
-    inputs_exceed_l2 = bytes_in > L2_BYTES
-    flush = None
-    if not inputs_exceed_l2:
-        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    # Consecutive steps must not find their inputs in L2: when one set of
+    # inputs fits in L2, steps rotate over enough copies to exceed it twice.
+    n_sets = 1 if bytes_in > L2_BYTES else -(-2 * L2_BYTES // bytes_in)
+    sets = [(q, k, v, out)] + [tuple(t.clone() for t in (q, k, v, out))
+                              for _ in range(n_sets - 1)]
+    cur = [0]
 
     def step():
-        binding.mha_fwd(q, k, v, out=out, mask_kind=w.mask_kind, key_lens=lens, stream=stream)
+        qq, kk, vv, oo = sets[cur[0] % n_sets]
+        cur[0] += 1
+        binding.mha_fwd(qq, kk, vv, out=oo, mask_kind=w.mask_kind, key_lens=lens,
+                        stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -256,8 +261,6 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         all_start.record(stream)
         for i in range(args.steps):
-            if flush is not None:
-                flush.zero_()
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
@@ -323,7 +326,8 @@ def run_ours(args):
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, no dataset)",
         "config": workload_config(w, {
             "parallelism": f"replicas x{world} (no collective)",
-            "inputs_exceed_l2": inputs_exceed_l2, "l2_flush": flush is not None,
+            "inputs_exceed_l2": bytes_in * n_sets > L2_BYTES, "l2_flush": False,
+            "input_sets_rotated": n_sets,
             "flops_per_step_per_gpu": flops_alg, "flops_nominal_per_step_per_gpu": flops_nominal}),
         "pct_of_peak": 100.0 * value / world / peak,
         "pct_of_sustained_peak": 100.0 * value / world / float(

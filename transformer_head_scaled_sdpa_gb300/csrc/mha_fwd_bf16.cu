@@ -12,9 +12,10 @@
 // and l are rescaled by 2^(m_old - m_new) when m moves.  Any reference value
 // gives the same weights, because adding one constant to all scores of a row
 // leaves the weights unchanged (formula page transformer-attention, section
-// 証明, weight-ratio step); m only has to keep p within range.  So m is moved
-// only when a tile's maximum exceeds it by more than 2^8 (p <= 256, exact
-// in bf16's range, float32 sums), which makes rescaling rare.
+// 証明, weight-ratio step); m only has to keep p within range.  So a row's m
+// is moved only when a tile's maximum exceeds it by more than 8 (log2 units:
+// p <= 2^8, well inside bf16's range, float32 sums), which makes rescaling
+// rare.
 //
 // One CTA = one work unit: (b, h, two 128-row query tiles Q0, Q1) sharing
 // every K/V tile.  384 threads (three warpgroups) in four roles:
@@ -337,21 +338,28 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Unit& u,
     const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c2;  // c2 > 0
     if (j == 0) {
       m_ref = (mx == -INFINITY) ? 0.f : mx;
-    } else if (__any_sync(0xffffffffu, mx > m_ref + kRescaleThreshold)) {
-      // Move the reference up to this tile's maximum and rescale the
-      // partial output (PV_g(j-1) is complete: S_g(j) was issued after it).
-      const float m_new = fmaxf(m_ref, mx);
-      const float alpha = ex2_approx(m_ref - m_new);
-      l *= alpha;
-      m_ref = m_new;
+    } else {
+      // Each row moves its own reference up to this tile's maximum when that
+      // maximum exceeds it by more than the threshold; the partial output is
+      // rescaled in place (PV_g(j-1) is complete: S_g(j) was issued after
+      // it).  Rows that keep their reference multiply by exactly 1, so a
+      // row's arithmetic never depends on its neighbours.
+      const bool move = mx > m_ref + kRescaleThreshold;
+      const float alpha = move ? ex2_approx(m_ref - mx) : 1.f;
+      if (move) {
+        l *= alpha;
+        m_ref = mx;
+      }
+      if (__any_sync(0xffffffffu, move)) {
 #pragma unroll
-      for (int c32 = 0; c32 < D / 32; ++c32) {
-        uint32_t o[32];
-        tmem_ld32(tO + 32u * c32, o);
-        tmem_ld_wait();
+        for (int c32 = 0; c32 < D / 32; ++c32) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32u * c32, o);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st32(tO + 32u * c32, o);
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + 32u * c32, o);
+        }
       }
     }
     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
