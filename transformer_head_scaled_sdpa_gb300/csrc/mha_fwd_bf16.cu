@@ -139,149 +139,158 @@ struct Ctx {
   }
 };
 
+// TMA producer (warp 9): Q0, K_0, Q1, V_0, then K_j / V_j into the ring.
+// The whole warp runs the loop and waits; one elected lane issues.
 template <int D>
 __device__ __forceinline__ void producer_role(const Bf16Params& p, const Unit& u, const Ctx& cx) {
   using C = Cfg<D>;
   using BA = Bars<C::NS>;
   constexpr int NS = C::NS;
-  const int lane = cx.lane;
   const int n_max = max(u.n[0], u.n[1]);
-  const uint32_t sQ = cx.sQ, sK = cx.sK, sV = cx.sV;
-  volatile int* abort_flag = cx.abort_flag;
-  auto bar = [&](int id) { return cx.bar(id); };
-  if (lane == 0 && n_max > 0) {
-    int issued[NS];
-#pragma unroll
-    for (int s = 0; s < NS; ++s) issued[s] = 0;
-    auto load_q = [&](int g) {
-      mbar_arrive_expect_tx(bar(BA::Q_FULL + g), C::TILE);
+  if (n_max == 0) return;
+  auto load_q = [&](int g) {
+    if (elect_one()) {
+      mbar_arrive_expect_tx(cx.bar(BA::Q_FULL + g), C::TILE);
 #pragma unroll
       for (int c = 0; c < C::KCH; ++c)
-        tma_load_4d(sQ + g * C::TILE + c * C::CHUNK, &p.tm_q, bar(BA::Q_FULL + g), 64 * c, u.h,
-                    u.q0 + g * kBlockM, u.b);
-    };
-    auto load_kv = [&](int j, bool is_v) {
-      const int s = j % NS;
-      const uint32_t dst = (is_v ? sV : sK) + s * C::TILE;
-      const int b_id = (is_v ? BA::V_FULL : BA::K_FULL) + s;
-      mbar_arrive_expect_tx(bar(b_id), C::TILE);
-#pragma unroll
-      for (int c = 0; c < C::KCH; ++c)
-        tma_load_4d(dst + c * C::CHUNK, is_v ? &p.tm_v : &p.tm_k, bar(b_id), 64 * c, u.h,
-                    j * kBlockN, u.b);
-    };
-    if (u.n[0] > 0) load_q(0);
-    load_kv(0, false);
-    if (u.n[1] > 0) load_q(1);
-    load_kv(0, true);
-    issued[0] = 1;
-    for (int j = 1; j < n_max; ++j) {
-      const int s = j % NS;
-      if (j >= NS) {
-        if (!mbar_wait(bar(BA::KV_EMPTY + s), ((j / NS) - 1) & 1, abort_flag, p.status,
-                       kRoleProducer * 64 + BA::KV_EMPTY + s))
-          break;
-      }
-      load_kv(j, false);
-      load_kv(j, true);
-      ++issued[s];
+        tma_load_4d(cx.sQ + g * C::TILE + c * C::CHUNK, &p.tm_q, cx.bar(BA::Q_FULL + g), 64 * c,
+                    u.h, u.q0 + g * kBlockM, u.b);
     }
-    // Leave only when every copy this thread started has landed (the
-    // normal path finds them complete already).
-    for (int g = 0; g < 2; ++g)
-      if (u.n[g] > 0)
-        mbar_wait(bar(BA::Q_FULL + g), 0, abort_flag, p.status, kRoleProducer * 64 + BA::Q_FULL);
+    __syncwarp();
+  };
+  auto load_kv = [&](int j, bool is_v) {
+    const int s = j % NS;
+    const uint32_t dst = (is_v ? cx.sV : cx.sK) + s * C::TILE;
+    const uint32_t full = cx.bar((is_v ? BA::V_FULL : BA::K_FULL) + s);
+    if (elect_one()) {
+      mbar_arrive_expect_tx(full, C::TILE);
 #pragma unroll
-    for (int s = 0; s < NS; ++s)
-      if (issued[s] > 0) {
-        mbar_wait(bar(BA::K_FULL + s), (issued[s] - 1) & 1, abort_flag, p.status,
-                  kRoleProducer * 64 + BA::K_FULL + s);
-        mbar_wait(bar(BA::V_FULL + s), (issued[s] - 1) & 1, abort_flag, p.status,
-                  kRoleProducer * 64 + BA::V_FULL + s);
-      }
+      for (int c = 0; c < C::KCH; ++c)
+        tma_load_4d(dst + c * C::CHUNK, is_v ? &p.tm_v : &p.tm_k, full, 64 * c, u.h,
+                    j * kBlockN, u.b);
+    }
+    __syncwarp();
+  };
+  if (u.n[0] > 0) load_q(0);
+  load_kv(0, false);
+  if (u.n[1] > 0) load_q(1);
+  load_kv(0, true);
+  int last = 0;  // last tile issued
+  for (int j = 1; j < n_max; ++j) {
+    const int s = j % NS;
+    if (j >= NS) {
+      if (!mbar_wait(cx.bar(BA::KV_EMPTY + s), ((j / NS) - 1) & 1, cx.abort_flag, p.status,
+                     kRoleProducer * 64 + BA::KV_EMPTY + s))
+        break;
+    }
+    load_kv(j, false);
+    load_kv(j, true);
+    last = j;
+  }
+  // Leave only when every copy this warp started has landed (the normal
+  // path finds them complete already): the last load into each used stage.
+  for (int g = 0; g < 2; ++g)
+    if (u.n[g] > 0)
+      mbar_wait(cx.bar(BA::Q_FULL + g), 0, cx.abort_flag, p.status, kRoleProducer * 64 + BA::Q_FULL);
+  for (int j = (last + 1 > NS ? last + 1 - NS : 0); j <= last; ++j) {
+    const int s = j % NS;
+    mbar_wait(cx.bar(BA::K_FULL + s), (j / NS) & 1, cx.abort_flag, p.status,
+              kRoleProducer * 64 + BA::K_FULL + s);
+    mbar_wait(cx.bar(BA::V_FULL + s), (j / NS) & 1, cx.abort_flag, p.status,
+              kRoleProducer * 64 + BA::V_FULL + s);
   }
 }
 
+// MMA issuer (warp 8): the whole warp runs the loop and the waits; one
+// elected lane issues every tcgen05.mma and tcgen05.commit, with
+// descriptors built once and stepped by compile-time offsets.
 template <int D>
 __device__ __forceinline__ void mma_role(const Bf16Params& p, const Unit& u, const Ctx& cx) {
   using C = Cfg<D>;
   using BA = Bars<C::NS>;
   constexpr int NS = C::NS;
-  const int lane = cx.lane;
   const int n_max = max(u.n[0], u.n[1]);
-  const uint32_t sQ = cx.sQ, sK = cx.sK, sV = cx.sV, tmem = cx.tmem;
-  volatile int* abort_flag = cx.abort_flag;
-  auto bar = [&](int id) { return cx.bar(id); };
-  if (lane == 0 && n_max > 0) {
-    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
-    constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
-    const uint32_t tm_s[2] = {tmem + C::TM_S0, tmem + C::TM_S1};
-    const uint32_t tm_o[2] = {tmem + C::TM_O0, tmem + C::TM_O1};
-    // S_g = Q_g K_j^T: M 128 queries, N 128 keys, K = d in steps of 16
-    auto issue_s = [&](int g, int j) {
-      const int s = j % NS;
+  if (n_max == 0) return;
+  constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+  constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+  // K-major Q and K tiles: 8-row groups 1024 B apart; V MN-major with its
+  // second 64-wide d chunk one CHUNK further.
+  const uint64_t dq0 = smem_desc_sw128(cx.sQ, 16, 1024);
+  const uint64_t dk0 = smem_desc_sw128(cx.sK, 16, 1024);
+  const uint64_t dv0 = smem_desc_sw128(cx.sV, C::CHUNK, 1024);
+  // S_g = Q_g K_j^T: M 128 queries, N 128 keys, K = d in steps of 16
+  auto issue_s = [&](int g, int j) {
+    const uint64_t a = dq0 + static_cast<uint64_t>((g * C::TILE) >> 4);
+    const uint64_t b = dk0 + static_cast<uint64_t>(((j % NS) * C::TILE) >> 4);
+    const uint32_t d_tmem = cx.tmem + (g ? C::TM_S1 : C::TM_S0);
+    if (elect_one()) {
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
-        const uint64_t a = smem_desc_sw128(sQ + g * C::TILE + off, 16, 1024);
-        const uint64_t bd = smem_desc_sw128(sK + s * C::TILE + off, 16, 1024);
-        umma_ss(tm_s[g], a, bd, idesc_s, ks > 0 ? 1u : 0u);
+        const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
+        umma_ss(d_tmem, a + off, b + off, idesc_s, ks > 0 ? 1u : 0u);
       }
-    };
-    // O_g += P_g V_j: A = P_g from TMEM (16 keys = 8 columns per step),
-    // B = V_j MN-major (d contiguous; 16 keys = 16 rows of 128 B; the
-    // second 64-wide d chunk one CHUNK further).
-    auto issue_pv = [&](int g, int j) {
-      const int s = j % NS;
+      umma_commit(cx.bar(BA::S_FULL + g));
+    }
+    __syncwarp();
+  };
+  // O_g += P_g V_j: A = P_g from TMEM (16 keys = 8 columns per step),
+  // B = V_j MN-major (16 keys = 16 rows of 128 B = 2048 B per step).
+  auto issue_pv = [&](int g, int j) {
+    const uint64_t b = dv0 + static_cast<uint64_t>(((j % NS) * C::TILE) >> 4);
+    const uint32_t a_tmem = cx.tmem + (g ? C::TM_S1 : C::TM_S0);
+    const uint32_t d_tmem = cx.tmem + (g ? C::TM_O1 : C::TM_O0);
+    const uint32_t acc0 = j > 0 ? 1u : 0u;
+    if (elect_one()) {
 #pragma unroll
-      for (int ks = 0; ks < kBlockN / 16; ++ks) {
-        const uint64_t bd = smem_desc_sw128(sV + s * C::TILE + ks * 2048, C::CHUNK, 1024);
-        umma_ts(tm_o[g], tm_s[g] + 8u * ks, bd, idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
-      }
-    };
-    bool ok = true;
-    // prologue: S0(0), S1(0)
-    ok = mbar_wait(bar(BA::K_FULL), 0, abort_flag, p.status, kRoleMma * 64 + BA::K_FULL);
-    for (int g = 0; ok && g < 2; ++g) {
-      if (u.n[g] == 0) continue;
-      ok = mbar_wait(bar(BA::Q_FULL + g), 0, abort_flag, p.status, kRoleMma * 64 + BA::Q_FULL);
+      for (int ks = 0; ks < kBlockN / 16; ++ks)
+        umma_ts(d_tmem, a_tmem + 8u * ks, b + static_cast<uint64_t>((ks * 2048) >> 4), idesc_o,
+                ks > 0 ? 1u : acc0);
+    }
+    __syncwarp();
+  };
+  auto commit = [&](int id) {
+    if (elect_one()) umma_commit(cx.bar(id));
+    __syncwarp();
+  };
+  bool ok = mbar_wait(cx.bar(BA::K_FULL), 0, cx.abort_flag, p.status, kRoleMma * 64 + BA::K_FULL);
+  // prologue: S0(0), S1(0)
+  for (int g = 0; ok && g < 2; ++g) {
+    if (u.n[g] == 0) continue;
+    ok = mbar_wait(cx.bar(BA::Q_FULL + g), 0, cx.abort_flag, p.status, kRoleMma * 64 + BA::Q_FULL);
+    if (!ok) break;
+    tc_fence_after();
+    issue_s(g, 0);
+  }
+  for (int j = 0; ok && j < n_max; ++j) {
+    const int s = j % NS;
+    const uint32_t ph = (j / NS) & 1;
+    for (int g = 0; g < 2; ++g) {
+      if (j >= u.n[g]) continue;
+      ok = mbar_wait(cx.bar(BA::P_FULL + g), j & 1, cx.abort_flag, p.status,
+                     kRoleMma * 64 + BA::P_FULL + g) &&
+           mbar_wait(cx.bar(BA::V_FULL + s), ph, cx.abort_flag, p.status,
+                     kRoleMma * 64 + BA::V_FULL + s);
       if (!ok) break;
       tc_fence_after();
-      issue_s(g, 0);
-      umma_commit(bar(BA::S_FULL + g));
-    }
-    for (int j = 0; ok && j < n_max; ++j) {
-      const int s = j % NS;
-      const uint32_t ph = (j / NS) & 1;
-      for (int g = 0; g < 2; ++g) {
-        if (j >= u.n[g]) continue;
-        ok = mbar_wait(bar(BA::P_FULL + g), j & 1, abort_flag, p.status,
-                       kRoleMma * 64 + BA::P_FULL + g) &&
-             mbar_wait(bar(BA::V_FULL + s), ph, abort_flag, p.status,
-                       kRoleMma * 64 + BA::V_FULL + s);
+      issue_pv(g, j);
+      if (j + 1 < u.n[g]) {
+        const int s1 = (j + 1) % NS;
+        ok = mbar_wait(cx.bar(BA::K_FULL + s1), ((j + 1) / NS) & 1, cx.abort_flag, p.status,
+                       kRoleMma * 64 + BA::K_FULL + s1);
         if (!ok) break;
         tc_fence_after();
-        issue_pv(g, j);
-        if (j + 1 < u.n[g]) {
-          const int s1 = (j + 1) % NS;
-          ok = mbar_wait(bar(BA::K_FULL + s1), ((j + 1) / NS) & 1, abort_flag, p.status,
-                         kRoleMma * 64 + BA::K_FULL + s1);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(g, j + 1);
-          umma_commit(bar(BA::S_FULL + g));
-        } else {
-          umma_commit(bar(BA::O_DONE + g));
-        }
+        issue_s(g, j + 1);
+      } else {
+        commit(BA::O_DONE + g);
       }
-      if (!ok) break;
-      umma_commit(bar(BA::KV_EMPTY + s));
     }
-    // Every MMA this thread issued completes before TMEM is released.
-    umma_commit(bar(BA::DRAIN));
-    volatile int never = 0;
-    mbar_wait(bar(BA::DRAIN), 0, &never, p.status, kRoleMma * 64 + BA::DRAIN);
+    if (!ok) break;
+    commit(BA::KV_EMPTY + s);
   }
+  // Every MMA this warp issued completes before TMEM is released.
+  commit(BA::DRAIN);
+  volatile int never = 0;
+  mbar_wait(cx.bar(BA::DRAIN), 0, &never, p.status, kRoleMma * 64 + BA::DRAIN);
 }
 
 template <int D>
@@ -478,7 +487,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     regs_decrease<kRegsOther>();
     if (cx.warp == 8) {
       mma_role<D>(p, u, cx);
-      __syncwarp();
     } else if (cx.warp == 9) {
       producer_role<D>(p, u, cx);
     }

@@ -32,8 +32,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-__device__ __forceinline__ uint32_t elect_lane0() {
-  return (threadIdx.x & 31) == 0;
+// One lane of a converged warp (the same lane each time for the same full
+// mask): tcgen05.mma and tcgen05.commit are issued by that lane while the
+// whole warp runs the issuing loop, so descriptors stay warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 // ---------------------------------------------------------------------------
