@@ -26,7 +26,8 @@
 //   warps 10-11 idle
 // The third warpgroup gives registers to the softmax warpgroups, which hold
 // a whole 128-score row per thread: launched at 168 per thread, it drops to
-// 64 and they rise to 216 (256*216 + 128*64 <= 384*168).
+// 64 (d_k 64) or 80 (d_k 128) and they rise to 216 or 208 (both splits total
+// 63488 <= 384*168 registers).
 // TMEM (512 columns): S0 | S1 | O0 | O1.  Softmax g reads S_g (float32),
 // writes P_g as bf16 pairs into the first 64 columns of S_g, and the P.V
 // MMA reads P_g from TMEM.  Per key tile j the MMA warp issues
@@ -46,9 +47,6 @@ namespace mha {
 namespace {
 
 constexpr int kThreads = 384;
-constexpr uint32_t kRegsSoftmax = 216;
-constexpr uint32_t kRegsOther = 64;
-static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= kThreads * 168, "register split");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p stays <= 2^8
 constexpr int kHeadGroup = 32;              // heads dispatched together (L2 reuse of K/V)
 
@@ -69,7 +67,11 @@ struct Cfg {
   static constexpr uint32_t TM_S0 = 0, TM_S1 = 128;
   static constexpr uint32_t TM_O0 = 256, TM_O1 = 256 + D;
   static constexpr uint32_t TMEM_COLS = 512;
+  // registers per thread after rebalancing (softmax warpgroups, the rest)
+  static constexpr uint32_t REGS_SOFTMAX = (D == 64) ? 216 : 208;
+  static constexpr uint32_t REGS_OTHER = (D == 64) ? 64 : 80;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(256 * REGS_SOFTMAX + 128 * REGS_OTHER <= kThreads * 168, "register split");
 };
 
 // barrier ids inside the barrier block
@@ -336,15 +338,17 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Unit& u,
       for (int c = 0; c < 128; ++c)
         if (c >= lim) x[c] = -INFINITY;
     }
-    float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+    // row maximum: eight independent chains of three-input max
+    float mk[8];
 #pragma unroll
-    for (int c = 4; c < 128; c += 4) {
-      mx0 = fmaxf(mx0, x[c]);
-      mx1 = fmaxf(mx1, x[c + 1]);
-      mx2 = fmaxf(mx2, x[c + 2]);
-      mx3 = fmaxf(mx3, x[c + 3]);
+    for (int k = 0; k < 8; ++k) mk[k] = fmaxf(x[2 * k], x[2 * k + 1]);
+#pragma unroll
+    for (int c = 16; c < 128; c += 16) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mk[k] = fmax3(mk[k], x[c + 2 * k], x[c + 2 * k + 1]);
     }
-    const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c2;  // c2 > 0
+    const float mx =
+        fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7])) * c2;
     if (j == 0) {
       m_ref = (mx == -INFINITY) ? 0.f : mx;
     } else {
@@ -366,24 +370,30 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Unit& u,
           tmem_ld32(tO + 32u * c32, o);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          for (int i = 0; i < 32; i += 2) {
+            float a0, a1;
+            mul2(a0, a1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
+            o[i] = __float_as_uint(a0);
+            o[i + 1] = __float_as_uint(a1);
+          }
           tmem_st32(tO + 32u * c32, o);
         }
       }
     }
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    // p = 2^(s*c2 - m_ref): packed scale-subtract, ex2 on the SFU, packed sums
+    const float nm = -m_ref;
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int c = 0; c < 128; c += 4) {
-      x[c] = ex2_approx(fmaf(x[c], c2, -m_ref));
-      x[c + 1] = ex2_approx(fmaf(x[c + 1], c2, -m_ref));
-      x[c + 2] = ex2_approx(fmaf(x[c + 2], c2, -m_ref));
-      x[c + 3] = ex2_approx(fmaf(x[c + 3], c2, -m_ref));
-      s0 += x[c];
-      s1 += x[c + 1];
-      s2 += x[c + 2];
-      s3 += x[c + 3];
+    for (int c = 0; c < 128; c += 2) {
+      fma2(x[c], x[c + 1], x[c], x[c + 1], c2, c2, nm, nm);
+      x[c] = ex2_approx(x[c]);
+      x[c + 1] = ex2_approx(x[c + 1]);
+      const int k = (c >> 1) & 3;
+      add2(sa[k], sb[k], sa[k], sb[k], x[c], x[c + 1]);
     }
-    l += (s0 + s1) + (s2 + s3);
+    add2(sa[0], sb[0], sa[0], sb[0], sa[1], sb[1]);
+    add2(sa[2], sb[2], sa[2], sb[2], sa[3], sb[3]);
+    l += (sa[0] + sb[0]) + (sa[2] + sb[2]);
     // P_g as bf16 pairs into the first 64 columns of S_g (A operand of P.V)
     uint32_t pk[64];
 #pragma unroll
@@ -481,10 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   cx.tmem = *tmem_slot;
 
   if (cx.warp < 8) {
-    regs_increase<kRegsSoftmax>();
+    regs_increase<C::REGS_SOFTMAX>();
     softmax_role<D>(p, u, cx);
   } else {
-    regs_decrease<kRegsOther>();
+    regs_decrease<C::REGS_OTHER>();
     if (cx.warp == 8) {
       mma_role<D>(p, u, cx);
     } else if (cx.warp == 9) {
