@@ -23,6 +23,7 @@ struct Bf16Params {
   CUtensorMap tm_q;  // [B, Lq, H, d] bf16, box {64, 1, 128, 1}, 128-byte swizzle
   CUtensorMap tm_k;  // [B, Lk, H, d]
   CUtensorMap tm_v;  // [B, Lk, H, d]
+  CUtensorMap tm_o;  // [B, Lq, H, d] bf16 output, same box and swizzle as tm_q
   void* out;         // [B, Lq, H, d] bf16
   const int32_t* key_lens;
   DeviceStatus* status;

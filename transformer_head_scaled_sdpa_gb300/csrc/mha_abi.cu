@@ -185,7 +185,7 @@ int mha_fwd(const void* q, const void* k, const void* v, void* out, int B, int H
   mha::Bf16Params p;
   std::memset(&p, 0, sizeof(p));
   if (!encode_map(&p.tm_q, q, B, Lq, H, d_k) || !encode_map(&p.tm_k, k, B, Lk, H, d_k) ||
-      !encode_map(&p.tm_v, v, B, Lk, H, d_k))
+      !encode_map(&p.tm_v, v, B, Lk, H, d_k) || !encode_map(&p.tm_o, out, B, Lq, H, d_k))
     return MHA_ERR_UNSUPPORTED;
   p.out = out;
   p.key_lens = key_lens;

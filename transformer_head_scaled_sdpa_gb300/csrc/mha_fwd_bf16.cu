@@ -410,11 +410,11 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Unit& u,
     tc_fence_after();
   }
   if (ok && q_start < p.Lq) {
-    // epilogue: O / l rounded to bf16; rows past Lq are not stored
+    // epilogue: O / l rounded to bf16, staged in shared memory (the Q_g tile
+    // buffer: every S_g MMA is complete) in the 128-byte-swizzled layout and
+    // written by TMA stores, which skip rows past Lq.
     const float inv = (l > 0.f) ? 1.f / l : 0.f;
-    uint4* dst = reinterpret_cast<uint4*>(
-        static_cast<__nv_bfloat16*>(p.out) +
-        ((static_cast<size_t>(u.b) * p.Lq + qi) * p.H + u.h) * D);
+    const uint32_t stage = cx.sQ + g * C::TILE;
 #pragma unroll
     for (int c32 = 0; c32 < D / 32; ++c32) {
       uint32_t o[32];
@@ -429,12 +429,23 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Unit& u,
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-      if (qi < p.Lq) {
+      // 32 columns = 64 bytes = four 16-byte units of the 128-byte row
 #pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4)
-          dst[c32 * 4 + v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+      for (int v4 = 0; v4 < 4; ++v4) {
+        const uint32_t unit = static_cast<uint32_t>((c32 & 1) * 4 + v4);
+        const uint32_t addr = stage + (c32 >> 1) * C::CHUNK + row * 128 + ((unit ^ (row & 7)) << 4);
+        st_shared_v4(addr, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
       }
     }
+    fence_proxy_async_smem();
+    named_barrier(1 + g, 128);
+    if (warp == 4 * g && elect_one()) {
+#pragma unroll
+      for (int c = 0; c < C::KCH; ++c) tma_store_4d(&p.tm_o, stage + c * C::CHUNK, 64 * c, u.h, q_start, u.b);
+      tma_store_commit();
+      tma_store_wait_read();  // the staging buffer must outlive the reads
+    }
+    __syncwarp();
   }
 }
 
