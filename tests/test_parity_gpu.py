@@ -237,6 +237,23 @@ def test_host_entry_matches_device_entry(mha):
     assert torch.equal(out, dev)
 
 
+def test_attention_kernel_timeout_path(mha):
+    """With one pipeline signal withheld, every CTA's bounded wait runs out
+    (about a second), the kernel aborts, drains and frees its tensor memory,
+    reports MHA_ERR_TIMEOUT, and the next launch computes correctly."""
+    case = inputs.random_case(12, 1, 2, 256, 256, 64)
+    g = pu.to_cuda(case)
+    mha.mha_debug_withhold_p(True)
+    try:
+        mha.mha_fwd(g["q"], g["k"], g["v"], mask_kind=CAUSAL)
+        assert mha.mha_sync_status() == 7
+    finally:
+        mha.mha_debug_withhold_p(False)
+    assert mha.mha_sync_status() == 0
+    out = pu.gpu_run(mha, case, CAUSAL)
+    pu.assert_bf16_close(out, pu.oracle_run(case, CAUSAL), "after kernel timeout")
+
+
 def test_bounded_wait_reports_timeout(mha):
     """A wait nothing completes gives up (~1 s), reports MHA_ERR_TIMEOUT, and
     the context stays usable."""

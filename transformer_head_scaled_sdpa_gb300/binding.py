@@ -65,6 +65,8 @@ def lib():
             h.mha_fwd_host.argtypes = _FWD_ARGS[:-1] + [_c_i, _c_p, ctypes.c_size_t, _c_p]
             h.mha_selftest_timeout.restype = _c_i
             h.mha_selftest_timeout.argtypes = [_c_p]
+            h.mha_debug_withhold_p.restype = None
+            h.mha_debug_withhold_p.argtypes = [_c_i]
             h.mha_sync_status.restype = _c_i
             h.mha_sync_status.argtypes = [_c_p]
             h.mha_status_string.restype = ctypes.c_char_p
@@ -183,6 +185,11 @@ def mha_selftest_timeout(stream=None) -> int:
     if rc != MHA_OK:
         raise MhaError(rc, "mha_selftest_timeout")
     return rc
+
+
+def mha_debug_withhold_p(on: bool) -> None:
+    """Test hook: make later mha_fwd launches run out a pipeline wait."""
+    lib().mha_debug_withhold_p(1 if on else 0)
 
 
 def last_launch_info() -> dict:

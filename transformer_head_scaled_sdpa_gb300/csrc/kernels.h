@@ -31,6 +31,7 @@ struct Bf16Params {
   int mask_kind;
   int n_qtiles;      // query blocks per head: ceil(Lq / kUnitRows)
   float scale_log2;  // scale * log2(e)
+  int withhold_p;    // test hook: softmax 0 withholds its first P arrival (0 = off)
 };
 
 struct F32Params {

@@ -28,6 +28,7 @@ struct DeviceState {
 };
 
 std::mutex g_mutex;
+int g_withhold_p = 0;  // test hook of mha_debug_withhold_p
 DeviceState g_dev[kMaxDevices];
 thread_local mha::LaunchInfo t_info;
 
@@ -197,6 +198,7 @@ int mha_fwd(const void* q, const void* k, const void* v, void* out, int B, int H
   p.mask_kind = mask_kind;
   p.n_qtiles = static_cast<int>(n_qtiles);
   p.scale_log2 = effective_scale(scale, d_k) * kLog2e;
+  p.withhold_p = g_withhold_p;
   return mha::launch_fwd_bf16(p, d_k, s, &t_info) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
 }
 
@@ -301,6 +303,8 @@ int mha_selftest_timeout(void* stream) {
   t_info.block = 32;
   return cudaGetLastError() == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
 }
+
+void mha_debug_withhold_p(int on) { g_withhold_p = on ? 1 : 0; }
 
 int mha_sync_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)

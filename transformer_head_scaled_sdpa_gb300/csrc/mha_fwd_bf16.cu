@@ -402,7 +402,9 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Unit& u,
     tmem_st32(tS + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
     tmem_st_wait();
     tc_fence_before();
-    mbar_arrive(bar(BA::P_FULL + g));
+    // (test hook) withholding the first P of tile 0 leaves the MMA warp's
+    // bounded wait to run out, which exercises the abort and drain path
+    if (!(p.withhold_p && g == 0 && j == 0)) mbar_arrive(bar(BA::P_FULL + g));
   }
   if (ok && n_tiles > 0) {
     ok = mbar_wait(bar(BA::O_DONE + g), 0, abort_flag, p.status,
