@@ -17,16 +17,24 @@
 // p <= 2^8, well inside bf16's range, float32 sums), which makes rescaling
 // rare.
 //
-// One CTA = one work unit: (b, h, two 128-row query tiles Q0, Q1) sharing
-// every K/V tile.  384 threads (three warpgroups) in four roles:
-//   warps 0-3   softmax for Q0 (thread r owns row r = TMEM lane r)
-//   warps 4-7   softmax for Q1
-//   warp 8      TMEM allocator and MMA issuer (one thread)
+// Work unit: (b, h, two 128-row query tiles Q0, Q1) sharing every K/V tile.
+// The grid has one CTA per unit, but CTAs are persistent: once a running CTA
+// has its own unit it cancels a CTA that has not started yet (cluster launch
+// control) and processes that CTA's unit too, so each SM keeps one CTA whose
+// set-up, tensor memory and pipelines carry over from unit to unit, the next
+// unit's Q is loaded while the current one finishes, and the hardware's
+// launch order (heavy causal blocks first) still balances the load.
+//
+// 384 threads (three warpgroups) in five roles:
+//   warps 0-3   softmax + epilogue for Q0 (thread r owns row r = TMEM lane r)
+//   warps 4-7   softmax + epilogue for Q1
+//   warp 8      TMEM allocator and MMA issuer
 //   warp 9      TMA producer: Q0, Q1, then K_j / V_j into an NS-stage ring
-//   warps 10-11 idle
+//   warp 10     scheduler: feeds a two-slot queue of units to the others
+//   warp 11     idle
 // The third warpgroup gives registers to the softmax warpgroups, which hold
 // a whole 128-score row per thread: launched at 168 per thread, it drops to
-// 64 (d_k 64) or 80 (d_k 128) and they rise to 216 or 208 (both splits total
+// 80 (d_k 64) or 96 (d_k 128) and they rise to 208 or 200 (both splits total
 // 63488 <= 384*168 registers).
 // TMEM (512 columns): S0 | S1 | O0 | O1.  Softmax g reads S_g (float32),
 // writes P_g as bf16 pairs into the first 64 columns of S_g, and the P.V
@@ -49,6 +57,7 @@ namespace {
 constexpr int kThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p stays <= 2^8
 constexpr int kHeadGroup = 32;              // heads dispatched together (L2 reuse of K/V)
+constexpr int kUnitConsumers = 10;          // unit-queue readers: 8 softmax warps, MMA, producer
 
 template <int D>
 struct Cfg {
@@ -59,17 +68,18 @@ struct Cfg {
   static constexpr int OFF_Q = 0;                // Q0, Q1
   static constexpr int OFF_K = OFF_Q + 2 * TILE;
   static constexpr int OFF_V = OFF_K + NS * TILE;
-  static constexpr int OFF_BAR = OFF_V + NS * TILE;
-  static constexpr int NBAR = 9 + 3 * NS;
-  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;
-  static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
+  static constexpr int OFF_STAGE = OFF_V + NS * TILE;  // epilogue staging, one CHUNK per softmax warpgroup
+  static constexpr int OFF_BAR = OFF_STAGE + 2 * CHUNK;
+  static constexpr int NBAR = 20 + 3 * NS;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;  // tmem slot, abort flag, unit queue, CLC response
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;    // + slack to align the base to 1024
   // TMEM columns
   static constexpr uint32_t TM_S0 = 0, TM_S1 = 128;
   static constexpr uint32_t TM_O0 = 256, TM_O1 = 256 + D;
   static constexpr uint32_t TMEM_COLS = 512;
   // registers per thread after rebalancing (softmax warpgroups, the rest)
-  static constexpr uint32_t REGS_SOFTMAX = (D == 64) ? 216 : 208;
-  static constexpr uint32_t REGS_OTHER = (D == 64) ? 64 : 80;
+  static constexpr uint32_t REGS_SOFTMAX = (D == 64) ? 208 : 200;
+  static constexpr uint32_t REGS_OTHER = (D == 64) ? 80 : 96;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(256 * REGS_SOFTMAX + 128 * REGS_OTHER <= kThreads * 168, "register split");
 };
@@ -77,18 +87,23 @@ struct Cfg {
 // barrier ids inside the barrier block
 template <int NS>
 struct Bars {
-  static constexpr int Q_FULL = 0;                // + g
-  static constexpr int S_FULL = 2;                // + g
-  static constexpr int P_FULL = 4;                // + g
-  static constexpr int O_DONE = 6;                // + g
-  static constexpr int DRAIN = 8;
-  static constexpr int K_FULL = 9;                // + stage
-  static constexpr int V_FULL = 9 + NS;           // + stage
-  static constexpr int KV_EMPTY = 9 + 2 * NS;     // + stage
+  static constexpr int Q_FULL = 0;                // + g: Q_g landed
+  static constexpr int Q_FREE = 2;                // + g: last S_g of the unit done (Q_g reusable)
+  static constexpr int S_FULL = 4;                // + g: S_g in TMEM
+  static constexpr int P_FULL = 6;                // + g: P_g in TMEM (128 arrivals)
+  static constexpr int O_DONE = 8;                // + g: last PV_g of the unit done
+  static constexpr int O_FREE = 10;               // + g: epilogue read O_g (128 arrivals)
+  static constexpr int UNIT_FULL = 12;            // + slot: unit published
+  static constexpr int UNIT_EMPTY = 14;           // + slot: all consumers read it
+  static constexpr int CLC = 16;                  // cancellation response landed
+  static constexpr int DRAIN = 17;
+  static constexpr int K_FULL = 20;               // + stage
+  static constexpr int V_FULL = 20 + NS;          // + stage
+  static constexpr int KV_EMPTY = 20 + 2 * NS;    // + stage
 };
 
 // role ids for the status "site" field
-constexpr int kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3;
+constexpr int kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleScheduler = 4;
 
 struct Unit {
   int b, h;
@@ -98,9 +113,9 @@ struct Unit {
 };
 
 __device__ __forceinline__ Unit decode_unit(const Bf16Params& p, int unit) {
-  // Units are dispatched in groups of kHeadGroup heads, so a group's K/V stay
-  // in L2 while all of its query blocks run; inside a group the causal blocks
-  // go heaviest first.
+  // Units are ordered in groups of kHeadGroup heads, so a group's K/V stay in
+  // L2 while all of its query blocks run; inside a group the causal blocks go
+  // heaviest first.
   const int bh_count = p.B * p.H;
   const int n_pairs = p.n_qtiles;  // query blocks of 256 rows
   const int group = unit / (kHeadGroup * n_pairs);
@@ -132,87 +147,144 @@ __device__ __forceinline__ Unit decode_unit(const Bf16Params& p, int unit) {
 
 // Per-CTA context shared by the roles.
 struct Ctx {
-  uint32_t sQ, sK, sV, s_bar;
+  uint32_t sQ, sK, sV, sStage, s_bar;
   uint32_t tmem;
+  uint32_t clc_resp;           // 16-byte cancellation response
   volatile int* abort_flag;
+  volatile int* unit_slot;     // [2]
   int warp, lane;
   __device__ __forceinline__ uint32_t bar(int id) const {
     return s_bar + 8u * static_cast<uint32_t>(id);
   }
 };
 
-// TMA producer (warp 9): Q0, K_0, Q1, V_0, then K_j / V_j into the ring.
-// The whole warp runs the loop and waits; one elected lane issues.
+// Waits for the k-th unit of this CTA from the queue; returns its index, or
+// -1 at the end of the work (or when the CTA gave up).  Every consumer calls
+// it once per unit, in the same order.
+template <int NS>
+__device__ __forceinline__ int next_unit(const Bf16Params& p, const Ctx& cx, int k, int role,
+                                         bool arrive) {
+  using BA = Bars<NS>;
+  const int slot = k & 1;
+  if (!mbar_wait(cx.bar(BA::UNIT_FULL + slot), (k >> 1) & 1, cx.abort_flag, p.status,
+                 role * 64 + BA::UNIT_FULL + slot))
+    return -1;
+  const int unit = cx.unit_slot[slot];
+  __syncwarp();
+  if (arrive) mbar_arrive(cx.bar(BA::UNIT_EMPTY + slot));
+  return unit;
+}
+
+// Scheduler (warp 10, one lane): publishes the CTA's own unit, then keeps one
+// unit of look-ahead by cancelling not-yet-launched CTAs and taking their
+// units, until no CTA is left to cancel.
 template <int D>
-__device__ __forceinline__ void producer_role(const Bf16Params& p, const Unit& u, const Ctx& cx) {
+__device__ __forceinline__ void scheduler_role(const Bf16Params& p, const Ctx& cx) {
+  using BA = Bars<Cfg<D>::NS>;
+  if (cx.lane != 0) return;
+  int unit = static_cast<int>(blockIdx.x);
+  for (int k = 0;; ++k) {
+    const int slot = k & 1;
+    if (k >= 2 && !mbar_wait(cx.bar(BA::UNIT_EMPTY + slot), ((k >> 1) - 1) & 1, cx.abort_flag,
+                             p.status, kRoleScheduler * 64 + BA::UNIT_EMPTY + slot))
+      unit = -1;
+    cx.unit_slot[slot] = unit;
+    mbar_arrive(cx.bar(BA::UNIT_FULL + slot));
+    if (unit < 0) break;
+    // ask for the next unit while this one runs
+    mbar_arrive_expect_tx(cx.bar(BA::CLC), 16);
+    clc_try_cancel(cx.clc_resp, cx.bar(BA::CLC));
+    // the response is written asynchronously: wait for it even when the CTA
+    // is giving up, so nothing lands in shared memory after exit
+    volatile int never = 0;
+    if (!mbar_wait(cx.bar(BA::CLC), k & 1, &never, p.status, kRoleScheduler * 64 + BA::CLC) ||
+        *cx.abort_flag) {
+      unit = -1;
+    } else {
+      unit = clc_query_first_ctaid_x(cx.clc_resp);  // -1 when nothing was cancelled
+    }
+  }
+}
+
+// TMA producer (warp 9): per unit Q0, K_0, Q1, V_0, then K_j / V_j into the
+// ring.  The whole warp runs the loop and waits; one elected lane issues.
+template <int D>
+__device__ __forceinline__ void producer_role(const Bf16Params& p, const Ctx& cx) {
   using C = Cfg<D>;
   using BA = Bars<C::NS>;
   constexpr int NS = C::NS;
-  const int n_max = max(u.n[0], u.n[1]);
-  if (n_max == 0) return;
-  auto load_q = [&](int g) {
-    if (elect_one()) {
-      mbar_arrive_expect_tx(cx.bar(BA::Q_FULL + g), C::TILE);
+  int q_cnt[2] = {0, 0};  // Q_g loads so far
+  int kv_cnt = 0;         // K/V tiles loaded so far
+  bool ok = true;
+  for (int k = 0; ok; ++k) {
+    const int unit = next_unit<NS>(p, cx, k, kRoleProducer, cx.lane == 0);
+    if (unit < 0) break;
+    const Unit u = decode_unit(p, unit);
+    const int n_max = max(u.n[0], u.n[1]);
+    auto load_q = [&](int g) {
+      // the previous unit's last S_g must be done with the Q_g buffer
+      if (q_cnt[g] > 0 && !mbar_wait(cx.bar(BA::Q_FREE + g), (q_cnt[g] - 1) & 1, cx.abort_flag,
+                                     p.status, kRoleProducer * 64 + BA::Q_FREE + g))
+        return false;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(cx.bar(BA::Q_FULL + g), C::TILE);
 #pragma unroll
-      for (int c = 0; c < C::KCH; ++c)
-        tma_load_4d(cx.sQ + g * C::TILE + c * C::CHUNK, &p.tm_q, cx.bar(BA::Q_FULL + g), 64 * c,
-                    u.h, u.q0 + g * kBlockM, u.b);
-    }
-    __syncwarp();
-  };
-  auto load_kv = [&](int j, bool is_v) {
-    const int s = j % NS;
-    const uint32_t dst = (is_v ? cx.sV : cx.sK) + s * C::TILE;
-    const uint32_t full = cx.bar((is_v ? BA::V_FULL : BA::K_FULL) + s);
-    if (elect_one()) {
-      mbar_arrive_expect_tx(full, C::TILE);
-#pragma unroll
-      for (int c = 0; c < C::KCH; ++c)
-        tma_load_4d(dst + c * C::CHUNK, is_v ? &p.tm_v : &p.tm_k, full, 64 * c, u.h,
-                    j * kBlockN, u.b);
-    }
-    __syncwarp();
-  };
-  if (u.n[0] > 0) load_q(0);
-  load_kv(0, false);
-  if (u.n[1] > 0) load_q(1);
-  load_kv(0, true);
-  int last = 0;  // last tile issued
-  for (int j = 1; j < n_max; ++j) {
-    const int s = j % NS;
-    if (j >= NS) {
-      if (!mbar_wait(cx.bar(BA::KV_EMPTY + s), ((j / NS) - 1) & 1, cx.abort_flag, p.status,
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d(cx.sQ + g * C::TILE + c * C::CHUNK, &p.tm_q, cx.bar(BA::Q_FULL + g), 64 * c,
+                      u.h, u.q0 + g * kBlockM, u.b);
+      }
+      __syncwarp();
+      ++q_cnt[g];
+      return true;
+    };
+    auto load_kv = [&](int j, bool is_v) {
+      const int t = kv_cnt + j;
+      const int s = t % NS;
+      const uint32_t dst = (is_v ? cx.sV : cx.sK) + s * C::TILE;
+      const uint32_t full = cx.bar((is_v ? BA::V_FULL : BA::K_FULL) + s);
+      if (!is_v && t >= NS &&
+          !mbar_wait(cx.bar(BA::KV_EMPTY + s), ((t / NS) - 1) & 1, cx.abort_flag, p.status,
                      kRoleProducer * 64 + BA::KV_EMPTY + s))
-        break;
-    }
-    load_kv(j, false);
-    load_kv(j, true);
-    last = j;
+        return false;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(full, C::TILE);
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d(dst + c * C::CHUNK, is_v ? &p.tm_v : &p.tm_k, full, 64 * c, u.h,
+                      j * kBlockN, u.b);
+      }
+      __syncwarp();
+      return true;
+    };
+    if (n_max == 0) continue;
+    ok = (u.n[0] == 0 || load_q(0)) && load_kv(0, false) && (u.n[1] == 0 || load_q(1)) &&
+         load_kv(0, true);
+    for (int j = 1; ok && j < n_max; ++j) ok = load_kv(j, false) && load_kv(j, true);
+    kv_cnt += n_max;
   }
-  // Leave only when every copy this warp started has landed (the normal
-  // path finds them complete already): the last load into each used stage.
+  // Leave only when every copy this warp started has landed (the normal path
+  // finds them complete already): the last Q_g and the last load of each stage.
   for (int g = 0; g < 2; ++g)
-    if (u.n[g] > 0)
-      mbar_wait(cx.bar(BA::Q_FULL + g), 0, cx.abort_flag, p.status, kRoleProducer * 64 + BA::Q_FULL);
-  for (int j = (last + 1 > NS ? last + 1 - NS : 0); j <= last; ++j) {
-    const int s = j % NS;
-    mbar_wait(cx.bar(BA::K_FULL + s), (j / NS) & 1, cx.abort_flag, p.status,
+    if (q_cnt[g] > 0)
+      mbar_wait(cx.bar(BA::Q_FULL + g), (q_cnt[g] - 1) & 1, cx.abort_flag, p.status,
+                kRoleProducer * 64 + BA::Q_FULL + g);
+  for (int t = (kv_cnt > NS ? kv_cnt - NS : 0); t < kv_cnt; ++t) {
+    const int s = t % NS;
+    mbar_wait(cx.bar(BA::K_FULL + s), (t / NS) & 1, cx.abort_flag, p.status,
               kRoleProducer * 64 + BA::K_FULL + s);
-    mbar_wait(cx.bar(BA::V_FULL + s), (j / NS) & 1, cx.abort_flag, p.status,
+    mbar_wait(cx.bar(BA::V_FULL + s), (t / NS) & 1, cx.abort_flag, p.status,
               kRoleProducer * 64 + BA::V_FULL + s);
   }
 }
 
 // MMA issuer (warp 8): the whole warp runs the loop and the waits; one
-// elected lane issues every tcgen05.mma and tcgen05.commit, with
-// descriptors built once and stepped by compile-time offsets.
+// elected lane issues every tcgen05.mma and tcgen05.commit, with descriptors
+// built once and stepped by compile-time offsets.
 template <int D>
-__device__ __forceinline__ void mma_role(const Bf16Params& p, const Unit& u, const Ctx& cx) {
+__device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx) {
   using C = Cfg<D>;
   using BA = Bars<C::NS>;
   constexpr int NS = C::NS;
-  const int n_max = max(u.n[0], u.n[1]);
-  if (n_max == 0) return;
   constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
   // K-major Q and K tiles: 8-row groups 1024 B apart; V MN-major with its
@@ -220,10 +292,14 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Unit& u, con
   const uint64_t dq0 = smem_desc_sw128(cx.sQ, 16, 1024);
   const uint64_t dk0 = smem_desc_sw128(cx.sK, 16, 1024);
   const uint64_t dv0 = smem_desc_sw128(cx.sV, C::CHUNK, 1024);
-  // S_g = Q_g K_j^T: M 128 queries, N 128 keys, K = d in steps of 16
-  auto issue_s = [&](int g, int j) {
+  auto commit = [&](int id) {
+    if (elect_one()) umma_commit(cx.bar(id));
+    __syncwarp();
+  };
+  // S_g = Q_g K_t^T: M 128 queries, N 128 keys, K = d in steps of 16
+  auto issue_s = [&](int g, int t) {
     const uint64_t a = dq0 + static_cast<uint64_t>((g * C::TILE) >> 4);
-    const uint64_t b = dk0 + static_cast<uint64_t>(((j % NS) * C::TILE) >> 4);
+    const uint64_t b = dk0 + static_cast<uint64_t>(((t % NS) * C::TILE) >> 4);
     const uint32_t d_tmem = cx.tmem + (g ? C::TM_S1 : C::TM_S0);
     if (elect_one()) {
 #pragma unroll
@@ -235,13 +311,13 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Unit& u, con
     }
     __syncwarp();
   };
-  // O_g += P_g V_j: A = P_g from TMEM (16 keys = 8 columns per step),
-  // B = V_j MN-major (16 keys = 16 rows of 128 B = 2048 B per step).
-  auto issue_pv = [&](int g, int j) {
-    const uint64_t b = dv0 + static_cast<uint64_t>(((j % NS) * C::TILE) >> 4);
+  // O_g += P_g V_t: A = P_g from TMEM (16 keys = 8 columns per step),
+  // B = V_t MN-major (16 keys = 16 rows of 128 B = 2048 B per step).
+  auto issue_pv = [&](int g, int t, bool first) {
+    const uint64_t b = dv0 + static_cast<uint64_t>(((t % NS) * C::TILE) >> 4);
     const uint32_t a_tmem = cx.tmem + (g ? C::TM_S1 : C::TM_S0);
     const uint32_t d_tmem = cx.tmem + (g ? C::TM_O1 : C::TM_O0);
-    const uint32_t acc0 = j > 0 ? 1u : 0u;
+    const uint32_t acc0 = first ? 0u : 1u;
     if (elect_one()) {
 #pragma unroll
       for (int ks = 0; ks < kBlockN / 16; ++ks)
@@ -250,44 +326,64 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Unit& u, con
     }
     __syncwarp();
   };
-  auto commit = [&](int id) {
-    if (elect_one()) umma_commit(cx.bar(id));
-    __syncwarp();
-  };
-  bool ok = mbar_wait(cx.bar(BA::K_FULL), 0, cx.abort_flag, p.status, kRoleMma * 64 + BA::K_FULL);
-  // prologue: S0(0), S1(0)
-  for (int g = 0; ok && g < 2; ++g) {
-    if (u.n[g] == 0) continue;
-    ok = mbar_wait(cx.bar(BA::Q_FULL + g), 0, cx.abort_flag, p.status, kRoleMma * 64 + BA::Q_FULL);
-    if (!ok) break;
-    tc_fence_after();
-    issue_s(g, 0);
-  }
-  for (int j = 0; ok && j < n_max; ++j) {
-    const int s = j % NS;
-    const uint32_t ph = (j / NS) & 1;
-    for (int g = 0; g < 2; ++g) {
-      if (j >= u.n[g]) continue;
-      ok = mbar_wait(cx.bar(BA::P_FULL + g), j & 1, cx.abort_flag, p.status,
-                     kRoleMma * 64 + BA::P_FULL + g) &&
-           mbar_wait(cx.bar(BA::V_FULL + s), ph, cx.abort_flag, p.status,
-                     kRoleMma * 64 + BA::V_FULL + s);
+  int q_cnt[2] = {0, 0};  // units with Q_g so far
+  int s_cnt[2] = {0, 0};  // S_g tiles so far
+  int o_cnt[2] = {0, 0};  // units with O_g so far
+  int kv_cnt = 0;
+  bool ok = true;
+  for (int k = 0; ok; ++k) {
+    const int unit = next_unit<NS>(p, cx, k, kRoleMma, cx.lane == 0);
+    if (unit < 0) break;
+    const Unit u = decode_unit(p, unit);
+    const int n_max = max(u.n[0], u.n[1]);
+    if (n_max == 0) continue;
+    // prologue: S0(0), S1(0)
+    ok = mbar_wait(cx.bar(BA::K_FULL + kv_cnt % NS), (kv_cnt / NS) & 1, cx.abort_flag, p.status,
+                   kRoleMma * 64 + BA::K_FULL);
+    for (int g = 0; ok && g < 2; ++g) {
+      if (u.n[g] == 0) continue;
+      ok = mbar_wait(cx.bar(BA::Q_FULL + g), q_cnt[g] & 1, cx.abort_flag, p.status,
+                     kRoleMma * 64 + BA::Q_FULL + g);
       if (!ok) break;
       tc_fence_after();
-      issue_pv(g, j);
-      if (j + 1 < u.n[g]) {
-        const int s1 = (j + 1) % NS;
-        ok = mbar_wait(cx.bar(BA::K_FULL + s1), ((j + 1) / NS) & 1, cx.abort_flag, p.status,
-                       kRoleMma * 64 + BA::K_FULL + s1);
-        if (!ok) break;
-        tc_fence_after();
-        issue_s(g, j + 1);
-      } else {
-        commit(BA::O_DONE + g);
-      }
+      issue_s(g, kv_cnt);
+      if (u.n[g] == 1) commit(BA::Q_FREE + g);
     }
-    if (!ok) break;
-    commit(BA::KV_EMPTY + s);
+    for (int j = 0; ok && j < n_max; ++j) {
+      const int t = kv_cnt + j;
+      const int s = t % NS;
+      for (int g = 0; g < 2; ++g) {
+        if (j >= u.n[g]) continue;
+        ok = mbar_wait(cx.bar(BA::P_FULL + g), s_cnt[g] & 1, cx.abort_flag, p.status,
+                       kRoleMma * 64 + BA::P_FULL + g) &&
+             mbar_wait(cx.bar(BA::V_FULL + s), (t / NS) & 1, cx.abort_flag, p.status,
+                       kRoleMma * 64 + BA::V_FULL + s);
+        // the previous unit's epilogue must have read O_g before it is overwritten
+        if (ok && j == 0 && o_cnt[g] > 0)
+          ok = mbar_wait(cx.bar(BA::O_FREE + g), (o_cnt[g] - 1) & 1, cx.abort_flag, p.status,
+                         kRoleMma * 64 + BA::O_FREE + g);
+        if (!ok) break;
+        ++s_cnt[g];
+        tc_fence_after();
+        issue_pv(g, t, j == 0);
+        if (j + 1 < u.n[g]) {
+          const int s1 = (t + 1) % NS;
+          ok = mbar_wait(cx.bar(BA::K_FULL + s1), ((t + 1) / NS) & 1, cx.abort_flag, p.status,
+                         kRoleMma * 64 + BA::K_FULL + s1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(g, t + 1);
+          if (j + 2 == u.n[g]) commit(BA::Q_FREE + g);
+        } else {
+          commit(BA::O_DONE + g);
+          ++o_cnt[g];
+        }
+      }
+      if (!ok) break;
+      commit(BA::KV_EMPTY + s);
+    }
+    for (int g = 0; g < 2; ++g) q_cnt[g] += (u.n[g] > 0);
+    kv_cnt += n_max;
   }
   // Every MMA this warp issued completes before TMEM is released.
   commit(BA::DRAIN);
@@ -296,159 +392,181 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Unit& u, con
 }
 
 template <int D>
-__device__ __forceinline__ void softmax_role(const Bf16Params& p, const Unit& u, const Ctx& cx) {
+__device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx) {
   using C = Cfg<D>;
   using BA = Bars<C::NS>;
   const int warp = cx.warp, lane = cx.lane;
-  const uint32_t tmem = cx.tmem;
-  volatile int* abort_flag = cx.abort_flag;
-  auto bar = [&](int id) { return cx.bar(id); };
   const int g = warp >> 2;                      // which query tile
   const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
   const int row = quarter * 32 + lane;          // query row within the tile
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-  const uint32_t tS = tmem + (g ? C::TM_S1 : C::TM_S0) + lane_off;
-  const uint32_t tO = tmem + (g ? C::TM_O1 : C::TM_O0) + lane_off;
+  const uint32_t tS = cx.tmem + (g ? C::TM_S1 : C::TM_S0) + lane_off;
+  const uint32_t tO = cx.tmem + (g ? C::TM_O1 : C::TM_O0) + lane_off;
+  const uint32_t stage = cx.sStage + g * C::CHUNK;  // this warpgroup's staging chunk
+  // one fixed thread issues, commits and waits for the TMA stores (bulk
+  // async-groups belong to the issuing thread)
+  const bool store_thread = (warp == 4 * g) && lane == 0;
   const float c2 = p.scale_log2;
-  const int q_start = u.q0 + g * kBlockM;
-  const int qi = q_start + row;
-  const int n_tiles = u.n[g];
-  float m_ref = 0.f;  // reference maximum (log2 units) the exponents use
-  float l = 0.f;      // running sum of 2^(s*c2 - m_ref)
+  int s_cnt = 0;  // S_g tiles so far
+  int o_cnt = 0;  // units with O_g so far
   bool ok = true;
-  for (int j = 0; j < n_tiles; ++j) {
-    ok = mbar_wait(bar(BA::S_FULL + g), j & 1, abort_flag, p.status,
-                   kRoleSoftmax * 64 + BA::S_FULL + g);
-    if (!ok) break;
-    tc_fence_after();
-    uint32_t r[128];
+  for (int k = 0; ok; ++k) {
+    const int unit = next_unit<C::NS>(p, cx, k, kRoleSoftmax, lane == 0);
+    if (unit < 0) break;
+    const Unit u = decode_unit(p, unit);
+    const int q_start = u.q0 + g * kBlockM;
+    const int qi = q_start + row;
+    const int n_tiles = u.n[g];
+    float m_ref = 0.f;  // reference maximum (log2 units) the exponents use
+    float l = 0.f;      // running sum of 2^(s*c2 - m_ref)
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = mbar_wait(cx.bar(BA::S_FULL + g), s_cnt & 1, cx.abort_flag, p.status,
+                     kRoleSoftmax * 64 + BA::S_FULL + g);
+      if (!ok) break;
+      ++s_cnt;
+      tc_fence_after();
+      uint32_t r[128];
 #pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4)
-      tmem_ld32(tS + 32u * c4, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * c4]));
-    tmem_ld_wait();
-    float x[128];
+      for (int c4 = 0; c4 < 4; ++c4)
+        tmem_ld32(tS + 32u * c4, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * c4]));
+      tmem_ld_wait();
+      float x[128];
 #pragma unroll
-    for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(r[c]);
-    // per-element mask on the diagonal tile and a ragged last tile
-    const int kbase = j * kBlockN;
-    int lim = u.kv_len - kbase;                                  // keys c < lim exist
-    if (p.mask_kind == kMaskCausal && qi - kbase + 1 < lim) lim = qi - kbase + 1;
-    if (lim < kBlockN) {
+      for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(r[c]);
+      // per-element mask on the diagonal tile and a ragged last tile
+      const int kbase = j * kBlockN;
+      int lim = u.kv_len - kbase;                                  // keys c < lim exist
+      if (p.mask_kind == kMaskCausal && qi - kbase + 1 < lim) lim = qi - kbase + 1;
+      if (lim < kBlockN) {
 #pragma unroll
-      for (int c = 0; c < 128; ++c)
-        if (c >= lim) x[c] = -INFINITY;
-    }
-    // row maximum: eight independent chains of three-input max
-    float mk[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) mk[k] = fmaxf(x[2 * k], x[2 * k + 1]);
-#pragma unroll
-    for (int c = 16; c < 128; c += 16) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mk[k] = fmax3(mk[k], x[c + 2 * k], x[c + 2 * k + 1]);
-    }
-    const float mx =
-        fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7])) * c2;
-    if (j == 0) {
-      m_ref = (mx == -INFINITY) ? 0.f : mx;
-    } else {
-      // Each row moves its own reference up to this tile's maximum when that
-      // maximum exceeds it by more than the threshold; the partial output is
-      // rescaled in place (PV_g(j-1) is complete: S_g(j) was issued after
-      // it).  Rows that keep their reference multiply by exactly 1, so a
-      // row's arithmetic never depends on its neighbours.
-      const bool move = mx > m_ref + kRescaleThreshold;
-      const float alpha = move ? ex2_approx(m_ref - mx) : 1.f;
-      if (move) {
-        l *= alpha;
-        m_ref = mx;
+        for (int c = 0; c < 128; ++c)
+          if (c >= lim) x[c] = -INFINITY;
       }
-      if (__any_sync(0xffffffffu, move)) {
+      // row maximum: eight independent chains of three-input max
+      float mk[8];
 #pragma unroll
-        for (int c32 = 0; c32 < D / 32; ++c32) {
-          uint32_t o[32];
-          tmem_ld32(tO + 32u * c32, o);
-          tmem_ld_wait();
+      for (int q = 0; q < 8; ++q) mk[q] = fmaxf(x[2 * q], x[2 * q + 1]);
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float a0, a1;
-            mul2(a0, a1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
-            o[i] = __float_as_uint(a0);
-            o[i + 1] = __float_as_uint(a1);
+      for (int c = 16; c < 128; c += 16) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mk[q] = fmax3(mk[q], x[c + 2 * q], x[c + 2 * q + 1]);
+      }
+      const float mx =
+          fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7])) * c2;
+      if (j == 0) {
+        m_ref = (mx == -INFINITY) ? 0.f : mx;
+      } else {
+        // Each row moves its own reference up to this tile's maximum when that
+        // maximum exceeds it by more than the threshold; the partial output is
+        // rescaled in place (PV_g(j-1) is complete: S_g(j) was issued after
+        // it).  Rows that keep their reference multiply by exactly 1, so a
+        // row's arithmetic never depends on its neighbours.
+        const bool move = mx > m_ref + kRescaleThreshold;
+        const float alpha = move ? ex2_approx(m_ref - mx) : 1.f;
+        if (move) {
+          l *= alpha;
+          m_ref = mx;
+        }
+        if (__any_sync(0xffffffffu, move)) {
+#pragma unroll
+          for (int c32 = 0; c32 < D / 32; ++c32) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32u * c32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float a0, a1;
+              mul2(a0, a1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
+              o[i] = __float_as_uint(a0);
+              o[i + 1] = __float_as_uint(a1);
+            }
+            tmem_st32(tO + 32u * c32, o);
           }
-          tmem_st32(tO + 32u * c32, o);
         }
       }
-    }
-    // p = 2^(s*c2 - m_ref): packed scale-subtract, ex2 on the SFU, packed sums
-    const float nm = -m_ref;
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      // p = 2^(s*c2 - m_ref): packed scale-subtract, ex2 on the SFU, packed sums
+      const float nm = -m_ref;
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int c = 0; c < 128; c += 2) {
-      fma2(x[c], x[c + 1], x[c], x[c + 1], c2, c2, nm, nm);
-      x[c] = ex2_approx(x[c]);
-      x[c + 1] = ex2_approx(x[c + 1]);
-      const int k = (c >> 1) & 3;
-      add2(sa[k], sb[k], sa[k], sb[k], x[c], x[c + 1]);
-    }
-    add2(sa[0], sb[0], sa[0], sb[0], sa[1], sb[1]);
-    add2(sa[2], sb[2], sa[2], sb[2], sa[3], sb[3]);
-    l += (sa[0] + sb[0]) + (sa[2] + sb[2]);
-    // P_g as bf16 pairs into the first 64 columns of S_g (A operand of P.V)
-    uint32_t pk[64];
+      for (int c = 0; c < 128; c += 2) {
+        fma2(x[c], x[c + 1], x[c], x[c + 1], c2, c2, nm, nm);
+        x[c] = ex2_approx(x[c]);
+        x[c + 1] = ex2_approx(x[c + 1]);
+        const int q = (c >> 1) & 3;
+        add2(sa[q], sb[q], sa[q], sb[q], x[c], x[c + 1]);
+      }
+      add2(sa[0], sb[0], sa[0], sb[0], sa[1], sb[1]);
+      add2(sa[2], sb[2], sa[2], sb[2], sa[3], sb[3]);
+      l += (sa[0] + sb[0]) + (sa[2] + sb[2]);
+      // P_g as bf16 pairs into the first 64 columns of S_g (A operand of P.V)
+      uint32_t pk[64];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) pk[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
-    tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-    tmem_st32(tS + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-    tmem_st_wait();
-    tc_fence_before();
-    // (test hook) withholding the first P of tile 0 leaves the MMA warp's
-    // bounded wait to run out, which exercises the abort and drain path
-    if (!(p.withhold_p && g == 0 && j == 0)) mbar_arrive(bar(BA::P_FULL + g));
-  }
-  if (ok && n_tiles > 0) {
-    ok = mbar_wait(bar(BA::O_DONE + g), 0, abort_flag, p.status,
-                   kRoleSoftmax * 64 + BA::O_DONE + g);
-    tc_fence_after();
-  }
-  if (ok && q_start < p.Lq) {
-    // epilogue: O / l rounded to bf16, staged in shared memory (the Q_g tile
-    // buffer: every S_g MMA is complete) in the 128-byte-swizzled layout and
-    // written by TMA stores, which skip rows past Lq.
+      for (int i = 0; i < 64; ++i) pk[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tS + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_st_wait();
+      tc_fence_before();
+      // (test hook) withholding this CTA's first P leaves the MMA warp's
+      // bounded wait to run out, which exercises the abort and drain path
+      if (!(p.withhold_p && g == 0 && k == 0 && j == 0)) mbar_arrive(cx.bar(BA::P_FULL + g));
+    }
+    if (!ok) break;
+    if (q_start >= p.Lq) continue;
+    // ---- epilogue: O / l rounded to bf16, 64 columns at a time through this
+    // warpgroup's staging chunk (128-byte swizzle) and a TMA store, which
+    // skips rows past Lq.
+    if (n_tiles > 0) {
+      ok = mbar_wait(cx.bar(BA::O_DONE + g), o_cnt & 1, cx.abort_flag, p.status,
+                     kRoleSoftmax * 64 + BA::O_DONE + g);
+      if (!ok) break;
+      tc_fence_after();
+    }
     const float inv = (l > 0.f) ? 1.f / l : 0.f;
-    const uint32_t stage = cx.sQ + g * C::TILE;
 #pragma unroll
-    for (int c32 = 0; c32 < D / 32; ++c32) {
-      uint32_t o[32];
-      if (n_tiles > 0) {
-        tmem_ld32(tO + 32u * c32, o);
-        tmem_ld_wait();
-      } else {
+    for (int c = 0; c < C::KCH; ++c) {
+      // the previous TMA store from the staging chunk must have read it
+      if (store_thread) tma_store_wait_read();
+      named_barrier(1 + g, 128);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0u;
+      for (int half = 0; half < 2; ++half) {
+        uint32_t o[32];
+        if (n_tiles > 0) {
+          tmem_ld32(tO + 64u * c + 32u * half, o);
+          tmem_ld_wait();
+          if (c == C::KCH - 1 && half == 1) {
+            // O_g may be overwritten by the next unit from here on
+            tc_fence_before();
+            mbar_arrive(cx.bar(BA::O_FREE + g));
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(o[8 * v4 + 2 * i]) * inv,
+                               __uint_as_float(o[8 * v4 + 2 * i + 1]) * inv);
+          const uint32_t unit16 = static_cast<uint32_t>(4 * half + v4);  // 16-byte unit of the row
+          const uint32_t addr = stage + row * 128 + ((unit16 ^ (row & 7)) << 4);
+          st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+        }
       }
-      uint32_t w[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-      // 32 columns = 64 bytes = four 16-byte units of the 128-byte row
-#pragma unroll
-      for (int v4 = 0; v4 < 4; ++v4) {
-        const uint32_t unit = static_cast<uint32_t>((c32 & 1) * 4 + v4);
-        const uint32_t addr = stage + (c32 >> 1) * C::CHUNK + row * 128 + ((unit ^ (row & 7)) << 4);
-        st_shared_v4(addr, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+      fence_proxy_async_smem();
+      named_barrier(1 + g, 128);
+      if (store_thread) {
+        tma_store_4d(&p.tm_o, stage, 64 * c, u.h, q_start, u.b);
+        tma_store_commit();
       }
+      __syncwarp();
     }
-    fence_proxy_async_smem();
-    named_barrier(1 + g, 128);
-    if (warp == 4 * g && elect_one()) {
-#pragma unroll
-      for (int c = 0; c < C::KCH; ++c) tma_store_4d(&p.tm_o, stage + c * C::CHUNK, 64 * c, u.h, q_start, u.b);
-      tma_store_commit();
-      tma_store_wait_read();  // the staging buffer must outlive the reads
-    }
-    __syncwarp();
+    if (n_tiles > 0) ++o_cnt;
   }
+  // the staging chunk must outlive the reads of the last store
+  if (store_thread) tma_store_wait_read();
+  __syncwarp();
 }
 
 template <int D>
@@ -465,21 +583,28 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   cx.sQ = s_base + C::OFF_Q;
   cx.sK = s_base + C::OFF_K;
   cx.sV = s_base + C::OFF_V;
+  cx.sStage = s_base + C::OFF_STAGE;
   cx.s_bar = s_base + C::OFF_BAR;
   cx.warp = static_cast<int>(threadIdx.x >> 5);
   cx.lane = static_cast<int>(threadIdx.x & 31);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   cx.abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  const Unit u = decode_unit(p, static_cast<int>(blockIdx.x));
+  cx.unit_slot = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+  cx.clc_resp = s_base + C::OFF_MISC + 16;  // 16-byte aligned
 
   // ---- setup ---------------------------------------------------------------
   if (threadIdx.x == 0) {
     for (int g = 0; g < 2; ++g) {
       mbar_init(cx.bar(BA::Q_FULL + g), 1);
+      mbar_init(cx.bar(BA::Q_FREE + g), 1);
       mbar_init(cx.bar(BA::S_FULL + g), 1);
       mbar_init(cx.bar(BA::P_FULL + g), 128);
       mbar_init(cx.bar(BA::O_DONE + g), 1);
+      mbar_init(cx.bar(BA::O_FREE + g), 128);
+      mbar_init(cx.bar(BA::UNIT_FULL + g), 1);
+      mbar_init(cx.bar(BA::UNIT_EMPTY + g), kUnitConsumers);
     }
+    mbar_init(cx.bar(BA::CLC), 1);
     mbar_init(cx.bar(BA::DRAIN), 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(cx.bar(BA::K_FULL + s), 1);
@@ -493,6 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
+    tma_prefetch_desc(&p.tm_o);
   }
   if (cx.warp == 8) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -505,13 +631,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
 
   if (cx.warp < 8) {
     regs_increase<C::REGS_SOFTMAX>();
-    softmax_role<D>(p, u, cx);
+    softmax_role<D>(p, cx);
   } else {
     regs_decrease<C::REGS_OTHER>();
     if (cx.warp == 8) {
-      mma_role<D>(p, u, cx);
+      mma_role<D>(p, cx);
     } else if (cx.warp == 9) {
-      producer_role<D>(p, u, cx);
+      producer_role<D>(p, cx);
+    } else if (cx.warp == 10) {
+      scheduler_role<D>(p, cx);
     }
   }
 

@@ -147,6 +147,34 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// cluster launch control: a running CTA cancels a CTA of the same grid that
+// has not started yet and takes over its work.  The 16-byte response lands in
+// shared memory at `resp`, counted in bytes on the mbarrier.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+      "[%0], [%1];" ::"r"(resp),
+      "r"(bar)
+      : "memory");
+}
+// blockIdx.x of the cancelled CTA, or -1 when nothing was cancelled (no
+// further cancellation may be requested after that).
+__device__ __forceinline__ int clc_query_first_ctaid_x(uint32_t resp) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n\t.reg .b128 rr;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 rr, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, rr;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, rr;\n\t}"
+      : "=r"(ok), "=r"(x)
+      : "r"(resp)
+      : "memory");
+  return ok ? static_cast<int>(x) : -1;
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor-core operand reads, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
