@@ -34,16 +34,19 @@
 //   warp 11     idle
 // The third warpgroup gives registers to the softmax warpgroups, which hold
 // a whole 128-score row per thread: launched at 168 per thread, it drops to
-// 80 (d_k 64) or 96 (d_k 128) and they rise to 208 or 200 (both splits total
-// 63488 <= 384*168 registers).
-// TMEM (512 columns): S0 | S1 | O0 | O1.  Softmax g reads S_g (float32),
-// writes P_g as bf16 pairs into the first 64 columns of S_g, and the P.V
-// MMA reads P_g from TMEM.  Per key tile j the MMA warp issues
+// 112 and they rise to 192 (256*192 + 128*112 = 63488 <= 384*168 registers).
+// TMEM (512 columns), d_k = 128: S0 | S1 | O0 | O1.  Softmax g reads S_g
+// (float32), writes P_g as bf16 pairs into the first 64 columns of S_g, and
+// the P.V MMA reads P_g from TMEM.  Per key tile j the MMA warp issues
 //   PV0(j), S0(j+1), PV1(j), S1(j+1)
 // so softmax 0 works on S0(j+1) while the tensor core runs PV1(j) and
 // S1(j+1), and vice versa.  MMAs of one thread run in issue order, so
 // S_g(j+1) overwrites P_g(j) only after PV_g(j) has read it, and once S_g(j+1)
 // is complete PV_g(j) is too: softmax g may rescale O_g in place then.
+// d_k = 64: S0 | S1 | O0 | O1 | P0 | P1.  Softmax g releases S_g as soon as it
+// has read it, so the MMA warp issues S0(j+1), S1(j+1), PV0(j), PV1(j) and the
+// next scores are ready when a softmax warpgroup finishes a tile; softmax g
+// waits for PV_g(j-1) only before it rewrites P_g (and rescales O_g).
 // Masks: causal tiles above the diagonal are never loaded or computed; the
 // diagonal tile and a ragged last key tile are masked per element (score set
 // to -inf, weight exactly 0: formula page, 応用, 先を読まない仕掛け).
@@ -70,16 +73,21 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + NS * TILE;
   static constexpr int OFF_STAGE = OFF_V + NS * TILE;  // epilogue staging, one CHUNK per softmax warpgroup
   static constexpr int OFF_BAR = OFF_STAGE + 2 * CHUNK;
-  static constexpr int NBAR = 20 + 3 * NS;
+  static constexpr int NBAR = 22 + 3 * NS;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;  // tmem slot, abort flag, unit queue, CLC response
   static constexpr int SMEM = OFF_MISC + 64 + 1024;    // + slack to align the base to 1024
-  // TMEM columns
+  // TMEM columns.  With d_k = 64 P has columns of its own (S0 | S1 | O0 | O1 |
+  // P0 | P1), so S_g(j+1) can be computed while softmax g still works on tile
+  // j; with d_k = 128 the 512 columns hold only S0 | S1 | O0 | O1 and P_g is
+  // written over the first 64 columns of S_g.
+  static constexpr bool SEPARATE_P = (D == 64);
   static constexpr uint32_t TM_S0 = 0, TM_S1 = 128;
   static constexpr uint32_t TM_O0 = 256, TM_O1 = 256 + D;
+  static constexpr uint32_t TM_P0 = SEPARATE_P ? 384 : TM_S0, TM_P1 = SEPARATE_P ? 448 : TM_S1;
   static constexpr uint32_t TMEM_COLS = 512;
   // registers per thread after rebalancing (softmax warpgroups, the rest)
-  static constexpr uint32_t REGS_SOFTMAX = (D == 64) ? 208 : 200;
-  static constexpr uint32_t REGS_OTHER = (D == 64) ? 80 : 96;
+  static constexpr uint32_t REGS_SOFTMAX = 192;
+  static constexpr uint32_t REGS_OTHER = 112;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(256 * REGS_SOFTMAX + 128 * REGS_OTHER <= kThreads * 168, "register split");
 };
@@ -97,9 +105,11 @@ struct Bars {
   static constexpr int UNIT_EMPTY = 14;           // + slot: all consumers read it
   static constexpr int CLC = 16;                  // cancellation response landed
   static constexpr int DRAIN = 17;
-  static constexpr int K_FULL = 20;               // + stage
-  static constexpr int V_FULL = 20 + NS;          // + stage
-  static constexpr int KV_EMPTY = 20 + 2 * NS;    // + stage
+  static constexpr int S_FREE = 18;               // + g: softmax read S_g (128 arrivals; separate P only)
+  static constexpr int PV_DONE = 20;              // + g: PV_g done (separate P only)
+  static constexpr int K_FULL = 22;               // + stage
+  static constexpr int V_FULL = 22 + NS;          // + stage
+  static constexpr int KV_EMPTY = 22 + 2 * NS;    // + stage
 };
 
 // role ids for the status "site" field
@@ -315,7 +325,7 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx) {
   // B = V_t MN-major (16 keys = 16 rows of 128 B = 2048 B per step).
   auto issue_pv = [&](int g, int t, bool first) {
     const uint64_t b = dv0 + static_cast<uint64_t>(((t % NS) * C::TILE) >> 4);
-    const uint32_t a_tmem = cx.tmem + (g ? C::TM_S1 : C::TM_S0);
+    const uint32_t a_tmem = cx.tmem + (g ? C::TM_P1 : C::TM_P0);
     const uint32_t d_tmem = cx.tmem + (g ? C::TM_O1 : C::TM_O0);
     const uint32_t acc0 = first ? 0u : 1u;
     if (elect_one()) {
@@ -327,10 +337,52 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx) {
     __syncwarp();
   };
   int q_cnt[2] = {0, 0};  // units with Q_g so far
-  int s_cnt[2] = {0, 0};  // S_g tiles so far
+  int s_cnt[2] = {0, 0};  // P_g tiles consumed so far
+  int s_iss[2] = {0, 0};  // S_g tiles issued so far
   int o_cnt[2] = {0, 0};  // units with O_g so far
   int kv_cnt = 0;
   bool ok = true;
+  // S_g(t) for the unit's key tile j; with separate P the softmax must first
+  // have read the previous S_g (any unit).  The last S_g of a unit frees Q_g.
+  auto next_s = [&](int g, int t, int j, int n) {
+    if constexpr (C::SEPARATE_P) {
+      if (s_iss[g] > 0 && !mbar_wait(cx.bar(BA::S_FREE + g), (s_iss[g] - 1) & 1, cx.abort_flag,
+                                     p.status, kRoleMma * 64 + BA::S_FREE + g))
+        return false;
+    }
+    if (!mbar_wait(cx.bar(BA::K_FULL + t % NS), (t / NS) & 1, cx.abort_flag, p.status,
+                   kRoleMma * 64 + BA::K_FULL + t % NS))
+      return false;
+    tc_fence_after();
+    issue_s(g, t);
+    ++s_iss[g];
+    if (j + 1 == n) commit(BA::Q_FREE + g);
+    return true;
+  };
+  // PV_g for key tile t (the unit's j-th); the unit's last PV_g releases O_g
+  // to the epilogue.
+  auto next_pv = [&](int g, int t, int j, int n) {
+    const int s = t % NS;
+    if (!mbar_wait(cx.bar(BA::P_FULL + g), s_cnt[g] & 1, cx.abort_flag, p.status,
+                   kRoleMma * 64 + BA::P_FULL + g) ||
+        !mbar_wait(cx.bar(BA::V_FULL + s), (t / NS) & 1, cx.abort_flag, p.status,
+                   kRoleMma * 64 + BA::V_FULL + s))
+      return false;
+    // the previous unit's epilogue must have read O_g before it is overwritten
+    if (j == 0 && o_cnt[g] > 0 &&
+        !mbar_wait(cx.bar(BA::O_FREE + g), (o_cnt[g] - 1) & 1, cx.abort_flag, p.status,
+                   kRoleMma * 64 + BA::O_FREE + g))
+      return false;
+    ++s_cnt[g];
+    tc_fence_after();
+    issue_pv(g, t, j == 0);
+    if constexpr (C::SEPARATE_P) commit(BA::PV_DONE + g);
+    if (j + 1 == n) {
+      commit(BA::O_DONE + g);
+      ++o_cnt[g];
+    }
+    return true;
+  };
   for (int k = 0; ok; ++k) {
     const int unit = next_unit<NS>(p, cx, k, kRoleMma, cx.lane == 0);
     if (unit < 0) break;
@@ -338,49 +390,29 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx) {
     const int n_max = max(u.n[0], u.n[1]);
     if (n_max == 0) continue;
     // prologue: S0(0), S1(0)
-    ok = mbar_wait(cx.bar(BA::K_FULL + kv_cnt % NS), (kv_cnt / NS) & 1, cx.abort_flag, p.status,
-                   kRoleMma * 64 + BA::K_FULL);
     for (int g = 0; ok && g < 2; ++g) {
       if (u.n[g] == 0) continue;
       ok = mbar_wait(cx.bar(BA::Q_FULL + g), q_cnt[g] & 1, cx.abort_flag, p.status,
-                     kRoleMma * 64 + BA::Q_FULL + g);
-      if (!ok) break;
-      tc_fence_after();
-      issue_s(g, kv_cnt);
-      if (u.n[g] == 1) commit(BA::Q_FREE + g);
+                     kRoleMma * 64 + BA::Q_FULL + g) &&
+           next_s(g, kv_cnt, 0, u.n[g]);
     }
     for (int j = 0; ok && j < n_max; ++j) {
       const int t = kv_cnt + j;
-      const int s = t % NS;
-      for (int g = 0; g < 2; ++g) {
-        if (j >= u.n[g]) continue;
-        ok = mbar_wait(cx.bar(BA::P_FULL + g), s_cnt[g] & 1, cx.abort_flag, p.status,
-                       kRoleMma * 64 + BA::P_FULL + g) &&
-             mbar_wait(cx.bar(BA::V_FULL + s), (t / NS) & 1, cx.abort_flag, p.status,
-                       kRoleMma * 64 + BA::V_FULL + s);
-        // the previous unit's epilogue must have read O_g before it is overwritten
-        if (ok && j == 0 && o_cnt[g] > 0)
-          ok = mbar_wait(cx.bar(BA::O_FREE + g), (o_cnt[g] - 1) & 1, cx.abort_flag, p.status,
-                         kRoleMma * 64 + BA::O_FREE + g);
-        if (!ok) break;
-        ++s_cnt[g];
-        tc_fence_after();
-        issue_pv(g, t, j == 0);
-        if (j + 1 < u.n[g]) {
-          const int s1 = (t + 1) % NS;
-          ok = mbar_wait(cx.bar(BA::K_FULL + s1), ((t + 1) / NS) & 1, cx.abort_flag, p.status,
-                         kRoleMma * 64 + BA::K_FULL + s1);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(g, t + 1);
-          if (j + 2 == u.n[g]) commit(BA::Q_FREE + g);
-        } else {
-          commit(BA::O_DONE + g);
-          ++o_cnt[g];
+      if constexpr (C::SEPARATE_P) {
+        // S0(j+1), S1(j+1), then PV0(j), PV1(j)
+        for (int g = 0; ok && g < 2; ++g)
+          if (j + 1 < u.n[g]) ok = next_s(g, t + 1, j + 1, u.n[g]);
+        for (int g = 0; ok && g < 2; ++g)
+          if (j < u.n[g]) ok = next_pv(g, t, j, u.n[g]);
+      } else {
+        // PV0(j), S0(j+1), PV1(j), S1(j+1)
+        for (int g = 0; ok && g < 2; ++g) {
+          if (j >= u.n[g]) continue;
+          ok = next_pv(g, t, j, u.n[g]) && (j + 1 >= u.n[g] || next_s(g, t + 1, j + 1, u.n[g]));
         }
       }
       if (!ok) break;
-      commit(BA::KV_EMPTY + s);
+      commit(BA::KV_EMPTY + t % NS);
     }
     for (int g = 0; g < 2; ++g) q_cnt[g] += (u.n[g] > 0);
     kv_cnt += n_max;
@@ -401,6 +433,7 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
   const int row = quarter * 32 + lane;          // query row within the tile
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t tS = cx.tmem + (g ? C::TM_S1 : C::TM_S0) + lane_off;
+  const uint32_t tP = cx.tmem + (g ? C::TM_P1 : C::TM_P0) + lane_off;
   const uint32_t tO = cx.tmem + (g ? C::TM_O1 : C::TM_O0) + lane_off;
   const uint32_t stage = cx.sStage + g * C::CHUNK;  // this warpgroup's staging chunk
   // one fixed thread issues, commits and waits for the TMA stores (bulk
@@ -430,6 +463,11 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
       for (int c4 = 0; c4 < 4; ++c4)
         tmem_ld32(tS + 32u * c4, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * c4]));
       tmem_ld_wait();
+      if constexpr (C::SEPARATE_P) {
+        // S_g has been read: the next S_g may be computed into it
+        tc_fence_before();
+        mbar_arrive(cx.bar(BA::S_FREE + g));
+      }
       float x[128];
 #pragma unroll
       for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(r[c]);
@@ -453,36 +491,19 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
       }
       const float mx =
           fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7])) * c2;
+      // Each row moves its own reference up to this tile's maximum when that
+      // maximum exceeds it by more than the threshold; l and the partial
+      // output are rescaled by alpha (rows that keep their reference use
+      // exactly 1, so a row's arithmetic never depends on its neighbours).
+      bool move = false;
+      float alpha = 1.f;
       if (j == 0) {
         m_ref = (mx == -INFINITY) ? 0.f : mx;
-      } else {
-        // Each row moves its own reference up to this tile's maximum when that
-        // maximum exceeds it by more than the threshold; the partial output is
-        // rescaled in place (PV_g(j-1) is complete: S_g(j) was issued after
-        // it).  Rows that keep their reference multiply by exactly 1, so a
-        // row's arithmetic never depends on its neighbours.
-        const bool move = mx > m_ref + kRescaleThreshold;
-        const float alpha = move ? ex2_approx(m_ref - mx) : 1.f;
-        if (move) {
-          l *= alpha;
-          m_ref = mx;
-        }
-        if (__any_sync(0xffffffffu, move)) {
-#pragma unroll
-          for (int c32 = 0; c32 < D / 32; ++c32) {
-            uint32_t o[32];
-            tmem_ld32(tO + 32u * c32, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              float a0, a1;
-              mul2(a0, a1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
-              o[i] = __float_as_uint(a0);
-              o[i + 1] = __float_as_uint(a1);
-            }
-            tmem_st32(tO + 32u * c32, o);
-          }
-        }
+      } else if (mx > m_ref + kRescaleThreshold) {
+        move = true;
+        alpha = ex2_approx(m_ref - mx);
+        l *= alpha;
+        m_ref = mx;
       }
       // p = 2^(s*c2 - m_ref): packed scale-subtract, ex2 on the SFU, packed sums
       const float nm = -m_ref;
@@ -498,12 +519,39 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
       add2(sa[0], sb[0], sa[0], sb[0], sa[1], sb[1]);
       add2(sa[2], sb[2], sa[2], sb[2], sa[3], sb[3]);
       l += (sa[0] + sb[0]) + (sa[2] + sb[2]);
-      // P_g as bf16 pairs into the first 64 columns of S_g (A operand of P.V)
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) pk[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
-      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tS + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      if constexpr (C::SEPARATE_P) {
+        // PV_g of the previous tile must be done before P_g is rewritten and
+        // O_g rescaled
+        if (s_cnt > 1 && !mbar_wait(cx.bar(BA::PV_DONE + g), (s_cnt - 2) & 1, cx.abort_flag,
+                                    p.status, kRoleSoftmax * 64 + BA::PV_DONE + g)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      // P_g as bf16 pairs (A operand of P.V)
+      tmem_st32(tP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tP + 32u, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      // (with P over S, PV_g(j-1) is complete already: S_g(j) was issued after it)
+      if (__any_sync(0xffffffffu, move)) {
+#pragma unroll
+        for (int c32 = 0; c32 < D / 32; ++c32) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32u * c32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float a0, a1;
+            mul2(a0, a1, __uint_as_float(o[i]), __uint_as_float(o[i + 1]), alpha, alpha);
+            o[i] = __float_as_uint(a0);
+            o[i + 1] = __float_as_uint(a1);
+          }
+          tmem_st32(tO + 32u * c32, o);
+        }
+      }
       tmem_st_wait();
       tc_fence_before();
       // (test hook) withholding this CTA's first P leaves the MMA warp's
@@ -603,6 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
       mbar_init(cx.bar(BA::O_FREE + g), 128);
       mbar_init(cx.bar(BA::UNIT_FULL + g), 1);
       mbar_init(cx.bar(BA::UNIT_EMPTY + g), kUnitConsumers);
+      mbar_init(cx.bar(BA::S_FREE + g), 128);
+      mbar_init(cx.bar(BA::PV_DONE + g), 1);
     }
     mbar_init(cx.bar(BA::CLC), 1);
     mbar_init(cx.bar(BA::DRAIN), 1);
