@@ -73,7 +73,10 @@ struct Cfg {
   static constexpr int OFF_STAGE = OFF_V + NS * TILE;  // epilogue staging, one CHUNK per softmax warpgroup
   static constexpr int OFF_BAR = OFF_STAGE + 2 * CHUNK;
   static constexpr int NBAR = 23 + 3 * NS;
-  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;  // tmem slot, abort flag, unit queue, CLC response
+  // tmem slot (+0), abort flag (+4), unit queue (+8, +12), CLC response (+16,
+  // 16 bytes, must be 16-byte aligned)
+  static constexpr int OFF_MISC = (OFF_BAR + 8 * NBAR + 63) / 64 * 64;
+  static constexpr int OFF_CLC = OFF_MISC + 16;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;    // + slack to align the base to 1024
   // TMEM columns.  With d_k = 64 P has columns of its own (S0 | S1 | O0 | O1 |
   // P0 | P1), so S_g(j+1) can be computed while softmax g still works on tile
@@ -88,6 +91,10 @@ struct Cfg {
   static constexpr uint32_t REGS_SOFTMAX = 192;
   static constexpr uint32_t REGS_OTHER = 112;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(OFF_BAR % 8 == 0 && OFF_CLC % 16 == 0, "barrier / response alignment");
+  static_assert(OFF_Q % 1024 == 0 && OFF_K % 1024 == 0 && OFF_V % 1024 == 0 &&
+                    OFF_STAGE % 1024 == 0,
+                "128-byte-swizzled tiles need 1024-byte alignment");
   static_assert(256 * REGS_SOFTMAX + 128 * REGS_OTHER <= kThreads * 168, "register split");
 };
 
@@ -624,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   cx.abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   cx.unit_slot = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
-  cx.clc_resp = s_base + C::OFF_MISC + 16;  // 16-byte aligned
+  cx.clc_resp = s_base + C::OFF_CLC;
 
   // ---- setup ---------------------------------------------------------------
   if (threadIdx.x == 0) {
