@@ -230,7 +230,9 @@ __device__ __forceinline__ void producer_role(const Bf16Params& p, const Ctx& cx
   using BA = Bars<C::NS>;
   constexpr int NS = C::NS;
   int q_cnt[2] = {0, 0};  // Q_g loads so far
-  int kv_cnt = 0;         // K/V tiles loaded so far
+  int kv_cnt = 0;         // K/V tiles of the units before the current one
+  int kv_issued = 0;      // K tile loads issued
+  int v_issued = 0;       // V tile loads issued
   bool ok = true;
   for (int k = 0; ok; ++k) {
     const int unit = next_unit<NS>(p, cx, k, kRoleProducer, cx.lane == 0);
@@ -270,6 +272,11 @@ __device__ __forceinline__ void producer_role(const Bf16Params& p, const Ctx& cx
                       j * kBlockN, u.b);
       }
       __syncwarp();
+      if (is_v) {
+        ++v_issued;
+      } else {
+        ++kv_issued;
+      }
       return true;
     };
     if (n_max == 0) continue;
@@ -279,17 +286,21 @@ __device__ __forceinline__ void producer_role(const Bf16Params& p, const Ctx& cx
     kv_cnt += n_max;
   }
   // Leave only when every copy this warp started has landed (the normal path
-  // finds them complete already): the last Q_g and the last load of each stage.
+  // finds them complete already): the last Q_g and the last load of each
+  // stage.  These waits ignore the abort flag: a copy still in flight must not
+  // land in the shared memory of a CTA that has exited.
+  volatile int never = 0;
   for (int g = 0; g < 2; ++g)
     if (q_cnt[g] > 0)
-      mbar_wait(cx.bar(BA::Q_FULL + g), (q_cnt[g] - 1) & 1, cx.abort_flag, p.status,
+      mbar_wait(cx.bar(BA::Q_FULL + g), (q_cnt[g] - 1) & 1, &never, p.status,
                 kRoleProducer * 64 + BA::Q_FULL + g);
-  for (int t = (kv_cnt > NS ? kv_cnt - NS : 0); t < kv_cnt; ++t) {
+  for (int t = (kv_issued > NS ? kv_issued - NS : 0); t < kv_issued; ++t) {
     const int s = t % NS;
-    mbar_wait(cx.bar(BA::K_FULL + s), (t / NS) & 1, cx.abort_flag, p.status,
+    mbar_wait(cx.bar(BA::K_FULL + s), (t / NS) & 1, &never, p.status,
               kRoleProducer * 64 + BA::K_FULL + s);
-    mbar_wait(cx.bar(BA::V_FULL + s), (t / NS) & 1, cx.abort_flag, p.status,
-              kRoleProducer * 64 + BA::V_FULL + s);
+    if (t < v_issued)
+      mbar_wait(cx.bar(BA::V_FULL + s), (t / NS) & 1, &never, p.status,
+                kRoleProducer * 64 + BA::V_FULL + s);
   }
 }
 
@@ -403,6 +414,12 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx, con
           // P_g(j) lives over S_g: S_g(j+1) must follow PV_g(j)
           ok = next_pv(t, j, n) && (j + 1 >= n || next_s(t + 1, j + 1, n));
         }
+      } else {
+        // A tile this query tile does not use: release its stage only once it
+        // was loaded, so each release phase gets one arrival per MMA warp (a
+        // warp running ahead would complete a phase with two of its own).
+        ok = mbar_wait(cx.bar(BA::K_FULL + t % NS), (t / NS) & 1, cx.abort_flag, p.status,
+                       site + BA::K_FULL + t % NS);
       }
       if (!ok) break;
       commit(BA::KV_EMPTY + t % NS);
