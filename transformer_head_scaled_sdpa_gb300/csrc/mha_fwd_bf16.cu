@@ -28,8 +28,8 @@
 // 384 threads (three warpgroups) in five roles:
 //   warps 0-3   softmax + epilogue for Q0 (thread r owns row r = TMEM lane r)
 //   warps 4-7   softmax + epilogue for Q1
-//   warp 8      TMEM allocator and MMA issuer for Q0
-//   warp 11     MMA issuer for Q1
+//   warp 8      TMEM allocator and MMA issuer (for Q0 only with d_k = 64)
+//   warp 11     MMA issuer for Q1 (d_k = 64; idle with d_k = 128)
 //   warp 9      TMA producer: Q0, Q1, then K_j / V_j into an NS-stage ring
 //   warp 10     scheduler: feeds a two-slot queue of units to the others
 // The third warpgroup gives registers to the softmax warpgroups, which hold
@@ -37,9 +37,10 @@
 // 112 and they rise to 192 (256*192 + 128*112 = 63488 <= 384*168 registers).
 // TMEM (512 columns), d_k = 128: S0 | S1 | O0 | O1.  Softmax g reads S_g
 // (float32), writes P_g as bf16 pairs into the first 64 columns of S_g, and
-// the P.V MMA reads P_g from TMEM.  Per key tile j MMA warp g issues PV_g(j)
-// then S_g(j+1), so softmax 0 works on S0(j+1) while the tensor core runs
-// PV1(j) and S1(j+1), and vice versa.  MMAs of one thread run in issue order, so
+// the P.V MMA reads P_g from TMEM.  Per key tile j the MMA warp issues
+//   PV0(j), S0(j+1), PV1(j), S1(j+1)
+// so softmax 0 works on S0(j+1) while the tensor core runs PV1(j) and
+// S1(j+1), and vice versa.  MMAs of one thread run in issue order, so
 // S_g(j+1) overwrites P_g(j) only after PV_g(j) has read it, and once S_g(j+1)
 // is complete PV_g(j) is too: softmax g may rescale O_g in place then.
 // d_k = 64: S0 | S1 | O0 | O1 | P0 | P1.  Softmax g releases S_g as soon as it
@@ -59,7 +60,9 @@ namespace {
 constexpr int kThreads = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p stays <= 2^8
 constexpr int kHeadGroup = 32;              // heads dispatched together (L2 reuse of K/V)
-constexpr int kUnitConsumers = 11;          // unit-queue readers: 8 softmax warps, 2 MMA, producer
+// unit-queue readers: 8 softmax warps, the producer and 1 or 2 MMA warps
+template <int D>
+constexpr int unit_consumers() { return D == 64 ? 11 : 10; }
 
 template <int D>
 struct Cfg {
@@ -304,14 +307,16 @@ __device__ __forceinline__ void producer_role(const Bf16Params& p, const Ctx& cx
   }
 }
 
-// MMA issuers (warp 8 for Q0, warp 11 for Q1): each warp follows the chain of
-// its own query tile, S_g and PV_g, so neither tile waits on the other's
-// softmax.  The whole warp runs the loop and the waits; one elected lane
-// issues every tcgen05.mma and tcgen05.commit, with descriptors built once
-// and stepped by compile-time offsets.  Both warps release every K/V stage
-// (the stage barrier counts two arrivals).
+// MMA issuer(s).  With separate P (d_k = 64) warp 8 serves Q0 and warp 11
+// Q1 (gsel 0 and 1): each follows only its own tile's chain, so neither waits
+// on the other's softmax, and both release every K/V stage (the stage barrier
+// counts two arrivals).  With P over S (d_k = 128) warp 8 serves both tiles
+// (gsel 2) in the fixed order PV0(j), S0(j+1), PV1(j), S1(j+1), which keeps
+// the two softmax warpgroups alternating on the tensor core.  The whole warp
+// runs the loop and the waits; one elected lane issues every tcgen05.mma and
+// tcgen05.commit, with descriptors built once and stepped by constants.
 template <int D>
-__device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx, const int g) {
+__device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx, const int gsel) {
   using C = Cfg<D>;
   using BA = Bars<C::NS>;
   constexpr int NS = C::NS;
@@ -319,68 +324,68 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx, con
   constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
   // K-major Q and K tiles: 8-row groups 1024 B apart; V MN-major with its
   // second 64-wide d chunk one CHUNK further.
-  const uint64_t dq = smem_desc_sw128(cx.sQ + g * C::TILE, 16, 1024);
+  const uint64_t dq0 = smem_desc_sw128(cx.sQ, 16, 1024);
   const uint64_t dk0 = smem_desc_sw128(cx.sK, 16, 1024);
   const uint64_t dv0 = smem_desc_sw128(cx.sV, C::CHUNK, 1024);
-  const uint32_t tm_s = cx.tmem + (g ? C::TM_S1 : C::TM_S0);
-  const uint32_t tm_p = cx.tmem + (g ? C::TM_P1 : C::TM_P0);
-  const uint32_t tm_o = cx.tmem + (g ? C::TM_O1 : C::TM_O0);
   const int site = kRoleMma * 64;
   auto commit = [&](int id) {
     if (elect_one()) umma_commit(cx.bar(id));
     __syncwarp();
   };
-  int q_cnt = 0;  // units with Q_g so far
-  int s_cnt = 0;  // P_g tiles consumed so far
-  int s_iss = 0;  // S_g tiles issued so far
-  int o_cnt = 0;  // units with O_g so far
+  // per query tile g: units with Q_g, P_g tiles consumed, S_g tiles issued,
+  // units with O_g
+  int q_cnt[2] = {0, 0}, s_cnt[2] = {0, 0}, s_iss[2] = {0, 0}, o_cnt[2] = {0, 0};
   int kv_cnt = 0;
   bool ok = true;
   // S_g = Q_g K_t^T (M 128 queries, N 128 keys, K = d in steps of 16) for the
   // unit's key tile j; with separate P the softmax must first have read the
   // previous S_g (any unit).  The last S_g of a unit frees Q_g.
-  auto next_s = [&](int t, int j, int n) {
+  auto next_s = [&](int g, int t, int j, int n) {
     if constexpr (C::SEPARATE_P) {
-      if (s_iss > 0 && !mbar_wait(cx.bar(BA::S_FREE + g), (s_iss - 1) & 1, cx.abort_flag,
-                                  p.status, site + BA::S_FREE + g))
+      if (s_iss[g] > 0 && !mbar_wait(cx.bar(BA::S_FREE + g), (s_iss[g] - 1) & 1, cx.abort_flag,
+                                     p.status, site + BA::S_FREE + g))
         return false;
     }
     if (!mbar_wait(cx.bar(BA::K_FULL + t % NS), (t / NS) & 1, cx.abort_flag, p.status,
                    site + BA::K_FULL + t % NS))
       return false;
     tc_fence_after();
+    const uint64_t a = dq0 + static_cast<uint64_t>((g * C::TILE) >> 4);
     const uint64_t b = dk0 + static_cast<uint64_t>(((t % NS) * C::TILE) >> 4);
+    const uint32_t tm_s = cx.tmem + (g ? C::TM_S1 : C::TM_S0);
     if (elect_one()) {
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
-        umma_ss(tm_s, dq + off, b + off, idesc_s, ks > 0 ? 1u : 0u);
+        umma_ss(tm_s, a + off, b + off, idesc_s, ks > 0 ? 1u : 0u);
       }
       umma_commit(cx.bar(BA::S_FULL + g));
       if (j + 1 == n) umma_commit(cx.bar(BA::Q_FREE + g));
     }
     __syncwarp();
-    ++s_iss;
+    ++s_iss[g];
     return true;
   };
   // O_g += P_g V_t (A = P_g from TMEM, 16 keys = 8 columns per step; B = V_t
   // MN-major, 16 keys = 16 rows of 128 B per step); the unit's last PV_g
   // releases O_g to the epilogue.
-  auto next_pv = [&](int t, int j, int n) {
+  auto next_pv = [&](int g, int t, int j, int n) {
     const int s = t % NS;
-    if (!mbar_wait(cx.bar(BA::P_FULL + g), s_cnt & 1, cx.abort_flag, p.status,
+    if (!mbar_wait(cx.bar(BA::P_FULL + g), s_cnt[g] & 1, cx.abort_flag, p.status,
                    site + BA::P_FULL + g) ||
         !mbar_wait(cx.bar(BA::V_FULL + s), (t / NS) & 1, cx.abort_flag, p.status,
                    site + BA::V_FULL + s))
       return false;
     // the previous unit's epilogue must have read O_g before it is overwritten
-    if (j == 0 && o_cnt > 0 &&
-        !mbar_wait(cx.bar(BA::O_FREE + g), (o_cnt - 1) & 1, cx.abort_flag, p.status,
+    if (j == 0 && o_cnt[g] > 0 &&
+        !mbar_wait(cx.bar(BA::O_FREE + g), (o_cnt[g] - 1) & 1, cx.abort_flag, p.status,
                    site + BA::O_FREE + g))
       return false;
-    ++s_cnt;
+    ++s_cnt[g];
     tc_fence_after();
     const uint64_t b = dv0 + static_cast<uint64_t>((s * C::TILE) >> 4);
+    const uint32_t tm_p = cx.tmem + (g ? C::TM_P1 : C::TM_P0);
+    const uint32_t tm_o = cx.tmem + (g ? C::TM_O1 : C::TM_O0);
     if (elect_one()) {
 #pragma unroll
       for (int ks = 0; ks < kBlockN / 16; ++ks)
@@ -390,47 +395,56 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx, con
       if (j + 1 == n) umma_commit(cx.bar(BA::O_DONE + g));
     }
     __syncwarp();
-    if (j + 1 == n) ++o_cnt;
+    if (j + 1 == n) ++o_cnt[g];
     return true;
   };
+  const int g_lo = (gsel == 2) ? 0 : gsel;
+  const int g_hi = (gsel == 2) ? 1 : gsel;
   for (int k = 0; ok; ++k) {
     const int unit = next_unit<NS>(p, cx, k, kRoleMma, cx.lane == 0);
     if (unit < 0) break;
     const Unit u = decode_unit(p, unit);
-    const int n = u.n[g];
     const int n_max = max(u.n[0], u.n[1]);
     if (n_max == 0) continue;
-    if (n > 0)
-      ok = mbar_wait(cx.bar(BA::Q_FULL + g), q_cnt & 1, cx.abort_flag, p.status,
-                     site + BA::Q_FULL + g) &&
-           next_s(kv_cnt, 0, n);
+    // prologue: S_g(0)
+    for (int g = g_lo; ok && g <= g_hi; ++g)
+      if (u.n[g] > 0)
+        ok = mbar_wait(cx.bar(BA::Q_FULL + g), q_cnt[g] & 1, cx.abort_flag, p.status,
+                       site + BA::Q_FULL + g) &&
+             next_s(g, kv_cnt, 0, u.n[g]);
     for (int j = 0; ok && j < n_max; ++j) {
       const int t = kv_cnt + j;
-      if (j < n) {
+      bool used = false;
+      for (int g = g_lo; ok && g <= g_hi; ++g) {
+        const int n = u.n[g];
+        if (j >= n) continue;
+        used = true;
         if constexpr (C::SEPARATE_P) {
           // S_g(j+1) first: it only needs the softmax to have read S_g(j)
-          ok = (j + 1 >= n || next_s(t + 1, j + 1, n)) && next_pv(t, j, n);
+          ok = (j + 1 >= n || next_s(g, t + 1, j + 1, n)) && next_pv(g, t, j, n);
         } else {
           // P_g(j) lives over S_g: S_g(j+1) must follow PV_g(j)
-          ok = next_pv(t, j, n) && (j + 1 >= n || next_s(t + 1, j + 1, n));
+          ok = next_pv(g, t, j, n) && (j + 1 >= n || next_s(g, t + 1, j + 1, n));
         }
-      } else {
-        // A tile this query tile does not use: release its stage only once it
-        // was loaded, so each release phase gets one arrival per MMA warp (a
-        // warp running ahead would complete a phase with two of its own).
+      }
+      if (ok && !used) {
+        // A tile none of this warp's query tiles uses: release its stage only
+        // once it was loaded, so each release phase gets one arrival per MMA
+        // warp (a warp running ahead would complete a phase on its own).
         ok = mbar_wait(cx.bar(BA::K_FULL + t % NS), (t / NS) & 1, cx.abort_flag, p.status,
                        site + BA::K_FULL + t % NS);
       }
       if (!ok) break;
       commit(BA::KV_EMPTY + t % NS);
     }
-    q_cnt += (n > 0);
+    for (int g = 0; g < 2; ++g) q_cnt[g] += (u.n[g] > 0);
     kv_cnt += n_max;
   }
   // Every MMA this warp issued completes before TMEM is released.
-  commit(BA::DRAIN + g);
+  const int dr = BA::DRAIN + (gsel == 1 ? 1 : 0);
+  commit(dr);
   volatile int never = 0;
-  mbar_wait(cx.bar(BA::DRAIN + g), 0, &never, p.status, site + BA::DRAIN + g);
+  mbar_wait(cx.bar(dr), 0, &never, p.status, site + dr);
 }
 
 template <int D>
@@ -660,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
       mbar_init(cx.bar(BA::O_DONE + g), 1);
       mbar_init(cx.bar(BA::O_FREE + g), 128);
       mbar_init(cx.bar(BA::UNIT_FULL + g), 1);
-      mbar_init(cx.bar(BA::UNIT_EMPTY + g), kUnitConsumers);
+      mbar_init(cx.bar(BA::UNIT_EMPTY + g), unit_consumers<D>());
       mbar_init(cx.bar(BA::S_FREE + g), 128);
       mbar_init(cx.bar(BA::PV_DONE + g), 1);
     }
@@ -670,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     for (int s = 0; s < NS; ++s) {
       mbar_init(cx.bar(BA::K_FULL + s), 1);
       mbar_init(cx.bar(BA::V_FULL + s), 1);
-      mbar_init(cx.bar(BA::KV_EMPTY + s), 2);
+      mbar_init(cx.bar(BA::KV_EMPTY + s), C::SEPARATE_P ? 2 : 1);
     }
     *cx.abort_flag = 0;
     fence_mbar_init();
@@ -696,9 +710,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   } else {
     regs_decrease<C::REGS_OTHER>();
     if (cx.warp == 8) {
-      mma_role<D>(p, cx, 0);
+      mma_role<D>(p, cx, C::SEPARATE_P ? 0 : 2);
     } else if (cx.warp == 11) {
-      mma_role<D>(p, cx, 1);
+      if (C::SEPARATE_P) mma_role<D>(p, cx, 1);
     } else if (cx.warp == 9) {
       producer_role<D>(p, cx);
     } else {
