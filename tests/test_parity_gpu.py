@@ -124,6 +124,30 @@ def test_peaked_rows(mha, d):
     pu.assert_bf16_close_rounding_aware(out, ref, f"peaked d={d}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mask", [NONE, CAUSAL])
+@pytest.mark.parametrize("step", [8.0, 40.0])
+def test_rising_rows(mha, d, mask, step):
+    """Scores that climb tile after tile.  Feature 0 of key j is step * (j //
+    128) and feature 0 of each query is +-3, so with scale 1 the rows with +3
+    climb by 24 (step 8) or 120 (step 40) per 128-key tile, i.e. 35 or 173
+    in log2 units (2^173 is past float32's range): every later tile lies far
+    above everything before it, so the running maximum moves on every tile,
+    while the rows with -3 fall and never move it.  Both kinds share every
+    warp."""
+    L = 640
+    case = inputs.random_case(79, 1, 2, L, L, d)
+    g = torch.Generator().manual_seed(80)
+    sign = torch.where(torch.rand((1, L, 2), generator=g) < 0.5, -3.0, 3.0)
+    case["q"][..., 0] = sign.to(torch.bfloat16)
+    tile = (torch.arange(L) // 128).to(torch.float32)
+    case["k"][..., 0] = (step * tile).view(1, L, 1).expand(1, L, 2).to(torch.bfloat16)
+    out = pu.gpu_run(mha, case, mask, scale=1.0)
+    ref = pu.oracle_run(case, mask, scale=1.0)
+    assert torch.isfinite(out.float()).all()
+    pu.assert_bf16_close_rounding_aware(out, ref, f"rising d={d} mask={mask} step={step}")
+
+
 # --------------------------------------------------------------------------
 # properties
 # --------------------------------------------------------------------------

@@ -75,7 +75,7 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + NS * TILE;
   static constexpr int OFF_STAGE = OFF_V + NS * TILE;  // epilogue staging, one CHUNK per softmax warpgroup
   static constexpr int OFF_BAR = OFF_STAGE + 2 * CHUNK;
-  static constexpr int NBAR = 23 + 3 * NS;
+  static constexpr int NBAR = 23 + 4 * NS;
   // tmem slot (+0), abort flag (+4), unit queue (+8, +12), CLC response (+16,
   // 16 bytes, must be 16-byte aligned)
   static constexpr int OFF_MISC = (OFF_BAR + 8 * NBAR + 63) / 64 * 64;
@@ -86,6 +86,11 @@ struct Cfg {
   // j; with d_k = 128 the 512 columns hold only S0 | S1 | O0 | O1 and P_g is
   // written over the first 64 columns of S_g.
   static constexpr bool SEPARATE_P = (D == 64);
+  // With two stages (d_k = 128) a stage's K tile is released after its last S
+  // MMA and its V tile after its last P.V MMA, which gives each load about
+  // one key tile of lead time; with four (d_k = 64) one release per stage
+  // (K_EMPTY) covers both.
+  static constexpr bool SPLIT_RELEASE = (NS == 2);
   static constexpr uint32_t TM_S0 = 0, TM_S1 = 128;
   static constexpr uint32_t TM_O0 = 256, TM_O1 = 256 + D;
   static constexpr uint32_t TM_P0 = SEPARATE_P ? 384 : TM_S0, TM_P1 = SEPARATE_P ? 448 : TM_S1;
@@ -118,7 +123,10 @@ struct Bars {
   static constexpr int DRAIN = 21;                // + g: MMA warp g's operations complete
   static constexpr int K_FULL = 23;               // + stage
   static constexpr int V_FULL = 23 + NS;          // + stage
-  static constexpr int KV_EMPTY = 23 + 2 * NS;    // + stage (2 arrivals: one per MMA warp)
+  static constexpr int K_EMPTY = 23 + 2 * NS;     // + stage: its K tile's last S MMA done (or,
+                                                  // without split release, the whole stage:
+                                                  // 2 arrivals, one per MMA warp)
+  static constexpr int V_EMPTY = 23 + 3 * NS;     // + stage: its V tile's last P.V MMA done
 };
 
 // role ids for the status "site" field
@@ -263,9 +271,11 @@ __device__ __forceinline__ void producer_role(const Bf16Params& p, const Ctx& cx
       const int s = t % NS;
       const uint32_t dst = (is_v ? cx.sV : cx.sK) + s * C::TILE;
       const uint32_t full = cx.bar((is_v ? BA::V_FULL : BA::K_FULL) + s);
-      if (!is_v && t >= NS &&
-          !mbar_wait(cx.bar(BA::KV_EMPTY + s), ((t / NS) - 1) & 1, cx.abort_flag, p.status,
-                     kRoleProducer * 64 + BA::KV_EMPTY + s))
+      // the stage's previous K (or V) tile must be done with
+      const int empty = (is_v ? BA::V_EMPTY : BA::K_EMPTY) + s;
+      if (t >= NS && (!is_v || C::SPLIT_RELEASE) &&
+          !mbar_wait(cx.bar(empty), ((t / NS) - 1) & 1, cx.abort_flag, p.status,
+                     kRoleProducer * 64 + empty))
         return false;
       if (elect_one()) {
         mbar_arrive_expect_tx(full, C::TILE);
@@ -399,6 +409,8 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx) {
     return true;
   };
   static_assert(GSEL == 0 || GSEL == 1, "one query tile per warp");
+  static_assert(C::SEPARATE_P && !C::SPLIT_RELEASE,
+                "one MMA warp per query tile: P apart from S, one release per stage");
   constexpr int g_lo = GSEL;
   constexpr int g_hi = GSEL;
   for (int k = 0; ok; ++k) {
@@ -422,13 +434,8 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx) {
         const int n = u.n[g];
         if (!ok || j >= n) continue;
         used = true;
-        if constexpr (C::SEPARATE_P) {
-          // S_g(j+1) first: it only needs the softmax to have read S_g(j)
-          ok = (j + 1 >= n || next_s(g, t + 1, j + 1, n)) && next_pv(g, t, j, n);
-        } else {
-          // P_g(j) lives over S_g: S_g(j+1) must follow PV_g(j)
-          ok = next_pv(g, t, j, n) && (j + 1 >= n || next_s(g, t + 1, j + 1, n));
-        }
+        // S_g(j+1) first: it only needs the softmax to have read S_g(j)
+        ok = (j + 1 >= n || next_s(g, t + 1, j + 1, n)) && next_pv(g, t, j, n);
       }
       if (ok && !used) {
         // A tile none of this warp's query tiles uses: release its stage only
@@ -438,7 +445,8 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx) {
                        site + BA::K_FULL + t % NS);
       }
       if (!ok) break;
-      commit(BA::KV_EMPTY + t % NS);
+      // the stage's K and V tiles are both done with (one release per stage)
+      commit(BA::K_EMPTY + t % NS);
     }
     for (int g = 0; g < 2; ++g) q_cnt[g] += (u.n[g] > 0);
     kv_cnt += n_max;
@@ -459,6 +467,7 @@ __device__ __forceinline__ void mma_role_pair(const Bf16Params& p, const Ctx& cx
   using C = Cfg<D>;
   using BA = Bars<C::NS>;
   constexpr int NS = C::NS;
+  static_assert(!C::SEPARATE_P && C::SPLIT_RELEASE, "pair order: P over S, split release");
   constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
   // K-major Q and K tiles: 8-row groups 1024 B apart; V MN-major with its
@@ -553,30 +562,25 @@ __device__ __forceinline__ void mma_role_pair(const Bf16Params& p, const Ctx& cx
     const Unit u = decode_unit(p, unit);
     const int n_max = max(u.n[0], u.n[1]);
     if (n_max == 0) continue;
-    // prologue: S0(0), S1(0)
+    // prologue: S0(0), S1(0); then K_0 is done with
     for (int g = 0; ok && g < 2; ++g) {
       if (u.n[g] == 0) continue;
       ok = mbar_wait(cx.bar(BA::Q_FULL + g), q_cnt[g] & 1, cx.abort_flag, p.status,
                      kRoleMma * 64 + BA::Q_FULL + g) &&
            next_s(g, kv_cnt, 0, u.n[g]);
     }
+    if (ok) commit(BA::K_EMPTY + kv_cnt % NS);
+    // Per key tile PV0(j), S0(j+1), PV1(j), S1(j+1).  V_j is released once
+    // PV1(j) is done and K_{j+1} once S1(j+1) is, so a stage's next K load
+    // starts a full key tile earlier than if both waited for the last MMA.
     for (int j = 0; ok && j < n_max; ++j) {
       const int t = kv_cnt + j;
-      if constexpr (C::SEPARATE_P) {
-        // S0(j+1), S1(j+1), then PV0(j), PV1(j)
-        for (int g = 0; ok && g < 2; ++g)
-          if (j + 1 < u.n[g]) ok = next_s(g, t + 1, j + 1, u.n[g]);
-        for (int g = 0; ok && g < 2; ++g)
-          if (j < u.n[g]) ok = next_pv(g, t, j, u.n[g]);
-      } else {
-        // PV0(j), S0(j+1), PV1(j), S1(j+1)
-        for (int g = 0; ok && g < 2; ++g) {
-          if (j >= u.n[g]) continue;
-          ok = next_pv(g, t, j, u.n[g]) && (j + 1 >= u.n[g] || next_s(g, t + 1, j + 1, u.n[g]));
-        }
+      for (int g = 0; ok && g < 2; ++g) {
+        if (j < u.n[g]) ok = next_pv(g, t, j, u.n[g]);
+        if (ok && g == 1) commit(BA::V_EMPTY + t % NS);
+        if (ok && j + 1 < u.n[g]) ok = next_s(g, t + 1, j + 1, u.n[g]);
       }
-      if (!ok) break;
-      commit(BA::KV_EMPTY + t % NS);
+      if (ok && j + 1 < n_max) commit(BA::K_EMPTY + (t + 1) % NS);
     }
     for (int g = 0; g < 2; ++g) q_cnt[g] += (u.n[g] > 0);
     kv_cnt += n_max;
@@ -824,7 +828,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     for (int s = 0; s < NS; ++s) {
       mbar_init(cx.bar(BA::K_FULL + s), 1);
       mbar_init(cx.bar(BA::V_FULL + s), 1);
-      mbar_init(cx.bar(BA::KV_EMPTY + s), C::SEPARATE_P ? 2 : 1);
+      mbar_init(cx.bar(BA::K_EMPTY + s), C::SEPARATE_P ? 2 : 1);
+      mbar_init(cx.bar(BA::V_EMPTY + s), 1);
     }
     *cx.abort_flag = 0;
     fence_mbar_init();
