@@ -62,7 +62,7 @@ typedef enum {
     MHA_ERR_SCALE = 5,       /* scale is NaN, infinite or negative */
     MHA_ERR_LAUNCH = 6,      /* a CUDA call failed (launch, copy, synchronise) */
     MHA_ERR_TIMEOUT = 7,     /* a bounded pipeline wait on the device gave up */
-    MHA_ERR_ALIAS = 8,       /* out overlaps q, k or v */
+    MHA_ERR_ALIAS = 8,       /* out (or lse) overlaps q, k or v (or out) */
     MHA_ERR_WORKSPACE = 9    /* workspace NULL or smaller than required */
 } mha_status;
 
@@ -106,6 +106,30 @@ int mha_fwd(const void* q, const void* k, const void* v, void* out,
 int mha_fwd_f32(const void* q, const void* k, const void* v, void* out,
                 int B, int H, int Lq, int Lk, int d_k, int mask_kind,
                 const int32_t* key_lens, float scale, void* stream);
+
+/*
+ * mha_fwd_lse, mha_fwd_f32_lse -- mha_fwd / mha_fwd_f32 that also store, for
+ * every row, the log of the softmax denominator (the log-sum-exp of the
+ * row's scaled scores over its visible keys):
+ *     lse[b, h, i] = log( sum_j exp(scale * q_i . k_j) )      (natural log)
+ * the normaliser of Equation (1)'s softmax ("Attention Is All You Need",
+ * Section 3.2.1; its exponentials are the e^{...} of the formula page
+ * transformer-attention, section 証明), with a_j = exp(s_j - lse).  It is
+ * what a backward pass needs to recompute the weights, and what lets partial
+ * results over disjoint key ranges be merged exactly.
+ *   lse   device pointer, float32 [B, H, Lq] (row i fastest), 4-byte aligned,
+ *         overlapping none of q, k, v, out; must not be NULL (MHA_ERR_NULL;
+ *         overlap gives MHA_ERR_ALIAS).  A row with no visible key gets -inf.
+ * The value is computed in float32 from the same running maximum and sum the
+ * kernel normalises the output with (before the probabilities are rounded to
+ * bf16).  Other arguments, errors and behaviour as mha_fwd / mha_fwd_f32.
+ */
+int mha_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse,
+                int B, int H, int Lq, int Lk, int d_k, int mask_kind,
+                const int32_t* key_lens, float scale, void* stream);
+int mha_fwd_f32_lse(const void* q, const void* k, const void* v, void* out, float* lse,
+                    int B, int H, int Lq, int Lk, int d_k, int mask_kind,
+                    const int32_t* key_lens, float scale, void* stream);
 
 /*
  * mha_fwd_host_workspace_bytes -- device workspace mha_fwd_host needs for
@@ -160,7 +184,7 @@ void mha_debug_withhold_p(int on);
 const char* mha_status_string(int status);
 
 /*
- * mha_last_launch_info -- diagnostics of the last mha_fwd / mha_fwd_f32 call
+ * mha_last_launch_info -- diagnostics of the last forward call (mha_fwd*)
  * on this thread: kernels launched, grid size (CTAs), threads per CTA and
  * dynamic shared memory bytes.  Any pointer may be NULL.
  */

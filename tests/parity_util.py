@@ -7,6 +7,16 @@ Tolerances (fixed by the target specification of this library):
 where O_ref is the float64 oracle evaluated on the exact float64 images of the
 values the GPU received.
 
+Row log-sum-exps (natural log, float32 on the GPU) are compared with
+    |lse - lse_ref| <= 5e-4 + 1e-6 |lse_ref|,   and -inf exactly where the oracle has -inf.
+Derivation: the row maximum comes from float32 scores whose tensor-core
+accumulation over d_k <= 128 bf16 products errs by at most about
+d_k * 2^-24 * sum|q_i k_i| * scale (about 1e-5 on the workloads, a few 1e-4 on
+peaked rows with scale 1), and log(l) from a float32 sum of at most 4096
+positive terms (relative error <= 4096 * 2^-24 = 2.4e-4 even in the worst
+order) of exponentials with relative error about 2^-22.  A wrong log base, a
+dropped maximum or a missing ln 2 errs by far more.
+
 Outside the workloads' input distribution (nearly one-hot softmax rows with
 |O| of several units) the bf16 rounding floor alone exceeds 1e-2: the kernel
 rounds every probability p and every output to bf16 (unit roundoff 2^-8), so
@@ -43,10 +53,36 @@ def gpu_run(binding, case, mask_kind, scale=0.0):
     return o
 
 
-def oracle_run(case, mask_kind, scale=None):
+def oracle_run(case, mask_kind, scale=None, return_lse=False):
     lens = case.get("key_lens")
     return oracle.mha(case["q"], case["k"], case["v"], mask_kind,
-                      key_lens=lens.numpy() if lens is not None else None, scale=scale)
+                      key_lens=lens.numpy() if lens is not None else None, scale=scale,
+                      return_lse=return_lse)
+
+
+def gpu_run_lse(binding, case, mask_kind, scale=0.0):
+    g = to_cuda(case)
+    fn = binding.mha_fwd if case["q"].dtype == torch.bfloat16 else binding.mha_fwd_f32
+    o, lse = fn(g["q"], g["k"], g["v"], mask_kind=mask_kind, key_lens=g["key_lens"],
+                scale=scale, return_lse=True)
+    assert binding.mha_sync_status() == 0
+    return o, lse
+
+
+LSE_ABS = 5e-4
+LSE_REL = 1e-6
+
+
+def assert_lse_close(lse, ref, what=""):
+    got = lse.detach().to("cpu", torch.float64).numpy()
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    inf_ref = np.isneginf(ref)
+    assert np.array_equal(np.isneginf(got), inf_ref), f"{what}: -inf rows differ"
+    assert np.all(np.isfinite(got[~inf_ref])), f"{what}: non-finite lse"
+    err = np.abs(got[~inf_ref] - ref[~inf_ref])
+    bound = LSE_ABS + LSE_REL * np.abs(ref[~inf_ref])
+    worst = float((err - bound).max()) if err.size else -1.0
+    assert worst <= 0, f"{what}: lse error exceeds 5e-4 + 1e-6|lse| by {worst:.3e} (max err {err.max():.3e})"
 
 
 def errors(out, ref):

@@ -89,3 +89,19 @@ def test_host_entry_errors(lib):
     assert lib.mha_fwd_host_workspace_bytes(2, 3, 64, 64, 64, 3) == 0
     assert lib.mha_fwd_host(Q, K, V, O, 2, 3, 64, 64, 64, 0, None, 0.0, 2, None, 0, None) == WORKSPACE
     assert lib.mha_fwd_host(Q, K, V, O, 2, 3, 64, 64, 64, 0, None, 0.0, 3, None, 0, None) == UNSUP
+
+
+LSE = 0x60000000
+
+
+@pytest.mark.parametrize("fn", ["mha_fwd_lse", "mha_fwd_f32_lse"])
+def test_lse_entry_errors(lib, fn):
+    def call(lse=LSE, o=O, B=2, H=3, Lq=64, Lk=64, d=64, mask=0):
+        return getattr(lib, fn)(Q, K, V, o, lse, B, H, Lq, Lk, d, mask, None, 0.0, None)
+    assert call(lse=None) == NULL
+    assert call(lse=LSE + 2) == UNSUP          # float32 lse needs 4-byte alignment
+    assert call(lse=O + 64) == ALIAS           # lse overlaps out
+    assert call(lse=Q) == ALIAS                # lse overlaps q
+    assert call(o=None) == NULL                # the base checks still come first
+    assert call(mask=1, Lk=65) == SHAPE
+    assert call(B=0, lse=None) == OK           # empty query side: nothing to store

@@ -149,6 +149,77 @@ def test_rising_rows(mha, d, mask, step):
 
 
 # --------------------------------------------------------------------------
+# row log-sum-exp (mha_fwd_lse, mha_fwd_f32_lse)
+# --------------------------------------------------------------------------
+LSE_SHAPES = [
+    # B, H, Lq, Lk, d, mask, key_lens, dtype
+    (2, 3, 200, 333, 64, NONE, None, torch.bfloat16),
+    (1, 8, 640, 640, 128, NONE, None, torch.bfloat16),
+    (3, 2, 300, 300, 128, CAUSAL, None, torch.bfloat16),
+    (2, 4, 129, 129, 64, CAUSAL, None, torch.bfloat16),
+    (4, 2, 130, 257, 128, KEYPAD, [257, 0, 127, 1], torch.bfloat16),
+    (2, 2, 70, 70, 17, CAUSAL, None, torch.float32),
+    (3, 2, 33, 90, 64, KEYPAD, [90, 1, 0], torch.float32),
+]
+
+
+@pytest.mark.parametrize("shape", LSE_SHAPES,
+                         ids=lambda s: "x".join(map(str, s[:5])) + f"-m{s[5]}-{str(s[7])[6:]}")
+def test_lse(mha, shape):
+    """The row log-sum-exp next to the output: -inf exactly on keyless rows,
+    else within the float32 bound; the output equals mha_fwd's bit for bit."""
+    B, H, Lq, Lk, d, mask, lens, dtype = shape
+    case = inputs.random_case(zlib.crc32(repr(shape[:7]).encode()) & 0xFFFF, B, H, Lq, Lk, d,
+                              dtype=dtype)
+    if lens is not None:
+        case["key_lens"] = torch.tensor(lens, dtype=torch.int32)
+    out, lse = pu.gpu_run_lse(mha, case, mask)
+    ref, lse_ref = pu.oracle_run(case, mask, return_lse=True)
+    if dtype == torch.float32:
+        pu.assert_f32_close(out, ref, str(shape))
+    else:
+        pu.assert_bf16_close(out, ref, str(shape))
+    pu.assert_lse_close(lse, lse_ref, str(shape))
+    assert torch.equal(out, pu.gpu_run(mha, case, mask))
+
+
+def test_lse_workload_sampled_heads(mha):
+    """GPT-3-like workload at full size: lse of sampled whole heads."""
+    w = inputs.BY_NAME["gpt3_causal"]
+    case = inputs.generate(w)
+    _, lse = pu.gpu_run_lse(mha, case, w.mask_kind)
+    lse = lse.cpu()
+    for b, h in ((0, 0), (w.B - 1, w.H - 1), (1, 37)):
+        sub = {n: case[n][b:b + 1, :, h:h + 1].contiguous() for n in ("q", "k", "v")}
+        sub["key_lens"] = None
+        _, lse_ref = pu.oracle_run(sub, w.mask_kind, return_lse=True)
+        pu.assert_lse_close(lse[b:b + 1, h:h + 1], lse_ref, f"gpt3 b={b} h={h}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_lse_peaked_rows(mha, d):
+    """Scale 1 on inputs x2: scores of tens of units, the float32 worst case."""
+    case = inputs.random_case(78, 2, 2, 256, 384, d, input_scale=2.0)
+    _, lse = pu.gpu_run_lse(mha, case, NONE, scale=1.0)
+    _, lse_ref = pu.oracle_run(case, NONE, scale=1.0, return_lse=True)
+    pu.assert_lse_close(lse, lse_ref, f"peaked d={d}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_lse_no_keys(mha, dtype):
+    """Lk == 0: zero output and lse -inf everywhere."""
+    q = torch.randn(2, 5, 3, 64, device="cuda").to(dtype)
+    k = torch.empty(2, 0, 3, 64, device="cuda", dtype=dtype)
+    fn = mha.mha_fwd if dtype == torch.bfloat16 else mha.mha_fwd_f32
+    out = torch.full_like(q, 7.0)
+    lse = torch.zeros(2, 3, 5, device="cuda")
+    fn(q, k, k, out=out, return_lse=True, lse=lse)
+    assert mha.mha_sync_status() == 0
+    assert torch.count_nonzero(out) == 0
+    assert torch.isneginf(lse).all()
+
+
+# --------------------------------------------------------------------------
 # properties
 # --------------------------------------------------------------------------
 def test_guard_bands_untouched(mha):

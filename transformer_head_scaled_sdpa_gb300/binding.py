@@ -29,6 +29,7 @@ _c_p = ctypes.c_void_p
 _c_i = ctypes.c_int
 _FWD_ARGS = [_c_p, _c_p, _c_p, _c_p, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_p,
              ctypes.c_float, _c_p]
+_FWD_LSE_ARGS = _FWD_ARGS[:4] + [_c_p] + _FWD_ARGS[4:]
 
 
 class MhaError(RuntimeError):
@@ -59,6 +60,10 @@ def lib():
             h.mha_fwd.argtypes = _FWD_ARGS
             h.mha_fwd_f32.restype = _c_i
             h.mha_fwd_f32.argtypes = _FWD_ARGS
+            h.mha_fwd_lse.restype = _c_i
+            h.mha_fwd_lse.argtypes = _FWD_LSE_ARGS
+            h.mha_fwd_f32_lse.restype = _c_i
+            h.mha_fwd_f32_lse.argtypes = _FWD_LSE_ARGS
             h.mha_fwd_host_workspace_bytes.restype = ctypes.c_size_t
             h.mha_fwd_host_workspace_bytes.argtypes = [_c_i] * 6
             h.mha_fwd_host.restype = _c_i
@@ -108,7 +113,8 @@ def _check_tensor(t, name, dtype, device_kind):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _call_fwd(fn_name, dtype, q, k, v, out, mask_kind, key_lens, scale, stream):
+def _call_fwd(fn_name, dtype, q, k, v, out, mask_kind, key_lens, scale, stream,
+              lse=None, want_lse=False):
     B, H, Lq, Lk, d = _shape(q, k, v)
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check_tensor(t, n, dtype, "cuda")
@@ -123,26 +129,41 @@ def _call_fwd(fn_name, dtype, q, k, v, out, mask_kind, key_lens, scale, stream):
         if tuple(key_lens.shape) != (B,):
             raise ValueError("key_lens must be [B]")
         lens_ptr = key_lens.data_ptr()
+    if not want_lse:
+        rc = getattr(lib(), fn_name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                     B, H, Lq, Lk, d, int(mask_kind), lens_ptr, float(scale),
+                                     _stream_handle(stream))
+        if rc != MHA_OK:
+            raise MhaError(rc, fn_name)
+        return out
+    if lse is None:
+        lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
+    _check_tensor(lse, "lse", torch.float32, "cuda")
+    if tuple(lse.shape) != (B, H, Lq):
+        raise ValueError("lse must be [B, H, Lq]")
+    fn_name += "_lse"
     rc = getattr(lib(), fn_name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                 B, H, Lq, Lk, d, int(mask_kind), lens_ptr, float(scale),
-                                 _stream_handle(stream))
+                                 lse.data_ptr(), B, H, Lq, Lk, d, int(mask_kind), lens_ptr,
+                                 float(scale), _stream_handle(stream))
     if rc != MHA_OK:
         raise MhaError(rc, fn_name)
-    return out
+    return out, lse
 
 
 def mha_fwd(q, k, v, out=None, mask_kind: int = 0, key_lens=None, scale: float = 0.0,
-            stream=None):
-    """bf16 attention forward on the GPU (tcgen05 kernel); returns ``out``."""
+            stream=None, return_lse: bool = False, lse=None):
+    """bf16 attention forward on the GPU (tcgen05 kernel); returns ``out``, or
+    ``(out, lse)`` with ``return_lse`` (lse: float32 [B, H, Lq], natural log)."""
     return _call_fwd("mha_fwd", torch.bfloat16, q, k, v, out, mask_kind, key_lens, scale,
-                     stream)
+                     stream, lse, return_lse)
 
 
 def mha_fwd_f32(q, k, v, out=None, mask_kind: int = 0, key_lens=None, scale: float = 0.0,
-                stream=None):
-    """float32 attention forward on the GPU (SIMT kernel); returns ``out``."""
+                stream=None, return_lse: bool = False, lse=None):
+    """float32 attention forward on the GPU (SIMT kernel); returns ``out``, or
+    ``(out, lse)`` with ``return_lse``."""
     return _call_fwd("mha_fwd_f32", torch.float32, q, k, v, out, mask_kind, key_lens, scale,
-                     stream)
+                     stream, lse, return_lse)
 
 
 def host_workspace_bytes(B, H, Lq, Lk, d_k, elem_bytes) -> int:

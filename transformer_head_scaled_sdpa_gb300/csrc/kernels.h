@@ -25,6 +25,7 @@ struct Bf16Params {
   CUtensorMap tm_v;  // [B, Lk, H, d]
   CUtensorMap tm_o;  // [B, Lq, H, d] bf16 output, same box and swizzle as tm_q
   void* out;         // [B, Lq, H, d] bf16
+  float* lse;        // [B, H, Lq] natural-log log-sum-exp per row, or null
   const int32_t* key_lens;
   DeviceStatus* status;
   int B, H, Lq, Lk;
@@ -39,6 +40,7 @@ struct F32Params {
   const float* k;
   const float* v;
   float* out;
+  float* lse;        // [B, H, Lq] natural-log log-sum-exp per row, or null
   const int32_t* key_lens;
   int B, H, Lq, Lk, d;
   int mask_kind;

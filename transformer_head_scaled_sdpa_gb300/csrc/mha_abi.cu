@@ -139,6 +139,40 @@ bool encode_map(CUtensorMap* m, const void* base, int B, int L, int H, int d) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// lse, when requested: [B, H, Lq] float32, 4-byte aligned, overlapping none of
+// q, k, v, out.
+int check_lse(const float* lse, const void* q, const void* k, const void* v, const void* out,
+              const Sizes& sz, int elem_bytes, long long rows_q) {
+  if (!lse) return MHA_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return MHA_ERR_UNSUPPORTED;
+  const size_t lb = static_cast<size_t>(rows_q) * 4;
+  const size_t ob = sz.q_elems * elem_bytes, kb = sz.kv_elems * elem_bytes;
+  if (overlaps(lse, lb, q, ob) || overlaps(lse, lb, out, ob) || overlaps(lse, lb, k, kb) ||
+      overlaps(lse, lb, v, kb))
+    return MHA_ERR_ALIAS;
+  return MHA_OK;
+}
+
+__global__ void fill_f32_kernel(float* p, size_t n, float value) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    p[i] = value;
+}
+
+// With no key anywhere every output row is 0 and every lse -inf.
+int no_keys(void* out, size_t out_bytes, float* lse, size_t rows, cudaStream_t s) {
+  if (cudaMemsetAsync(out, 0, out_bytes, s) != cudaSuccess) return MHA_ERR_LAUNCH;
+  if (lse) {
+    const unsigned blocks = static_cast<unsigned>(rows < 256 * 1024 ? (rows + 255) / 256 : 1024);
+    fill_f32_kernel<<<blocks, 256, 0, s>>>(lse, rows, -INFINITY);
+    if (cudaGetLastError() != cudaSuccess) return MHA_ERR_LAUNCH;
+    t_info.kernels = 1;
+    t_info.grid = static_cast<int>(blocks);
+    t_info.block = 256;
+  }
+  return MHA_OK;
+}
+
 // One CTA waits on an mbarrier that nothing ever arrives on, with the same
 // bounded wait the pipelines use: after the limit it records
 // MHA_ERR_TIMEOUT in the status word and returns.
@@ -159,12 +193,9 @@ float effective_scale(float scale, int d_k) {
   return scale == 0.f ? 1.f / std::sqrt(static_cast<float>(d_k)) : scale;
 }
 
-}  // namespace
-
-extern "C" {
-
-int mha_fwd(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq, int Lk,
-            int d_k, int mask_kind, const int32_t* key_lens, float scale, void* stream) {
+int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse, bool want_lse,
+             int B, int H, int Lq, int Lk, int d_k, int mask_kind, const int32_t* key_lens,
+             float scale, void* stream) {
   t_info = mha::LaunchInfo{};
   bool empty = false;
   Sizes sz;
@@ -173,14 +204,13 @@ int mha_fwd(const void* q, const void* k, const void* v, void* out, int B, int H
   if (rc != MHA_OK) return rc;
   if (d_k != 64 && d_k != 128) return MHA_ERR_UNSUPPORTED;
   if (empty) return MHA_OK;
+  const long long rows_q = static_cast<long long>(B) * H * Lq;
+  if (want_lse && (rc = check_lse(lse, q, k, v, out, sz, 2, rows_q)) != MHA_OK) return rc;
   DeviceState* dev = nullptr;
   rc = device_state(&dev);
   if (rc != MHA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (Lk == 0) {
-    // no key anywhere: every row is 0 (bf16 zero is the all-zero pattern)
-    return cudaMemsetAsync(out, 0, sz.q_elems * 2, s) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
-  }
+  if (Lk == 0) return no_keys(out, sz.q_elems * 2, lse, static_cast<size_t>(rows_q), s);
   const long long n_qtiles = (Lq + mha::kUnitRows - 1) / mha::kUnitRows;
   if (n_qtiles * B * H > 0x7fffffffll) return MHA_ERR_SHAPE;
   mha::Bf16Params p;
@@ -189,6 +219,7 @@ int mha_fwd(const void* q, const void* k, const void* v, void* out, int B, int H
       !encode_map(&p.tm_v, v, B, Lk, H, d_k) || !encode_map(&p.tm_o, out, B, Lq, H, d_k))
     return MHA_ERR_UNSUPPORTED;
   p.out = out;
+  p.lse = lse;
   p.key_lens = key_lens;
   p.status = dev->status;
   p.B = B;
@@ -202,9 +233,9 @@ int mha_fwd(const void* q, const void* k, const void* v, void* out, int B, int H
   return mha::launch_fwd_bf16(p, d_k, s, &t_info) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
 }
 
-int mha_fwd_f32(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq,
-                int Lk, int d_k, int mask_kind, const int32_t* key_lens, float scale,
-                void* stream) {
+int fwd_f32(const void* q, const void* k, const void* v, void* out, float* lse, bool want_lse,
+            int B, int H, int Lq, int Lk, int d_k, int mask_kind, const int32_t* key_lens,
+            float scale, void* stream) {
   t_info = mha::LaunchInfo{};
   bool empty = false;
   Sizes sz;
@@ -213,18 +244,20 @@ int mha_fwd_f32(const void* q, const void* k, const void* v, void* out, int B, i
   if (rc != MHA_OK) return rc;
   if (d_k > 256) return MHA_ERR_UNSUPPORTED;
   if (empty) return MHA_OK;
+  const long long rows_q = static_cast<long long>(B) * H * Lq;
+  if (want_lse && (rc = check_lse(lse, q, k, v, out, sz, 4, rows_q)) != MHA_OK) return rc;
   DeviceState* dev = nullptr;
   rc = device_state(&dev);
   if (rc != MHA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (Lk == 0)
-    return cudaMemsetAsync(out, 0, sz.q_elems * 4, s) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
+  if (Lk == 0) return no_keys(out, sz.q_elems * 4, lse, static_cast<size_t>(rows_q), s);
   if ((static_cast<long long>(B) * H * Lq + 7) / 8 > 0x7fffffffll) return MHA_ERR_SHAPE;
   mha::F32Params p;
   p.q = static_cast<const float*>(q);
   p.k = static_cast<const float*>(k);
   p.v = static_cast<const float*>(v);
   p.out = static_cast<float*>(out);
+  p.lse = lse;
   p.key_lens = key_lens;
   p.B = B;
   p.H = H;
@@ -234,6 +267,35 @@ int mha_fwd_f32(const void* q, const void* k, const void* v, void* out, int B, i
   p.mask_kind = mask_kind;
   p.scale_log2 = effective_scale(scale, d_k) * kLog2e;
   return mha::launch_fwd_f32(p, s, &t_info) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mha_fwd(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq, int Lk,
+            int d_k, int mask_kind, const int32_t* key_lens, float scale, void* stream) {
+  return fwd_bf16(q, k, v, out, nullptr, false, B, H, Lq, Lk, d_k, mask_kind, key_lens, scale,
+                  stream);
+}
+
+int mha_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
+                int Lq, int Lk, int d_k, int mask_kind, const int32_t* key_lens, float scale,
+                void* stream) {
+  return fwd_bf16(q, k, v, out, lse, true, B, H, Lq, Lk, d_k, mask_kind, key_lens, scale, stream);
+}
+
+int mha_fwd_f32(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq,
+                int Lk, int d_k, int mask_kind, const int32_t* key_lens, float scale,
+                void* stream) {
+  return fwd_f32(q, k, v, out, nullptr, false, B, H, Lq, Lk, d_k, mask_kind, key_lens, scale,
+                 stream);
+}
+
+int mha_fwd_f32_lse(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                    int H, int Lq, int Lk, int d_k, int mask_kind, const int32_t* key_lens,
+                    float scale, void* stream) {
+  return fwd_f32(q, k, v, out, lse, true, B, H, Lq, Lk, d_k, mask_kind, key_lens, scale, stream);
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -334,7 +396,7 @@ const char* mha_status_string(int status) {
     case MHA_ERR_SCALE: return "scale must be finite and >= 0 (0 selects 1/sqrt(d_k))";
     case MHA_ERR_LAUNCH: return "a CUDA call failed";
     case MHA_ERR_TIMEOUT: return "a pipeline wait on the device timed out";
-    case MHA_ERR_ALIAS: return "out overlaps q, k or v";
+    case MHA_ERR_ALIAS: return "out (or lse) overlaps q, k or v (or out)";
     case MHA_ERR_WORKSPACE: return "workspace missing or too small";
     default: return "unknown status";
   }

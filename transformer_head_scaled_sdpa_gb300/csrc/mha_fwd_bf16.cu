@@ -738,6 +738,12 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
       tc_fence_after();
     }
     const float inv = (l > 0.f) ? 1.f / l : 0.f;
+    if (p.lse && qi < p.Lq) {
+      // log of the softmax denominator, natural units: m_ref and the
+      // exponents are in log2 units of the scaled scores
+      p.lse[(static_cast<size_t>(u.b) * p.H + u.h) * p.Lq + qi] =
+          (l > 0.f) ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+    }
 #pragma unroll
     for (int c = 0; c < C::KCH; ++c) {
       // the previous TMA store from the staging chunk must have read it

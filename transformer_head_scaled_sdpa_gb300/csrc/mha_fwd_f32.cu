@@ -14,6 +14,8 @@
 //     coalesced.
 // Masks remove keys before the softmax: causal keeps keys j <= i, key padding
 // keeps j < key_lens[b] (clamped to [0, Lk]).  A row with no key stores 0.
+// Optionally each row's log-sum-exp (the log of the softmax denominator) is
+// stored as well; -inf for a row with no key.
 #include "kernels.h"
 
 namespace mha {
@@ -102,6 +104,12 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) fwd_f32_kernel(const F32P
 
   float* o_row = p.out + static_cast<size_t>(row) * d;
   const float inv = (l > 0.f) ? 1.f / l : 0.f;
+  if (p.lse && lane == 0) {
+    // log of the softmax denominator, natural units: m and the exponents are
+    // in log2 units of the scaled scores, so lse = (m + log2 l) * ln 2
+    p.lse[(static_cast<size_t>(b) * p.H + h) * p.Lq + i] =
+        (l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+  }
 #pragma unroll
   for (int u = 0; u < kPerLane; ++u) {
     const int c = lane + 32 * u;
