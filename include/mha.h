@@ -132,6 +132,45 @@ int mha_fwd_f32_lse(const void* q, const void* k, const void* v, void* out, floa
                     const int32_t* key_lens, float scale, void* stream);
 
 /*
+ * mha_decode -- one decode step of attention over a key/value cache, bf16.
+ * At inference the decoder emits one token per step and runs again on the
+ * sequence extended by it (cookipedia article, section "Transformer 全体";
+ * beam search keeps four sequences going); the decoder's masked
+ * self-attention then sees a usable length that grows by one per step (D2L
+ * notes, the three kinds of attention, decoder layer A).  For each sequence b
+ * (one per beam) and head h the step attends one query row to the first
+ * cache_lens[b] cached keys and values:
+ *     o[b, h] = sum_j softmax_j(scale * q[b, h] . k[b, j, h]) v[b, j, h],
+ *               j < cache_lens[b]
+ * -- exactly mha_fwd with Lq = 1, MHA_MASK_KEY_PADDING and key_lens =
+ * cache_lens (the new token's own key and value are expected in the cache
+ * already, at position cache_lens[b] - 1).
+ *   q          device, bf16 [B, H, d_k] (= [B, 1, H, d_k]), 16-byte aligned.
+ *   k_cache, v_cache  device, bf16 [B, Lk, H, d_k] (Lk = cache capacity),
+ *              16-byte aligned; rows 0 .. Lk-1 must hold finite values.
+ *   out        device, bf16 [B, H, d_k]; must not overlap q or the caches.
+ *   lse        NULL, or device float32 [B, H] receiving each row's natural-log
+ *              log-sum-exp (-inf when cache_lens[b] <= 0).
+ *   cache_lens device int32 [B], clamped to [0, Lk]; required (MHA_ERR_MASK
+ *              when NULL).  A sequence with no key gets output 0.
+ *   d_k        64 or 128.   scale as in mha_fwd (0 selects 1/sqrt(d_k)).
+ *   workspace  device scratch of at least mha_decode_workspace_bytes(B, H, Lk,
+ *              d_k) bytes, 16-byte aligned, owned by the caller (NULL allowed
+ *              when that is 0); not shared with a concurrent call.
+ * Keys are split into chunks handled by separate CTAs when B*H alone would
+ * leave SMs idle; the partial results (output, maximum and sum per chunk) are
+ * merged exactly by a second kernel.  Products and sums are float32.
+ * Returns MHA_OK once enqueued, MHA_ERR_WORKSPACE when the workspace is
+ * missing or too small, or the argument codes of mha_fwd.
+ */
+int mha_decode(const void* q, const void* k_cache, const void* v_cache, void* out,
+               float* lse, int B, int H, int Lk, int d_k, const int32_t* cache_lens,
+               float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/* mha_decode_workspace_bytes -- workspace mha_decode needs (0: none). */
+size_t mha_decode_workspace_bytes(int B, int H, int Lk, int d_k);
+
+/*
  * mha_fwd_host_workspace_bytes -- device workspace mha_fwd_host needs for
  * these sizes (elem_bytes 2 for bf16, 4 for float32).  0 on bad sizes.
  */

@@ -105,3 +105,36 @@ def test_lse_entry_errors(lib, fn):
     assert call(o=None) == NULL                # the base checks still come first
     assert call(mask=1, Lk=65) == SHAPE
     assert call(B=0, lse=None) == OK           # empty query side: nothing to store
+
+
+WS = 0x70000000
+LENS_D = 0x78000000
+
+
+def dec(lib, q=Q, k=K, v=V, o=O, lse=None, B=2, H=3, Lk=64, d=64, lens=LENS_D, scale=0.0,
+        ws=None, ws_bytes=0):
+    return lib.mha_decode(q, k, v, o, lse, B, H, Lk, d, lens, scale, ws, ws_bytes, None)
+
+
+def test_decode_entry_errors(lib):
+    assert dec(lib, B=-1) == SHAPE
+    assert dec(lib, Lk=-1) == SHAPE
+    assert dec(lib, d=96) == UNSUP
+    assert dec(lib, scale=math.nan) == SCALE
+    assert dec(lib, q=None) == NULL
+    assert dec(lib, k=None) == NULL
+    assert dec(lib, lens=None) == MASK                     # cache lengths are required
+    assert dec(lib, q=Q + 8) == UNSUP
+    assert dec(lib, lse=0x60000002) == UNSUP
+    assert dec(lib, o=Q) == ALIAS
+    assert dec(lib, lse=O) == ALIAS
+    assert dec(lib, B=0) == OK and dec(lib, H=0, q=None) == OK
+    # a small batch over a long cache is split: it needs the workspace
+    need = lib.mha_decode_workspace_bytes(1, 4, 8192, 128)
+    assert need > 0
+    assert dec(lib, B=1, H=4, Lk=8192, d=128) == WORKSPACE
+    assert dec(lib, B=1, H=4, Lk=8192, d=128, ws=WS, ws_bytes=need - 1) == WORKSPACE
+    assert dec(lib, B=1, H=4, Lk=8192, d=128, ws=WS + 4, ws_bytes=need) == WORKSPACE
+    # many heads over a short cache run in one pass and need none
+    assert lib.mha_decode_workspace_bytes(64, 16, 256, 64) == 0
+    assert lib.mha_decode_workspace_bytes(2, 3, 64, 96) == 0

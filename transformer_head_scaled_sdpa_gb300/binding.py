@@ -64,6 +64,11 @@ def lib():
             h.mha_fwd_lse.argtypes = _FWD_LSE_ARGS
             h.mha_fwd_f32_lse.restype = _c_i
             h.mha_fwd_f32_lse.argtypes = _FWD_LSE_ARGS
+            h.mha_decode.restype = _c_i
+            h.mha_decode.argtypes = [_c_p] * 5 + [_c_i] * 4 + [_c_p, ctypes.c_float, _c_p,
+                                                               ctypes.c_size_t, _c_p]
+            h.mha_decode_workspace_bytes.restype = ctypes.c_size_t
+            h.mha_decode_workspace_bytes.argtypes = [_c_i] * 4
             h.mha_fwd_host_workspace_bytes.restype = ctypes.c_size_t
             h.mha_fwd_host_workspace_bytes.argtypes = [_c_i] * 6
             h.mha_fwd_host.restype = _c_i
@@ -164,6 +169,59 @@ def mha_fwd_f32(q, k, v, out=None, mask_kind: int = 0, key_lens=None, scale: flo
     ``(out, lse)`` with ``return_lse``."""
     return _call_fwd("mha_fwd_f32", torch.float32, q, k, v, out, mask_kind, key_lens, scale,
                      stream, lse, return_lse)
+
+
+def decode_workspace_bytes(B, H, Lk, d_k) -> int:
+    return int(lib().mha_decode_workspace_bytes(B, H, Lk, d_k))
+
+
+def mha_decode(q, k_cache, v_cache, cache_lens, out=None, scale: float = 0.0, workspace=None,
+               stream=None, return_lse: bool = False, lse=None):
+    """One decode step (bf16): q [B, H, d] (or [B, 1, H, d]) against the first
+    cache_lens[b] rows of k_cache / v_cache [B, Lk, H, d].  Returns out
+    [B, H, d] (q's shape), or (out, lse) with ``return_lse``.  ``workspace``
+    (uint8 CUDA tensor) is allocated when not given."""
+    if q.dim() == 4:
+        if q.shape[1] != 1:
+            raise ValueError("q must be [B, H, d] or [B, 1, H, d]")
+    elif q.dim() != 3:
+        raise ValueError("q must be [B, H, d] or [B, 1, H, d]")
+    B, H, d = q.shape[0], q.shape[-2], q.shape[-1]
+    if k_cache.dim() != 4 or tuple(k_cache.shape[::2]) != (B, H) or k_cache.shape[3] != d \
+            or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError(f"caches {tuple(k_cache.shape)} / {tuple(v_cache.shape)} do not match q")
+    Lk = k_cache.shape[1]
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check_tensor(t, n, torch.bfloat16, "cuda")
+    _check_tensor(cache_lens, "cache_lens", torch.int32, "cuda")
+    if tuple(cache_lens.shape) != (B,):
+        raise ValueError("cache_lens must be [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    _check_tensor(out, "out", torch.bfloat16, "cuda")
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have q's shape")
+    lse_ptr = None
+    if return_lse:
+        if lse is None:
+            lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+        _check_tensor(lse, "lse", torch.float32, "cuda")
+        if tuple(lse.shape) != (B, H):
+            raise ValueError("lse must be [B, H]")
+        lse_ptr = lse.data_ptr()
+    need = decode_workspace_bytes(B, H, Lk, d)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _check_tensor(workspace, "workspace", torch.uint8, "cuda")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    rc = lib().mha_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                          lse_ptr, B, H, Lk, d, cache_lens.data_ptr(), float(scale), ws_ptr,
+                          ws_bytes, _stream_handle(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "mha_decode")
+    return (out, lse) if return_lse else out
 
 
 def host_workspace_bytes(B, H, Lq, Lk, d_k, elem_bytes) -> int:

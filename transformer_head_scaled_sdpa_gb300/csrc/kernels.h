@@ -54,6 +54,35 @@ struct LaunchInfo {
   int smem = 0;
 };
 
+// Decode step: one query row per (sequence, head) against a key/value cache.
+struct DecodeParams {
+  CUtensorMap tm_k;  // [B, Lk, H, d] bf16 cache, box {64, 1, 64, 1}, 128-byte swizzle
+  CUtensorMap tm_v;
+  const void* q;     // [B, H, d] bf16
+  void* out;         // [B, H, d] bf16
+  float* lse;        // [B, H] or null
+  const int32_t* cache_lens;  // [B] keys per sequence (clamped to [0, Lk])
+  float* part_o;     // [n_splits, B*H, d]  (n_splits > 1)
+  float* part_m;     // [n_splits, B*H]
+  float* part_l;     // [n_splits, B*H]
+  DeviceStatus* status;
+  int B, H, Lk;
+  int chunk;         // keys per split, a multiple of 64
+  int n_splits;
+  float scale_log2;  // scale * log2(e)
+};
+
+constexpr int kDecChunkMin = 256;   // fewest keys a split is given
+constexpr int kDecMaxSplits = 64;
+
+// Splits the decode kernel uses for these sizes (the workspace holds that many
+// partial results unless it is 1).
+int decode_splits(int B, int H, int Lk);
+
+// Launches the decode step (d in {64, 128}): the split kernel and, with more
+// than one split, the combine kernel.
+cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream, LaunchInfo* info);
+
 // Launches the bf16 tcgen05 forward for d in {64, 128}.
 cudaError_t launch_fwd_bf16(const Bf16Params& p, int d, cudaStream_t stream, LaunchInfo* info);
 

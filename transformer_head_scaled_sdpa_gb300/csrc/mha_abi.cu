@@ -121,15 +121,16 @@ int check_args(const void* q, const void* k, const void* v, void* out, int B, in
   return MHA_OK;
 }
 
-// 4-D map over a [B, L, H, d] bf16 tensor; box = 64 features x 1 head x 128
-// rows x 1 sequence, 128-byte swizzle (the tcgen05 operand layout).
-bool encode_map(CUtensorMap* m, const void* base, int B, int L, int H, int d) {
+// 4-D map over a [B, L, H, d] bf16 tensor; box = 64 features x 1 head x `rows`
+// rows (128 for the forward's tiles, 64 for the decode step's) x 1 sequence,
+// 128-byte swizzle (the tcgen05 operand layout).
+bool encode_map(CUtensorMap* m, const void* base, int B, int L, int H, int d, int rows = 128) {
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(H) * d * 2,
                                  static_cast<cuuint64_t>(L) * H * d * 2};
-  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(rows), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -299,6 +300,88 @@ int mha_fwd_f32_lse(const void* q, const void* k, const void* v, void* out, floa
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Workspace of the decode step: partial outputs, maxima and sums of every
+// split (none with a single split).
+static size_t decode_ws_bytes(int B, int H, int Lk, int d_k, int* splits_out) {
+  const int S = mha::decode_splits(B, H, Lk);
+  if (splits_out) *splits_out = S;
+  if (S <= 1) return 0;
+  const size_t bh = static_cast<size_t>(B) * H;
+  return align256(static_cast<size_t>(S) * bh * d_k * 4) + 2 * align256(static_cast<size_t>(S) * bh * 4);
+}
+
+size_t mha_decode_workspace_bytes(int B, int H, int Lk, int d_k) {
+  if (B < 0 || H < 0 || Lk < 0 || (d_k != 64 && d_k != 128)) return 0;
+  return decode_ws_bytes(B, H, Lk, d_k, nullptr);
+}
+
+int mha_decode(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,
+               int B, int H, int Lk, int d_k, const int32_t* cache_lens, float scale,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  t_info = mha::LaunchInfo{};
+  if (B < 0 || H < 0 || Lk < 0) return MHA_ERR_SHAPE;
+  if (!std::isfinite(scale) || scale < 0.f) return MHA_ERR_SCALE;
+  if (d_k != 64 && d_k != 128) return MHA_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long cache_rows = bh * Lk;
+  if (bh > 0x7fffffffll || cache_rows > (1ll << 40)) return MHA_ERR_SHAPE;
+  if (bh == 0) return MHA_OK;
+  if (!q || !out) return MHA_ERR_NULL;
+  if (!cache_lens) return MHA_ERR_MASK;
+  if (Lk > 0 && (!k_cache || !v_cache)) return MHA_ERR_NULL;
+  const uintptr_t mis = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out) |
+                         (Lk > 0 ? (reinterpret_cast<uintptr_t>(k_cache) |
+                                    reinterpret_cast<uintptr_t>(v_cache))
+                                 : 0)) &
+                        15u;
+  if (mis || (reinterpret_cast<uintptr_t>(lse) & 3u)) return MHA_ERR_UNSUPPORTED;
+  const size_t qb = static_cast<size_t>(bh) * d_k * 2;
+  const size_t kb = static_cast<size_t>(cache_rows) * d_k * 2;
+  const size_t lb = static_cast<size_t>(bh) * 4;
+  if (overlaps(out, qb, q, qb) || overlaps(out, qb, k_cache, kb) || overlaps(out, qb, v_cache, kb))
+    return MHA_ERR_ALIAS;
+  if (lse && (overlaps(lse, lb, out, qb) || overlaps(lse, lb, q, qb) ||
+              overlaps(lse, lb, k_cache, kb) || overlaps(lse, lb, v_cache, kb)))
+    return MHA_ERR_ALIAS;
+  int S = 1;
+  const size_t need = decode_ws_bytes(B, H, Lk, d_k, &S);
+  if (need > 0 && (!workspace || workspace_bytes < need ||
+                   (reinterpret_cast<uintptr_t>(workspace) & 15u)))
+    return MHA_ERR_WORKSPACE;
+  if (need > 0 && overlaps(workspace, need, out, qb)) return MHA_ERR_ALIAS;
+  DeviceState* dev = nullptr;
+  int rc = device_state(&dev);
+  if (rc != MHA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (Lk == 0) return no_keys(out, qb, lse, static_cast<size_t>(bh), s);
+  mha::DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (!encode_map(&p.tm_k, k_cache, B, Lk, H, d_k, 64) ||
+      !encode_map(&p.tm_v, v_cache, B, Lk, H, d_k, 64))
+    return MHA_ERR_UNSUPPORTED;
+  p.q = q;
+  p.out = out;
+  p.lse = lse;
+  p.cache_lens = cache_lens;
+  if (S > 1) {
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    p.part_o = reinterpret_cast<float*>(w);
+    w += align256(static_cast<size_t>(S) * bh * d_k * 4);
+    p.part_m = reinterpret_cast<float*>(w);
+    w += align256(static_cast<size_t>(S) * bh * 4);
+    p.part_l = reinterpret_cast<float*>(w);
+  }
+  p.status = dev->status;
+  p.B = B;
+  p.H = H;
+  p.Lk = Lk;
+  p.n_splits = S;
+  const int per = (Lk + S - 1) / S;
+  p.chunk = (per + 63) / 64 * 64;
+  p.scale_log2 = effective_scale(scale, d_k) * kLog2e;
+  return mha::launch_decode(p, d_k, s, &t_info) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
+}
 
 size_t mha_fwd_host_workspace_bytes(int B, int H, int Lq, int Lk, int d_k, int elem_bytes) {
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || d_k < 1) return 0;

@@ -131,3 +131,65 @@ def random_case(seed: int, B: int, H: int, Lq: int, Lk: int, d_k: int,
         out["key_lens"] = torch.randint(lo, hi + 1, (B,), generator=g,
                                         dtype=torch.int64).to(torch.int32)
     return out
+
+
+# ---------------------------------------------------------------------------
+# decode steps: one new query per sequence against a key/value cache
+# ---------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    """One decode step of a batch of `sources` inputs with `beams` beams each
+    (the pages' beam search keeps 4): B = sources * beams sequences, each with
+    its own cache of capacity Lk; the beams of a source share one cache length,
+    drawn uniformly from [len_lo, len_hi]."""
+    name: str
+    sources: int
+    beams: int
+    H: int
+    d_k: int
+    Lk: int
+    len_lo: int
+    len_hi: int
+    input_scale: float = 1.0
+    note: str = ""
+
+    @property
+    def B(self) -> int:
+        return self.sources * self.beams
+
+    @property
+    def seed(self) -> int:
+        return 2000 + DECODE_INDEX[self.name]
+
+
+DECODE_WORKLOADS = [
+    DecodeWorkload("base_decode", 32, 4, 8, 64, 256, 16, 256,
+                   note="base model decoder self-attention, 32 sentences x beam 4"),
+    DecodeWorkload("gpt3_decode", 4, 4, 96, 128, 2048, 1024, 2048, input_scale=0.5,
+                   note="GPT-3-like, 4 prompts x beam 4, 2048 context"),
+    DecodeWorkload("gpt3_decode_b1", 1, 4, 96, 128, 2048, 1024, 2048, input_scale=0.5,
+                   note="GPT-3-like, one prompt x beam 4"),
+]
+DECODE_INDEX = {w.name: i for i, w in enumerate(DECODE_WORKLOADS)}
+DECODE_BY_NAME = {w.name: w for w in DECODE_WORKLOADS}
+
+
+def generate_decode(w: DecodeWorkload, seed: int | None = None):
+    """Return dict(q [B, H, d], k_cache, v_cache [B, Lk, H, d], cache_lens [B]
+    int32) on the CPU.  Same recipe as `generate`: q, then K, then V as
+    float32 N(0, 1) times the input scale, cast to bf16; then one length per
+    source, repeated for its beams."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed if seed is None else seed)
+    out = {}
+    for name, shape in (("q", (w.B, w.H, w.d_k)), ("k_cache", (w.B, w.Lk, w.H, w.d_k)),
+                        ("v_cache", (w.B, w.Lk, w.H, w.d_k))):
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        if w.input_scale != 1.0:
+            x.mul_(w.input_scale)
+        out[name] = x.to(torch.bfloat16)
+    per_source = torch.randint(w.len_lo, w.len_hi + 1, (w.sources,), generator=g,
+                               dtype=torch.int64)
+    out["cache_lens"] = per_source.repeat_interleave(w.beams).to(torch.int32)
+    return out
+
