@@ -15,6 +15,12 @@ N > 1 (torchrun, one rank per GPU): weak scaling; every rank runs its own
 replica of the workload (rank-specific seed), no data-path collective.
 ``--impl reference`` times the float64 CPU oracle on the host cores on a
 bounded sample of the same workload (rank 0 only).
+
+Decode workloads (``--workload gpt3_decode`` / ``base_decode`` /
+``gpt3_decode_b1``): one step = one mha_decode call (every sequence's new
+query against its key/value cache); the metric is the step's algorithmic
+bytes (q, out, and the visible K and V rows) per second, against the measured
+HBM bandwidth.
 """
 from __future__ import annotations
 
@@ -400,13 +406,238 @@ def run_reference(args):
     }), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# decode steps
+# ---------------------------------------------------------------------------
+DEC_METRIC = "attention decode step GB/s (bf16 K/V cache read, 1 GB300) and % of measured HBM bandwidth"
+DEC_UNIT = "GB/s"
+
+
+def decode_bytes(w, lens):
+    """Algorithmic bytes of one step: q and out once, the visible K and V rows."""
+    visible = float(lens.clamp(0, w.Lk).to(torch.int64).sum().item())
+    return 2.0 * visible * w.H * w.d_k * 2 + 2.0 * w.B * w.H * w.d_k * 2
+
+
+def decode_config(w, extra=None):
+    cfg = {"workload": w.name, "B": w.B, "sources": w.sources, "beams": w.beams, "H": w.H,
+           "d_k": w.d_k, "Lk_capacity": w.Lk, "cache_len_range": [w.len_lo, w.len_hi],
+           "input_scale": w.input_scale, "seed": w.seed,
+           "layout": "q [B, H, d_k]; caches [B, Lk, H, d_k]"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def decode_oracle_rows(w, case, rows, start):
+    """The oracle on `rows` (b, h) decode rows; returns the algorithmic bytes done."""
+    import oracle
+    done = 0.0
+    for i in range(rows):
+        r = (start + i) % (w.B * w.H)
+        b, h = divmod(r, w.H)
+        n = int(case["cache_lens"][b])
+        q = case["q"][b:b + 1, h:h + 1].reshape(1, 1, 1, w.d_k)
+        k = case["k_cache"][b:b + 1, :, h:h + 1]
+        v = case["v_cache"][b:b + 1, :, h:h + 1]
+        oracle.mha(q, k, v, inputs.MASK_KEY_PADDING,
+                   key_lens=case["cache_lens"][b:b + 1].numpy())
+        done += 2.0 * min(max(n, 0), w.Lk) * w.d_k * 2 + 2.0 * w.d_k * 2
+    return done
+
+
+def run_decode(args):
+    rank, world = mdist.init("nccl")
+    _, _, local_rank = mdist.env_rank_world()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from transformer_head_scaled_sdpa_gb300 import binding, build
+    if rank == 0:
+        build.build()
+    mdist.barrier(dev)
+    build.build()
+    w = inputs.DECODE_BY_NAME[args.workload]
+    case = inputs.generate_decode(w, seed=mdist.rank_seed(w.seed, rank))
+    g = {n: t.to(dev) for n, t in case.items()}
+    bytes_alg = decode_bytes(w, case["cache_lens"])
+    cache_bytes = 2 * g["k_cache"].numel() * 2
+    n_sets = 1 if cache_bytes > L2_BYTES else -(-2 * L2_BYTES // cache_bytes)
+    sets = [g] + [{n: t.clone() for n, t in g.items()} for _ in range(n_sets - 1)]
+    outs = [torch.empty_like(g["q"]) for _ in range(n_sets)]
+    ws = torch.empty(max(1, binding.decode_workspace_bytes(w.B, w.H, w.Lk, w.d_k)),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    cur = [0]
+
+    def step():
+        i = cur[0] % n_sets
+        cur[0] += 1
+        c = sets[i]
+        binding.mha_decode(c["q"], c["k_cache"], c["v_cache"], c["cache_lens"], out=outs[i],
+                           workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    rc = binding.mha_sync_status(stream)
+    if rc != 0:
+        raise binding.MhaError(rc, "warm-up")
+    launches_per_step = binding.last_launch_info()["kernels"]
+    sampler = ClockSampler(gpu_id(dev))
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    all_start = torch.cuda.Event(enable_timing=True)
+    all_end = torch.cuda.Event(enable_timing=True)
+    mdist.barrier(dev)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        all_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        all_end.record(stream)
+    torch.cuda.synchronize(dev)
+    mdist.barrier(dev)
+    t_wall1 = time.time()
+    rc = binding.mha_sync_status(stream)
+    if rc != 0:
+        raise binding.MhaError(rc, "timed region")
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    total_ms = all_start.elapsed_time(all_end)
+    max_total_ms = mdist.max_over_ranks(total_ms, dev)
+    total_bytes = mdist.sum_over_ranks(bytes_alg * args.steps, dev)
+    if rank == 0:
+        time.sleep(0.3)
+        sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1) if rank == 0 else None
+
+    # end to end through the public API: each step brings q (and the cache
+    # lengths) from pinned host memory, runs the step on the resident cache and
+    # reads the output back
+    hq = case["q"].pin_memory()
+    hlens = case["cache_lens"].pin_memory()
+    hout = torch.empty_like(hq).pin_memory()
+    dq = torch.empty_like(g["q"])
+    dlens = torch.empty_like(g["cache_lens"])
+    n_e2e = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dlens.copy_(hlens, non_blocking=True)
+        binding.mha_decode(dq, g["k_cache"], g["v_cache"], dlens, out=outs[0], workspace=ws,
+                           stream=stream)
+        hout.copy_(outs[0], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+    mdist.barrier(dev)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = mdist.max_over_ranks(e0.elapsed_time(e1) / n_e2e, dev)
+    e2e_bytes = mdist.sum_over_ranks(bytes_alg, dev)
+    if rank != 0:
+        mdist.finish()
+        return
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["hbm_gbs"])
+    value = total_bytes / (max_total_ms * 1e-3) / 1e9
+    achieved = bytes_alg / (step_ms * 1e-3) / 1e9
+    line = {
+        "metric": DEC_METRIC, "value": value, "unit": DEC_UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, no dataset)",
+        "config": decode_config(w, {
+            "parallelism": f"replicas x{world} (no collective)",
+            "inputs_exceed_l2": cache_bytes * n_sets > L2_BYTES, "l2_flush": False,
+            "input_sets_rotated": n_sets, "bytes_per_step_per_gpu": bytes_alg,
+            "splits": binding.last_launch_info()["kernels"] > 1}),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": DEC_UNIT,
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_src} HBM copy bandwidth",
+                     "kernel": "decode_split_kernel (+ decode_combine_kernel when split)",
+                     "kernel_ms": step_ms, "algorithmic_bytes": bytes_alg},
+        "clocks": clocks,
+        "e2e": {"value": e2e_bytes / (e2e_ms * 1e-3) / 1e9, "unit": DEC_UNIT,
+                "h2d_bytes_per_step": int(hq.numel() * 2 + hlens.numel() * 4),
+                "d2h_bytes_per_step": int(hout.numel() * 2), "steps": n_e2e,
+                "ms_per_step": e2e_ms,
+                "path": "pinned host q, cache_lens -> device, mha_decode on the resident cache, "
+                        "out -> host"},
+        "gpu_launches": int(launches_per_step * args.steps),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        t0 = time.perf_counter()
+        done, rows = 0.0, 0
+        while time.perf_counter() - t0 < 10.0 and rows < 4 * w.B * w.H:
+            done += decode_oracle_rows(w, case, 8, rows)
+            rows += 8
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {
+            "value": done / dt / 1e9, "unit": DEC_UNIT, "cores": oracle.default_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"{rows} (b, h) decode rows of {w.name} in float64, {dt:.1f} s wall"}
+    print(json.dumps(line), flush=True)
+    mdist.finish()
+
+
+def run_reference_decode(args):
+    rank, world, _ = mdist.env_rank_world()
+    if rank != 0:
+        return
+    import oracle
+    w = inputs.DECODE_BY_NAME[args.workload]
+    case = inputs.generate_decode(w)
+    cores = oracle.default_threads()
+    t0 = time.perf_counter()
+    decode_oracle_rows(w, case, 1, 0)
+    t_row = time.perf_counter() - t0
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    per_step = max(1, int(budget / max(t_row, 1e-6)))
+    for i in range(args.warmup):
+        decode_oracle_rows(w, case, per_step, i * per_step)
+    t0 = time.perf_counter()
+    done = 0.0
+    for i in range(args.steps):
+        done += decode_oracle_rows(w, case, per_step, (args.warmup + i) * per_step)
+    dt = time.perf_counter() - t0
+    value = done / dt / 1e9
+    sample = f"{per_step} (b, h) decode row(s) of {w.name} per step, float64 oracle, {cores} threads"
+    print(json.dumps({
+        "impl": "reference", "metric": DEC_METRIC, "value": value, "unit": DEC_UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) inputs, no dataset)",
+        "config": decode_config(w, {"parallelism": "host cores (OpenMP)"}),
+        "cpu_baseline": {"value": value, "unit": DEC_UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": DEC_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     # default: ~0.8 s timed on gpt3_causal, long enough for several clock samples
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="gpt3_causal", choices=sorted(inputs.BY_NAME))
+    ap.add_argument("--workload", default="gpt3_causal",
+                    choices=sorted(inputs.BY_NAME) + sorted(inputs.DECODE_BY_NAME))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -414,10 +645,11 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.steps < 1:
         ap.error("--steps must be >= 1")
+    decode = args.workload in inputs.DECODE_BY_NAME
     if args.impl == "reference":
-        run_reference(args)
+        (run_reference_decode if decode else run_reference)(args)
     else:
-        run_ours(args)
+        (run_decode if decode else run_ours)(args)
 
 
 if __name__ == "__main__":
