@@ -171,6 +171,28 @@ int mha_decode(const void* q, const void* k_cache, const void* v_cache, void* ou
 size_t mha_decode_workspace_bytes(int B, int H, int Lk, int d_k);
 
 /*
+ * mha_decode_static -- mha_decode without a workspace argument: the split
+ * partials go to a fixed device array inside the library (1 MiB per device,
+ * mha_decode_static_scratch_bytes()), so the call allocates nothing and needs
+ * no scratch from the caller.  Not from the pages: they have no counterpart;
+ * it exists for callers that cannot hand over device memory.
+ *   Arguments, results and errors as mha_decode; MHA_ERR_WORKSPACE when the
+ *   sizes would need more than the array holds (never for d_k <= 128: the
+ *   split count keeps the partials under 1215 rows of d_k + 2 floats).
+ *   Nothing in the array has to start at zero: each call's split kernel
+ *   writes every partial its combine kernel reads.
+ *   Every call on a device shares the one array: calls that overlap in time
+ *   (on different streams or host threads) race and give undefined results;
+ *   serialise them, or use mha_decode with a workspace per stream.
+ */
+int mha_decode_static(const void* q, const void* k_cache, const void* v_cache, void* out,
+                      float* lse, int B, int H, int Lk, int d_k, const int32_t* cache_lens,
+                      float scale, void* stream);
+
+/* mha_decode_static_scratch_bytes -- size of mha_decode_static's array. */
+size_t mha_decode_static_scratch_bytes(void);
+
+/*
  * mha_fwd_host_workspace_bytes -- device workspace mha_fwd_host needs for
  * these sizes (elem_bytes 2 for bf16, 4 for float32).  0 on bad sizes.
  */

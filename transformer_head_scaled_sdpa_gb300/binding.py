@@ -67,6 +67,10 @@ def lib():
             h.mha_decode.restype = _c_i
             h.mha_decode.argtypes = [_c_p] * 5 + [_c_i] * 4 + [_c_p, ctypes.c_float, _c_p,
                                                                ctypes.c_size_t, _c_p]
+            h.mha_decode_static.restype = _c_i
+            h.mha_decode_static.argtypes = [_c_p] * 5 + [_c_i] * 4 + [_c_p, ctypes.c_float, _c_p]
+            h.mha_decode_static_scratch_bytes.restype = ctypes.c_size_t
+            h.mha_decode_static_scratch_bytes.argtypes = []
             h.mha_decode_workspace_bytes.restype = ctypes.c_size_t
             h.mha_decode_workspace_bytes.argtypes = [_c_i] * 4
             h.mha_fwd_host_workspace_bytes.restype = ctypes.c_size_t
@@ -175,8 +179,16 @@ def decode_workspace_bytes(B, H, Lk, d_k) -> int:
     return int(lib().mha_decode_workspace_bytes(B, H, Lk, d_k))
 
 
+def mha_decode_static(q, k_cache, v_cache, cache_lens, out=None, scale: float = 0.0,
+                      stream=None, return_lse: bool = False, lse=None):
+    """mha_decode with the library's fixed device scratch instead of a
+    workspace (calls on one device must not overlap in time)."""
+    return mha_decode(q, k_cache, v_cache, cache_lens, out=out, scale=scale, stream=stream,
+                      return_lse=return_lse, lse=lse, _static=True)
+
+
 def mha_decode(q, k_cache, v_cache, cache_lens, out=None, scale: float = 0.0, workspace=None,
-               stream=None, return_lse: bool = False, lse=None):
+               stream=None, return_lse: bool = False, lse=None, _static: bool = False):
     """One decode step (bf16): q [B, H, d] (or [B, 1, H, d]) against the first
     cache_lens[b] rows of k_cache / v_cache [B, Lk, H, d].  Returns out
     [B, H, d] (q's shape), or (out, lse) with ``return_lse``.  ``workspace``
@@ -209,6 +221,13 @@ def mha_decode(q, k_cache, v_cache, cache_lens, out=None, scale: float = 0.0, wo
         if tuple(lse.shape) != (B, H):
             raise ValueError("lse must be [B, H]")
         lse_ptr = lse.data_ptr()
+    if _static:
+        rc = lib().mha_decode_static(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                     out.data_ptr(), lse_ptr, B, H, Lk, d,
+                                     cache_lens.data_ptr(), float(scale), _stream_handle(stream))
+        if rc != MHA_OK:
+            raise MhaError(rc, "mha_decode_static")
+        return (out, lse) if return_lse else out
     need = decode_workspace_bytes(B, H, Lk, d)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)

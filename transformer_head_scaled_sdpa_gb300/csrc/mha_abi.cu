@@ -19,12 +19,19 @@ using mha::DeviceStatus;
 // One status word per device: kernels record a bounded wait that gave up.
 __device__ DeviceStatus g_status;
 
+// Scratch of mha_decode_static (the split partials of one decode step), for
+// callers that pass no workspace: 1 MiB per device, shared by every call of
+// that entry on the device.
+constexpr size_t kDecodeStaticScratchBytes = size_t(1) << 20;
+static __device__ __align__(256) uint8_t g_decode_scratch[kDecodeStaticScratchBytes];
+
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
   bool ready = false;
   int supported = 0;  // MHA_OK or MHA_ERR_UNSUPPORTED
   DeviceStatus* status = nullptr;
+  void* decode_scratch = nullptr;  // device address of g_decode_scratch
 };
 
 std::mutex g_mutex;
@@ -56,6 +63,8 @@ int device_state(DeviceState** out) {
       void* addr = nullptr;
       if (cudaGetSymbolAddress(&addr, g_status) != cudaSuccess) return MHA_ERR_LAUNCH;
       st.status = static_cast<DeviceStatus*>(addr);
+      if (cudaGetSymbolAddress(&st.decode_scratch, g_decode_scratch) != cudaSuccess)
+        return MHA_ERR_LAUNCH;
       if (!g_encode) {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -316,9 +325,12 @@ size_t mha_decode_workspace_bytes(int B, int H, int Lk, int d_k) {
   return decode_ws_bytes(B, H, Lk, d_k, nullptr);
 }
 
-int mha_decode(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,
-               int B, int H, int Lk, int d_k, const int32_t* cache_lens, float scale,
-               void* workspace, size_t workspace_bytes, void* stream) {
+// The decode step with the split partials in `workspace` (from the caller) or,
+// with use_static, in this device's static scratch.
+static int decode_step(const void* q, const void* k_cache, const void* v_cache, void* out,
+                       float* lse, int B, int H, int Lk, int d_k, const int32_t* cache_lens,
+                       float scale, void* workspace, size_t workspace_bytes, bool use_static,
+                       void* stream) {
   t_info = mha::LaunchInfo{};
   if (B < 0 || H < 0 || Lk < 0) return MHA_ERR_SHAPE;
   if (!std::isfinite(scale) || scale < 0.f) return MHA_ERR_SCALE;
@@ -346,13 +358,18 @@ int mha_decode(const void* q, const void* k_cache, const void* v_cache, void* ou
     return MHA_ERR_ALIAS;
   int S = 1;
   const size_t need = decode_ws_bytes(B, H, Lk, d_k, &S);
-  if (need > 0 && (!workspace || workspace_bytes < need ||
-                   (reinterpret_cast<uintptr_t>(workspace) & 15u)))
-    return MHA_ERR_WORKSPACE;
-  if (need > 0 && overlaps(workspace, need, out, qb)) return MHA_ERR_ALIAS;
+  if (use_static) {
+    if (need > kDecodeStaticScratchBytes) return MHA_ERR_WORKSPACE;
+  } else {
+    if (need > 0 && (!workspace || workspace_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 15u)))
+      return MHA_ERR_WORKSPACE;
+    if (need > 0 && overlaps(workspace, need, out, qb)) return MHA_ERR_ALIAS;
+  }
   DeviceState* dev = nullptr;
   int rc = device_state(&dev);
   if (rc != MHA_OK) return rc;
+  if (use_static) workspace = dev->decode_scratch;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (Lk == 0) return no_keys(out, qb, lse, static_cast<size_t>(bh), s);
   mha::DecodeParams p;
@@ -365,6 +382,8 @@ int mha_decode(const void* q, const void* k_cache, const void* v_cache, void* ou
   p.lse = lse;
   p.cache_lens = cache_lens;
   if (S > 1) {
+    // every split CTA writes its whole partial (an empty split: output 0,
+    // maximum -inf, sum 0) before the combine reads it: nothing starts at zero
     uint8_t* w = static_cast<uint8_t*>(workspace);
     p.part_o = reinterpret_cast<float*>(w);
     w += align256(static_cast<size_t>(S) * bh * d_k * 4);
@@ -382,6 +401,22 @@ int mha_decode(const void* q, const void* k_cache, const void* v_cache, void* ou
   p.scale_log2 = effective_scale(scale, d_k) * kLog2e;
   return mha::launch_decode(p, d_k, s, &t_info) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
 }
+
+int mha_decode(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,
+               int B, int H, int Lk, int d_k, const int32_t* cache_lens, float scale,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_step(q, k_cache, v_cache, out, lse, B, H, Lk, d_k, cache_lens, scale, workspace,
+                     workspace_bytes, false, stream);
+}
+
+int mha_decode_static(const void* q, const void* k_cache, const void* v_cache, void* out,
+                      float* lse, int B, int H, int Lk, int d_k, const int32_t* cache_lens,
+                      float scale, void* stream) {
+  return decode_step(q, k_cache, v_cache, out, lse, B, H, Lk, d_k, cache_lens, scale, nullptr, 0,
+                     true, stream);
+}
+
+size_t mha_decode_static_scratch_bytes(void) { return kDecodeStaticScratchBytes; }
 
 size_t mha_fwd_host_workspace_bytes(int B, int H, int Lq, int Lk, int d_k, int elem_bytes) {
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || d_k < 1) return 0;
