@@ -157,10 +157,10 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def traffic_record(kernel_fp: str, workload: str):
+def traffic_record(kernel_fp: str, workload: str, kernel: str = "fwd_bf16_kernel"):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel source (null otherwise)."""
-    path = os.path.join(ROOT, "profiles", f"fwd_bf16_kernel_{workload}.traffic.json")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
@@ -567,7 +567,8 @@ def run_decode(args):
             "splits": binding.last_launch_info()["kernels"] > 1}),
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": DEC_UNIT,
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": traffic_record(kernel_fingerprint(), w.name, "decode_split_kernel"),
                      "peak_source": f"{peak_src} HBM copy bandwidth",
                      "kernel": "decode_split_kernel (+ decode_combine_kernel when split)",
                      "kernel_ms": step_ms, "algorithmic_bytes": bytes_alg},
