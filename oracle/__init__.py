@@ -78,6 +78,11 @@ class Oracle:
             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_double,
             ctypes.c_int]
+        lib.oracle_mha_bwd_f64.restype = ctypes.c_int
+        lib.oracle_mha_bwd_f64.argtypes = [ctypes.c_void_p] * 7 + [
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_double,
+            ctypes.c_int]
         lib.oracle_default_threads.restype = ctypes.c_int
         lib.oracle_default_threads.argtypes = []
         self.lib = lib
@@ -126,12 +131,51 @@ class Oracle:
         return (out, lse) if return_lse else out
 
 
+    def mha_bwd(self, q, k, v, dout, mask_kind: int = MASK_NONE, key_lens=None, scale=None,
+                threads: int | None = None):
+        """Gradient of attention for a loss with dL/dout = ``dout``
+        ([B,Lq,H,d]): returns (dq, dk, dv) in the layouts of q, k, v."""
+        q, k, v, dout = (_as_f64(x) for x in (q, k, v, dout))
+        if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
+            raise ValueError("q, k, v must be [B, L, H, d]")
+        B, Lq, H, d = q.shape
+        Lk = k.shape[1]
+        if k.shape != (B, Lk, H, d) or v.shape != (B, Lk, H, d) or dout.shape != q.shape:
+            raise ValueError("shapes do not match")
+        if scale is None:
+            scale = 1.0 / math.sqrt(d)
+        lens = None
+        if mask_kind == MASK_KEY_PADDING:
+            if key_lens is None:
+                raise ValueError("key padding needs key_lens")
+            if hasattr(key_lens, "detach"):
+                key_lens = key_lens.detach().cpu().numpy()
+            lens = np.ascontiguousarray(np.asarray(key_lens, dtype=np.int32))
+        dq = np.empty_like(q)
+        dk = np.empty_like(k)
+        dv = np.empty_like(v)
+        rc = self.lib.oracle_mha_bwd_f64(
+            q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data,
+            dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, B, H, Lq, Lk, d, int(mask_kind),
+            lens.ctypes.data if lens is not None else None, float(scale),
+            int(threads) if threads else 0)
+        if rc != 0:
+            raise ValueError(f"oracle_mha_bwd_f64 rejected its arguments (code {rc})")
+        return dq, dk, dv
+
+
 def _get() -> Oracle:
     global _default
     with _lock:
         if _default is None:
             _default = Oracle(build())
     return _default
+
+
+def mha_bwd(q, k, v, dout, mask_kind: int = MASK_NONE, key_lens=None, scale=None,
+            threads: int | None = None):
+    """Module-level convenience over the default oracle build (see Oracle.mha_bwd)."""
+    return _get().mha_bwd(q, k, v, dout, mask_kind, key_lens, scale, threads)
 
 
 def default_threads() -> int:

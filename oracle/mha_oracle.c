@@ -161,6 +161,118 @@ int oracle_mha_f64(const double* q, const double* k, const double* v,
     return 0;
 }
 
+/*
+ * Gradient ("backward") of the same operation for a loss L whose gradient
+ * with respect to the output is dout (layout of out): dq, dk, dv receive
+ * dL/dq, dL/dk, dL/dv (layouts of q, k, v).  For every row, with the scores
+ * s_j and weights a_j of steps 1 and 2:
+ *
+ *   4. g_j      = dL/da_j = dout . v_j           (step 3: o = sum_j a_j v_j)
+ *   5. dL/ds_i  = sum_j g_j da_j/ds_i with the formula page's derivative of the
+ *                 weights by the scores, da_j/ds_i = a_j (delta_ij - a_i)
+ *                 (証明, the step after the temperature form), which sums to
+ *                 dL/ds_i = a_i (g_i - sum_j a_j g_j)
+ *   6. dq      += scale * sum_j dL/ds_j k_j        (step 1: s_j = scale q . k_j)
+ *      dk_j    += scale * dL/ds_j q
+ *      dv_j    += a_j dout                        (step 3)
+ *
+ * Removed keys (mask, padding, rows past Lk) get no gradient; a row with no
+ * visible key contributes nothing.  (b, h) pairs are independent and the rows
+ * of one pair are visited in order, so no result depends on the thread count.
+ * Returns as oracle_mha_f64.
+ */
+int oracle_mha_bwd_f64(const double* q, const double* k, const double* v,
+                       const double* dout, double* dq, double* dk, double* dv,
+                       int64_t B, int64_t H, int64_t Lq, int64_t Lk, int64_t d,
+                       int mask_kind, const int32_t* key_lens, double scale,
+                       int n_threads)
+{
+    if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || d < 1) return 1;
+    if (mask_kind != ORACLE_MASK_NONE && mask_kind != ORACLE_MASK_CAUSAL &&
+        mask_kind != ORACLE_MASK_KEY_PADDING)
+        return 1;
+    if (mask_kind == ORACLE_MASK_CAUSAL && Lq != Lk) return 1;
+    if (mask_kind == ORACLE_MASK_KEY_PADDING && key_lens == NULL && B > 0) return 1;
+    if (B * H == 0) return 0;
+    if (Lq > 0 && (q == NULL || dout == NULL || dq == NULL)) return 1;
+    if (Lk > 0 && (k == NULL || v == NULL || dk == NULL || dv == NULL)) return 1;
+    for (int64_t x = 0; x < B * Lk * H * d; ++x) {
+        dk[x] = 0.0;
+        dv[x] = 0.0;
+    }
+
+#ifdef _OPENMP
+    if (n_threads <= 0) n_threads = omp_get_max_threads();
+#else
+    n_threads = 1;
+#endif
+    /* weights a and upstream gradients g: 2 Lk doubles per thread */
+    const int64_t per_thread = 2 * (Lk > 0 ? Lk : 1);
+    double* scratch = (double*)malloc((size_t)n_threads * (size_t)per_thread * sizeof(double));
+    if (scratch == NULL) return 2;
+    const int64_t pairs = B * H;
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(n_threads) schedule(dynamic, 1)
+#endif
+    for (int64_t bh = 0; bh < pairs; ++bh) {
+#ifdef _OPENMP
+        double* a = scratch + (int64_t)omp_get_thread_num() * per_thread;
+#else
+        double* a = scratch;
+#endif
+        double* g = a + per_thread / 2;
+        const int64_t b = bh / H, h = bh % H;
+        const int64_t rs = H * d;  /* stride between consecutive rows of one head */
+        const int64_t kv_off = (b * Lk * H + h) * d;  /* key 0 of head h */
+        const double* k_bh = k ? k + kv_off : NULL;
+        const double* v_bh = v ? v + kv_off : NULL;
+        double* dk_bh = dk ? dk + kv_off : NULL;
+        double* dv_bh = dv ? dv + kv_off : NULL;
+        for (int64_t i = 0; i < Lq; ++i) {
+            const int64_t row_off = ((b * Lq + i) * H + h) * d;  /* row i of head h */
+            const double* q_row = q + row_off;
+            const double* do_row = dout + row_off;
+            double* dq_row = dq + row_off;
+            for (int64_t c = 0; c < d; ++c) dq_row[c] = 0.0;
+            const int64_t n = visible_keys(i, b, Lk, mask_kind, key_lens);
+            if (n == 0) continue;
+            /* steps 1-2: scores and weights (row maximum taken out) */
+            double m = -INFINITY;
+            for (int64_t j = 0; j < n; ++j) {
+                double dot = 0.0;
+                for (int64_t c = 0; c < d; ++c) dot += q_row[c] * k_bh[j * rs + c];
+                a[j] = scale * dot;
+                if (a[j] > m) m = a[j];
+            }
+            double sum = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+                a[j] = exp(a[j] - m);
+                sum += a[j];
+            }
+            for (int64_t j = 0; j < n; ++j) a[j] /= sum;
+            /* step 4: g_j = dout . v_j, and sum_j a_j g_j */
+            double ag = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+                double dot = 0.0;
+                for (int64_t c = 0; c < d; ++c) dot += do_row[c] * v_bh[j * rs + c];
+                g[j] = dot;
+                ag += a[j] * dot;
+            }
+            /* steps 5-6 */
+            for (int64_t j = 0; j < n; ++j) {
+                const double ds = a[j] * (g[j] - ag);
+                for (int64_t c = 0; c < d; ++c) {
+                    dq_row[c] += scale * ds * k_bh[j * rs + c];
+                    dk_bh[j * rs + c] += scale * ds * q_row[c];
+                    dv_bh[j * rs + c] += a[j] * do_row[c];
+                }
+            }
+        }
+    }
+    free(scratch);
+    return 0;
+}
+
 /* Threads the OpenMP runtime would use by default (1 without OpenMP). */
 int oracle_default_threads(void)
 {

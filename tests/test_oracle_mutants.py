@@ -6,7 +6,7 @@ import os
 import pytest
 
 import oracle
-from tests import oracle_pins
+from tests import oracle_bwd_pins, oracle_pins
 
 # (name, text in mha_oracle.c, replacement)
 C_MUTANTS = [
@@ -56,3 +56,33 @@ def test_default_scale_mutant_is_caught():
         return base.mha(q, k, v, mask_kind, key_lens, scale, threads, return_lse)
 
     assert _run_checks(mha_over_dk)
+
+
+# planted in the gradient (oracle_mha_bwd_f64); the forward stays correct
+BWD_MUTANTS = [
+    ("bwd_jacobian_mean_dropped", "const double ds = a[j] * (g[j] - ag);", "const double ds = a[j] * g[j];"),
+    ("bwd_jacobian_sign", "const double ds = a[j] * (g[j] - ag);", "const double ds = a[j] * (ag - g[j]);"),
+    ("bwd_dq_scale_dropped", "dq_row[c] += scale * ds * k_bh[j * rs + c];", "dq_row[c] += ds * k_bh[j * rs + c];"),
+    ("bwd_dv_from_ds", "dv_bh[j * rs + c] += a[j] * do_row[c];", "dv_bh[j * rs + c] += ds * do_row[c];"),
+    ("bwd_dk_from_keys", "dk_bh[j * rs + c] += scale * ds * q_row[c];", "dk_bh[j * rs + c] += scale * ds * k_bh[j * rs + c];"),
+    ("bwd_g_from_keys", "dot += do_row[c] * v_bh[j * rs + c];", "dot += do_row[c] * k_bh[j * rs + c];"),
+    ("bwd_weights_unnormalised", "for (int64_t j = 0; j < n; ++j) a[j] /= sum;", ""),
+    ("bwd_score_scale_dropped", "a[j] = scale * dot;", "a[j] = dot;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", BWD_MUTANTS, ids=[m[0] for m in BWD_MUTANTS])
+def test_bwd_mutant_is_caught(tmp_path, name, old, new):
+    src = open(oracle.SOURCE, encoding="utf-8").read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique"
+    mutated = tmp_path / f"{name}.c"
+    mutated.write_text(src.replace(old, new), encoding="utf-8")
+    mutant = oracle.Oracle(oracle.compile_source(str(mutated), str(tmp_path / f"lib{name}.so")))
+    failed = []
+    for check in oracle_bwd_pins.ALL_BWD_CHECKS:
+        try:
+            check(oracle.mha, mutant.mha_bwd)
+        except (AssertionError, ValueError, IndexError):
+            failed.append(check.__name__)
+    assert failed, f"mutant {name} passed every gradient pin"
+
