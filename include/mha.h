@@ -132,6 +132,37 @@ int mha_fwd_f32_lse(const void* q, const void* k, const void* v, void* out, floa
                     const int32_t* key_lens, float scale, void* stream);
 
 /*
+ * mha_bwd -- gradient of mha_fwd for a loss L, given dL/dout (bf16).
+ * With the row weights a_ij = exp(s_ij - lse_i) recomputed from q, k and the
+ * forward's lse, g_ij = dout_i . v_j, and the formula page's derivative of
+ * the weights by the scores (transformer-attention, section 証明:
+ * da_j/ds_i = a_j (delta_ij - a_i)):
+ *     dS_ij = a_ij (g_ij - D_i),  D_i = dout_i . out_i,
+ *     dv_j = sum_i a_ij dout_i,  dk_j = scale sum_i dS_ij q_i,
+ *     dq_i = scale sum_j dS_ij k_j
+ * over the visible (query, key) pairs of mask_kind / key_lens; keys no query
+ * sees get zero gradient.
+ *   q, k, v, out  the forward's inputs and output (bf16, layouts of mha_fwd).
+ *   dout          device bf16 [B, Lq, H, d_k], 16-byte aligned.
+ *   lse           device float32 [B, H, Lq] from mha_fwd_lse on the same inputs.
+ *   dq, dk, dv    device bf16 in the layouts of q, k, v, 16-byte aligned;
+ *                 overlapping no input and each other (MHA_ERR_ALIAS).
+ *   workspace     device scratch of mha_bwd_workspace_bytes(...) bytes
+ *                 (D_i, float32), 16-byte aligned, owned by the caller.
+ *   Other arguments as mha_fwd; d_k 64 or 128.
+ * Products on the tensor cores in float32; the weights and dS are rounded to
+ * bf16 before their products, the gradients to bf16 at the end.
+ * Returns MHA_OK once enqueued, or an argument / workspace error code.
+ */
+int mha_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+            const float* lse, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk,
+            int d_k, int mask_kind, const int32_t* key_lens, float scale, void* workspace,
+            size_t workspace_bytes, void* stream);
+
+/* mha_bwd_workspace_bytes -- workspace mha_bwd needs (0 on bad sizes). */
+size_t mha_bwd_workspace_bytes(int B, int H, int Lq, int Lk, int d_k);
+
+/*
  * mha_decode -- one decode step of attention over a key/value cache, bf16.
  * At inference the decoder emits one token per step and runs again on the
  * sequence extended by it (cookipedia article, section "Transformer 全体";

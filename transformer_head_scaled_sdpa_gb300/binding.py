@@ -64,6 +64,11 @@ def lib():
             h.mha_fwd_lse.argtypes = _FWD_LSE_ARGS
             h.mha_fwd_f32_lse.restype = _c_i
             h.mha_fwd_f32_lse.argtypes = _FWD_LSE_ARGS
+            h.mha_bwd.restype = _c_i
+            h.mha_bwd.argtypes = [_c_p] * 9 + [_c_i] * 6 + [_c_p, ctypes.c_float, _c_p,
+                                                            ctypes.c_size_t, _c_p]
+            h.mha_bwd_workspace_bytes.restype = ctypes.c_size_t
+            h.mha_bwd_workspace_bytes.argtypes = [_c_i] * 5
             h.mha_decode.restype = _c_i
             h.mha_decode.argtypes = [_c_p] * 5 + [_c_i] * 4 + [_c_p, ctypes.c_float, _c_p,
                                                                ctypes.c_size_t, _c_p]
@@ -173,6 +178,42 @@ def mha_fwd_f32(q, k, v, out=None, mask_kind: int = 0, key_lens=None, scale: flo
     ``(out, lse)`` with ``return_lse``."""
     return _call_fwd("mha_fwd_f32", torch.float32, q, k, v, out, mask_kind, key_lens, scale,
                      stream, lse, return_lse)
+
+
+def mha_bwd(q, k, v, out, dout, lse, mask_kind: int = 0, key_lens=None, scale: float = 0.0,
+            dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradient of mha_fwd (bf16): returns (dq, dk, dv) for dL/dout = ``dout``,
+    given the forward's ``out`` and ``lse`` (from mha_fwd(..., return_lse=True))."""
+    B, H, Lq, Lk, d = _shape(q, k, v)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _check_tensor(t, n, torch.bfloat16, "cuda")
+    if tuple(out.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("out and dout must have q's shape")
+    _check_tensor(lse, "lse", torch.float32, "cuda")
+    if tuple(lse.shape) != (B, H, Lq):
+        raise ValueError("lse must be [B, H, Lq]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, ref, n in ((dq, q, "dq"), (dk, k, "dk"), (dv, v, "dv")):
+        _check_tensor(t, n, torch.bfloat16, "cuda")
+        if tuple(t.shape) != tuple(ref.shape):
+            raise ValueError(f"{n} must have the shape of its input")
+    lens_ptr = None
+    if key_lens is not None:
+        _check_tensor(key_lens, "key_lens", torch.int32, "cuda")
+        lens_ptr = key_lens.data_ptr()
+    need = int(lib().mha_bwd_workspace_bytes(B, H, Lq, Lk, d))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check_tensor(workspace, "workspace", torch.uint8, "cuda")
+    rc = lib().mha_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                       dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                       dv.data_ptr(), B, H, Lq, Lk, d, int(mask_kind), lens_ptr, float(scale),
+                       workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "mha_bwd")
+    return dq, dk, dv
 
 
 def decode_workspace_bytes(B, H, Lk, d_k) -> int:

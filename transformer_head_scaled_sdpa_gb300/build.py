@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libmha.so")
 
-SOURCES = ["mha_abi.cu", "mha_fwd_bf16.cu", "mha_fwd_f32.cu", "mha_decode.cu"]
+SOURCES = ["mha_abi.cu", "mha_fwd_bf16.cu", "mha_fwd_f32.cu", "mha_decode.cu", "mha_bwd.cu"]
 HEADERS = [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "kernels.h"),
            os.path.join(INCLUDE, "mha.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

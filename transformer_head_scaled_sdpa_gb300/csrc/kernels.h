@@ -83,6 +83,27 @@ int decode_splits(int B, int H, int Lk);
 // than one split, the combine kernel.
 cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream, LaunchInfo* info);
 
+// Gradient of the bf16 forward.
+struct BwdParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // [B, L, H, d] bf16, box {64, 1, 128, 1}, 128-byte swizzle
+  const void* out;    // [B, Lq, H, d] bf16 forward output
+  const void* dout;   // [B, Lq, H, d] bf16 dL/dO
+  const float* lse;   // [B, H, Lq] forward row log-sum-exp (natural log)
+  float* dvec;        // [B, H, Lq] workspace: D_i = dO_i . O_i
+  void* dq;           // [B, Lq, H, d] bf16
+  void* dk;           // [B, Lk, H, d] bf16
+  void* dv;           // [B, Lk, H, d] bf16
+  const int32_t* key_lens;
+  DeviceStatus* status;
+  int B, H, Lq, Lk;
+  int mask_kind;
+  float scale;        // multiplier of q . k
+  float scale_log2;   // scale * log2(e)
+};
+
+// Launches the gradient: the D pre-pass, the dK/dV kernel and the dQ kernel.
+cudaError_t launch_bwd(const BwdParams& p, int d, cudaStream_t stream, LaunchInfo* info);
+
 // Launches the bf16 tcgen05 forward for d in {64, 128}.
 cudaError_t launch_fwd_bf16(const Bf16Params& p, int d, cudaStream_t stream, LaunchInfo* info);
 

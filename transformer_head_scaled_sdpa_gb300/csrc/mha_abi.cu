@@ -418,6 +418,85 @@ int mha_decode_static(const void* q, const void* k_cache, const void* v_cache, v
 
 size_t mha_decode_static_scratch_bytes(void) { return kDecodeStaticScratchBytes; }
 
+size_t mha_bwd_workspace_bytes(int B, int H, int Lq, int Lk, int d_k) {
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || (d_k != 64 && d_k != 128)) return 0;
+  return align256(static_cast<size_t>(B) * H * Lq * 4);
+}
+
+int mha_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+            const float* lse, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk,
+            int d_k, int mask_kind, const int32_t* key_lens, float scale, void* workspace,
+            size_t workspace_bytes, void* stream) {
+  t_info = mha::LaunchInfo{};
+  bool empty = false;
+  Sizes sz;
+  // the forward's checks on q, k, v, out (and the mask, scale, sizes)
+  int rc = check_args(q, k, v, const_cast<void*>(out), B, H, Lq, Lk, d_k, mask_kind, key_lens,
+                      scale, 2, 16, &empty, &sz);
+  if (rc != MHA_OK) return rc;
+  if (d_k != 64 && d_k != 128) return MHA_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh == 0) return MHA_OK;
+  const size_t qb = sz.q_elems * 2, kb = sz.kv_elems * 2;
+  const size_t lb = static_cast<size_t>(bh) * Lq * 4;
+  if ((Lq > 0 && (!dout || !dq || !lse)) || (Lk > 0 && (!dk || !dv))) return MHA_ERR_NULL;
+  const uintptr_t mis = (reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
+                         reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) &
+                        15u;
+  if (mis || (reinterpret_cast<uintptr_t>(lse) & 3u)) return MHA_ERR_UNSUPPORTED;
+  // gradients overlap nothing they are computed from, nor each other
+  const void* ins[6] = {q, k, v, out, dout, lse};
+  const size_t ins_b[6] = {qb, kb, kb, qb, qb, lb};
+  void* outs[3] = {dq, dk, dv};
+  const size_t outs_b[3] = {qb, kb, kb};
+  for (int o = 0; o < 3; ++o) {
+    for (int i = 0; i < 6; ++i)
+      if (overlaps(outs[o], outs_b[o], ins[i], ins_b[i])) return MHA_ERR_ALIAS;
+    for (int o2 = o + 1; o2 < 3; ++o2)
+      if (overlaps(outs[o], outs_b[o], outs[o2], outs_b[o2])) return MHA_ERR_ALIAS;
+  }
+  const size_t need = align256(lb);
+  if (Lq > 0 && Lk > 0 && (!workspace || workspace_bytes < need ||
+                            (reinterpret_cast<uintptr_t>(workspace) & 15u)))
+    return MHA_ERR_WORKSPACE;
+  DeviceState* dev = nullptr;
+  rc = device_state(&dev);
+  if (rc != MHA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // no queries: no gradient reaches the keys; no keys: every row's output is 0
+  if (Lq == 0 || Lk == 0) {
+    if (Lq > 0 && cudaMemsetAsync(dq, 0, qb, s) != cudaSuccess) return MHA_ERR_LAUNCH;
+    if (Lk > 0 && (cudaMemsetAsync(dk, 0, kb, s) != cudaSuccess ||
+                   cudaMemsetAsync(dv, 0, kb, s) != cudaSuccess))
+      return MHA_ERR_LAUNCH;
+    return MHA_OK;
+  }
+  if (bh * ((Lk + 127) / 128) > 0x7fffffffll || bh * ((Lq + 127) / 128) > 0x7fffffffll)
+    return MHA_ERR_SHAPE;
+  mha::BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (!encode_map(&p.tm_q, q, B, Lq, H, d_k) || !encode_map(&p.tm_k, k, B, Lk, H, d_k) ||
+      !encode_map(&p.tm_v, v, B, Lk, H, d_k) || !encode_map(&p.tm_do, dout, B, Lq, H, d_k))
+    return MHA_ERR_UNSUPPORTED;
+  p.out = out;
+  p.dout = dout;
+  p.lse = lse;
+  p.dvec = static_cast<float*>(workspace);
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.key_lens = key_lens;
+  p.status = dev->status;
+  p.B = B;
+  p.H = H;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.mask_kind = mask_kind;
+  p.scale = effective_scale(scale, d_k);
+  p.scale_log2 = p.scale * kLog2e;
+  return mha::launch_bwd(p, d_k, s, &t_info) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
+}
+
 size_t mha_fwd_host_workspace_bytes(int B, int H, int Lq, int Lk, int d_k, int elem_bytes) {
   if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || d_k < 1) return 0;
   if (elem_bytes != 2 && elem_bytes != 4) return 0;

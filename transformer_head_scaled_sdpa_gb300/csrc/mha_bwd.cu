@@ -1,0 +1,623 @@
+// mha_bwd.cu -- gradient of the bf16 attention forward (dQ, dK, dV), sm_103a.
+//
+// For a loss L with dL/dO given, every row i of (b, h) has weights
+// a_ij = exp(s_ij - lse_i) (s = scale * q . k over its visible keys, lse the
+// forward's row log-sum-exp) and, with g_ij = dO_i . v_j, the formula page's
+// derivative of the weights by the scores (transformer-attention, section 証明:
+// da_j/ds_i = a_j (delta_ij - a_i)) gives
+//   dS_ij = a_ij (g_ij - D_i),   D_i = sum_j a_ij g_ij = dO_i . O_i
+//   dV_j  = sum_i a_ij dO_i,     dK_j = scale sum_i dS_ij q_i,
+//   dQ_i  = scale sum_j dS_ij k_j.
+// Three kernels:
+//   bwd_prep_kernel   D_i = dO_i . O_i (float32, one warp per row).
+//   bwd_dkdv_kernel   one CTA per (b, h, 128-key tile); the query tiles that
+//                     see the keys stream through a two-stage ring.  Per query
+//                     tile: S^T = K Q^T and dP^T = V dO^T on the tensor cores
+//                     (keys on TMEM lanes), the four gradient warps turn them
+//                     into P^T and dS^T (bf16, written over S^T and dP^T in
+//                     TMEM), and dV += P^T dO, dK += dS^T Q accumulate in TMEM
+//                     (A operands from TMEM).
+//   bwd_dq_kernel     one CTA per (b, h, 128-query tile); the key tiles it
+//                     sees stream through a two-stage ring.  S = Q K^T and
+//                     dP = dO V^T, then dS (bf16, over S), then dQ += dS K.
+// Every operand reuses the forward's shared-memory layout (128-row tiles of
+// 64-feature, 128-byte swizzled chunks): K-major as an operand whose
+// reduction runs over d, MN-major where it runs over the rows.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+
+namespace mha {
+namespace {
+
+constexpr int kBwdThreads = 192;  // warps 0-3 gradient, 4 MMA, 5 TMA
+constexpr int kRoleBwdProducer = 8, kRoleBwdMma = 9, kRoleBwdGrad = 10;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int KCH = D / 64;
+  static constexpr int CHUNK = 128 * 128;
+  static constexpr int TILE = KCH * CHUNK;     // one 128-row operand tile
+  // fixed tiles A0, A1 (K, V or Q, dO) and a two-stage ring of tile pairs
+  static constexpr int OFF_A0 = 0;
+  static constexpr int OFF_A1 = TILE;
+  static constexpr int OFF_RING = 2 * TILE;    // stage s: pair at OFF_RING + s * 2 * TILE
+  static constexpr int OFF_VEC = OFF_RING + 4 * TILE;  // lse2[128], D[128] (dK/dV kernel)
+  static constexpr int OFF_BAR = OFF_VEC + 2 * 128 * 4;
+  static constexpr int NBAR = 10;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;  // tmem slot, abort flag
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  // TMEM: accumulators of the two score-shaped matrices, then the d-wide ones
+  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_ACC0 = 256, TM_ACC1 = 256 + D;
+  static constexpr uint32_t TMEM_COLS = 512;
+};
+
+// barrier ids
+enum { kFixFull = 0, kRingFull = 1, kRingEmpty = 3, kSdFull = 5, kPdFull = 6, kAccDone = 7,
+       kDrain = 8 };
+
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// ---------------------------------------------------------------------------
+// D_i = dO_i . O_i, one warp per row (b, i, h) of [B, Lq, H, d]; stored [B, H, Lq]
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ BwdParams p) {
+  const long long rows = static_cast<long long>(p.B) * p.H * p.Lq;
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  if (row >= rows) return;
+  const int h = static_cast<int>(row % p.H);
+  const int i = static_cast<int>((row / p.H) % p.Lq);
+  const int b = static_cast<int>(row / (static_cast<long long>(p.H) * p.Lq));
+  const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(p.out) + row * D;
+  const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(p.dout) + row * D;
+  float acc = 0.f;
+#pragma unroll
+  for (int c = lane; c < D; c += 32) acc = fmaf(__bfloat162float(o[c]), __bfloat162float(g[c]), acc);
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (lane == 0) p.dvec[(static_cast<size_t>(b) * p.H + h) * p.Lq + i] = acc;
+}
+
+// Visible keys of sequence b (key padding), all keys otherwise.
+__device__ __forceinline__ int kv_len_of(const BwdParams& p, int b) {
+  int n = p.Lk;
+  if (p.mask_kind == kMaskKeyPadding) {
+    const int len = __ldg(p.key_lens + b);
+    n = len < 0 ? 0 : (len > p.Lk ? p.Lk : len);
+  }
+  return n;
+}
+
+// ---------------------------------------------------------------------------
+// dK, dV: one CTA per (b, h, key tile)
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t s_base = smem_u32(smem);
+  auto bar = [&](int id) { return s_base + C::OFF_BAR + 8u * id; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  float* lse2_s = reinterpret_cast<float*>(smem + C::OFF_VEC);
+  float* dvec_s = lse2_s + 128;
+  const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+
+  const int n_kt = (p.Lk + 127) / 128;
+  const int unit = static_cast<int>(blockIdx.x);
+  const int kt = unit % n_kt;
+  const int bh = unit / n_kt;
+  const int b = bh / p.H, h = bh % p.H;
+  const int k0 = kt * 128;
+  const int kv_len = kv_len_of(p, b);
+  const int n_qt = (p.Lq + 127) / 128;
+  // query tiles that see a key of this tile (causal: from the diagonal on)
+  const int qt_begin = (p.mask_kind == kMaskCausal) ? kt : 0;
+  const int n_iter = (k0 < kv_len) ? (n_qt - qt_begin) : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kFixFull), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kRingFull + s), 1);
+      mbar_init(bar(kRingEmpty + s), 1);
+    }
+    mbar_init(bar(kSdFull), 1);
+    mbar_init(bar(kPdFull), 128);
+    mbar_init(bar(kAccDone), 1);
+    mbar_init(bar(kDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 5) {
+    // ---- TMA: K and V of this key tile once, then Q_i, dO_i per query tile
+    if (lane == 0 && n_iter > 0) {
+      mbar_arrive_expect_tx(bar(kFixFull), 2 * C::TILE);
+      for (int c = 0; c < C::KCH; ++c) {
+        tma_load_4d(s_base + C::OFF_A0 + c * C::CHUNK, &p.tm_k, bar(kFixFull), 64 * c, h, k0, b);
+        tma_load_4d(s_base + C::OFF_A1 + c * C::CHUNK, &p.tm_v, bar(kFixFull), 64 * c, h, k0, b);
+      }
+      int it = 0;
+      for (; it < n_iter; ++it) {
+        const int s = it & 1;
+        if (it >= 2 && !mbar_wait(bar(kRingEmpty + s), ((it >> 1) - 1) & 1, abort_flag, p.status,
+                                  kRoleBwdProducer * 64 + s))
+          break;
+        const int q0 = (qt_begin + it) * 128;
+        const uint32_t dst = s_base + C::OFF_RING + s * 2 * C::TILE;
+        mbar_arrive_expect_tx(bar(kRingFull + s), 2 * C::TILE);
+        for (int c = 0; c < C::KCH; ++c) {
+          tma_load_4d(dst + c * C::CHUNK, &p.tm_q, bar(kRingFull + s), 64 * c, h, q0, b);
+          tma_load_4d(dst + C::TILE + c * C::CHUNK, &p.tm_do, bar(kRingFull + s), 64 * c, h, q0, b);
+        }
+      }
+      // every copy started lands before the CTA exits
+      volatile int never = 0;
+      mbar_wait(bar(kFixFull), 0, &never, p.status, kRoleBwdProducer * 64 + 8);
+      for (int t = (it > 2 ? it - 2 : 0); t < it; ++t)
+        mbar_wait(bar(kRingFull + (t & 1)), (t >> 1) & 1, &never, p.status,
+                  kRoleBwdProducer * 64 + 9);
+    }
+    __syncwarp();
+  } else if (warp == 4) {
+    // ---- MMA issuer
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);  // K-major A and B
+    constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);     // B MN-major
+    const uint64_t dA0 = smem_desc_sw128(s_base + C::OFF_A0, 16, 1024);   // K tile, K-major
+    const uint64_t dA1 = smem_desc_sw128(s_base + C::OFF_A1, 16, 1024);   // V tile, K-major
+    bool ok = true;
+    if (n_iter > 0)
+      ok = mbar_wait(bar(kFixFull), 0, abort_flag, p.status, kRoleBwdMma * 64 + kFixFull);
+    for (int it = 0; ok && it < n_iter; ++it) {
+      const int s = it & 1;
+      const uint32_t ring = s_base + C::OFF_RING + s * 2 * C::TILE;
+      if (!mbar_wait(bar(kRingFull + s), (it >> 1) & 1, abort_flag, p.status,
+                     kRoleBwdMma * 64 + kRingFull + s)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t dQk = smem_desc_sw128(ring, 16, 1024);                 // Q, K-major
+      const uint64_t dDk = smem_desc_sw128(ring + C::TILE, 16, 1024);       // dO, K-major
+      const uint64_t dQm = smem_desc_sw128(ring, C::CHUNK, 1024);           // Q, MN-major
+      const uint64_t dDm = smem_desc_sw128(ring + C::TILE, C::CHUNK, 1024); // dO, MN-major
+      if (elect_one()) {
+        // S^T = K Q^T, dP^T = V dO^T (keys on lanes, queries on columns)
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
+          umma_ss(tmem + C::TM_S, dA0 + off, dQk + off, idesc_s, ks > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
+          umma_ss(tmem + C::TM_DP, dA1 + off, dDk + off, idesc_s, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(kSdFull));
+      }
+      __syncwarp();
+      if (!mbar_wait(bar(kPdFull), it & 1, abort_flag, p.status, kRoleBwdMma * 64 + kPdFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (elect_one()) {
+        // dV += P^T dO, dK += dS^T Q (16 queries = 8 TMEM columns of A per step)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma_ts(tmem + C::TM_ACC0, tmem + C::TM_S + 8u * ks,
+                  dDm + static_cast<uint64_t>((ks * 2048) >> 4), idesc_o, (ks > 0 || it > 0) ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma_ts(tmem + C::TM_ACC1, tmem + C::TM_DP + 8u * ks,
+                  dQm + static_cast<uint64_t>((ks * 2048) >> 4), idesc_o, (ks > 0 || it > 0) ? 1u : 0u);
+        umma_commit(bar(kRingEmpty + s));
+        if (it + 1 == n_iter) umma_commit(bar(kAccDone));
+      }
+      __syncwarp();
+    }
+    if (elect_one()) umma_commit(bar(kDrain));
+    __syncwarp();
+    volatile int never = 0;
+    mbar_wait(bar(kDrain), 0, &never, p.status, kRoleBwdMma * 64 + kDrain);
+  } else {
+    // ---- gradient warps: thread r owns key row k0 + r (TMEM lane r)
+    const int quarter = warp;
+    const int r = quarter * 32 + lane;
+    const int key = k0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float c2 = p.scale_log2;
+    bool ok = true;
+    for (int it = 0; ok && it < n_iter; ++it) {
+      const int q0 = (qt_begin + it) * 128;
+      // this query tile's lse (log2 units) and D into shared memory; the
+      // previous tile's readers are past their barrier.  (A named barrier
+      // cannot time out: after each one the abort flag is checked, and a warp
+      // that gives up arrives once on it on its way out.)
+      named_barrier(1, 128);
+      if (*abort_flag) {
+        ok = false;
+        break;
+      }
+      {
+        const int qi = q0 + r;
+        float l2 = -INFINITY, dv = 0.f;
+        if (qi < p.Lq) {
+          const size_t idx = (static_cast<size_t>(b) * p.H + h) * p.Lq + qi;
+          l2 = p.lse[idx] * 1.4426950408889634f;
+          dv = p.dvec[idx];
+        }
+        lse2_s[r] = l2;
+        dvec_s[r] = dv;
+      }
+      named_barrier(1, 128);
+      if (*abort_flag) {
+        ok = false;
+        break;
+      }
+      if (!mbar_wait(bar(kSdFull), it & 1, abort_flag, p.status, kRoleBwdGrad * 64 + kSdFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // the queries this key row may be seen by: q >= key under the causal mask
+#pragma unroll 1
+      for (int c32 = 0; c32 < 4; ++c32) {
+        uint32_t sr[32], pr[32];
+        tmem_ld32(tmem + C::TM_S + lane_off + 32u * c32, sr);
+        tmem_ld32(tmem + C::TM_DP + lane_off + 32u * c32, pr);
+        tmem_ld_wait();
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          float pp[2], dd[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col = 32 * c32 + t + u;
+            const int qi = q0 + col;
+            const bool vis = key < kv_len && qi < p.Lq &&
+                             !(p.mask_kind == kMaskCausal && key > qi) && lse2_s[col] != -INFINITY;
+            const float pv = vis ? ex2_approx(fmaf(__uint_as_float(sr[t + u]), c2, -lse2_s[col])) : 0.f;
+            pp[u] = pv;
+            // dS = P (dP - D); P rounded to bf16 as in the dV product
+            dd[u] = bf16_round(pv) * (__uint_as_float(pr[t + u]) - dvec_s[col]);
+          }
+          pk[t >> 1] = pack_bf16x2(pp[0], pp[1]);
+          dk[t >> 1] = pack_bf16x2(dd[0], dd[1]);
+        }
+        // P^T over the first half of S^T, dS^T over the first half of dP^T
+        // (columns already read: chunk c32 writes columns 16 c32 .. 16 c32 + 15)
+        tmem_st16(tmem + C::TM_S + lane_off + 16u * c32, pk);
+        tmem_st16(tmem + C::TM_DP + lane_off + 16u * c32, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(kPdFull));
+    }
+    // ---- epilogue: dV and scale * dK rows to global (rows past Lk skipped)
+    if (ok && n_iter > 0)
+      ok = mbar_wait(bar(kAccDone), 0, abort_flag, p.status, kRoleBwdGrad * 64 + kAccDone);
+    if (ok) {
+      tc_fence_after();
+      const size_t row_off = ((static_cast<size_t>(b) * p.Lk + key) * p.H + h) * D;
+      __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(p.dv) + row_off;
+      __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(p.dk) + row_off;
+#pragma unroll 1
+      for (int c32 = 0; c32 < D / 32; ++c32) {
+        uint32_t a[32], k[32];
+        if (n_iter > 0) {
+          tmem_ld32(tmem + C::TM_ACC0 + lane_off + 32u * c32, a);
+          tmem_ld32(tmem + C::TM_ACC1 + lane_off + 32u * c32, k);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) a[t] = k[t] = 0u;
+        }
+        if (key < p.Lk) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 wa, wk;
+            wa.x = pack_bf16x2(__uint_as_float(a[8 * v4 + 0]), __uint_as_float(a[8 * v4 + 1]));
+            wa.y = pack_bf16x2(__uint_as_float(a[8 * v4 + 2]), __uint_as_float(a[8 * v4 + 3]));
+            wa.z = pack_bf16x2(__uint_as_float(a[8 * v4 + 4]), __uint_as_float(a[8 * v4 + 5]));
+            wa.w = pack_bf16x2(__uint_as_float(a[8 * v4 + 6]), __uint_as_float(a[8 * v4 + 7]));
+            wk.x = pack_bf16x2(__uint_as_float(k[8 * v4 + 0]) * p.scale, __uint_as_float(k[8 * v4 + 1]) * p.scale);
+            wk.y = pack_bf16x2(__uint_as_float(k[8 * v4 + 2]) * p.scale, __uint_as_float(k[8 * v4 + 3]) * p.scale);
+            wk.z = pack_bf16x2(__uint_as_float(k[8 * v4 + 4]) * p.scale, __uint_as_float(k[8 * v4 + 5]) * p.scale);
+            wk.w = pack_bf16x2(__uint_as_float(k[8 * v4 + 6]) * p.scale, __uint_as_float(k[8 * v4 + 7]) * p.scale);
+            *reinterpret_cast<uint4*>(dv_row + 32 * c32 + 8 * v4) = wa;
+            *reinterpret_cast<uint4*>(dk_row + 32 * c32 + 8 * v4) = wk;
+          }
+        }
+      }
+    } else {
+      named_barrier_arrive(1, 128);  // release a gradient warp blocked on the barrier
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dQ: one CTA per (b, h, query tile)
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t s_base = smem_u32(smem);
+  auto bar = [&](int id) { return s_base + C::OFF_BAR + 8u * id; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+
+  const int n_qt = (p.Lq + 127) / 128;
+  const int unit = static_cast<int>(blockIdx.x);
+  const int qt = unit % n_qt;
+  const int bh = unit / n_qt;
+  const int b = bh / p.H, h = bh % p.H;
+  const int q0 = qt * 128;
+  const int kv_len = kv_len_of(p, b);
+  int n_kt = (kv_len + 127) / 128;
+  if (p.mask_kind == kMaskCausal && n_kt > qt + 1) n_kt = qt + 1;
+  const int n_iter = n_kt;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kFixFull), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kRingFull + s), 1);
+      mbar_init(bar(kRingEmpty + s), 1);
+    }
+    mbar_init(bar(kSdFull), 1);
+    mbar_init(bar(kPdFull), 128);
+    mbar_init(bar(kAccDone), 1);
+    mbar_init(bar(kDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 5) {
+    // ---- TMA: Q_i and dO_i once, then K_j, V_j per key tile
+    if (lane == 0 && n_iter > 0) {
+      mbar_arrive_expect_tx(bar(kFixFull), 2 * C::TILE);
+      for (int c = 0; c < C::KCH; ++c) {
+        tma_load_4d(s_base + C::OFF_A0 + c * C::CHUNK, &p.tm_q, bar(kFixFull), 64 * c, h, q0, b);
+        tma_load_4d(s_base + C::OFF_A1 + c * C::CHUNK, &p.tm_do, bar(kFixFull), 64 * c, h, q0, b);
+      }
+      int it = 0;
+      for (; it < n_iter; ++it) {
+        const int s = it & 1;
+        if (it >= 2 && !mbar_wait(bar(kRingEmpty + s), ((it >> 1) - 1) & 1, abort_flag, p.status,
+                                  kRoleBwdProducer * 64 + 16 + s))
+          break;
+        const int k0 = it * 128;
+        const uint32_t dst = s_base + C::OFF_RING + s * 2 * C::TILE;
+        mbar_arrive_expect_tx(bar(kRingFull + s), 2 * C::TILE);
+        for (int c = 0; c < C::KCH; ++c) {
+          tma_load_4d(dst + c * C::CHUNK, &p.tm_k, bar(kRingFull + s), 64 * c, h, k0, b);
+          tma_load_4d(dst + C::TILE + c * C::CHUNK, &p.tm_v, bar(kRingFull + s), 64 * c, h, k0, b);
+        }
+      }
+      volatile int never = 0;
+      mbar_wait(bar(kFixFull), 0, &never, p.status, kRoleBwdProducer * 64 + 24);
+      for (int t = (it > 2 ? it - 2 : 0); t < it; ++t)
+        mbar_wait(bar(kRingFull + (t & 1)), (t >> 1) & 1, &never, p.status,
+                  kRoleBwdProducer * 64 + 25);
+    }
+    __syncwarp();
+  } else if (warp == 4) {
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+    const uint64_t dQk = smem_desc_sw128(s_base + C::OFF_A0, 16, 1024);   // Q, K-major
+    const uint64_t dDk = smem_desc_sw128(s_base + C::OFF_A1, 16, 1024);   // dO, K-major
+    bool ok = true;
+    if (n_iter > 0)
+      ok = mbar_wait(bar(kFixFull), 0, abort_flag, p.status, kRoleBwdMma * 64 + 16 + kFixFull);
+    for (int it = 0; ok && it < n_iter; ++it) {
+      const int s = it & 1;
+      const uint32_t ring = s_base + C::OFF_RING + s * 2 * C::TILE;
+      if (!mbar_wait(bar(kRingFull + s), (it >> 1) & 1, abort_flag, p.status,
+                     kRoleBwdMma * 64 + 16 + kRingFull + s)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t dKk = smem_desc_sw128(ring, 16, 1024);                 // K, K-major
+      const uint64_t dVk = smem_desc_sw128(ring + C::TILE, 16, 1024);       // V, K-major
+      const uint64_t dKm = smem_desc_sw128(ring, C::CHUNK, 1024);           // K, MN-major
+      if (elect_one()) {
+        // S = Q K^T, dP = dO V^T (queries on lanes, keys on columns)
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
+          umma_ss(tmem + C::TM_S, dQk + off, dKk + off, idesc_s, ks > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
+          umma_ss(tmem + C::TM_DP, dDk + off, dVk + off, idesc_s, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(kSdFull));
+      }
+      __syncwarp();
+      if (!mbar_wait(bar(kPdFull), it & 1, abort_flag, p.status, kRoleBwdMma * 64 + 16 + kPdFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (elect_one()) {
+        // dQ += dS K (16 keys = 8 TMEM columns of A per step)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma_ts(tmem + C::TM_ACC0, tmem + C::TM_S + 8u * ks,
+                  dKm + static_cast<uint64_t>((ks * 2048) >> 4), idesc_o, (ks > 0 || it > 0) ? 1u : 0u);
+        umma_commit(bar(kRingEmpty + s));
+        if (it + 1 == n_iter) umma_commit(bar(kAccDone));
+      }
+      __syncwarp();
+    }
+    if (elect_one()) umma_commit(bar(kDrain));
+    __syncwarp();
+    volatile int never = 0;
+    mbar_wait(bar(kDrain), 0, &never, p.status, kRoleBwdMma * 64 + 16 + kDrain);
+  } else {
+    // ---- gradient warps: thread r owns query row q0 + r
+    const int quarter = warp;
+    const int r = quarter * 32 + lane;
+    const int qi = q0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float c2 = p.scale_log2;
+    float l2 = -INFINITY, dvv = 0.f;
+    if (qi < p.Lq) {
+      const size_t idx = (static_cast<size_t>(b) * p.H + h) * p.Lq + qi;
+      l2 = p.lse[idx] * 1.4426950408889634f;
+      dvv = p.dvec[idx];
+    }
+    bool ok = true;
+    for (int it = 0; ok && it < n_iter; ++it) {
+      if (!mbar_wait(bar(kSdFull), it & 1, abort_flag, p.status, kRoleBwdGrad * 64 + 16 + kSdFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int k0 = it * 128;
+#pragma unroll 1
+      for (int c32 = 0; c32 < 4; ++c32) {
+        uint32_t sr[32], pr[32];
+        tmem_ld32(tmem + C::TM_S + lane_off + 32u * c32, sr);
+        tmem_ld32(tmem + C::TM_DP + lane_off + 32u * c32, pr);
+        tmem_ld_wait();
+        uint32_t dk[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          float dd[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int key = k0 + 32 * c32 + t + u;
+            const bool vis = key < kv_len && qi < p.Lq &&
+                             !(p.mask_kind == kMaskCausal && key > qi) && l2 != -INFINITY;
+            const float pv = vis ? ex2_approx(fmaf(__uint_as_float(sr[t + u]), c2, -l2)) : 0.f;
+            dd[u] = bf16_round(pv) * (__uint_as_float(pr[t + u]) - dvv);
+          }
+          dk[t >> 1] = pack_bf16x2(dd[0], dd[1]);
+        }
+        tmem_st16(tmem + C::TM_S + lane_off + 16u * c32, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(kPdFull));
+    }
+    if (ok && n_iter > 0)
+      ok = mbar_wait(bar(kAccDone), 0, abort_flag, p.status, kRoleBwdGrad * 64 + 16 + kAccDone);
+    if (ok) {
+      tc_fence_after();
+      __nv_bfloat16* dq_row = reinterpret_cast<__nv_bfloat16*>(p.dq) +
+                              ((static_cast<size_t>(b) * p.Lq + qi) * p.H + h) * D;
+#pragma unroll 1
+      for (int c32 = 0; c32 < D / 32; ++c32) {
+        uint32_t a[32];
+        if (n_iter > 0) {
+          tmem_ld32(tmem + C::TM_ACC0 + lane_off + 32u * c32, a);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) a[t] = 0u;
+        }
+        if (qi < p.Lq) {
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(a[8 * v4 + 0]) * p.scale, __uint_as_float(a[8 * v4 + 1]) * p.scale);
+            w.y = pack_bf16x2(__uint_as_float(a[8 * v4 + 2]) * p.scale, __uint_as_float(a[8 * v4 + 3]) * p.scale);
+            w.z = pack_bf16x2(__uint_as_float(a[8 * v4 + 4]) * p.scale, __uint_as_float(a[8 * v4 + 5]) * p.scale);
+            w.w = pack_bf16x2(__uint_as_float(a[8 * v4 + 6]) * p.scale, __uint_as_float(a[8 * v4 + 7]) * p.scale);
+            *reinterpret_cast<uint4*>(dq_row + 32 * c32 + 8 * v4) = w;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, LaunchInfo* info) {
+  using C = BwdCfg<D>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool attr_set[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const long long rows = static_cast<long long>(p.B) * p.H * p.Lq;
+  bwd_prep_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long bh = static_cast<long long>(p.B) * p.H;
+  const long long kv_units = bh * ((p.Lk + 127) / 128);
+  const long long q_units = bh * ((p.Lq + 127) / 128);
+  bwd_dkdv_kernel<D><<<static_cast<unsigned>(kv_units), kBwdThreads, C::SMEM, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_dq_kernel<D><<<static_cast<unsigned>(q_units), kBwdThreads, C::SMEM, stream>>>(p);
+  e = cudaGetLastError();
+  if (info) {
+    info->kernels = 3;
+    info->grid = static_cast<int>(kv_units + q_units);
+    info->block = kBwdThreads;
+    info->smem = C::SMEM;
+  }
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdParams& p, int d, cudaStream_t stream, LaunchInfo* info) {
+  if (d == 64) return launch_bwd_d<64>(p, stream, info);
+  if (d == 128) return launch_bwd_d<128>(p, stream, info);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mha
