@@ -57,9 +57,9 @@ struct BwdCfg {
 enum { kFixFull = 0, kRingFull = 1, kRingEmpty = 3, kSdFull = 5, kPdFull = 6, kAccDone = 7,
        kDrain = 8 };
 
-__device__ __forceinline__ float bf16_round(float x) {
-  return __bfloat162float(__float2bfloat16_rn(x));
-}
+// bf16 halves of a packed pair -> float (exact)
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // ---------------------------------------------------------------------------
 // D_i = dO_i . O_i, one warp per row (b, i, h) of [B, Lq, H, d]; stored [B, H, Lq]
@@ -275,7 +275,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         break;
       }
       tc_fence_after();
-      // the queries this key row may be seen by: q >= key under the causal mask
+      // Every (key, query) pair of the tile is visible unless the tile holds
+      // keys past the key length, queries past Lq, or the causal diagonal.
+      const bool all_visible = k0 + 127 < kv_len && q0 + 127 < p.Lq &&
+                               !(p.mask_kind == kMaskCausal && q0 < k0 + 127);
 #pragma unroll 1
       for (int c32 = 0; c32 < 4; ++c32) {
         uint32_t sr[32], pr[32];
@@ -285,20 +288,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         uint32_t pk[16], dk[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
-          float pp[2], dd[2];
+          float pp[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int col = 32 * c32 + t + u;
-            const int qi = q0 + col;
-            const bool vis = key < kv_len && qi < p.Lq &&
-                             !(p.mask_kind == kMaskCausal && key > qi) && lse2_s[col] != -INFINITY;
-            const float pv = vis ? ex2_approx(fmaf(__uint_as_float(sr[t + u]), c2, -lse2_s[col])) : 0.f;
-            pp[u] = pv;
-            // dS = P (dP - D); P rounded to bf16 as in the dV product
-            dd[u] = bf16_round(pv) * (__uint_as_float(pr[t + u]) - dvec_s[col]);
+            const float arg = fmaf(__uint_as_float(sr[t + u]), c2, -lse2_s[col]);
+            if (all_visible) {
+              pp[u] = ex2_approx(arg);
+            } else {
+              const int qi = q0 + col;
+              const bool vis = key < kv_len && qi < p.Lq &&
+                               !(p.mask_kind == kMaskCausal && key > qi) &&
+                               lse2_s[col] != -INFINITY;
+              pp[u] = vis ? ex2_approx(arg) : 0.f;
+            }
           }
           pk[t >> 1] = pack_bf16x2(pp[0], pp[1]);
-          dk[t >> 1] = pack_bf16x2(dd[0], dd[1]);
+          // dS = P (dP - D) with P as rounded to bf16 for the dV product
+          const float d0 = bf_lo(pk[t >> 1]) * (__uint_as_float(pr[t]) - dvec_s[32 * c32 + t]);
+          const float d1 = bf_hi(pk[t >> 1]) * (__uint_as_float(pr[t + 1]) - dvec_s[32 * c32 + t + 1]);
+          dk[t >> 1] = pack_bf16x2(d0, d1);
         }
         // P^T over the first half of S^T, dS^T over the first half of dP^T
         // (columns already read: chunk c32 writes columns 16 c32 .. 16 c32 + 15)
@@ -511,6 +520,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       }
       tc_fence_after();
       const int k0 = it * 128;
+      // every key of the tile visible to every query of the CTA's tile?
+      const bool all_visible = k0 + 127 < kv_len && q0 + 127 < p.Lq &&
+                               !(p.mask_kind == kMaskCausal && q0 < k0 + 127);
+      const bool row_ok = qi < p.Lq && l2 != -INFINITY;
 #pragma unroll 1
       for (int c32 = 0; c32 < 4; ++c32) {
         uint32_t sr[32], pr[32];
@@ -520,16 +533,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         uint32_t dk[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
-          float dd[2];
+          float pp[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const int key = k0 + 32 * c32 + t + u;
-            const bool vis = key < kv_len && qi < p.Lq &&
-                             !(p.mask_kind == kMaskCausal && key > qi) && l2 != -INFINITY;
-            const float pv = vis ? ex2_approx(fmaf(__uint_as_float(sr[t + u]), c2, -l2)) : 0.f;
-            dd[u] = bf16_round(pv) * (__uint_as_float(pr[t + u]) - dvv);
+            const float arg = fmaf(__uint_as_float(sr[t + u]), c2, -l2);
+            if (all_visible) {
+              pp[u] = ex2_approx(arg);
+            } else {
+              const int key = k0 + 32 * c32 + t + u;
+              const bool vis = row_ok && key < kv_len && !(p.mask_kind == kMaskCausal && key > qi);
+              pp[u] = vis ? ex2_approx(arg) : 0.f;
+            }
           }
-          dk[t >> 1] = pack_bf16x2(dd[0], dd[1]);
+          // dS = P (dP - D) with P rounded to bf16 (as the dK/dV kernel uses it)
+          const uint32_t pw = pack_bf16x2(pp[0], pp[1]);
+          dk[t >> 1] = pack_bf16x2(bf_lo(pw) * (__uint_as_float(pr[t]) - dvv),
+                                   bf_hi(pw) * (__uint_as_float(pr[t + 1]) - dvv));
         }
         tmem_st16(tmem + C::TM_S + lane_off + 16u * c32, dk);
       }
