@@ -16,6 +16,10 @@ replica of the workload (rank-specific seed), no data-path collective.
 ``--impl reference`` times the float64 CPU oracle on the host cores on a
 bounded sample of the same workload (rank 0 only).
 
+``--pass bwd``: one step = one mha_bwd call (the gradient dq, dk, dv of the
+workload for a seeded dout, with the forward's output and row lse resident);
+FLOPs = 2.5x the forward's (five products over the visible pairs).
+
 Decode workloads (``--workload gpt3_decode`` / ``base_decode`` /
 ``gpt3_decode_b1``): one step = one mha_decode call (every sequence's new
 query against its key/value cache); the metric is the step's algorithmic
@@ -631,6 +635,200 @@ def run_reference_decode(args):
     }), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# backward pass
+# ---------------------------------------------------------------------------
+BWD_METRIC = "attention bwd TFLOP/s (bf16, 1 GB300; 2.5x forward flops) and % of dense BF16 tensor peak"
+
+
+def timed_steps(step, args, dev, stream, rank):
+    """Warm-up, then args.steps steps between a barrier + synchronize, CUDA
+    events per step and around all; clocks sampled meanwhile.  Returns
+    (mean ms per step, total ms max over ranks, clock summary or None)."""
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(gpu_id(dev))
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    all_start = torch.cuda.Event(enable_timing=True)
+    all_end = torch.cuda.Event(enable_timing=True)
+    mdist.barrier(dev)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        all_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        all_end.record(stream)
+    torch.cuda.synchronize(dev)
+    mdist.barrier(dev)
+    t_wall1 = time.time()
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    max_total_ms = mdist.max_over_ranks(all_start.elapsed_time(all_end), dev)
+    if rank == 0:
+        time.sleep(0.3)
+        sampler.stop()
+    return step_ms, max_total_ms, (sampler.summary(t_wall0, t_wall1) if rank == 0 else None)
+
+
+def run_bwd(args):
+    rank, world = mdist.init("nccl")
+    _, _, local_rank = mdist.env_rank_world()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from transformer_head_scaled_sdpa_gb300 import binding, build
+    if rank == 0:
+        build.build()
+    mdist.barrier(dev)
+    build.build()
+    w = inputs.BY_NAME[args.workload]
+    if w.dtype != torch.bfloat16:
+        raise SystemExit("--pass bwd needs a bf16 workload")
+    seed = mdist.rank_seed(w.seed, rank)
+    case = inputs.generate(w, seed=seed)
+    dout_h = inputs.generate(w, seed=seed + 77)["q"]
+    q, k, v = (case[n].to(dev) for n in ("q", "k", "v"))
+    dout = dout_h.to(dev)
+    lens = case["key_lens"].to(dev) if case["key_lens"] is not None else None
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        out, lse = binding.mha_fwd(q, k, v, mask_kind=w.mask_kind, key_lens=lens,
+                                   return_lse=True, stream=stream)
+    dq, dk, dv = (torch.empty_like(t) for t in (q, k, v))
+    ws = torch.empty(max(1, binding.lib().mha_bwd_workspace_bytes(w.B, w.H, w.Lq, w.Lk, w.d_k)),
+                     dtype=torch.uint8, device=dev)
+    flops_alg = 2.5 * 4.0 * w.d_k * visible_pairs(w, case["key_lens"])
+    io = [q, k, v, out, dout, lse, dq, dk, dv]
+    bytes_alg = sum(t.numel() * t.element_size() for t in io)
+
+    def step():
+        binding.mha_bwd(q, k, v, out, dout, lse, mask_kind=w.mask_kind, key_lens=lens, dq=dq,
+                        dk=dk, dv=dv, workspace=ws, stream=stream)
+
+    step_ms, max_total_ms, clocks = timed_steps(step, args, dev, stream, rank)
+    rc = binding.mha_sync_status(stream)
+    if rc != 0:
+        raise binding.MhaError(rc, "timed region")
+    launches_per_step = binding.last_launch_info()["kernels"]
+    total_flops = mdist.sum_over_ranks(flops_alg * args.steps, dev)
+    # end to end: host inputs (pinned) in, gradients out, every step
+    host_in = [t.cpu().pin_memory() for t in (q, k, v, out, dout, lse)]
+    host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in (dq, dk, dv)]
+    dev_in = [torch.empty_like(t) for t in (q, k, v, out, dout, lse)]
+    n_e2e = max(3, min(args.steps, 10))
+
+    def e2e_step():
+        for d_, h_ in zip(dev_in, host_in):
+            d_.copy_(h_, non_blocking=True)
+        binding.mha_bwd(*dev_in, mask_kind=w.mask_kind, key_lens=lens, dq=dq, dk=dk, dv=dv,
+                        workspace=ws, stream=stream)
+        for h_, d_ in zip(host_out, (dq, dk, dv)):
+            h_.copy_(d_, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+    mdist.barrier(dev)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = mdist.max_over_ranks(e0.elapsed_time(e1) / n_e2e, dev)
+    e2e_flops = mdist.sum_over_ranks(flops_alg, dev)
+    if rank != 0:
+        mdist.finish()
+        return
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    value = total_flops / (max_total_ms * 1e-3) / 1e12
+    achieved = flops_alg / (step_ms * 1e-3) / 1e12
+    line = {
+        "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) inputs and dout, no dataset)",
+        "config": workload_config(w, {"pass": "bwd", "parallelism": f"replicas x{world} (no collective)",
+                                      "inputs_exceed_l2": bytes_alg > L2_BYTES, "l2_flush": False,
+                                      "flops_per_step_per_gpu": flops_alg}),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_src} dense bf16 (burst)",
+                     "kernel": "bwd_prep_kernel + bwd_dkdv_kernel + bwd_dq_kernel (whole step)",
+                     "kernel_ms": step_ms, "algorithmic_bytes": bytes_alg},
+        "clocks": clocks,
+        "e2e": {"value": e2e_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host_in)),
+                "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host_out)),
+                "steps": n_e2e, "ms_per_step": e2e_ms,
+                "path": "pinned host q,k,v,out,dout,lse -> device, mha_bwd, dq,dk,dv -> host"},
+        "gpu_launches": int(launches_per_step * args.steps),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = bwd_oracle_baseline(w, case, dout_h, 10.0)
+    print(json.dumps(line), flush=True)
+    mdist.finish()
+
+
+def bwd_oracle_baseline(w, case, dout, budget_s):
+    """The oracle's gradient on whole (b, h) heads within a time budget."""
+    import oracle
+    t0 = time.perf_counter()
+    flops, heads = 0.0, 0
+    one = inputs.Workload(w.name, 1, 1, w.d_k, w.Lq, w.Lk, w.mask_kind, w.dtype)
+    while heads < w.B * w.H and (heads == 0 or time.perf_counter() - t0 < budget_s):
+        b, h = divmod(heads, w.H)
+        sub = {n: case[n][b:b + 1, :, h:h + 1] for n in ("q", "k", "v")}
+        lens = case["key_lens"][b:b + 1] if case["key_lens"] is not None else None
+        oracle.mha_bwd(sub["q"], sub["k"], sub["v"], dout[b:b + 1, :, h:h + 1], w.mask_kind,
+                       key_lens=lens.numpy() if lens is not None else None)
+        flops += 2.5 * 4.0 * w.d_k * visible_pairs(one, lens)
+        heads += 1
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.default_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"gradient of {heads} whole (b, h) head(s) of {w.name} in float64 "
+                      f"(parallel over heads only), {dt:.1f} s wall"}
+
+
+def run_reference_bwd(args):
+    rank, world, _ = mdist.env_rank_world()
+    if rank != 0:
+        return
+    import oracle
+    w = inputs.BY_NAME[args.workload]
+    case = inputs.generate(w)
+    dout = inputs.generate(w, seed=w.seed + 77)["q"]
+    budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        bwd_oracle_baseline(w, case, dout, budget)
+    vals = [bwd_oracle_baseline(w, case, dout, budget) for _ in range(args.steps)]
+    value = sum(x["value"] for x in vals) / len(vals)
+    base = vals[-1]
+    print(json.dumps({
+        "impl": "reference", "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sum(x["seconds"] for x in vals) / len(vals),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) inputs and dout, no dataset)",
+        "config": workload_config(w, {"pass": "bwd", "parallelism": "host cores (OpenMP)"}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": base["cores"], "kind": "oracle",
+                         "sample": base["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -640,6 +838,7 @@ def main():
     ap.add_argument("--workload", default="gpt3_causal",
                     choices=sorted(inputs.BY_NAME) + sorted(inputs.DECODE_BY_NAME))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -647,7 +846,11 @@ def main():
     if args.steps < 1:
         ap.error("--steps must be >= 1")
     decode = args.workload in inputs.DECODE_BY_NAME
-    if args.impl == "reference":
+    if args.pass_ == "bwd":
+        if decode:
+            ap.error("--pass bwd applies to the forward workloads")
+        (run_reference_bwd if args.impl == "reference" else run_bwd)(args)
+    elif args.impl == "reference":
         (run_reference_decode if decode else run_reference)(args)
     else:
         (run_decode if decode else run_ours)(args)
