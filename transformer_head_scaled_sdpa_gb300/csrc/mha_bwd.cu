@@ -73,11 +73,21 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ B
   const int h = static_cast<int>(row % p.H);
   const int i = static_cast<int>((row / p.H) % p.Lq);
   const int b = static_cast<int>(row / (static_cast<long long>(p.H) * p.Lq));
-  const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(p.out) + row * D;
-  const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(p.dout) + row * D;
+  // lane reads D/32 consecutive elements of each row (one 4- or 8-byte load)
+  constexpr int EPL = D / 32;
+  const uint16_t* o = reinterpret_cast<const uint16_t*>(p.out) + row * D + EPL * lane;
+  const uint16_t* g = reinterpret_cast<const uint16_t*>(p.dout) + row * D + EPL * lane;
   float acc = 0.f;
-#pragma unroll
-  for (int c = lane; c < D; c += 32) acc = fmaf(__bfloat162float(o[c]), __bfloat162float(g[c]), acc);
+  if constexpr (EPL == 4) {
+    const uint2 ov = *reinterpret_cast<const uint2*>(o);
+    const uint2 gv = *reinterpret_cast<const uint2*>(g);
+    acc = bf_lo(ov.x) * bf_lo(gv.x) + bf_hi(ov.x) * bf_hi(gv.x) + bf_lo(ov.y) * bf_lo(gv.y) +
+          bf_hi(ov.y) * bf_hi(gv.y);
+  } else {
+    const uint32_t ov = *reinterpret_cast<const uint32_t*>(o);
+    const uint32_t gv = *reinterpret_cast<const uint32_t*>(g);
+    acc = bf_lo(ov) * bf_lo(gv) + bf_hi(ov) * bf_hi(gv);
+  }
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
   if (lane == 0) p.dvec[(static_cast<size_t>(b) * p.H + h) * p.Lq + i] = acc;
@@ -286,27 +296,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         tmem_ld32(tmem + C::TM_DP + lane_off + 32u * c32, pr);
         tmem_ld_wait();
         uint32_t pk[16], dk[16];
+        const float* l2c = lse2_s + 32 * c32;
+        const float* dvc = dvec_s + 32 * c32;
+        // (the mask test stays outside the element loops, which then have no
+        // branches and interleave their 32 independent chains)
+        if (all_visible) {
 #pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          float pp[2];
+          for (int t = 0; t < 32; t += 2) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -l2c[t]));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[t + 1]), c2, -l2c[t + 1]));
+            pk[t >> 1] = pack_bf16x2(p0, p1);
+          }
+        } else {
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = 32 * c32 + t + u;
-            const float arg = fmaf(__uint_as_float(sr[t + u]), c2, -lse2_s[col]);
-            if (all_visible) {
-              pp[u] = ex2_approx(arg);
-            } else {
+          for (int t = 0; t < 32; t += 2) {
+            float pp[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int col = 32 * c32 + t + u;
               const int qi = q0 + col;
               const bool vis = key < kv_len && qi < p.Lq &&
                                !(p.mask_kind == kMaskCausal && key > qi) &&
-                               lse2_s[col] != -INFINITY;
-              pp[u] = vis ? ex2_approx(arg) : 0.f;
+                               l2c[t + u] != -INFINITY;
+              const float e = ex2_approx(fmaf(__uint_as_float(sr[t + u]), c2, -l2c[t + u]));
+              pp[u] = vis ? e : 0.f;
             }
+            pk[t >> 1] = pack_bf16x2(pp[0], pp[1]);
           }
-          pk[t >> 1] = pack_bf16x2(pp[0], pp[1]);
-          // dS = P (dP - D) with P as rounded to bf16 for the dV product
-          const float d0 = bf_lo(pk[t >> 1]) * (__uint_as_float(pr[t]) - dvec_s[32 * c32 + t]);
-          const float d1 = bf_hi(pk[t >> 1]) * (__uint_as_float(pr[t + 1]) - dvec_s[32 * c32 + t + 1]);
+        }
+        // dS = P (dP - D) with P as rounded to bf16 for the dV product
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          const float d0 = bf_lo(pk[t >> 1]) * (__uint_as_float(pr[t]) - dvc[t]);
+          const float d1 = bf_hi(pk[t >> 1]) * (__uint_as_float(pr[t + 1]) - dvc[t + 1]);
           dk[t >> 1] = pack_bf16x2(d0, d1);
         }
         // P^T over the first half of S^T, dS^T over the first half of dP^T
@@ -530,26 +552,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         tmem_ld32(tmem + C::TM_S + lane_off + 32u * c32, sr);
         tmem_ld32(tmem + C::TM_DP + lane_off + 32u * c32, pr);
         tmem_ld_wait();
-        uint32_t dk[16];
+        uint32_t pw[16], dk[16];
+        if (all_visible) {
 #pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          float pp[2];
+          for (int t = 0; t < 32; t += 2)
+            pw[t >> 1] = pack_bf16x2(ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -l2)),
+                                     ex2_approx(fmaf(__uint_as_float(sr[t + 1]), c2, -l2)));
+        } else {
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float arg = fmaf(__uint_as_float(sr[t + u]), c2, -l2);
-            if (all_visible) {
-              pp[u] = ex2_approx(arg);
-            } else {
+          for (int t = 0; t < 32; t += 2) {
+            float pp[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
               const int key = k0 + 32 * c32 + t + u;
               const bool vis = row_ok && key < kv_len && !(p.mask_kind == kMaskCausal && key > qi);
-              pp[u] = vis ? ex2_approx(arg) : 0.f;
+              const float e = ex2_approx(fmaf(__uint_as_float(sr[t + u]), c2, -l2));
+              pp[u] = vis ? e : 0.f;
             }
+            pw[t >> 1] = pack_bf16x2(pp[0], pp[1]);
           }
-          // dS = P (dP - D) with P rounded to bf16 (as the dK/dV kernel uses it)
-          const uint32_t pw = pack_bf16x2(pp[0], pp[1]);
-          dk[t >> 1] = pack_bf16x2(bf_lo(pw) * (__uint_as_float(pr[t]) - dvv),
-                                   bf_hi(pw) * (__uint_as_float(pr[t + 1]) - dvv));
         }
+        // dS = P (dP - D) with P rounded to bf16 (as the dK/dV kernel uses it)
+#pragma unroll
+        for (int t = 0; t < 32; t += 2)
+          dk[t >> 1] = pack_bf16x2(bf_lo(pw[t >> 1]) * (__uint_as_float(pr[t]) - dvv),
+                                   bf_hi(pw[t >> 1]) * (__uint_as_float(pr[t + 1]) - dvv));
         tmem_st16(tmem + C::TM_S + lane_off + 16u * c32, dk);
       }
       tmem_st_wait();
