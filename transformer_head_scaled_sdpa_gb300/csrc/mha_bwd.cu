@@ -13,13 +13,16 @@
 //   bwd_dkdv_kernel   one CTA per (b, h, 128-key tile); the query tiles that
 //                     see the keys stream through a two-stage ring.  Per query
 //                     tile: S^T = K Q^T and dP^T = V dO^T on the tensor cores
-//                     (keys on TMEM lanes), the four gradient warps turn them
+//                     (keys on TMEM lanes), the eight gradient warps turn them
 //                     into P^T and dS^T (bf16, written over S^T and dP^T in
 //                     TMEM), and dV += P^T dO, dK += dS^T Q accumulate in TMEM
 //                     (A operands from TMEM).
 //   bwd_dq_kernel     one CTA per (b, h, 128-query tile); the key tiles it
 //                     sees stream through a two-stage ring.  S = Q K^T and
 //                     dP = dO V^T, then dS (bf16, over S), then dQ += dS K.
+// Both take each streamed tile in two halves of 64 rows with TMEM regions of
+// their own: the tensor cores run one half's products (and the next tile's
+// scores) while the gradient warps turn the other half's scores into P, dS.
 // Every operand reuses the forward's shared-memory layout (128-row tiles of
 // 64-feature, 128-byte swizzled chunks): K-major as an operand whose
 // reduction runs over d, MN-major where it runs over the rows.
@@ -30,7 +33,9 @@
 namespace mha {
 namespace {
 
-constexpr int kBwdThreads = 192;  // warps 0-3 gradient, 4 MMA, 5 TMA
+constexpr int kBwdThreads = 320;  // warps 0-7 gradient, 8 MMA, 9 TMA
+constexpr int kGradThreads = 256;
+constexpr int kMmaWarp = 8, kTmaWarp = 9;
 constexpr int kRoleBwdProducer = 8, kRoleBwdMma = 9, kRoleBwdGrad = 10;
 
 template <int D>
@@ -44,18 +49,27 @@ struct BwdCfg {
   static constexpr int OFF_RING = 2 * TILE;    // stage s: pair at OFF_RING + s * 2 * TILE
   static constexpr int OFF_VEC = OFF_RING + 4 * TILE;  // lse2[128], D[128] (dK/dV kernel)
   static constexpr int OFF_BAR = OFF_VEC + 2 * 128 * 4;
-  static constexpr int NBAR = 10;
+  static constexpr int NBAR = 11;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;  // tmem slot, abort flag
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
-  // TMEM: accumulators of the two score-shaped matrices, then the d-wide ones
-  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_ACC0 = 256, TM_ACC1 = 256 + D;
+  // TMEM: a tile's score-shaped matrices in two halves of 64 columns, half
+  // hf at columns 128 hf (S or S^T) and 128 hf + 64 (dP or dP^T); then the
+  // d-wide accumulators
+  static constexpr uint32_t TM_HALF = 128, TM_DP = 64, TM_ACC0 = 256, TM_ACC1 = 256 + D;
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
-// barrier ids
-enum { kFixFull = 0, kRingFull = 1, kRingEmpty = 3, kSdFull = 5, kPdFull = 6, kAccDone = 7,
-       kDrain = 8 };
+// barrier ids.  kScores + hf: the score products of half hf are in TMEM;
+// kGrads + hf: the gradient warps have written P and dS of half hf.
+enum { kFixFull = 0, kRingFull = 1, kRingEmpty = 3, kScores = 5, kGrads = 7, kAccDone = 9,
+       kDrain = 10 };
+
+// TMEM column of the 16 rows of K16 step ks (0..3) of a half, packed as bf16
+// pairs: chunk ks / 2 (32 rows) keeps them in the first 16 of its 32 columns
+__device__ __forceinline__ constexpr uint32_t a_col(int ks) {
+  return 32u * static_cast<uint32_t>(ks >> 1) + 8u * static_cast<uint32_t>(ks & 1);
+}
 
 // bf16 halves of a packed pair -> float (exact)
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -138,14 +152,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       mbar_init(bar(kRingFull + s), 1);
       mbar_init(bar(kRingEmpty + s), 1);
     }
-    mbar_init(bar(kSdFull), 1);
-    mbar_init(bar(kPdFull), 128);
+    for (int hf = 0; hf < 2; ++hf) {
+      mbar_init(bar(kScores + hf), 1);
+      mbar_init(bar(kGrads + hf), kGradThreads);
+    }
     mbar_init(bar(kAccDone), 1);
     mbar_init(bar(kDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -154,7 +170,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 5) {
+  if (warp == kTmaWarp) {
     // ---- TMA: K and V of this key tile once, then Q_i, dO_i per query tile
     if (lane == 0 && n_iter > 0) {
       mbar_arrive_expect_tx(bar(kFixFull), 2 * C::TILE);
@@ -184,120 +200,163 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
                   kRoleBwdProducer * 64 + 9);
     }
     __syncwarp();
-  } else if (warp == 4) {
-    // ---- MMA issuer
-    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);  // K-major A and B
+  } else if (warp == kMmaWarp) {
+    // ---- MMA issuer.  A query tile is taken in two halves of 64 queries with
+    // score regions of their own, so the tensor cores work on one half while
+    // the gradient warps work on the other: per half, dV/dK of this tile, then
+    // S^T/dP^T of the next tile into the region just consumed.
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);   // K-major A and B
     constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);     // B MN-major
     const uint64_t dA0 = smem_desc_sw128(s_base + C::OFF_A0, 16, 1024);   // K tile, K-major
     const uint64_t dA1 = smem_desc_sw128(s_base + C::OFF_A1, 16, 1024);   // V tile, K-major
+    // queries 64 hf .. 64 hf + 63 of ring stage (t & 1): 64 rows of 128 bytes on
+    auto half_rows = [&](int t, int hf) {
+      return s_base + C::OFF_RING + (t & 1) * 2 * C::TILE + hf * 64 * 128;
+    };
+    // S^T = K Q^T, dP^T = V dO^T of half hf (keys on lanes, queries on columns)
+    auto issue_scores = [&](int t, int hf) {
+      const uint32_t rows = half_rows(t, hf);
+      const uint64_t dQk = smem_desc_sw128(rows, 16, 1024);
+      const uint64_t dDk = smem_desc_sw128(rows + C::TILE, 16, 1024);
+      const uint32_t ts = tmem + C::TM_HALF * hf;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
+        umma_ss(ts, dA0 + off, dQk + off, idesc_s, ks > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
+        umma_ss(ts + C::TM_DP, dA1 + off, dDk + off, idesc_s, ks > 0 ? 1u : 0u);
+      }
+      umma_commit(bar(kScores + hf));
+    };
+    // dV += P^T dO, dK += dS^T Q over half hf.  The 16 queries of step ks are
+    // 8 packed TMEM columns: chunk ks / 2 of the half keeps its 32 queries in
+    // the first 16 columns of its own 32.
+    auto issue_grads = [&](int t, int hf) {
+      const uint32_t rows = half_rows(t, hf);
+      const uint64_t dQm = smem_desc_sw128(rows, C::CHUNK, 1024);
+      const uint64_t dDm = smem_desc_sw128(rows + C::TILE, C::CHUNK, 1024);
+      const uint32_t ts = tmem + C::TM_HALF * hf;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        umma_ts(tmem + C::TM_ACC0, ts + a_col(ks), dDm + static_cast<uint64_t>((ks * 2048) >> 4),
+                idesc_o, (ks > 0 || t > 0 || hf > 0) ? 1u : 0u);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        umma_ts(tmem + C::TM_ACC1, ts + C::TM_DP + a_col(ks), dQm + static_cast<uint64_t>((ks * 2048) >> 4),
+                idesc_o, (ks > 0 || t > 0 || hf > 0) ? 1u : 0u);
+    };
     bool ok = true;
-    if (n_iter > 0)
-      ok = mbar_wait(bar(kFixFull), 0, abort_flag, p.status, kRoleBwdMma * 64 + kFixFull);
+    if (n_iter > 0) {
+      ok = mbar_wait(bar(kFixFull), 0, abort_flag, p.status, kRoleBwdMma * 64 + kFixFull) &&
+           mbar_wait(bar(kRingFull), 0, abort_flag, p.status, kRoleBwdMma * 64 + kRingFull);
+      if (ok) {
+        tc_fence_after();
+        if (elect_one()) {
+          issue_scores(0, 0);
+          issue_scores(0, 1);
+        }
+        __syncwarp();
+      }
+    }
     for (int it = 0; ok && it < n_iter; ++it) {
-      const int s = it & 1;
-      const uint32_t ring = s_base + C::OFF_RING + s * 2 * C::TILE;
-      if (!mbar_wait(bar(kRingFull + s), (it >> 1) & 1, abort_flag, p.status,
-                     kRoleBwdMma * 64 + kRingFull + s)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint64_t dQk = smem_desc_sw128(ring, 16, 1024);                 // Q, K-major
-      const uint64_t dDk = smem_desc_sw128(ring + C::TILE, 16, 1024);       // dO, K-major
-      const uint64_t dQm = smem_desc_sw128(ring, C::CHUNK, 1024);           // Q, MN-major
-      const uint64_t dDm = smem_desc_sw128(ring + C::TILE, C::CHUNK, 1024); // dO, MN-major
-      if (elect_one()) {
-        // S^T = K Q^T, dP^T = V dO^T (keys on lanes, queries on columns)
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
-          umma_ss(tmem + C::TM_S, dA0 + off, dQk + off, idesc_s, ks > 0 ? 1u : 0u);
+      const bool more = it + 1 < n_iter;
+      for (int hf = 0; hf < 2; ++hf) {
+        if (!mbar_wait(bar(kGrads + hf), it & 1, abort_flag, p.status, kRoleBwdMma * 64 + kGrads + hf)) {
+          ok = false;
+          break;
         }
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
-          umma_ss(tmem + C::TM_DP, dA1 + off, dDk + off, idesc_s, ks > 0 ? 1u : 0u);
+        tc_fence_after();
+        if (elect_one()) {
+          issue_grads(it, hf);
+          if (hf == 1) {
+            umma_commit(bar(kRingEmpty + (it & 1)));
+            if (!more) umma_commit(bar(kAccDone));
+          }
         }
-        umma_commit(bar(kSdFull));
+        __syncwarp();
+        if (!more) continue;
+        const int sn = (it + 1) & 1;
+        if (hf == 0 && !mbar_wait(bar(kRingFull + sn), ((it + 1) >> 1) & 1, abort_flag, p.status,
+                                  kRoleBwdMma * 64 + kRingFull + sn)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) issue_scores(it + 1, hf);
+        __syncwarp();
       }
-      __syncwarp();
-      if (!mbar_wait(bar(kPdFull), it & 1, abort_flag, p.status, kRoleBwdMma * 64 + kPdFull)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (elect_one()) {
-        // dV += P^T dO, dK += dS^T Q (16 queries = 8 TMEM columns of A per step)
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          umma_ts(tmem + C::TM_ACC0, tmem + C::TM_S + 8u * ks,
-                  dDm + static_cast<uint64_t>((ks * 2048) >> 4), idesc_o, (ks > 0 || it > 0) ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          umma_ts(tmem + C::TM_ACC1, tmem + C::TM_DP + 8u * ks,
-                  dQm + static_cast<uint64_t>((ks * 2048) >> 4), idesc_o, (ks > 0 || it > 0) ? 1u : 0u);
-        umma_commit(bar(kRingEmpty + s));
-        if (it + 1 == n_iter) umma_commit(bar(kAccDone));
-      }
-      __syncwarp();
     }
     if (elect_one()) umma_commit(bar(kDrain));
     __syncwarp();
     volatile int never = 0;
     mbar_wait(bar(kDrain), 0, &never, p.status, kRoleBwdMma * 64 + kDrain);
   } else {
-    // ---- gradient warps: thread r owns key row k0 + r (TMEM lane r)
-    const int quarter = warp;
+    // ---- gradient warps: warp w owns key rows k0 + 32 (w % 4) .. (its TMEM
+    // lane quarter) and, of each half tile, the 32 queries of chunk w / 4
+    const int quarter = warp & 3, cq = warp >> 2;
     const int r = quarter * 32 + lane;
     const int key = k0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c2 = p.scale_log2;
+    // one entry of a query tile's lse (threads 0-127) or D (128-255), loaded
+    // a tile ahead into a register that is read only at the next tile
+    const int vi = static_cast<int>(threadIdx.x) & 127;
+    const bool v_lse = threadIdx.x < 128;
+    const float* v_src = v_lse ? p.lse : p.dvec;
+    float* v_dst = (v_lse ? lse2_s : dvec_s) + vi;
+    float vn = 0.f;
+    auto fetch = [&](int t) {
+      const int qi = (qt_begin + t) * 128 + vi;
+      vn = qi < p.Lq ? v_src[(static_cast<size_t>(b) * p.H + h) * p.Lq + qi] : -INFINITY;
+    };
+    if (n_iter > 0) fetch(0);
     bool ok = true;
     for (int it = 0; ok && it < n_iter; ++it) {
       const int q0 = (qt_begin + it) * 128;
-      // this query tile's lse (log2 units) and D into shared memory; the
-      // previous tile's readers are past their barrier.  (A named barrier
-      // cannot time out: after each one the abort flag is checked, and a warp
-      // that gives up arrives once on it on its way out.)
-      named_barrier(1, 128);
+      // the tile's lse (log2 units) and D into shared memory once the previous
+      // tile's readers are past the barrier.  (A named barrier cannot time out:
+      // after each one the abort flag is checked, and a warp that gives up
+      // arrives once on it on its way out.)
+      named_barrier(1, kGradThreads);
       if (*abort_flag) {
         ok = false;
         break;
       }
-      {
-        const int qi = q0 + r;
-        float l2 = -INFINITY, dv = 0.f;
-        if (qi < p.Lq) {
-          const size_t idx = (static_cast<size_t>(b) * p.H + h) * p.Lq + qi;
-          l2 = p.lse[idx] * 1.4426950408889634f;
-          dv = p.dvec[idx];
-        }
-        lse2_s[r] = l2;
-        dvec_s[r] = dv;
-      }
-      named_barrier(1, 128);
+      *v_dst = v_lse ? vn * 1.4426950408889634f : (vn == -INFINITY ? 0.f : vn);
+      named_barrier(1, kGradThreads);
       if (*abort_flag) {
         ok = false;
         break;
       }
-      if (!mbar_wait(bar(kSdFull), it & 1, abort_flag, p.status, kRoleBwdGrad * 64 + kSdFull)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+      if (it + 1 < n_iter) fetch(it + 1);
       // Every (key, query) pair of the tile is visible unless the tile holds
       // keys past the key length, queries past Lq, or the causal diagonal.
       const bool all_visible = k0 + 127 < kv_len && q0 + 127 < p.Lq &&
                                !(p.mask_kind == kMaskCausal && q0 < k0 + 127);
-#pragma unroll 1
-      for (int c32 = 0; c32 < 4; ++c32) {
+      for (int hf = 0; hf < 2; ++hf) {
+        if (!mbar_wait(bar(kScores + hf), it & 1, abort_flag, p.status, kRoleBwdGrad * 64 + kScores + hf)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ts = tmem + C::TM_HALF * hf + lane_off + 32u * cq;
+        const int col0 = 64 * hf + 32 * cq;  // first query column of the chunk
         uint32_t sr[32], pr[32];
-        tmem_ld32(tmem + C::TM_S + lane_off + 32u * c32, sr);
-        tmem_ld32(tmem + C::TM_DP + lane_off + 32u * c32, pr);
+        tmem_ld32(ts, sr);
+        tmem_ld32(ts + C::TM_DP, pr);
+        float l2c[32], dvc[32];
+#pragma unroll
+        for (int v4 = 0; v4 < 8; ++v4) {
+          const float4 lv = reinterpret_cast<const float4*>(lse2_s + col0)[v4];
+          const float4 dv = reinterpret_cast<const float4*>(dvec_s + col0)[v4];
+          l2c[4 * v4] = lv.x, l2c[4 * v4 + 1] = lv.y, l2c[4 * v4 + 2] = lv.z, l2c[4 * v4 + 3] = lv.w;
+          dvc[4 * v4] = dv.x, dvc[4 * v4 + 1] = dv.y, dvc[4 * v4 + 2] = dv.z, dvc[4 * v4 + 3] = dv.w;
+        }
         tmem_ld_wait();
         uint32_t pk[16], dk[16];
-        const float* l2c = lse2_s + 32 * c32;
-        const float* dvc = dvec_s + 32 * c32;
         // (the mask test stays outside the element loops, which then have no
         // branches and interleave their 32 independent chains)
         if (all_visible) {
@@ -313,8 +372,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             float pp[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              const int col = 32 * c32 + t + u;
-              const int qi = q0 + col;
+              const int qi = q0 + col0 + t + u;
               const bool vis = key < kv_len && qi < p.Lq &&
                                !(p.mask_kind == kMaskCausal && key > qi) &&
                                l2c[t + u] != -INFINITY;
@@ -331,16 +389,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
           const float d1 = bf_hi(pk[t >> 1]) * (__uint_as_float(pr[t + 1]) - dvc[t + 1]);
           dk[t >> 1] = pack_bf16x2(d0, d1);
         }
-        // P^T over the first half of S^T, dS^T over the first half of dP^T
-        // (columns already read: chunk c32 writes columns 16 c32 .. 16 c32 + 15)
-        tmem_st16(tmem + C::TM_S + lane_off + 16u * c32, pk);
-        tmem_st16(tmem + C::TM_DP + lane_off + 16u * c32, dk);
+        // P^T over the first 16 of the chunk's S^T columns, dS^T over the first
+        // 16 of its dP^T columns (this thread has read them; no other has)
+        tmem_st16(ts, pk);
+        tmem_st16(ts + C::TM_DP, dk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kGrads + hf));
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(kPdFull));
     }
-    // ---- epilogue: dV and scale * dK rows to global (rows past Lk skipped)
+    // ---- epilogue: dV and scale * dK rows to global (rows past Lk skipped);
+    // warp w takes the 32-column chunks c with c % 2 == w / 4
     if (ok && n_iter > 0)
       ok = mbar_wait(bar(kAccDone), 0, abort_flag, p.status, kRoleBwdGrad * 64 + kAccDone);
     if (ok) {
@@ -349,7 +408,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(p.dv) + row_off;
       __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(p.dk) + row_off;
 #pragma unroll 1
-      for (int c32 = 0; c32 < D / 32; ++c32) {
+      for (int c32 = cq; c32 < D / 32; c32 += 2) {
         uint32_t a[32], k[32];
         if (n_iter > 0) {
           tmem_ld32(tmem + C::TM_ACC0 + lane_off + 32u * c32, a);
@@ -377,13 +436,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         }
       }
     } else {
-      named_barrier_arrive(1, 128);  // release a gradient warp blocked on the barrier
+      named_barrier_arrive(1, kGradThreads);  // release gradient warps blocked on the barrier
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -421,14 +480,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       mbar_init(bar(kRingFull + s), 1);
       mbar_init(bar(kRingEmpty + s), 1);
     }
-    mbar_init(bar(kSdFull), 1);
-    mbar_init(bar(kPdFull), 128);
+    for (int hf = 0; hf < 2; ++hf) {
+      mbar_init(bar(kScores + hf), 1);
+      mbar_init(bar(kGrads + hf), kGradThreads);
+    }
     mbar_init(bar(kAccDone), 1);
     mbar_init(bar(kDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -437,7 +498,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 5) {
+  if (warp == kTmaWarp) {
     // ---- TMA: Q_i and dO_i once, then K_j, V_j per key tile
     if (lane == 0 && n_iter > 0) {
       mbar_arrive_expect_tx(bar(kFixFull), 2 * C::TILE);
@@ -466,64 +527,93 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
                   kRoleBwdProducer * 64 + 25);
     }
     __syncwarp();
-  } else if (warp == 4) {
-    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+  } else if (warp == kMmaWarp) {
+    // ---- MMA issuer, in halves of 64 keys as in the dK/dV kernel
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
     constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
     const uint64_t dQk = smem_desc_sw128(s_base + C::OFF_A0, 16, 1024);   // Q, K-major
     const uint64_t dDk = smem_desc_sw128(s_base + C::OFF_A1, 16, 1024);   // dO, K-major
+    // keys 64 hf .. 64 hf + 63 of ring stage (t & 1)
+    auto half_rows = [&](int t, int hf) {
+      return s_base + C::OFF_RING + (t & 1) * 2 * C::TILE + hf * 64 * 128;
+    };
+    // S = Q K^T, dP = dO V^T of half hf (queries on lanes, keys on columns)
+    auto issue_scores = [&](int t, int hf) {
+      const uint32_t rows = half_rows(t, hf);
+      const uint64_t dKk = smem_desc_sw128(rows, 16, 1024);
+      const uint64_t dVk = smem_desc_sw128(rows + C::TILE, 16, 1024);
+      const uint32_t ts = tmem + C::TM_HALF * hf;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
+        umma_ss(ts, dQk + off, dKk + off, idesc_s, ks > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
+        umma_ss(ts + C::TM_DP, dDk + off, dVk + off, idesc_s, ks > 0 ? 1u : 0u);
+      }
+      umma_commit(bar(kScores + hf));
+    };
+    // dQ += dS K over half hf (16 keys = 8 packed TMEM columns of A per step)
+    auto issue_grads = [&](int t, int hf) {
+      const uint64_t dKm = smem_desc_sw128(half_rows(t, hf), C::CHUNK, 1024);  // K, MN-major
+      const uint32_t ts = tmem + C::TM_HALF * hf;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        umma_ts(tmem + C::TM_ACC0, ts + a_col(ks), dKm + static_cast<uint64_t>((ks * 2048) >> 4),
+                idesc_o, (ks > 0 || t > 0 || hf > 0) ? 1u : 0u);
+    };
     bool ok = true;
-    if (n_iter > 0)
-      ok = mbar_wait(bar(kFixFull), 0, abort_flag, p.status, kRoleBwdMma * 64 + 16 + kFixFull);
+    if (n_iter > 0) {
+      ok = mbar_wait(bar(kFixFull), 0, abort_flag, p.status, kRoleBwdMma * 64 + 16 + kFixFull) &&
+           mbar_wait(bar(kRingFull), 0, abort_flag, p.status, kRoleBwdMma * 64 + 16 + kRingFull);
+      if (ok) {
+        tc_fence_after();
+        if (elect_one()) {
+          issue_scores(0, 0);
+          issue_scores(0, 1);
+        }
+        __syncwarp();
+      }
+    }
     for (int it = 0; ok && it < n_iter; ++it) {
-      const int s = it & 1;
-      const uint32_t ring = s_base + C::OFF_RING + s * 2 * C::TILE;
-      if (!mbar_wait(bar(kRingFull + s), (it >> 1) & 1, abort_flag, p.status,
-                     kRoleBwdMma * 64 + 16 + kRingFull + s)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint64_t dKk = smem_desc_sw128(ring, 16, 1024);                 // K, K-major
-      const uint64_t dVk = smem_desc_sw128(ring + C::TILE, 16, 1024);       // V, K-major
-      const uint64_t dKm = smem_desc_sw128(ring, C::CHUNK, 1024);           // K, MN-major
-      if (elect_one()) {
-        // S = Q K^T, dP = dO V^T (queries on lanes, keys on columns)
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
-          umma_ss(tmem + C::TM_S, dQk + off, dKk + off, idesc_s, ks > 0 ? 1u : 0u);
+      const bool more = it + 1 < n_iter;
+      for (int hf = 0; hf < 2; ++hf) {
+        if (!mbar_wait(bar(kGrads + hf), it & 1, abort_flag, p.status,
+                       kRoleBwdMma * 64 + 16 + kGrads + hf)) {
+          ok = false;
+          break;
         }
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
-          umma_ss(tmem + C::TM_DP, dDk + off, dVk + off, idesc_s, ks > 0 ? 1u : 0u);
+        tc_fence_after();
+        if (elect_one()) {
+          issue_grads(it, hf);
+          if (hf == 1) {
+            umma_commit(bar(kRingEmpty + (it & 1)));
+            if (!more) umma_commit(bar(kAccDone));
+          }
         }
-        umma_commit(bar(kSdFull));
+        __syncwarp();
+        if (!more) continue;
+        const int sn = (it + 1) & 1;
+        if (hf == 0 && !mbar_wait(bar(kRingFull + sn), ((it + 1) >> 1) & 1, abort_flag, p.status,
+                                  kRoleBwdMma * 64 + 16 + kRingFull + sn)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (elect_one()) issue_scores(it + 1, hf);
+        __syncwarp();
       }
-      __syncwarp();
-      if (!mbar_wait(bar(kPdFull), it & 1, abort_flag, p.status, kRoleBwdMma * 64 + 16 + kPdFull)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (elect_one()) {
-        // dQ += dS K (16 keys = 8 TMEM columns of A per step)
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          umma_ts(tmem + C::TM_ACC0, tmem + C::TM_S + 8u * ks,
-                  dKm + static_cast<uint64_t>((ks * 2048) >> 4), idesc_o, (ks > 0 || it > 0) ? 1u : 0u);
-        umma_commit(bar(kRingEmpty + s));
-        if (it + 1 == n_iter) umma_commit(bar(kAccDone));
-      }
-      __syncwarp();
     }
     if (elect_one()) umma_commit(bar(kDrain));
     __syncwarp();
     volatile int never = 0;
     mbar_wait(bar(kDrain), 0, &never, p.status, kRoleBwdMma * 64 + 16 + kDrain);
   } else {
-    // ---- gradient warps: thread r owns query row q0 + r
-    const int quarter = warp;
+    // ---- gradient warps: warp w owns query rows q0 + 32 (w % 4) .. and, of
+    // each half tile, the 32 keys of chunk w / 4
+    const int quarter = warp & 3, cq = warp >> 2;
     const int r = quarter * 32 + lane;
     const int qi = q0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -534,23 +624,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       l2 = p.lse[idx] * 1.4426950408889634f;
       dvv = p.dvec[idx];
     }
+    const bool row_ok = qi < p.Lq && l2 != -INFINITY;
     bool ok = true;
     for (int it = 0; ok && it < n_iter; ++it) {
-      if (!mbar_wait(bar(kSdFull), it & 1, abort_flag, p.status, kRoleBwdGrad * 64 + 16 + kSdFull)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
       const int k0 = it * 128;
       // every key of the tile visible to every query of the CTA's tile?
       const bool all_visible = k0 + 127 < kv_len && q0 + 127 < p.Lq &&
                                !(p.mask_kind == kMaskCausal && q0 < k0 + 127);
-      const bool row_ok = qi < p.Lq && l2 != -INFINITY;
-#pragma unroll 1
-      for (int c32 = 0; c32 < 4; ++c32) {
+      for (int hf = 0; hf < 2; ++hf) {
+        if (!mbar_wait(bar(kScores + hf), it & 1, abort_flag, p.status,
+                       kRoleBwdGrad * 64 + 16 + kScores + hf)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ts = tmem + C::TM_HALF * hf + lane_off + 32u * cq;
         uint32_t sr[32], pr[32];
-        tmem_ld32(tmem + C::TM_S + lane_off + 32u * c32, sr);
-        tmem_ld32(tmem + C::TM_DP + lane_off + 32u * c32, pr);
+        tmem_ld32(ts, sr);
+        tmem_ld32(ts + C::TM_DP, pr);
         tmem_ld_wait();
         uint32_t pw[16], dk[16];
         if (all_visible) {
@@ -564,7 +655,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             float pp[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              const int key = k0 + 32 * c32 + t + u;
+              const int key = k0 + 64 * hf + 32 * cq + t + u;
               const bool vis = row_ok && key < kv_len && !(p.mask_kind == kMaskCausal && key > qi);
               const float e = ex2_approx(fmaf(__uint_as_float(sr[t + u]), c2, -l2));
               pp[u] = vis ? e : 0.f;
@@ -577,11 +668,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         for (int t = 0; t < 32; t += 2)
           dk[t >> 1] = pack_bf16x2(bf_lo(pw[t >> 1]) * (__uint_as_float(pr[t]) - dvv),
                                    bf_hi(pw[t >> 1]) * (__uint_as_float(pr[t + 1]) - dvv));
-        tmem_st16(tmem + C::TM_S + lane_off + 16u * c32, dk);
+        // dS over the first 16 of the chunk's S columns (read by this thread only)
+        tmem_st16(ts, dk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kGrads + hf));
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(kPdFull));
     }
     if (ok && n_iter > 0)
       ok = mbar_wait(bar(kAccDone), 0, abort_flag, p.status, kRoleBwdGrad * 64 + 16 + kAccDone);
@@ -590,7 +682,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       __nv_bfloat16* dq_row = reinterpret_cast<__nv_bfloat16*>(p.dq) +
                               ((static_cast<size_t>(b) * p.Lq + qi) * p.H + h) * D;
 #pragma unroll 1
-      for (int c32 = 0; c32 < D / 32; ++c32) {
+      for (int c32 = cq; c32 < D / 32; c32 += 2) {
         uint32_t a[32];
         if (n_iter > 0) {
           tmem_ld32(tmem + C::TM_ACC0 + lane_off + 32u * c32, a);
@@ -616,7 +708,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
