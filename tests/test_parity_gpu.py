@@ -87,6 +87,11 @@ SHAPES = [
     (4, 2, 130, 257, 128, KEYPAD, [257, 128, 127, 1]),
     (2, 3, 384, 640, 64, KEYPAD, [640, 300]),
     (1, 8, 640, 640, 128, NONE, None),
+    # d 64 with four or more key tiles and no causal mask: the kernel whose two
+    # query tiles take turns at the exponentials (ragged Lq leaves the last
+    # unit's second tile empty; ragged Lk masks the last key tile)
+    (2, 3, 300, 700, 64, NONE, None),
+    (3, 2, 256, 1024, 64, KEYPAD, [1024, 513, 0]),
 ]
 
 
@@ -154,6 +159,7 @@ def test_rising_rows(mha, d, mask, step):
 LSE_SHAPES = [
     # B, H, Lq, Lk, d, mask, key_lens, dtype
     (2, 3, 200, 333, 64, NONE, None, torch.bfloat16),
+    (2, 3, 300, 700, 64, NONE, None, torch.bfloat16),
     (1, 8, 640, 640, 128, NONE, None, torch.bfloat16),
     (3, 2, 300, 300, 128, CAUSAL, None, torch.bfloat16),
     (2, 4, 129, 129, 64, CAUSAL, None, torch.bfloat16),
@@ -347,6 +353,23 @@ def test_attention_kernel_timeout_path(mha):
     assert mha.mha_sync_status() == 0
     out = pu.gpu_run(mha, case, CAUSAL)
     pu.assert_bf16_close(out, pu.oracle_run(case, CAUSAL), "after kernel timeout")
+
+
+def test_attention_kernel_timeout_path_with_turns(mha):
+    """The same with the d_k = 64 kernel that passes exponential turns
+    between its two query tiles (no mask): the withheld signal still ends in
+    MHA_ERR_TIMEOUT, every role leaves, and the next launch is correct."""
+    case = inputs.random_case(13, 1, 2, 256, 512, 64)
+    g = pu.to_cuda(case)
+    mha.mha_debug_withhold_p(True)
+    try:
+        mha.mha_fwd(g["q"], g["k"], g["v"], mask_kind=NONE)
+        assert mha.mha_sync_status() == 7
+    finally:
+        mha.mha_debug_withhold_p(False)
+    assert mha.mha_sync_status() == 0
+    out = pu.gpu_run(mha, case, NONE)
+    pu.assert_bf16_close(out, pu.oracle_run(case, NONE), "after kernel timeout")
 
 
 def test_bounded_wait_reports_timeout(mha):

@@ -58,6 +58,9 @@ namespace mha {
 namespace {
 
 constexpr int kThreads = 384;
+// warp roles: softmax warps 0-3 (Q0) and 4-7 (Q1), then the third warpgroup
+constexpr int kSoftmaxWarp0 = 0;
+constexpr int kMmaWarp = 8, kProducerWarp = 9, kMma1Warp = 11;  // warp 10: scheduler
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p stays <= 2^8
 constexpr int kHeadGroup = 32;              // heads dispatched together (L2 reuse of K/V)
 // unit-queue readers: 8 softmax warps, the producer and 1 or 2 MMA warps
@@ -75,7 +78,7 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + NS * TILE;
   static constexpr int OFF_STAGE = OFF_V + NS * TILE;  // epilogue staging, one CHUNK per softmax warpgroup
   static constexpr int OFF_BAR = OFF_STAGE + 2 * CHUNK;
-  static constexpr int NBAR = 23 + 4 * NS;
+  static constexpr int NBAR = 31 + 4 * NS;
   // tmem slot (+0), abort flag (+4), unit queue (+8, +12), CLC response (+16,
   // 16 bytes, must be 16-byte aligned)
   static constexpr int OFF_MISC = (OFF_BAR + 8 * NBAR + 63) / 64 * 64;
@@ -127,6 +130,8 @@ struct Bars {
                                                   // without split release, the whole stage:
                                                   // 2 arrivals, one per MMA warp)
   static constexpr int V_EMPTY = 23 + 3 * NS;     // + stage: its V tile's last P.V MMA done
+  static constexpr int TOK_A = 23 + 4 * NS;       // + quarter: Q0's warp may take its exponentials (32 arrivals)
+  static constexpr int TOK_B = 27 + 4 * NS;       // + quarter: Q1's warp may take its exponentials (32 arrivals)
 };
 
 // role ids for the status "site" field
@@ -591,13 +596,18 @@ __device__ __forceinline__ void mma_role_pair(const Bf16Params& p, const Ctx& cx
   mbar_wait(cx.bar(BA::DRAIN + 0), 0, &never, p.status, kRoleMma * 64 + BA::DRAIN);
 }
 
-template <int D>
+// TOK: the two softmax warps on one sub-partition (the same lane quarter of Q0
+// and Q1) take turns at the exponentials, passing a token through an mbarrier
+// pair.  That keeps their SFU-bound phases apart, so each runs at the full SFU
+// rate while the other does its loads, maxima and stores (d_k = 64 without the
+// causal mask, where the SFU work per score equals the tensor work: +5 %).
+template <int D, bool TOK>
 __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx) {
   using C = Cfg<D>;
   using BA = Bars<C::NS>;
-  const int warp = cx.warp, lane = cx.lane;
+  const int warp = cx.warp - kSoftmaxWarp0, lane = cx.lane;
   const int g = warp >> 2;                      // which query tile
-  const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
+  const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31 (= hardware warp % 4)
   const int row = quarter * 32 + lane;          // query row within the tile
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
   const uint32_t tS = cx.tmem + (g ? C::TM_S1 : C::TM_S0) + lane_off;
@@ -610,6 +620,10 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
   const float c2 = p.scale_log2;
   int s_cnt = 0;  // S_g tiles so far
   int o_cnt = 0;  // units with O_g so far
+  int tok_cnt = 0;  // exponential turns taken so far
+  // this warp's turn barrier and its partner's (same quarter, other tile)
+  const int tok_wait = (g ? BA::TOK_B : BA::TOK_A) + quarter;
+  const int tok_pass = (g ? BA::TOK_A : BA::TOK_B) + quarter;
   bool ok = true;
   for (int k = 0; ok; ++k) {
     const int unit = next_unit<C::NS>(p, cx, k, kRoleSoftmax, lane == 0);
@@ -618,6 +632,12 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
     const int q_start = u.q0 + g * kBlockM;
     const int qi = q_start + row;
     const int n_tiles = u.n[g];
+    // Turns alternate Q0, Q1, Q0, ... over the key tiles both query tiles
+    // have; Q1's warp hands Q0's the first turn of each unit.  Each side
+    // passes only after it has waited for the other's pass, so no turn
+    // barrier ever gets two phases ahead of its waiter.
+    const int n_turns = TOK ? min(u.n[0], u.n[1]) : 0;
+    if (g == 1 && n_turns > 0) mbar_arrive(cx.bar(tok_pass));
     float m_ref = 0.f;  // reference maximum (log2 units) the exponents use
     float l = 0.f;      // running sum of 2^(s*c2 - m_ref)
     for (int j = 0; j < n_tiles; ++j) {
@@ -673,6 +693,12 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
         l *= alpha;
         m_ref = mx;
       }
+      if (j < n_turns) {
+        ok = mbar_wait(cx.bar(tok_wait), tok_cnt & 1, cx.abort_flag, p.status,
+                       kRoleSoftmax * 64 + tok_wait);
+        if (!ok) break;
+        ++tok_cnt;
+      }
       // p = 2^(s*c2 - m_ref): packed scale-subtract, ex2 on the SFU, packed sums
       const float nm = -m_ref;
       float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
@@ -687,6 +713,7 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
       add2(sa[0], sb[0], sa[0], sb[0], sa[1], sb[1]);
       add2(sa[2], sb[2], sa[2], sb[2], sa[3], sb[3]);
       l += (sa[0] + sb[0]) + (sa[2] + sb[2]);
+      if (j < n_turns && (g == 0 || j + 1 < n_turns)) mbar_arrive(cx.bar(tok_pass));
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) pk[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
@@ -791,7 +818,7 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
   __syncwarp();
 }
 
-template <int D>
+template <int D, bool TOK>
 __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_constant__ Bf16Params p) {
   using C = Cfg<D>;
   using BA = Bars<C::NS>;
@@ -829,6 +856,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
       mbar_init(cx.bar(BA::PV_DONE + g), 1);
     }
     mbar_init(cx.bar(BA::CLC), 1);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(cx.bar(BA::TOK_A + q), 32);
+      mbar_init(cx.bar(BA::TOK_B + q), 32);
+    }
     mbar_init(cx.bar(BA::DRAIN + 0), 1);
     mbar_init(cx.bar(BA::DRAIN + 1), 1);
     for (int s = 0; s < NS; ++s) {
@@ -840,13 +871,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
     *cx.abort_flag = 0;
     fence_mbar_init();
   }
-  if (cx.warp == 9 && cx.lane == 0) {
+  if (cx.warp == kProducerWarp && cx.lane == 0) {
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
     tma_prefetch_desc(&p.tm_o);
   }
-  if (cx.warp == 8) {
+  if (cx.warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -855,20 +886,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   tc_fence_after();
   cx.tmem = *tmem_slot;
 
-  if (cx.warp < 8) {
+  if (cx.warp < kSoftmaxWarp0 + 8) {
     regs_increase<C::REGS_SOFTMAX>();
-    softmax_role<D>(p, cx);
+    softmax_role<D, TOK>(p, cx);
   } else {
     regs_decrease<C::REGS_OTHER>();
-    if (cx.warp == 8) {
+    if (cx.warp == kMmaWarp) {
       if constexpr (C::SEPARATE_P) {
         mma_role<D, 0>(p, cx);
       } else {
         mma_role_pair<D>(p, cx);
       }
-    } else if (cx.warp == 11) {
+    } else if (cx.warp == kMma1Warp) {
       if constexpr (C::SEPARATE_P) mma_role<D, 1>(p, cx);
-    } else if (cx.warp == 9) {
+    } else if (cx.warp == kProducerWarp) {
       producer_role<D>(p, cx);
     } else {
       scheduler_role<D>(p, cx);
@@ -878,13 +909,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   // ---- teardown ------------------------------------------------------------
   tc_fence_before();
   __syncthreads();
-  if (cx.warp == 8) {
+  if (cx.warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(cx.tmem, C::TMEM_COLS);
   }
 }
 
-template <int D>
+template <int D, bool TOK>
 cudaError_t launch_d(const Bf16Params& p, cudaStream_t stream, LaunchInfo* info) {
   using C = Cfg<D>;
   int dev = 0;
@@ -893,14 +924,14 @@ cudaError_t launch_d(const Bf16Params& p, cudaStream_t stream, LaunchInfo* info)
   static bool attr_set[64] = {};  // the attribute is per device and function
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fwd_bf16_kernel<D, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const long long units = static_cast<long long>(p.n_qtiles) * p.B * p.H;
   const dim3 grid(static_cast<unsigned>(units));
-  fwd_bf16_kernel<D><<<grid, kThreads, C::SMEM, stream>>>(p);
+  fwd_bf16_kernel<D, TOK><<<grid, kThreads, C::SMEM, stream>>>(p);
   if (info) {
     info->kernels = 1;
     info->grid = static_cast<int>(units);
@@ -913,8 +944,14 @@ cudaError_t launch_d(const Bf16Params& p, cudaStream_t stream, LaunchInfo* info)
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const Bf16Params& p, int d, cudaStream_t stream, LaunchInfo* info) {
-  if (d == 64) return launch_d<64>(p, stream, info);
-  if (d == 128) return launch_d<128>(p, stream, info);
+  // (the exponential turn-taking pays off at d_k = 64 without the causal
+  // mask once units span several key tiles; with one or two key tiles the
+  // hand-over at the start of each unit costs more than it saves)
+  if (d == 64)
+    return (p.mask_kind != kMaskCausal && p.Lk >= 4 * kBlockN)
+               ? launch_d<64, true>(p, stream, info)
+               : launch_d<64, false>(p, stream, info);
+  if (d == 128) return launch_d<128, false>(p, stream, info);
   return cudaErrorInvalidValue;
 }
 
