@@ -175,15 +175,23 @@ def traffic_record(kernel_fp: str, workload: str, kernel: str = "fwd_bf16_kernel
     return rec.get("dram_bytes_per_launch")
 
 
-def kernel_fingerprint() -> str:
+# the sources each profiled kernel is compiled from
+KERNEL_SOURCES = {
+    "fwd_bf16_kernel": ("kernels.h", "mha_fwd_bf16.cu", "ptx.cuh"),
+    "decode_split_kernel": ("kernels.h", "mha_decode.cu", "ptx.cuh"),
+    "bwd_dkdv_kernel": ("kernels.h", "mha_bwd.cu", "ptx.cuh"),
+}
+
+
+def kernel_fingerprint(kernel: str = "fwd_bf16_kernel") -> str:
+    """sha256 over the source files the kernel is compiled from."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "transformer_head_scaled_sdpa_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()
 
 
@@ -328,7 +336,7 @@ def run_ours(args):
     value = total_flops / (max_total_ms * 1e-3) / 1e12
     achieved = flops_alg / (kernel_ms * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
-    traffic = traffic_record(kernel_fingerprint(), w.name)
+    traffic = traffic_record(kernel_fingerprint("fwd_bf16_kernel"), w.name)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_total_ms / args.steps,
@@ -572,7 +580,7 @@ def run_decode(args):
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": DEC_UNIT,
                      "frac": achieved / peak,
-                     "traffic": traffic_record(kernel_fingerprint(), w.name, "decode_split_kernel"),
+                     "traffic": traffic_record(kernel_fingerprint("decode_split_kernel"), w.name, "decode_split_kernel"),
                      "peak_source": f"{peak_src} HBM copy bandwidth",
                      "kernel": "decode_split_kernel (+ decode_combine_kernel when split)",
                      "kernel_ms": step_ms, "algorithmic_bytes": bytes_alg},
