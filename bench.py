@@ -66,6 +66,11 @@ def visible_pairs(w, key_lens) -> float:
     if w.mask_kind == inputs.MASK_CAUSAL:
         L = w.Lq
         return w.B * w.H * L * (L + 1) / 2
+    if w.mask_kind == inputs.MASK_CAUSAL_KEY_PADDING:
+        # row i of sequence b sees min(i + 1, len_b) keys
+        i = torch.arange(w.Lq, dtype=torch.int64)
+        lens = key_lens.clamp(0, w.Lk).to(torch.int64)
+        return float(w.H * torch.minimum(i[None, :] + 1, lens[:, None]).sum().item())
     if w.mask_kind == inputs.MASK_KEY_PADDING:
         lens = key_lens.clamp(0, w.Lk).to(torch.int64).sum().item()
         return w.H * w.Lq * float(lens)

@@ -29,6 +29,7 @@ import numpy as np
 MASK_NONE = 0
 MASK_CAUSAL = 1
 MASK_KEY_PADDING = 2
+MASK_CAUSAL_KEY_PADDING = 3  # both masks (a decoder over padded sequences)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "mha_oracle.c")
@@ -78,6 +79,13 @@ class Oracle:
             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_double,
             ctypes.c_int]
+        lib.oracle_mha_dv_f64.restype = ctypes.c_int
+        lib.oracle_mha_dv_f64.argtypes = [
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_double,
+            ctypes.c_int]
         lib.oracle_mha_bwd_f64.restype = ctypes.c_int
         lib.oracle_mha_bwd_f64.argtypes = [ctypes.c_void_p] * 7 + [
             ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
@@ -92,11 +100,13 @@ class Oracle:
 
     def mha(self, q, k, v, mask_kind: int = MASK_NONE, key_lens=None, scale=None,
             threads: int | None = None, return_lse: bool = False):
-        """Attention over all heads: q [B,Lq,H,d], k and v [B,Lk,H,d] -> o [B,Lq,H,d].
+        """Attention over all heads: q [B,Lq,H,d_k], k [B,Lk,H,d_k] and v
+        [B,Lk,H,d_v] -> o [B,Lq,H,d_v] (d_v may differ from d_k).
 
-        ``scale`` None means 1/sqrt(d).  ``key_lens`` ([B] integers) is read
-        only under ``MASK_KEY_PADDING``.  With ``return_lse`` also returns the
-        row log-sum-exp of the scaled scores, shape [B, H, Lq].
+        ``scale`` None means 1/sqrt(d_k).  ``key_lens`` ([B] integers) is read
+        only when the mask includes key padding (``MASK_KEY_PADDING``,
+        ``MASK_CAUSAL_KEY_PADDING``).  With ``return_lse`` also returns the row
+        log-sum-exp of the scaled scores, shape [B, H, Lq].
         """
         q = _as_f64(q)
         k = _as_f64(k)
@@ -105,12 +115,13 @@ class Oracle:
             raise ValueError("q, k, v must be [B, L, H, d]")
         B, Lq, H, d = q.shape
         Lk = k.shape[1]
-        if k.shape != (B, Lk, H, d) or v.shape != (B, Lk, H, d):
-            raise ValueError("k and v must be [B, Lk, H, d] matching q")
+        d_v = v.shape[3]
+        if k.shape != (B, Lk, H, d) or v.shape != (B, Lk, H, d_v):
+            raise ValueError("k must be [B, Lk, H, d_k] and v [B, Lk, H, d_v] matching q")
         if scale is None:
             scale = 1.0 / math.sqrt(d)
         lens = None
-        if mask_kind == MASK_KEY_PADDING:
+        if int(mask_kind) & MASK_KEY_PADDING:
             if key_lens is None:
                 raise ValueError("key padding needs key_lens")
             if hasattr(key_lens, "detach"):
@@ -118,16 +129,16 @@ class Oracle:
             lens = np.ascontiguousarray(np.asarray(key_lens, dtype=np.int32))
             if lens.shape != (B,):
                 raise ValueError("key_lens must have shape [B]")
-        out = np.empty((B, Lq, H, d), dtype=np.float64)
+        out = np.empty((B, Lq, H, d_v), dtype=np.float64)
         lse = np.empty((B, H, Lq), dtype=np.float64) if return_lse else None
-        rc = self.lib.oracle_mha_f64(
+        rc = self.lib.oracle_mha_dv_f64(
             q.ctypes.data, k.ctypes.data, v.ctypes.data, out.ctypes.data,
             lse.ctypes.data if lse is not None else None,
-            B, H, Lq, Lk, d, int(mask_kind),
+            B, H, Lq, Lk, d, d_v, int(mask_kind),
             lens.ctypes.data if lens is not None else None,
             float(scale), int(threads) if threads else 0)
         if rc != 0:
-            raise ValueError(f"oracle_mha_f64 rejected its arguments (code {rc})")
+            raise ValueError(f"oracle_mha_dv_f64 rejected its arguments (code {rc})")
         return (out, lse) if return_lse else out
 
 
@@ -145,7 +156,7 @@ class Oracle:
         if scale is None:
             scale = 1.0 / math.sqrt(d)
         lens = None
-        if mask_kind == MASK_KEY_PADDING:
+        if int(mask_kind) & MASK_KEY_PADDING:
             if key_lens is None:
                 raise ValueError("key padding needs key_lens")
             if hasattr(key_lens, "detach"):

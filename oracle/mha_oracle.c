@@ -26,15 +26,21 @@
  *     key has weight exactly 0 and is left out of the sum.
  *   - key padding (not on the pages): keys j >= key_lens[b] are removed for
  *     every head and query of sequence b; key_lens[b] is clamped to [0, Lk].
+ *   - both masks together (mask kind 3, a decoder over padded sequences):
+ *     key j is visible to row i when it passes both, j <= i and
+ *     j < key_lens[b].
+ *   - d_v may differ from d_k (Equation (1) takes values of dimension d_v):
+ *     scores use the d_k columns of q and k, the output has the d_v columns
+ *     of v.
  *   - a row with no visible key has output 0 and log-sum-exp -inf.
  *   - before the exponentials the row maximum m is subtracted from every
  *     score.  The formula page (証明, weight-ratio step) shows that adding one
  *     constant to all scores leaves the weights unchanged, so this changes
  *     nothing but the rounding and keeps e^{s} from overflowing.
  *
- * Layout: q is [B, Lq, H, d], k and v are [B, Lk, H, d], out is [B, Lq, H, d],
- * all row-major float64 (the head split of a d_model = H*d vector per step is
- * the innermost H*d block).  lse (optional, may be NULL) is [B, H, Lq] and
+ * Layout: q is [B, Lq, H, d_k], k is [B, Lk, H, d_k], v is [B, Lk, H, d_v],
+ * out is [B, Lq, H, d_v], all row-major float64 (the head split of a
+ * d_model = H*d vector per step is the innermost H*d block).  lse (optional, may be NULL) is [B, H, Lq] and
  * receives m + log(sum_j e^{s_j - m}) of each row.
  */
 #include <math.h>
@@ -48,7 +54,8 @@
 enum {
     ORACLE_MASK_NONE = 0,
     ORACLE_MASK_CAUSAL = 1,
-    ORACLE_MASK_KEY_PADDING = 2
+    ORACLE_MASK_KEY_PADDING = 2,
+    ORACLE_MASK_CAUSAL_KEY_PADDING = 3  /* both */
 };
 
 /* Number of keys row i of sequence b may attend to: keys 0 .. n-1. */
@@ -56,32 +63,44 @@ static int64_t visible_keys(int64_t i, int64_t b, int64_t Lk, int mask_kind,
                             const int32_t* key_lens)
 {
     int64_t n = Lk;
-    if (mask_kind == ORACLE_MASK_CAUSAL) {
+    if (mask_kind & ORACLE_MASK_CAUSAL) {
         n = i + 1 < Lk ? i + 1 : Lk;
-    } else if (mask_kind == ORACLE_MASK_KEY_PADDING) {
+    }
+    if (mask_kind & ORACLE_MASK_KEY_PADDING) {
         int64_t len = key_lens[b];
         if (len < 0) len = 0;
         if (len > Lk) len = Lk;
-        n = len;
+        if (len < n) n = len;
     }
     return n;
 }
 
+/* The argument rules both entry points share: 0 when the mask is usable. */
+static int check_mask(int mask_kind, int64_t B, int64_t Lq, int64_t Lk,
+                      const int32_t* key_lens)
+{
+    if (mask_kind < ORACLE_MASK_NONE || mask_kind > ORACLE_MASK_CAUSAL_KEY_PADDING) return 1;
+    if ((mask_kind & ORACLE_MASK_CAUSAL) && Lq != Lk) return 1;
+    if ((mask_kind & ORACLE_MASK_KEY_PADDING) && key_lens == NULL && B > 0) return 1;
+    return 0;
+}
+
 /* One query row.  s is caller-provided scratch of at least Lk doubles. */
 static void attend_row(const double* q_row, const double* k, const double* v,
-                       double* o_row, double* lse_out, int64_t n, int64_t d,
-                       int64_t kv_row_stride, double scale, double* s)
+                       double* o_row, double* lse_out, int64_t n, int64_t d_k,
+                       int64_t d_v, int64_t k_row_stride, int64_t v_row_stride,
+                       double scale, double* s)
 {
     if (n == 0) {
-        for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
+        for (int64_t c = 0; c < d_v; ++c) o_row[c] = 0.0;
         if (lse_out) *lse_out = -INFINITY;
         return;
     }
     /* 1. scores */
     for (int64_t j = 0; j < n; ++j) {
-        const double* k_row = k + j * kv_row_stride;
+        const double* k_row = k + j * k_row_stride;
         double dot = 0.0;
-        for (int64_t c = 0; c < d; ++c) dot += q_row[c] * k_row[c];
+        for (int64_t c = 0; c < d_k; ++c) dot += q_row[c] * k_row[c];
         s[j] = scale * dot;
     }
     /* 2. weights, with the row maximum taken out of every exponent */
@@ -95,10 +114,10 @@ static void attend_row(const double* q_row, const double* k, const double* v,
     }
     for (int64_t j = 0; j < n; ++j) s[j] /= sum;
     /* 3. weighted mean of the value rows */
-    for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
+    for (int64_t c = 0; c < d_v; ++c) o_row[c] = 0.0;
     for (int64_t j = 0; j < n; ++j) {
-        const double* v_row = v + j * kv_row_stride;
-        for (int64_t c = 0; c < d; ++c) o_row[c] += s[j] * v_row[c];
+        const double* v_row = v + j * v_row_stride;
+        for (int64_t c = 0; c < d_v; ++c) o_row[c] += s[j] * v_row[c];
     }
     if (lse_out) *lse_out = m + log(sum);
 }
@@ -110,18 +129,14 @@ static void attend_row(const double* q_row, const double* k, const double* v,
  * n_threads <= 0 uses the OpenMP default.  Rows are independent, so the
  * thread count changes no result bit.
  */
-int oracle_mha_f64(const double* q, const double* k, const double* v,
-                   double* out, double* lse,
-                   int64_t B, int64_t H, int64_t Lq, int64_t Lk, int64_t d,
-                   int mask_kind, const int32_t* key_lens, double scale,
-                   int n_threads)
+int oracle_mha_dv_f64(const double* q, const double* k, const double* v,
+                      double* out, double* lse,
+                      int64_t B, int64_t H, int64_t Lq, int64_t Lk, int64_t d_k,
+                      int64_t d_v, int mask_kind, const int32_t* key_lens, double scale,
+                      int n_threads)
 {
-    if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || d < 1) return 1;
-    if (mask_kind != ORACLE_MASK_NONE && mask_kind != ORACLE_MASK_CAUSAL &&
-        mask_kind != ORACLE_MASK_KEY_PADDING)
-        return 1;
-    if (mask_kind == ORACLE_MASK_CAUSAL && Lq != Lk) return 1;
-    if (mask_kind == ORACLE_MASK_KEY_PADDING && key_lens == NULL && B > 0) return 1;
+    if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || d_k < 1 || d_v < 1) return 1;
+    if (check_mask(mask_kind, B, Lq, Lk, key_lens) != 0) return 1;
     const int64_t rows = B * H * Lq;
     if (rows == 0) return 0;
     if (q == NULL || out == NULL) return 1;
@@ -150,15 +165,26 @@ int oracle_mha_f64(const double* q, const double* k, const double* v,
         const int64_t h = (r / Lq) % H;
         const int64_t b = r / (Lq * H);
         const int64_t n = visible_keys(i, b, Lk, mask_kind, key_lens);
-        const double* q_row = q + ((b * Lq + i) * H + h) * d;
-        const double* k_bh = k ? k + (b * Lk * H + h) * d : NULL;
-        const double* v_bh = v ? v + (b * Lk * H + h) * d : NULL;
-        double* o_row = out + ((b * Lq + i) * H + h) * d;
+        const double* q_row = q + ((b * Lq + i) * H + h) * d_k;
+        const double* k_bh = k ? k + (b * Lk * H + h) * d_k : NULL;
+        const double* v_bh = v ? v + (b * Lk * H + h) * d_v : NULL;
+        double* o_row = out + ((b * Lq + i) * H + h) * d_v;
         double* lse_row = lse ? lse + (b * H + h) * Lq + i : NULL;
-        attend_row(q_row, k_bh, v_bh, o_row, lse_row, n, d, H * d, scale, s);
+        attend_row(q_row, k_bh, v_bh, o_row, lse_row, n, d_k, d_v, H * d_k, H * d_v, scale, s);
     }
     free(scratch);
     return 0;
+}
+
+/* The same with d_v = d_k = d. */
+int oracle_mha_f64(const double* q, const double* k, const double* v,
+                   double* out, double* lse,
+                   int64_t B, int64_t H, int64_t Lq, int64_t Lk, int64_t d,
+                   int mask_kind, const int32_t* key_lens, double scale,
+                   int n_threads)
+{
+    return oracle_mha_dv_f64(q, k, v, out, lse, B, H, Lq, Lk, d, d, mask_kind, key_lens,
+                             scale, n_threads);
 }
 
 /*
@@ -188,11 +214,7 @@ int oracle_mha_bwd_f64(const double* q, const double* k, const double* v,
                        int n_threads)
 {
     if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || d < 1) return 1;
-    if (mask_kind != ORACLE_MASK_NONE && mask_kind != ORACLE_MASK_CAUSAL &&
-        mask_kind != ORACLE_MASK_KEY_PADDING)
-        return 1;
-    if (mask_kind == ORACLE_MASK_CAUSAL && Lq != Lk) return 1;
-    if (mask_kind == ORACLE_MASK_KEY_PADDING && key_lens == NULL && B > 0) return 1;
+    if (check_mask(mask_kind, B, Lq, Lk, key_lens) != 0) return 1;
     if (B * H == 0) return 0;
     if (Lq > 0 && (q == NULL || dout == NULL || dq == NULL)) return 1;
     if (Lk > 0 && (k == NULL || v == NULL || dk == NULL || dv == NULL)) return 1;

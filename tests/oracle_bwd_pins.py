@@ -32,7 +32,8 @@ def _case(seed, B, Lq, H, Lk, d):
 def check_bwd_finite_differences(mha, bwd):
     cases = [((1, 3, 2, 3, 3), NONE, None, None),
              ((2, 4, 1, 4, 3), CAUSAL, None, 0.7),
-             ((2, 3, 2, 5, 2), KEYPAD, [5, 2], None)]
+             ((2, 3, 2, 5, 2), KEYPAD, [5, 2], None),
+             ((2, 4, 1, 4, 2), CAUSAL | KEYPAD, [4, 2], None)]
     h = 1e-6
     for seed, (shape, mask, lens, scale) in enumerate(cases):
         q, k, v, dout = _case(100 + seed, *shape)
@@ -59,16 +60,17 @@ def check_bwd_torch_autograd(mha, bwd):
     import torch
     for seed, (shape, mask, lens) in enumerate([((2, 9, 3, 11, 5), NONE, None),
                                                 ((2, 10, 2, 10, 4), CAUSAL, None),
-                                                ((3, 7, 2, 12, 6), KEYPAD, [12, 1, 5])]):
+                                                ((3, 7, 2, 12, 6), KEYPAD, [12, 1, 5]),
+                                                ((3, 8, 2, 8, 4), CAUSAL | KEYPAD, [8, 1, 5])]):
         q, k, v, dout = _case(200 + seed, *shape)
         B, Lq, H, Lk, d = shape
         scale = 1.0 / np.sqrt(d)
         tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
         s = torch.einsum("bihd,bjhd->bhij", tq, tk) * scale
         keep = torch.ones(B, 1, Lq, Lk, dtype=torch.bool)
-        if mask == CAUSAL:
+        if mask & CAUSAL:
             keep = keep & torch.tril(torch.ones(Lq, Lk, dtype=torch.bool))
-        if mask == KEYPAD:
+        if mask & KEYPAD:
             for b, n in enumerate(lens):
                 keep[b, :, :, n:] = False
         s = s.masked_fill(~keep, float("-inf"))

@@ -302,6 +302,81 @@ def check_key_padding(mha):
     assert np.array_equal(o2[1], mha(q[1:2], k[1:2], v[1:2])[0])
 
 
+def check_combined_mask(mha):
+    """Both masks (kind 3): row i of sequence b sees keys j <= i with
+    j < key_lens[b].  Rows below the length equal the causal rows and rows at or
+    past it equal the key-padding rows, bit for bit; keys a row may not see do
+    not matter at all."""
+    rng = _rng(14)
+    B, L, H, d = 4, 9, 2, 5
+    q = rng.standard_normal((B, L, H, d))
+    k = rng.standard_normal((B, L, H, d))
+    v = rng.standard_normal((B, L, H, d))
+    lens = np.array([9, 3, 0, 6], dtype=np.int32)
+    o, lse = mha(q, k, v, CAUSAL | KEYPAD, key_lens=lens, return_lse=True)
+    oc = mha(q, k, v, CAUSAL)
+    op = mha(q, k, v, KEYPAD, key_lens=lens)
+    for b in range(B):
+        n = int(lens[b])
+        assert np.array_equal(o[b, :n], oc[b, :n])
+        assert np.array_equal(o[b, n:], op[b, n:])
+    # sequence 2 has no key: every row is 0 with log-sum-exp -inf
+    assert np.all(o[2] == 0.0) and np.all(np.isneginf(lse[2]))
+    # perturbing every key a row may not see changes nothing
+    for b in range(B):
+        for i in range(L):
+            n_vis = min(i + 1, int(lens[b]))
+            k2 = k.copy()
+            v2 = v.copy()
+            k2[b, n_vis:] = rng.standard_normal(k2[b, n_vis:].shape) * 7
+            v2[b, n_vis:] = rng.standard_normal(v2[b, n_vis:].shape) * 7
+            o2 = mha(q, k2, v2, CAUSAL | KEYPAD, key_lens=lens)
+            assert np.array_equal(o2[b, i], o[b, i])
+    # removed weights are exactly 0, the rest sum to 1
+    vd = np.zeros((B, L, H, L))
+    for j in range(L):
+        vd[:, j, :, j] = 1.0
+    a = mha(q, k, vd, CAUSAL | KEYPAD, key_lens=lens)
+    for b in range(B):
+        for i in range(L):
+            n_vis = min(i + 1, int(lens[b]))
+            assert np.all(a[b, i, :, n_vis:] == 0.0)
+            if n_vis > 0:
+                assert np.all(a[b, i, :, :n_vis] > 0.0)
+                assert np.allclose(a[b, i].sum(axis=-1), 1.0, rtol=0, atol=1e-14)
+
+
+def check_value_width(mha):
+    """d_v != d_k (Equation (1) takes values of width d_v): every output column
+    is the same weighted mean of one value column, so splitting the value
+    columns splits the output columns bit for bit, and the weights (read off
+    with one-hot values, d_v = Lk) do not depend on d_v."""
+    rng = _rng(15)
+    B, Lq, Lk, H, d = 2, 6, 7, 3, 4
+    q = rng.standard_normal((B, Lq, H, d))
+    k = rng.standard_normal((B, Lk, H, d))
+    v = rng.standard_normal((B, Lk, H, 11))
+    for mask, lens in ((NONE, None), (KEYPAD, np.array([7, 2], dtype=np.int32))):
+        o = mha(q, k, v, mask, key_lens=lens)
+        assert o.shape == (B, Lq, H, 11)
+        o1 = mha(q, k, np.ascontiguousarray(v[..., :5]), mask, key_lens=lens)
+        o2 = mha(q, k, np.ascontiguousarray(v[..., 5:]), mask, key_lens=lens)
+        assert np.array_equal(o[..., :5], o1) and np.array_equal(o[..., 5:], o2)
+        for c in range(11):
+            oc = mha(q, k, np.ascontiguousarray(v[..., c:c + 1]), mask, key_lens=lens)
+            assert np.array_equal(o[..., c:c + 1], oc)
+    # the scale defaults to 1/sqrt(d_k), not 1/sqrt(d_v)
+    onehot = np.zeros((B, Lk, H, Lk))
+    for j in range(Lk):
+        onehot[:, j, :, j] = 1.0
+    a = mha(q, k, onehot)
+    a_ref = mha(q, k, onehot, scale=1.0 / math.sqrt(d))
+    assert np.array_equal(a, a_ref)
+    s = np.einsum("bihc,bjhc->bihj", q, k) / math.sqrt(d)
+    e = np.exp(s - s.max(axis=-1, keepdims=True))
+    assert np.allclose(a, e / e.sum(axis=-1, keepdims=True), rtol=0, atol=1e-14)
+
+
 def check_empty(mha):
     rng = _rng(10)
     q = rng.standard_normal((2, 3, 2, 4))
@@ -316,44 +391,46 @@ def check_empty(mha):
 # --------------------------------------------------------------------------
 def brute_force(q, k, v, mask_kind=NONE, key_lens=None, scale=None):
     """Pure Python with math.fsum: weights e^{s_j} / sum e^{s_i} exactly as
-    written, no max-subtraction (inputs kept small so nothing overflows)."""
+    written, no max-subtraction (inputs kept small so nothing overflows).
+    The value width d_v (v's last axis) may differ from d_k; mask kind 3
+    keeps key j for row i only when j <= i and j < key_lens[b]."""
     B, Lq, H, d = q.shape
     Lk = k.shape[1]
+    d_v = v.shape[3]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    out = np.zeros((B, Lq, H, d))
+    out = np.zeros((B, Lq, H, d_v))
     for b in range(B):
         for h in range(H):
             for i in range(Lq):
-                keys = range(Lk)
-                if mask_kind == CAUSAL:
-                    keys = range(min(i + 1, Lk))
-                elif mask_kind == KEYPAD:
-                    keys = range(max(0, min(int(key_lens[b]), Lk)))
-                keys = list(keys)
+                keys = [j for j in range(Lk)
+                        if not (mask_kind & CAUSAL and j > i)
+                        and not (mask_kind & KEYPAD and j >= int(key_lens[b]))]
                 if not keys:
                     continue
                 e = {j: math.exp(scale * math.fsum(float(q[b, i, h, c]) * float(k[b, j, h, c])
                                                    for c in range(d))) for j in keys}
                 total = math.fsum(e.values())
-                for c in range(d):
+                for c in range(d_v):
                     out[b, i, h, c] = math.fsum(e[j] / total * float(v[b, j, h, c]) for j in keys)
     return out
 
 
 def check_brute_force(mha):
     rng = _rng(12)
-    for trial in range(12):
+    for trial in range(16):
         B = int(rng.integers(1, 3))
         H = int(rng.integers(1, 3))
         d = int(rng.integers(1, 5))
+        # every third trial a wider value row (d_v > d_k)
+        d_v = d + int(rng.integers(1, 4)) if trial % 3 == 2 else d
         Lk = int(rng.integers(1, 6))
-        mask = trial % 3
-        Lq = Lk if mask == CAUSAL else int(rng.integers(1, 6))
+        mask = trial % 4
+        Lq = Lk if mask & CAUSAL else int(rng.integers(1, 6))
         q = rng.standard_normal((B, Lq, H, d))
         k = rng.standard_normal((B, Lk, H, d))
-        v = rng.standard_normal((B, Lk, H, d))
-        lens = rng.integers(0, Lk + 1, size=B).astype(np.int32) if mask == KEYPAD else None
+        v = rng.standard_normal((B, Lk, H, d_v))
+        lens = rng.integers(0, Lk + 1, size=B).astype(np.int32) if mask & KEYPAD else None
         scale = None if trial % 2 == 0 else float(rng.uniform(0.1, 2.0))
         o = mha(q, k, v, mask, key_lens=lens, scale=scale)
         ref = brute_force(q, k, v, mask, lens, scale)
@@ -365,20 +442,23 @@ def check_torch_sdpa(mha):
     import torch
     import torch.nn.functional as F
     rng = _rng(13)
-    for mask in (NONE, CAUSAL, KEYPAD):
+    for mask, d_v in ((NONE, 16), (CAUSAL, 16), (KEYPAD, 16), (CAUSAL | KEYPAD, 16),
+                      (NONE, 24), (CAUSAL | KEYPAD, 40)):
         B, H, d = 3, 4, 16
-        Lq, Lk = (37, 37) if mask == CAUSAL else (29, 41)
+        Lq, Lk = (41, 41) if mask & CAUSAL else (29, 41)
         q = rng.standard_normal((B, Lq, H, d))
         k = rng.standard_normal((B, Lk, H, d))
-        v = rng.standard_normal((B, Lk, H, d))
-        lens = np.array([41, 1, 17], dtype=np.int32) if mask == KEYPAD else None
+        v = rng.standard_normal((B, Lk, H, d_v))
+        lens = np.array([41, 1, 17], dtype=np.int32) if mask & KEYPAD else None
         o = mha(q, k, v, mask, key_lens=lens)
         allowed = torch.ones(B, 1, Lq, Lk, dtype=torch.bool)
-        if mask == CAUSAL:
+        if mask & CAUSAL:
             allowed &= torch.ones(Lq, Lk, dtype=torch.bool).tril()
-        if mask == KEYPAD:
+        if mask & KEYPAD:
             for b in range(B):
                 allowed[b, :, :, int(lens[b]):] = False
+        # every row keeps at least key 0 (torch's softmax of an empty row is NaN)
+        assert allowed.any(dim=-1).all()
         tq, tk, tv = (torch.from_numpy(x).permute(0, 2, 1, 3) for x in (q, k, v))
         ref = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=allowed)
         ref = ref.permute(0, 2, 1, 3).numpy()
@@ -389,5 +469,6 @@ ALL_CHECKS = [
     check_worked_example, check_two_key_example, check_toy_shape,
     check_weights_positive_sum_one, check_shift_invariance, check_weight_ratio,
     check_temperature_form, check_limits, check_lse_bounds, check_causal,
-    check_key_padding, check_empty, check_brute_force, check_torch_sdpa,
+    check_key_padding, check_combined_mask, check_value_width, check_empty, check_brute_force,
+    check_torch_sdpa,
 ]

@@ -11,8 +11,8 @@ from tests import oracle_bwd_pins, oracle_pins
 # (name, text in mha_oracle.c, replacement)
 C_MUTANTS = [
     ("scale_dropped", "s[j] = scale * dot;", "s[j] = dot;"),
-    ("values_read_from_keys", "const double* v_row = v + j * kv_row_stride;",
-     "const double* v_row = k + j * kv_row_stride;"),
+    ("values_read_from_keys", "const double* v_row = v + j * v_row_stride;",
+     "const double* v_row = k + j * k_row_stride;"),
     ("diagonal_masked", "n = i + 1 < Lk ? i + 1 : Lk;", "n = i < Lk ? i : Lk;"),
     ("causal_ignored", "n = i + 1 < Lk ? i + 1 : Lk;", "n = Lk;"),
     ("no_normalisation", "for (int64_t j = 0; j < n; ++j) s[j] /= sum;", ""),
@@ -21,6 +21,13 @@ C_MUTANTS = [
     ("row_order_wrong", "const int64_t h = (r / Lq) % H;", "const int64_t h = r % H;"),
     ("padding_length_off_by_one", "n = len;", "n = len > 0 ? len - 1 : 0;"),
     ("query_row_stride_wrong", "q + ((b * Lq + i) * H + h) * d", "q + ((b * Lq + h) * H + i) * d"),
+    # both masks together: padding dropped whenever the causal bit is set
+    ("combined_mask_padding_dropped", "if (len < n) n = len;",
+     "if (len < n && !(mask_kind & ORACLE_MASK_CAUSAL)) n = len;"),
+    # d_v != d_k: value rows or output rows laid out with the key width
+    ("value_stride_uses_dk", "H * d_k, H * d_v, scale, s", "H * d_k, H * d_k, scale, s"),
+    ("output_stride_uses_dk", "double* o_row = out + ((b * Lq + i) * H + h) * d_v;",
+     "double* o_row = out + ((b * Lq + i) * H + h) * d_k;"),
 ]
 
 

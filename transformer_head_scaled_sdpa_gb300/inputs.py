@@ -28,8 +28,10 @@ import torch
 MASK_NONE = 0
 MASK_CAUSAL = 1
 MASK_KEY_PADDING = 2
+MASK_CAUSAL_KEY_PADDING = 3  # both masks (a decoder over padded sequences)
 
-MASK_NAMES = {MASK_NONE: "none", MASK_CAUSAL: "causal", MASK_KEY_PADDING: "key_padding"}
+MASK_NAMES = {MASK_NONE: "none", MASK_CAUSAL: "causal", MASK_KEY_PADDING: "key_padding",
+              MASK_CAUSAL_KEY_PADDING: "causal_key_padding"}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -101,7 +103,7 @@ def generate(w: Workload, seed: int | None = None, batch: slice | None = None):
             x.mul_(w.input_scale)
         out[name] = x.to(w.dtype)
     key_lens = None
-    if w.mask_kind == MASK_KEY_PADDING:
+    if w.mask_kind & MASK_KEY_PADDING:
         key_lens = torch.randint(w.len_lo, w.len_hi + 1, (w.B,), generator=g,
                                  dtype=torch.int64).to(torch.int32)
     out["key_lens"] = key_lens
