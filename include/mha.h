@@ -27,12 +27,19 @@
  *                         decoder's second attention layer, cookipedia
  *                         decoder section).  Not on the pages: its meaning
  *                         is this library's definition.
+ *   MHA_MASK_CAUSAL_KEY_PADDING  both: key j is visible to query i of
+ *                         sequence b only if j <= i and j < key_lens[b] (a
+ *                         decoder's self-attention over padded sequences).
+ *                         Requires Lq == Lk and key_lens.  Also this
+ *                         library's definition: a key passes both masks.
  * A row with no visible key (Lk == 0, or key_lens[b] <= 0) gets output 0.
  *
  * Layout: q and out are [B, Lq, H, d_k], k and v are [B, Lk, H, d_k], dense
  * row-major (d_k fastest, then H, then L, then B).  The output therefore comes
  * out already concatenated over heads: row (b, i) holds H*d_k contiguous
- * values, ready for the output projection W^O.  d_v = d_k.
+ * values, ready for the output projection W^O.  d_v = d_k except in the
+ * *_dv entries, where v and out rows have their own width d_v (Equation (1)
+ * takes values of dimension d_v).
  *
  * Ownership: the caller owns every buffer and the stream.  No entry point
  * allocates device memory, and the device entry points never synchronise.
@@ -69,7 +76,8 @@ typedef enum {
 typedef enum {
     MHA_MASK_NONE = 0,
     MHA_MASK_CAUSAL = 1,
-    MHA_MASK_KEY_PADDING = 2
+    MHA_MASK_KEY_PADDING = 2,
+    MHA_MASK_CAUSAL_KEY_PADDING = 3 /* both (a bit set: causal | key padding) */
 } mha_mask_kind;
 
 /*
@@ -80,10 +88,13 @@ typedef enum {
  *             even from float32 accumulators.
  *   B, H, Lq, Lk   sizes >= 0.  B*H*Lq == 0 is a no-op returning MHA_OK;
  *             Lk == 0 writes zeros.  k and v may be NULL when Lk == 0.
- *   d_k       64 or 128.
+ *   d_k       a multiple of 8 from 8 to 128 (64 and 128 are the kernels'
+ *             widths; other sizes run on the next wider kernel, the tensor
+ *             maps reading the missing features as 0 and writing only d_k
+ *             output columns).
  *   mask_kind one of mha_mask_kind.
- *   key_lens  device pointer to B int32 values, read only under
- *             MHA_MASK_KEY_PADDING (may be NULL otherwise).
+ *   key_lens  device pointer to B int32 values, read only when the mask
+ *             includes key padding (may be NULL otherwise).
  *   scale     multiplier of q.k (the inverse temperature; the formula page
  *             transformer-attention, section 証明, takes the divisor tau > 0);
  *             0 selects 1/sqrt(d_k).  NaN, infinite or negative values are
@@ -132,6 +143,24 @@ int mha_fwd_f32_lse(const void* q, const void* k, const void* v, void* out, floa
                     const int32_t* key_lens, float scale, void* stream);
 
 /*
+ * mha_fwd_dv, mha_fwd_f32_dv -- the forward with a value width d_v of its own
+ * ("Attention Is All You Need", Section 3.2.1: values of dimension d_v).
+ *   q [B, Lq, H, d_k], k [B, Lk, H, d_k], v [B, Lk, H, d_v], out
+ *   [B, Lq, H, d_v]; scores use the d_k columns of q and k, the output is the
+ *   weighted mean of the d_v columns of v.  scale 0 selects 1/sqrt(d_k).
+ *   lse   as mha_fwd_lse, or NULL for none.
+ *   bf16: d_k and d_v multiples of 8 from 8 to 128 (both run on the kernel
+ *   wide enough for the larger); float32: 1 to 256 each.
+ * Other arguments, errors and behaviour as mha_fwd / mha_fwd_f32.
+ */
+int mha_fwd_dv(const void* q, const void* k, const void* v, void* out, float* lse,
+               int B, int H, int Lq, int Lk, int d_k, int d_v, int mask_kind,
+               const int32_t* key_lens, float scale, void* stream);
+int mha_fwd_f32_dv(const void* q, const void* k, const void* v, void* out, float* lse,
+                   int B, int H, int Lq, int Lk, int d_k, int d_v, int mask_kind,
+                   const int32_t* key_lens, float scale, void* stream);
+
+/*
  * mha_bwd -- gradient of mha_fwd for a loss L, given dL/dout (bf16).
  * With the row weights a_ij = exp(s_ij - lse_i) recomputed from q, k and the
  * forward's lse, g_ij = dout_i . v_j, and the formula page's derivative of
@@ -149,7 +178,8 @@ int mha_fwd_f32_lse(const void* q, const void* k, const void* v, void* out, floa
  *                 overlapping no input and each other (MHA_ERR_ALIAS).
  *   workspace     device scratch of mha_bwd_workspace_bytes(...) bytes
  *                 (D_i, float32), 16-byte aligned, owned by the caller.
- *   Other arguments as mha_fwd; d_k 64 or 128.
+ *   Other arguments as mha_fwd (d_v = d_k, any mask kind); d_k a multiple of
+ *   8 from 8 to 128.
  * Products on the tensor cores in float32; the weights and dS are rounded to
  * bf16 before their products, the gradients to bf16 at the end.
  * Returns MHA_OK once enqueued, or an argument / workspace error code.

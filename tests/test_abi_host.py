@@ -59,8 +59,11 @@ def test_argument_errors(lib, fn):
     assert fwd(lib, fn, Lk=-5) == SHAPE
     assert fwd(lib, fn, d=0) == SHAPE
     assert fwd(lib, fn, mask=1, Lq=64, Lk=65) == SHAPE          # causal needs Lq == Lk
-    assert fwd(lib, fn, mask=3) == MASK
+    assert fwd(lib, fn, mask=4) == MASK                           # unknown mask kind
+    assert fwd(lib, fn, mask=-1) == MASK
     assert fwd(lib, fn, mask=2, lens=None) == MASK               # key padding needs key_lens
+    assert fwd(lib, fn, mask=3, lens=None) == MASK               # so do both masks together
+    assert fwd(lib, fn, mask=3, lens=LENS, Lq=64, Lk=65) == SHAPE  # and the causal part Lq == Lk
     assert fwd(lib, fn, scale=math.nan) == SCALE
     assert fwd(lib, fn, scale=math.inf) == SCALE
     assert fwd(lib, fn, scale=-0.5) == SCALE
@@ -77,8 +80,9 @@ def test_argument_errors(lib, fn):
 
 
 def test_bf16_specific_errors(lib):
-    assert fwd(lib, d=96) == UNSUP          # bf16 path: d_k in {64, 128}
-    assert fwd(lib, d=32) == UNSUP
+    assert fwd(lib, d=12) == UNSUP          # bf16 path: d_k a multiple of 8 ...
+    assert fwd(lib, d=4) == UNSUP
+    assert fwd(lib, d=136) == UNSUP         # ... up to 128
     assert fwd(lib, q=Q + 8) == UNSUP       # TMA needs 16-byte aligned bases
     assert fwd(lib, fn="mha_fwd_f32", d=257) == UNSUP
     assert fwd(lib, fn="mha_fwd_f32", q=Q + 2) == UNSUP
@@ -92,6 +96,31 @@ def test_host_entry_errors(lib):
 
 
 LSE = 0x60000000
+
+
+def fwd_dv(lib, fn="mha_fwd_dv", q=Q, k=K, v=V, o=O, lse=None, B=2, H=3, Lq=64, Lk=64, d_k=64,
+           d_v=64, mask=0, lens=None, scale=0.0):
+    return getattr(lib, fn)(q, k, v, o, lse, B, H, Lq, Lk, d_k, d_v, mask, lens, scale, None)
+
+
+@pytest.mark.parametrize("fn", ["mha_fwd_dv", "mha_fwd_f32_dv"])
+def test_dv_entry_errors(lib, fn):
+    assert fwd_dv(lib, fn, d_v=0) == SHAPE
+    assert fwd_dv(lib, fn, d_v=-8) == SHAPE
+    assert fwd_dv(lib, fn, mask=3) == MASK
+    assert fwd_dv(lib, fn, lse=LSE + 2) == UNSUP
+    assert fwd_dv(lib, fn, lse=Q) == ALIAS
+    # out is [B, Lq, H, d_v]: with d_v = 128 it reaches 2*64*3*128 elements past O
+    elem = 2 if fn == "mha_fwd_dv" else 4
+    assert fwd_dv(lib, fn, d_v=128, o=V - 2 * 64 * 3 * 128 * elem + 64) == ALIAS
+    assert fwd_dv(lib, fn, B=0) == OK
+
+
+def test_dv_width_limits(lib):
+    assert fwd_dv(lib, d_v=12) == UNSUP       # bf16: multiples of 8 ...
+    assert fwd_dv(lib, d_v=136) == UNSUP      # ... up to 128
+    assert fwd_dv(lib, d_k=20) == UNSUP
+    assert fwd_dv(lib, fn="mha_fwd_f32_dv", d_v=257) == UNSUP
 
 
 @pytest.mark.parametrize("fn", ["mha_fwd_lse", "mha_fwd_f32_lse"])
@@ -138,3 +167,22 @@ def test_decode_entry_errors(lib):
     # many heads over a short cache run in one pass and need none
     assert lib.mha_decode_workspace_bytes(64, 16, 256, 64) == 0
     assert lib.mha_decode_workspace_bytes(2, 3, 64, 96) == 0
+
+
+DOUT, DQ, DK, DVG = 0x80000000, 0x90000000, 0xA0000000, 0xB0000000
+
+
+def bwd(lib, d=64, mask=0, lens=None, lse=LSE, ws=WS, ws_bytes=1 << 20):
+    return lib.mha_bwd(Q, K, V, O, DOUT, lse, DQ, DK, DVG, 2, 3, 64, 64, d, mask, lens, 0.0, ws,
+                       ws_bytes, None)
+
+
+def test_bwd_entry_errors(lib):
+    assert bwd(lib, d=12) == UNSUP            # multiples of 8 up to 128
+    assert bwd(lib, d=136) == UNSUP
+    assert bwd(lib, mask=4) == MASK
+    assert bwd(lib, mask=3) == MASK           # both masks need key_lens
+    assert bwd(lib, lse=None) == NULL
+    assert bwd(lib, ws=None) == WORKSPACE
+    assert lib.mha_bwd_workspace_bytes(2, 3, 64, 64, 96) > 0
+    assert lib.mha_bwd_workspace_bytes(2, 3, 64, 64, 12) == 0

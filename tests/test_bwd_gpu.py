@@ -57,6 +57,12 @@ SHAPES = [
     (3, 2, 300, 300, 128, CAUSAL, None),
     (2, 4, 129, 129, 64, CAUSAL, None),
     (4, 2, 130, 257, 128, KEYPAD, [257, 0, 127, 1]),
+    # both masks together (kind 3); other head sizes on the 64 / 128 kernels
+    (3, 2, 300, 300, 64, 3, [300, 129, 0]),
+    (2, 2, 256, 256, 128, 3, [200, 256]),
+    (2, 3, 200, 333, 32, NONE, None),
+    (3, 2, 300, 300, 96, CAUSAL, None),
+    (2, 2, 130, 257, 8, KEYPAD, [257, 40]),
 ]
 
 

@@ -323,6 +323,84 @@ def test_f32_shapes(mha, shape):
 
 
 # --------------------------------------------------------------------------
+# other head sizes, a value width of its own (d_v != d_k), both masks together
+# --------------------------------------------------------------------------
+BOTH = inputs.MASK_CAUSAL_KEY_PADDING
+WIDTH_SHAPES = [
+    # B, H, Lq, Lk, d_k, d_v, mask, key_lens
+    (2, 3, 200, 333, 32, 32, NONE, None),
+    (2, 2, 300, 700, 32, 32, NONE, None),        # d 64 kernel with exponential turns
+    (3, 2, 300, 300, 96, 96, CAUSAL, None),
+    (2, 3, 130, 257, 8, 8, KEYPAD, [257, 3]),
+    (2, 2, 256, 256, 120, 120, NONE, None),
+    (2, 2, 200, 333, 64, 128, NONE, None),
+    (2, 2, 256, 256, 128, 64, CAUSAL, None),
+    (2, 3, 128, 640, 32, 96, KEYPAD, [640, 100]),
+    (1, 4, 100, 100, 48, 16, NONE, None),
+    (3, 2, 300, 300, 64, 64, BOTH, [300, 129, 0]),
+    (2, 3, 384, 384, 128, 128, BOTH, [200, 384]),
+    (2, 2, 1, 1, 64, 64, BOTH, [1, 0]),
+    (4, 2, 700, 700, 64, 64, BOTH, [700, 1, 513, 256]),
+    (2, 2, 260, 260, 40, 72, BOTH, [260, 77]),
+]
+
+
+def _width_case(shape, dtype=torch.bfloat16):
+    B, H, Lq, Lk, d_k, d_v, mask, lens = shape
+    case = inputs.random_case(zlib.crc32(repr(shape).encode()) & 0xFFFF, B, H, Lq, Lk, d_k,
+                              dtype=dtype, d_v=d_v)
+    if lens is not None:
+        case["key_lens"] = torch.tensor(lens, dtype=torch.int32)
+    return case, mask
+
+
+@pytest.mark.parametrize("shape", WIDTH_SHAPES,
+                         ids=lambda s: "x".join(map(str, s[:6])) + f"-m{s[6]}")
+def test_widths_and_both_masks(mha, shape):
+    """bf16 on the tensor-core kernels: head sizes other than 64 / 128 run on
+    the next wider kernel (tensor maps zero-fill the missing features and clip
+    the output), d_v may differ from d_k, and mask kind 3 applies both masks.
+    The row log-sum-exp comes out of the same launch."""
+    case, mask = _width_case(shape)
+    out, lse = pu.gpu_run_lse(mha, case, mask)
+    ref, ref_lse = pu.oracle_run(case, mask, return_lse=True)
+    assert tuple(out.shape) == ref.shape
+    pu.assert_bf16_close(out.cpu(), ref, f"widths {shape}")
+    pu.assert_lse_close(lse.cpu(), ref_lse, f"widths {shape}")
+    # the plain entry gives the same output bit for bit
+    g = pu.to_cuda(case)
+    plain = mha.mha_fwd(g["q"], g["k"], g["v"], mask_kind=mask, key_lens=g["key_lens"])
+    assert torch.equal(plain, out)
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 5, 9, 3, 5, NONE, None),
+                                   (2, 3, 70, 70, 17, 40, BOTH, [70, 9]),
+                                   (2, 2, 33, 90, 64, 8, KEYPAD, [90, 0]),
+                                   (1, 2, 40, 40, 256, 200, CAUSAL, None)],
+                         ids=lambda s: "x".join(map(str, s[:6])) + f"-m{s[6]}")
+def test_f32_widths_and_both_masks(mha, shape):
+    case, mask = _width_case(shape, torch.float32)
+    out, lse = pu.gpu_run_lse(mha, case, mask)
+    ref, ref_lse = pu.oracle_run(case, mask, return_lse=True)
+    pu.assert_f32_close(out.cpu(), ref, f"f32 widths {shape}")
+    pu.assert_lse_close(lse.cpu(), ref_lse, f"f32 widths {shape}")
+
+
+def test_both_masks_equal_their_parts(mha):
+    """Under both masks, rows below the sequence's key length equal the causal
+    launch's rows and rows at or past it equal the key-padding launch's, bit
+    for bit (the kernel visits the same keys in the same order)."""
+    shape = (3, 2, 520, 520, 64, 64, BOTH, [520, 200, 333])
+    case, _ = _width_case(shape)
+    both = pu.gpu_run(mha, case, BOTH).cpu()
+    causal = pu.gpu_run(mha, case, CAUSAL).cpu()
+    pad = pu.gpu_run(mha, case, KEYPAD).cpu()
+    for b, n in enumerate(shape[7]):
+        assert torch.equal(both[b, :n], causal[b, :n])
+        assert torch.equal(both[b, n:], pad[b, n:])
+
+
+# --------------------------------------------------------------------------
 # host-buffer entry and device-side failure reporting
 # --------------------------------------------------------------------------
 def test_host_entry_matches_device_entry(mha):

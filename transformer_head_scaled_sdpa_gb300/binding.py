@@ -64,6 +64,9 @@ def lib():
             h.mha_fwd_lse.argtypes = _FWD_LSE_ARGS
             h.mha_fwd_f32_lse.restype = _c_i
             h.mha_fwd_f32_lse.argtypes = _FWD_LSE_ARGS
+            for name in ("mha_fwd_dv", "mha_fwd_f32_dv"):
+                getattr(h, name).restype = _c_i
+                getattr(h, name).argtypes = [_c_p] * 5 + [_c_i] * 7 + [_c_p, ctypes.c_float, _c_p]
             h.mha_bwd.restype = _c_i
             h.mha_bwd.argtypes = [_c_p] * 9 + [_c_i] * 6 + [_c_p, ctypes.c_float, _c_p,
                                                             ctypes.c_size_t, _c_p]
@@ -108,12 +111,13 @@ def _stream_handle(stream) -> int:
     return stream.cuda_stream
 
 
-def _shape(q, k, v):
+def _shape(q, k, v, allow_dv=False):
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be [B, L, H, d_k]")
     B, Lq, H, d = q.shape
     Lk = k.shape[1]
-    if tuple(k.shape) != (B, Lk, H, d) or tuple(v.shape) != (B, Lk, H, d):
+    d_v = v.shape[3] if allow_dv else d
+    if tuple(k.shape) != (B, Lk, H, d) or tuple(v.shape) != (B, Lk, H, d_v):
         raise ValueError(f"k {tuple(k.shape)} / v {tuple(v.shape)} do not match q {tuple(q.shape)}")
     return B, H, Lq, Lk, d
 
@@ -129,20 +133,37 @@ def _check_tensor(t, name, dtype, device_kind):
 
 def _call_fwd(fn_name, dtype, q, k, v, out, mask_kind, key_lens, scale, stream,
               lse=None, want_lse=False):
-    B, H, Lq, Lk, d = _shape(q, k, v)
+    B, H, Lq, Lk, d = _shape(q, k, v, allow_dv=True)
+    d_v = v.shape[3]
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check_tensor(t, n, dtype, "cuda")
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty((B, Lq, H, d_v), dtype=dtype, device=q.device)
     _check_tensor(out, "out", dtype, "cuda")
-    if tuple(out.shape) != tuple(q.shape):
-        raise ValueError("out must have q's shape")
+    if tuple(out.shape) != (B, Lq, H, d_v):
+        raise ValueError("out must be [B, Lq, H, d_v]")
     lens_ptr = None
     if key_lens is not None:
         _check_tensor(key_lens, "key_lens", torch.int32, "cuda")
         if tuple(key_lens.shape) != (B,):
             raise ValueError("key_lens must be [B]")
         lens_ptr = key_lens.data_ptr()
+    if d_v != d:
+        # value rows of their own width: the *_dv entry (lse optional)
+        if want_lse:
+            if lse is None:
+                lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
+            _check_tensor(lse, "lse", torch.float32, "cuda")
+            if tuple(lse.shape) != (B, H, Lq):
+                raise ValueError("lse must be [B, H, Lq]")
+        fn_name += "_dv"
+        rc = getattr(lib(), fn_name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                     lse.data_ptr() if want_lse else None, B, H, Lq, Lk, d, d_v,
+                                     int(mask_kind), lens_ptr, float(scale),
+                                     _stream_handle(stream))
+        if rc != MHA_OK:
+            raise MhaError(rc, fn_name)
+        return (out, lse) if want_lse else out
     if not want_lse:
         rc = getattr(lib(), fn_name)(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                      B, H, Lq, Lk, d, int(mask_kind), lens_ptr, float(scale),
@@ -167,7 +188,8 @@ def _call_fwd(fn_name, dtype, q, k, v, out, mask_kind, key_lens, scale, stream,
 def mha_fwd(q, k, v, out=None, mask_kind: int = 0, key_lens=None, scale: float = 0.0,
             stream=None, return_lse: bool = False, lse=None):
     """bf16 attention forward on the GPU (tcgen05 kernel); returns ``out``, or
-    ``(out, lse)`` with ``return_lse`` (lse: float32 [B, H, Lq], natural log)."""
+    ``(out, lse)`` with ``return_lse`` (lse: float32 [B, H, Lq], natural log).
+    v (and out) may have a width d_v of their own: q, k [.., d_k], v [.., d_v]."""
     return _call_fwd("mha_fwd", torch.bfloat16, q, k, v, out, mask_kind, key_lens, scale,
                      stream, lse, return_lse)
 

@@ -11,7 +11,10 @@
 
 namespace mha {
 
-enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskKeyPadding = 2 };
+// Mask kinds are bit sets: kMaskCausalKeyPadding applies both masks.
+enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskKeyPadding = 2, kMaskCausalKeyPadding = 3 };
+__host__ __device__ __forceinline__ bool masks_causal(int mask_kind) { return (mask_kind & kMaskCausal) != 0; }
+__host__ __device__ __forceinline__ bool masks_padding(int mask_kind) { return (mask_kind & kMaskKeyPadding) != 0; }
 
 // Queries per tile (M of the tcgen05 MMA), keys per K/V tile, and query rows
 // per work unit of the bf16 kernel (two tiles share every K/V tile).
@@ -42,7 +45,8 @@ struct F32Params {
   float* out;
   float* lse;        // [B, H, Lq] natural-log log-sum-exp per row, or null
   const int32_t* key_lens;
-  int B, H, Lq, Lk, d;
+  int B, H, Lq, Lk, d;  // d: width of q and k rows (d_k)
+  int dv;               // width of v and output rows (d_v)
   int mask_kind;
   float scale_log2;
 };
@@ -96,6 +100,8 @@ struct BwdParams {
   const int32_t* key_lens;
   DeviceStatus* status;
   int B, H, Lq, Lk;
+  int d;              // row width of q, k, v, out and the gradients (a multiple of 8,
+                      // at most the kernel's width; the tensor maps zero-fill the rest)
   int mask_kind;
   float scale;        // multiplier of q . k
   float scale_log2;   // scale * log2(e)

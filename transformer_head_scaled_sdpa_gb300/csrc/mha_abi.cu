@@ -89,50 +89,65 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 struct Sizes {
-  size_t q_elems = 0, kv_elems = 0;
+  size_t q_elems = 0, kv_elems = 0;  // q (and k) rows of d_k elements
+  size_t v_elems = 0, o_elems = 0;   // v and out rows of d_v elements
 };
 
-// Checks shared by the device entries.  Returns MHA_OK and sets *empty when
-// there is nothing to compute.
+bool mask_known(int mask_kind) {
+  return mask_kind >= MHA_MASK_NONE && mask_kind <= MHA_MASK_CAUSAL_KEY_PADDING;
+}
+bool has_causal(int mask_kind) { return (mask_kind & MHA_MASK_CAUSAL) != 0; }
+bool has_padding(int mask_kind) { return (mask_kind & MHA_MASK_KEY_PADDING) != 0; }
+
+// Checks shared by the device entries (d_v: the width of v and out rows).
+// Returns MHA_OK and sets *empty when there is nothing to compute.
 int check_args(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq,
-               int Lk, int d_k, int mask_kind, const int32_t* key_lens, float scale,
+               int Lk, int d_k, int d_v, int mask_kind, const int32_t* key_lens, float scale,
                int elem_bytes, size_t align, bool* empty, Sizes* sz) {
   *empty = false;
-  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || d_k < 0) return MHA_ERR_SHAPE;
-  if (mask_kind != MHA_MASK_NONE && mask_kind != MHA_MASK_CAUSAL &&
-      mask_kind != MHA_MASK_KEY_PADDING)
-    return MHA_ERR_MASK;
-  if (mask_kind == MHA_MASK_CAUSAL && Lq != Lk) return MHA_ERR_SHAPE;
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || d_k < 0 || d_v < 0) return MHA_ERR_SHAPE;
+  if (!mask_known(mask_kind)) return MHA_ERR_MASK;
+  if (has_causal(mask_kind) && Lq != Lk) return MHA_ERR_SHAPE;
   if (!std::isfinite(scale) || scale < 0.f) return MHA_ERR_SCALE;
-  if (d_k == 0) return MHA_ERR_SHAPE;
+  if (d_k == 0 || d_v == 0) return MHA_ERR_SHAPE;
   // every element index must fit comfortably in 64 bits and every row count in 31
   const long long rows_q = static_cast<long long>(B) * H * Lq;
   const long long rows_k = static_cast<long long>(B) * H * Lk;
   if (rows_q > (1ll << 40) || rows_k > (1ll << 40)) return MHA_ERR_SHAPE;
   sz->q_elems = static_cast<size_t>(rows_q) * d_k;
   sz->kv_elems = static_cast<size_t>(rows_k) * d_k;
+  sz->v_elems = static_cast<size_t>(rows_k) * d_v;
+  sz->o_elems = static_cast<size_t>(rows_q) * d_v;
   if (rows_q == 0) {
     *empty = true;
     return MHA_OK;
   }
   if (!q || !out) return MHA_ERR_NULL;
   if (Lk > 0 && (!k || !v)) return MHA_ERR_NULL;
-  if (mask_kind == MHA_MASK_KEY_PADDING && !key_lens) return MHA_ERR_MASK;
+  if (has_padding(mask_kind) && !key_lens) return MHA_ERR_MASK;
   const uintptr_t mis = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out) |
                          (Lk > 0 ? (reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v))
                                  : 0)) &
                         (align - 1);
   if (mis) return MHA_ERR_UNSUPPORTED;
-  const size_t ob = sz->q_elems * elem_bytes;
-  const size_t kb = sz->kv_elems * elem_bytes;
-  if (overlaps(out, ob, q, ob) || overlaps(out, ob, k, kb) || overlaps(out, ob, v, kb))
+  const size_t ob = sz->o_elems * elem_bytes;
+  if (overlaps(out, ob, q, sz->q_elems * elem_bytes) ||
+      overlaps(out, ob, k, sz->kv_elems * elem_bytes) ||
+      overlaps(out, ob, v, sz->v_elems * elem_bytes))
     return MHA_ERR_ALIAS;
   return MHA_OK;
 }
 
+// bf16 rows on the tensor-core kernels: a multiple of 8 elements (16-byte row
+// strides for the tensor maps) up to 128; narrower rows are zero-filled by the
+// tensor-map loads up to the kernel's width (64 or 128) and clipped on store.
+bool bf16_width_ok(int d) { return d >= 8 && d <= 128 && d % 8 == 0; }
+int bf16_kernel_width(int d_k, int d_v) { return (d_k <= 64 && d_v <= 64) ? 64 : 128; }
+
 // 4-D map over a [B, L, H, d] bf16 tensor; box = 64 features x 1 head x `rows`
 // rows (128 for the forward's tiles, 64 for the decode step's) x 1 sequence,
-// 128-byte swizzle (the tcgen05 operand layout).
+// 128-byte swizzle (the tcgen05 operand layout).  Features past d read as 0
+// and are not written by stores.
 bool encode_map(CUtensorMap* m, const void* base, int B, int L, int H, int d, int rows = 128) {
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
@@ -156,9 +171,10 @@ int check_lse(const float* lse, const void* q, const void* k, const void* v, con
   if (!lse) return MHA_ERR_NULL;
   if (reinterpret_cast<uintptr_t>(lse) & 3u) return MHA_ERR_UNSUPPORTED;
   const size_t lb = static_cast<size_t>(rows_q) * 4;
-  const size_t ob = sz.q_elems * elem_bytes, kb = sz.kv_elems * elem_bytes;
-  if (overlaps(lse, lb, q, ob) || overlaps(lse, lb, out, ob) || overlaps(lse, lb, k, kb) ||
-      overlaps(lse, lb, v, kb))
+  if (overlaps(lse, lb, q, sz.q_elems * elem_bytes) ||
+      overlaps(lse, lb, out, sz.o_elems * elem_bytes) ||
+      overlaps(lse, lb, k, sz.kv_elems * elem_bytes) ||
+      overlaps(lse, lb, v, sz.v_elems * elem_bytes))
     return MHA_ERR_ALIAS;
   return MHA_OK;
 }
@@ -204,15 +220,15 @@ float effective_scale(float scale, int d_k) {
 }
 
 int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse, bool want_lse,
-             int B, int H, int Lq, int Lk, int d_k, int mask_kind, const int32_t* key_lens,
-             float scale, void* stream) {
+             int B, int H, int Lq, int Lk, int d_k, int d_v, int mask_kind,
+             const int32_t* key_lens, float scale, void* stream) {
   t_info = mha::LaunchInfo{};
   bool empty = false;
   Sizes sz;
-  int rc = check_args(q, k, v, out, B, H, Lq, Lk, d_k, mask_kind, key_lens, scale, 2, 16, &empty,
-                      &sz);
+  int rc = check_args(q, k, v, out, B, H, Lq, Lk, d_k, d_v, mask_kind, key_lens, scale, 2, 16,
+                      &empty, &sz);
   if (rc != MHA_OK) return rc;
-  if (d_k != 64 && d_k != 128) return MHA_ERR_UNSUPPORTED;
+  if (!bf16_width_ok(d_k) || !bf16_width_ok(d_v)) return MHA_ERR_UNSUPPORTED;
   if (empty) return MHA_OK;
   const long long rows_q = static_cast<long long>(B) * H * Lq;
   if (want_lse && (rc = check_lse(lse, q, k, v, out, sz, 2, rows_q)) != MHA_OK) return rc;
@@ -220,13 +236,13 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
   rc = device_state(&dev);
   if (rc != MHA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (Lk == 0) return no_keys(out, sz.q_elems * 2, lse, static_cast<size_t>(rows_q), s);
+  if (Lk == 0) return no_keys(out, sz.o_elems * 2, lse, static_cast<size_t>(rows_q), s);
   const long long n_qtiles = (Lq + mha::kUnitRows - 1) / mha::kUnitRows;
   if (n_qtiles * B * H > 0x7fffffffll) return MHA_ERR_SHAPE;
   mha::Bf16Params p;
   std::memset(&p, 0, sizeof(p));
   if (!encode_map(&p.tm_q, q, B, Lq, H, d_k) || !encode_map(&p.tm_k, k, B, Lk, H, d_k) ||
-      !encode_map(&p.tm_v, v, B, Lk, H, d_k) || !encode_map(&p.tm_o, out, B, Lq, H, d_k))
+      !encode_map(&p.tm_v, v, B, Lk, H, d_v) || !encode_map(&p.tm_o, out, B, Lq, H, d_v))
     return MHA_ERR_UNSUPPORTED;
   p.out = out;
   p.lse = lse;
@@ -240,19 +256,21 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
   p.n_qtiles = static_cast<int>(n_qtiles);
   p.scale_log2 = effective_scale(scale, d_k) * kLog2e;
   p.withhold_p = g_withhold_p;
-  return mha::launch_fwd_bf16(p, d_k, s, &t_info) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
+  return mha::launch_fwd_bf16(p, bf16_kernel_width(d_k, d_v), s, &t_info) == cudaSuccess
+             ? MHA_OK
+             : MHA_ERR_LAUNCH;
 }
 
 int fwd_f32(const void* q, const void* k, const void* v, void* out, float* lse, bool want_lse,
-            int B, int H, int Lq, int Lk, int d_k, int mask_kind, const int32_t* key_lens,
-            float scale, void* stream) {
+            int B, int H, int Lq, int Lk, int d_k, int d_v, int mask_kind,
+            const int32_t* key_lens, float scale, void* stream) {
   t_info = mha::LaunchInfo{};
   bool empty = false;
   Sizes sz;
-  int rc = check_args(q, k, v, out, B, H, Lq, Lk, d_k, mask_kind, key_lens, scale, 4, 4, &empty,
-                      &sz);
+  int rc = check_args(q, k, v, out, B, H, Lq, Lk, d_k, d_v, mask_kind, key_lens, scale, 4, 4,
+                      &empty, &sz);
   if (rc != MHA_OK) return rc;
-  if (d_k > 256) return MHA_ERR_UNSUPPORTED;
+  if (d_k > 256 || d_v > 256) return MHA_ERR_UNSUPPORTED;
   if (empty) return MHA_OK;
   const long long rows_q = static_cast<long long>(B) * H * Lq;
   if (want_lse && (rc = check_lse(lse, q, k, v, out, sz, 4, rows_q)) != MHA_OK) return rc;
@@ -260,7 +278,7 @@ int fwd_f32(const void* q, const void* k, const void* v, void* out, float* lse, 
   rc = device_state(&dev);
   if (rc != MHA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (Lk == 0) return no_keys(out, sz.q_elems * 4, lse, static_cast<size_t>(rows_q), s);
+  if (Lk == 0) return no_keys(out, sz.o_elems * 4, lse, static_cast<size_t>(rows_q), s);
   if ((static_cast<long long>(B) * H * Lq + 7) / 8 > 0x7fffffffll) return MHA_ERR_SHAPE;
   mha::F32Params p;
   p.q = static_cast<const float*>(q);
@@ -274,6 +292,7 @@ int fwd_f32(const void* q, const void* k, const void* v, void* out, float* lse, 
   p.Lq = Lq;
   p.Lk = Lk;
   p.d = d_k;
+  p.dv = d_v;
   p.mask_kind = mask_kind;
   p.scale_log2 = effective_scale(scale, d_k) * kLog2e;
   return mha::launch_fwd_f32(p, s, &t_info) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
@@ -285,27 +304,43 @@ extern "C" {
 
 int mha_fwd(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq, int Lk,
             int d_k, int mask_kind, const int32_t* key_lens, float scale, void* stream) {
-  return fwd_bf16(q, k, v, out, nullptr, false, B, H, Lq, Lk, d_k, mask_kind, key_lens, scale,
-                  stream);
+  return fwd_bf16(q, k, v, out, nullptr, false, B, H, Lq, Lk, d_k, d_k, mask_kind, key_lens,
+                  scale, stream);
 }
 
 int mha_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
                 int Lq, int Lk, int d_k, int mask_kind, const int32_t* key_lens, float scale,
                 void* stream) {
-  return fwd_bf16(q, k, v, out, lse, true, B, H, Lq, Lk, d_k, mask_kind, key_lens, scale, stream);
+  return fwd_bf16(q, k, v, out, lse, true, B, H, Lq, Lk, d_k, d_k, mask_kind, key_lens, scale,
+                  stream);
+}
+
+int mha_fwd_dv(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
+               int Lq, int Lk, int d_k, int d_v, int mask_kind, const int32_t* key_lens,
+               float scale, void* stream) {
+  return fwd_bf16(q, k, v, out, lse, lse != nullptr, B, H, Lq, Lk, d_k, d_v, mask_kind, key_lens,
+                  scale, stream);
 }
 
 int mha_fwd_f32(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq,
                 int Lk, int d_k, int mask_kind, const int32_t* key_lens, float scale,
                 void* stream) {
-  return fwd_f32(q, k, v, out, nullptr, false, B, H, Lq, Lk, d_k, mask_kind, key_lens, scale,
+  return fwd_f32(q, k, v, out, nullptr, false, B, H, Lq, Lk, d_k, d_k, mask_kind, key_lens, scale,
                  stream);
 }
 
 int mha_fwd_f32_lse(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                     int H, int Lq, int Lk, int d_k, int mask_kind, const int32_t* key_lens,
                     float scale, void* stream) {
-  return fwd_f32(q, k, v, out, lse, true, B, H, Lq, Lk, d_k, mask_kind, key_lens, scale, stream);
+  return fwd_f32(q, k, v, out, lse, true, B, H, Lq, Lk, d_k, d_k, mask_kind, key_lens, scale,
+                 stream);
+}
+
+int mha_fwd_f32_dv(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                   int H, int Lq, int Lk, int d_k, int d_v, int mask_kind,
+                   const int32_t* key_lens, float scale, void* stream) {
+  return fwd_f32(q, k, v, out, lse, lse != nullptr, B, H, Lq, Lk, d_k, d_v, mask_kind, key_lens,
+                 scale, stream);
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -419,7 +454,7 @@ int mha_decode_static(const void* q, const void* k_cache, const void* v_cache, v
 size_t mha_decode_static_scratch_bytes(void) { return kDecodeStaticScratchBytes; }
 
 size_t mha_bwd_workspace_bytes(int B, int H, int Lq, int Lk, int d_k) {
-  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || (d_k != 64 && d_k != 128)) return 0;
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || !bf16_width_ok(d_k)) return 0;
   return align256(static_cast<size_t>(B) * H * Lq * 4);
 }
 
@@ -431,10 +466,10 @@ int mha_bwd(const void* q, const void* k, const void* v, const void* out, const 
   bool empty = false;
   Sizes sz;
   // the forward's checks on q, k, v, out (and the mask, scale, sizes)
-  int rc = check_args(q, k, v, const_cast<void*>(out), B, H, Lq, Lk, d_k, mask_kind, key_lens,
-                      scale, 2, 16, &empty, &sz);
+  int rc = check_args(q, k, v, const_cast<void*>(out), B, H, Lq, Lk, d_k, d_k, mask_kind,
+                      key_lens, scale, 2, 16, &empty, &sz);
   if (rc != MHA_OK) return rc;
-  if (d_k != 64 && d_k != 128) return MHA_ERR_UNSUPPORTED;
+  if (!bf16_width_ok(d_k)) return MHA_ERR_UNSUPPORTED;
   const long long bh = static_cast<long long>(B) * H;
   if (bh == 0) return MHA_OK;
   const size_t qb = sz.q_elems * 2, kb = sz.kv_elems * 2;
@@ -492,9 +527,12 @@ int mha_bwd(const void* q, const void* k, const void* v, const void* out, const 
   p.Lq = Lq;
   p.Lk = Lk;
   p.mask_kind = mask_kind;
+  p.d = d_k;
   p.scale = effective_scale(scale, d_k);
   p.scale_log2 = p.scale * kLog2e;
-  return mha::launch_bwd(p, d_k, s, &t_info) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
+  return mha::launch_bwd(p, bf16_kernel_width(d_k, d_k), s, &t_info) == cudaSuccess
+             ? MHA_OK
+             : MHA_ERR_LAUNCH;
 }
 
 size_t mha_fwd_host_workspace_bytes(int B, int H, int Lq, int Lk, int d_k, int elem_bytes) {
@@ -516,7 +554,8 @@ int mha_fwd_host(const void* q, const void* k, const void* v, void* out, int B, 
   if (qb == 0) return MHA_OK;
   if (!workspace || workspace_bytes < need) return MHA_ERR_WORKSPACE;
   if (!q || !out || (kb > 0 && (!k || !v))) return MHA_ERR_NULL;
-  if (mask_kind == MHA_MASK_KEY_PADDING && !key_lens) return MHA_ERR_MASK;
+  if (!mask_known(mask_kind)) return MHA_ERR_MASK;
+  if (has_padding(mask_kind) && !key_lens) return MHA_ERR_MASK;
   uint8_t* w = static_cast<uint8_t*>(workspace);
   uint8_t* dq = w;
   uint8_t* dk = dq + align256(qb);
@@ -531,7 +570,7 @@ int mha_fwd_host(const void* q, const void* k, const void* v, void* out, int B, 
       return MHA_ERR_LAUNCH;
   }
   const int32_t* lens = nullptr;
-  if (mask_kind == MHA_MASK_KEY_PADDING) {
+  if (has_padding(mask_kind)) {
     if (cudaMemcpyAsync(dlens, key_lens, static_cast<size_t>(B) * 4, cudaMemcpyHostToDevice, s) !=
         cudaSuccess)
       return MHA_ERR_LAUNCH;

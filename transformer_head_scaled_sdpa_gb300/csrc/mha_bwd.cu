@@ -9,7 +9,7 @@
 //   dV_j  = sum_i a_ij dO_i,     dK_j = scale sum_i dS_ij q_i,
 //   dQ_i  = scale sum_j dS_ij k_j.
 // Three kernels:
-//   bwd_prep_kernel   D_i = dO_i . O_i (float32, one warp per row).
+//   bwd_prep_kernel   D_i = dO_i . O_i (float32; a group of lanes per row).
 //   bwd_dkdv_kernel   one CTA per (b, h, 128-key tile); the query tiles that
 //                     see the keys stream through a two-stage ring.  Per query
 //                     tile: S^T = K Q^T and dP^T = V dO^T on the tensor cores
@@ -76,41 +76,47 @@ __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w <<
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // ---------------------------------------------------------------------------
-// D_i = dO_i . O_i, one warp per row (b, i, h) of [B, Lq, H, d]; stored [B, H, Lq]
+// D_i = dO_i . O_i for every row (b, i, h) of [B, Lq, H, d]; stored [B, H, Lq].
+// A group of G lanes (a power of two, G >= d / 8 up to 16) takes one row, each
+// lane 16-byte pieces of O and dO, so a warp reads 32 / G consecutive rows.
 // ---------------------------------------------------------------------------
-template <int D>
+__host__ __device__ __forceinline__ int prep_group(int d) {
+  const int pieces = d / 8;
+  return pieces <= 1 ? 1 : pieces <= 2 ? 2 : pieces <= 4 ? 4 : pieces <= 8 ? 8 : 16;
+}
+
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ BwdParams p) {
   const long long rows = static_cast<long long>(p.B) * p.H * p.Lq;
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31);
-  if (row >= rows) return;
-  const int h = static_cast<int>(row % p.H);
-  const int i = static_cast<int>((row / p.H) % p.Lq);
-  const int b = static_cast<int>(row / (static_cast<long long>(p.H) * p.Lq));
-  // lane reads D/32 consecutive elements of each row (one 4- or 8-byte load)
-  constexpr int EPL = D / 32;
-  const uint16_t* o = reinterpret_cast<const uint16_t*>(p.out) + row * D + EPL * lane;
-  const uint16_t* g = reinterpret_cast<const uint16_t*>(p.dout) + row * D + EPL * lane;
+  const int G = prep_group(p.d);
+  const int pieces = p.d / 8;
+  const int piece = lane % G;
+  const long long row = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * (32 / G) +
+                        lane / G;
   float acc = 0.f;
-  if constexpr (EPL == 4) {
-    const uint2 ov = *reinterpret_cast<const uint2*>(o);
-    const uint2 gv = *reinterpret_cast<const uint2*>(g);
-    acc = bf_lo(ov.x) * bf_lo(gv.x) + bf_hi(ov.x) * bf_hi(gv.x) + bf_lo(ov.y) * bf_lo(gv.y) +
-          bf_hi(ov.y) * bf_hi(gv.y);
-  } else {
-    const uint32_t ov = *reinterpret_cast<const uint32_t*>(o);
-    const uint32_t gv = *reinterpret_cast<const uint32_t*>(g);
-    acc = bf_lo(ov) * bf_lo(gv) + bf_hi(ov) * bf_hi(gv);
+  if (row < rows) {
+    const uint4* o = reinterpret_cast<const uint4*>(p.out) + row * pieces;
+    const uint4* g = reinterpret_cast<const uint4*>(p.dout) + row * pieces;
+    for (int c = piece; c < pieces; c += G) {
+      const uint4 ov = o[c], gv = g[c];
+      acc += bf_lo(ov.x) * bf_lo(gv.x) + bf_hi(ov.x) * bf_hi(gv.x) + bf_lo(ov.y) * bf_lo(gv.y) +
+             bf_hi(ov.y) * bf_hi(gv.y) + bf_lo(ov.z) * bf_lo(gv.z) + bf_hi(ov.z) * bf_hi(gv.z) +
+             bf_lo(ov.w) * bf_lo(gv.w) + bf_hi(ov.w) * bf_hi(gv.w);
+    }
   }
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) p.dvec[(static_cast<size_t>(b) * p.H + h) * p.Lq + i] = acc;
+  for (int s = G / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (piece == 0 && row < rows) {
+    const int h = static_cast<int>(row % p.H);
+    const int i = static_cast<int>((row / p.H) % p.Lq);
+    const int b = static_cast<int>(row / (static_cast<long long>(p.H) * p.Lq));
+    p.dvec[(static_cast<size_t>(b) * p.H + h) * p.Lq + i] = acc;
+  }
 }
 
 // Visible keys of sequence b (key padding), all keys otherwise.
 __device__ __forceinline__ int kv_len_of(const BwdParams& p, int b) {
   int n = p.Lk;
-  if (p.mask_kind == kMaskKeyPadding) {
+  if (masks_padding(p.mask_kind)) {
     const int len = __ldg(p.key_lens + b);
     n = len < 0 ? 0 : (len > p.Lk ? p.Lk : len);
   }
@@ -143,7 +149,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
   const int kv_len = kv_len_of(p, b);
   const int n_qt = (p.Lq + 127) / 128;
   // query tiles that see a key of this tile (causal: from the diagonal on)
-  const int qt_begin = (p.mask_kind == kMaskCausal) ? kt : 0;
+  const int qt_begin = masks_causal(p.mask_kind) ? kt : 0;
   const int n_iter = (k0 < kv_len) ? (n_qt - qt_begin) : 0;
 
   if (threadIdx.x == 0) {
@@ -335,7 +341,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       // Every (key, query) pair of the tile is visible unless the tile holds
       // keys past the key length, queries past Lq, or the causal diagonal.
       const bool all_visible = k0 + 127 < kv_len && q0 + 127 < p.Lq &&
-                               !(p.mask_kind == kMaskCausal && q0 < k0 + 127);
+                               !(masks_causal(p.mask_kind) && q0 < k0 + 127);
       for (int hf = 0; hf < 2; ++hf) {
         if (!mbar_wait(bar(kScores + hf), it & 1, abort_flag, p.status, kRoleBwdGrad * 64 + kScores + hf)) {
           ok = false;
@@ -374,7 +380,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             for (int u = 0; u < 2; ++u) {
               const int qi = q0 + col0 + t + u;
               const bool vis = key < kv_len && qi < p.Lq &&
-                               !(p.mask_kind == kMaskCausal && key > qi) &&
+                               !(masks_causal(p.mask_kind) && key > qi) &&
                                l2c[t + u] != -INFINITY;
               const float e = ex2_approx(fmaf(__uint_as_float(sr[t + u]), c2, -l2c[t + u]));
               pp[u] = vis ? e : 0.f;
@@ -404,7 +410,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       ok = mbar_wait(bar(kAccDone), 0, abort_flag, p.status, kRoleBwdGrad * 64 + kAccDone);
     if (ok) {
       tc_fence_after();
-      const size_t row_off = ((static_cast<size_t>(b) * p.Lk + key) * p.H + h) * D;
+      const size_t row_off = ((static_cast<size_t>(b) * p.Lk + key) * p.H + h) * p.d;
       __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(p.dv) + row_off;
       __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(p.dk) + row_off;
 #pragma unroll 1
@@ -421,6 +427,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         if (key < p.Lk) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
+            if (32 * c32 + 8 * v4 >= p.d) break;  // columns past d are padding
             uint4 wa, wk;
             wa.x = pack_bf16x2(__uint_as_float(a[8 * v4 + 0]), __uint_as_float(a[8 * v4 + 1]));
             wa.y = pack_bf16x2(__uint_as_float(a[8 * v4 + 2]), __uint_as_float(a[8 * v4 + 3]));
@@ -471,7 +478,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
   const int q0 = qt * 128;
   const int kv_len = kv_len_of(p, b);
   int n_kt = (kv_len + 127) / 128;
-  if (p.mask_kind == kMaskCausal && n_kt > qt + 1) n_kt = qt + 1;
+  if (masks_causal(p.mask_kind) && n_kt > qt + 1) n_kt = qt + 1;
   const int n_iter = n_kt;
 
   if (threadIdx.x == 0) {
@@ -630,7 +637,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       const int k0 = it * 128;
       // every key of the tile visible to every query of the CTA's tile?
       const bool all_visible = k0 + 127 < kv_len && q0 + 127 < p.Lq &&
-                               !(p.mask_kind == kMaskCausal && q0 < k0 + 127);
+                               !(masks_causal(p.mask_kind) && q0 < k0 + 127);
       for (int hf = 0; hf < 2; ++hf) {
         if (!mbar_wait(bar(kScores + hf), it & 1, abort_flag, p.status,
                        kRoleBwdGrad * 64 + 16 + kScores + hf)) {
@@ -656,7 +663,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
               const int key = k0 + 64 * hf + 32 * cq + t + u;
-              const bool vis = row_ok && key < kv_len && !(p.mask_kind == kMaskCausal && key > qi);
+              const bool vis = row_ok && key < kv_len && !(masks_causal(p.mask_kind) && key > qi);
               const float e = ex2_approx(fmaf(__uint_as_float(sr[t + u]), c2, -l2));
               pp[u] = vis ? e : 0.f;
             }
@@ -680,7 +687,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     if (ok) {
       tc_fence_after();
       __nv_bfloat16* dq_row = reinterpret_cast<__nv_bfloat16*>(p.dq) +
-                              ((static_cast<size_t>(b) * p.Lq + qi) * p.H + h) * D;
+                              ((static_cast<size_t>(b) * p.Lq + qi) * p.H + h) * p.d;
 #pragma unroll 1
       for (int c32 = cq; c32 < D / 32; c32 += 2) {
         uint32_t a[32];
@@ -694,6 +701,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         if (qi < p.Lq) {
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
+            if (32 * c32 + 8 * v4 >= p.d) break;  // columns past d are padding
             uint4 w;
             w.x = pack_bf16x2(__uint_as_float(a[8 * v4 + 0]) * p.scale, __uint_as_float(a[8 * v4 + 1]) * p.scale);
             w.y = pack_bf16x2(__uint_as_float(a[8 * v4 + 2]) * p.scale, __uint_as_float(a[8 * v4 + 3]) * p.scale);
@@ -730,7 +738,9 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, LaunchInfo* in
     attr_set[dev] = true;
   }
   const long long rows = static_cast<long long>(p.B) * p.H * p.Lq;
-  bwd_prep_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
+  const long long rows_per_block = 8ll * (32 / prep_group(p.d));
+  bwd_prep_kernel<<<static_cast<unsigned>((rows + rows_per_block - 1) / rows_per_block), 256, 0,
+                    stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long bh = static_cast<long long>(p.B) * p.H;

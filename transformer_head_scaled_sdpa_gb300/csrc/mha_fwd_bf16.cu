@@ -155,13 +155,13 @@ __device__ __forceinline__ Unit decode_unit(const Bf16Params& p, int unit) {
   const int heads_here = min(kHeadGroup, bh_count - group * kHeadGroup);
   const int pair_idx = within / heads_here;
   const int bh = group * kHeadGroup + within % heads_here;
-  const int t = (p.mask_kind == kMaskCausal) ? (n_pairs - 1 - pair_idx) : pair_idx;
+  const int t = masks_causal(p.mask_kind) ? (n_pairs - 1 - pair_idx) : pair_idx;
   Unit u;
   u.b = bh / p.H;
   u.h = bh % p.H;
   u.q0 = t * kUnitRows;
   int kv_len = p.Lk;
-  if (p.mask_kind == kMaskKeyPadding) {
+  if (masks_padding(p.mask_kind)) {
     const int len = __ldg(p.key_lens + u.b);
     kv_len = len < 0 ? 0 : (len > p.Lk ? p.Lk : len);
   }
@@ -171,7 +171,7 @@ __device__ __forceinline__ Unit decode_unit(const Bf16Params& p, int unit) {
   for (int g = 0; g < 2; ++g) {
     const int qs = u.q0 + g * kBlockM;
     int n = (qs < p.Lq) ? n_kv : 0;
-    if (p.mask_kind == kMaskCausal && n > qs / kBlockN + 1) n = qs / kBlockN + 1;
+    if (masks_causal(p.mask_kind) && n > qs / kBlockN + 1) n = qs / kBlockN + 1;
     u.n[g] = n;
   }
   return u;
@@ -662,7 +662,7 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
       // per-element mask on the diagonal tile and a ragged last tile
       const int kbase = j * kBlockN;
       int lim = u.kv_len - kbase;                                  // keys c < lim exist
-      if (p.mask_kind == kMaskCausal && qi - kbase + 1 < lim) lim = qi - kbase + 1;
+      if (masks_causal(p.mask_kind) && qi - kbase + 1 < lim) lim = qi - kbase + 1;
       if (lim < kBlockN) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)
@@ -948,7 +948,7 @@ cudaError_t launch_fwd_bf16(const Bf16Params& p, int d, cudaStream_t stream, Lau
   // mask once units span several key tiles; with one or two key tiles the
   // hand-over at the start of each unit costs more than it saves)
   if (d == 64)
-    return (p.mask_kind != kMaskCausal && p.Lk >= 4 * kBlockN)
+    return (!masks_causal(p.mask_kind) && p.Lk >= 4 * kBlockN)
                ? launch_d<64, true>(p, stream, info)
                : launch_d<64, false>(p, stream, info);
   if (d == 128) return launch_d<128, false>(p, stream, info);

@@ -2,7 +2,8 @@
 //
 // The same operation as the bf16 path ("Attention Is All You Need",
 // Section 3.2.1, Equation (1), every head in parallel), all in float32, for
-// any head size 1 <= d <= 256.  One warp owns one query row (b, i, h):
+// any head size 1 <= d_k, d_v <= 256 (d_v, the value width, may differ from
+// d_k).  One warp owns one query row (b, i, h):
 //   - q (pre-multiplied by scale * log2(e)) is staged in shared memory;
 //   - keys are visited 32 at a time, one per lane: lane t scores key j0 + t;
 //   - the online softmax keeps a running maximum m and sum l per row and
@@ -13,7 +14,8 @@
 //     32 keys, whose weights are broadcast with shuffles, so V rows are read
 //     coalesced.
 // Masks remove keys before the softmax: causal keeps keys j <= i, key padding
-// keeps j < key_lens[b] (clamped to [0, Lk]).  A row with no key stores 0.
+// keeps j < key_lens[b] (clamped to [0, Lk]), both together keep keys that
+// pass both.  A row with no key stores 0.
 // Optionally each row's log-sum-exp (the log of the softmax denominator) is
 // stored as well; -inf for a row with no key.
 #include "kernels.h"
@@ -48,14 +50,14 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) fwd_f32_kernel(const F32P
   const int h = static_cast<int>(row % p.H);
   const int i = static_cast<int>((row / p.H) % p.Lq);
   const int b = static_cast<int>(row / (static_cast<long long>(p.H) * p.Lq));
-  const int d = p.d;
+  const int d = p.d, dv = p.dv;
 
   int n = p.Lk;
-  if (p.mask_kind == kMaskCausal) {
-    n = (i + 1 < p.Lk) ? i + 1 : p.Lk;
-  } else if (p.mask_kind == kMaskKeyPadding) {
+  if (masks_causal(p.mask_kind)) n = (i + 1 < p.Lk) ? i + 1 : p.Lk;
+  if (masks_padding(p.mask_kind)) {
     const int len = __ldg(p.key_lens + b);
-    n = len < 0 ? 0 : (len > p.Lk ? p.Lk : len);
+    const int clamped = len < 0 ? 0 : (len > p.Lk ? p.Lk : len);
+    if (clamped < n) n = clamped;
   }
 
   float* q_s = s_q + warp * d;
@@ -63,9 +65,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) fwd_f32_kernel(const F32P
   for (int c = lane; c < d; c += 32) q_s[c] = q_row[c] * p.scale_log2;
   __syncwarp();
 
-  const size_t kv_stride = static_cast<size_t>(p.H) * d;  // between consecutive keys
+  const size_t kv_stride = static_cast<size_t>(p.H) * d;   // between consecutive keys
+  const size_t v_stride = static_cast<size_t>(p.H) * dv;   // between consecutive value rows
   const float* k_bh = p.k + (static_cast<size_t>(b) * p.Lk * p.H + h) * d;
-  const float* v_bh = p.v + (static_cast<size_t>(b) * p.Lk * p.H + h) * d;
+  const float* v_bh = p.v + (static_cast<size_t>(b) * p.Lk * p.H + h) * dv;
 
   constexpr int kPerLane = kMaxD / 32;
   float acc[kPerLane];
@@ -93,16 +96,16 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) fwd_f32_kernel(const F32P
     const int cnt = (n - j0 < 32) ? (n - j0) : 32;
     for (int t = 0; t < cnt; ++t) {
       const float pt = __shfl_sync(0xffffffffu, pj, t);
-      const float* v_row = v_bh + static_cast<size_t>(j0 + t) * kv_stride;
+      const float* v_row = v_bh + static_cast<size_t>(j0 + t) * v_stride;
 #pragma unroll
       for (int u = 0; u < kPerLane; ++u) {
         const int c = lane + 32 * u;
-        if (c < d) acc[u] = fmaf(pt, v_row[c], acc[u]);
+        if (c < dv) acc[u] = fmaf(pt, v_row[c], acc[u]);
       }
     }
   }
 
-  float* o_row = p.out + static_cast<size_t>(row) * d;
+  float* o_row = p.out + static_cast<size_t>(row) * dv;
   const float inv = (l > 0.f) ? 1.f / l : 0.f;
   if (p.lse && lane == 0) {
     // log of the softmax denominator, natural units: m and the exponents are
@@ -113,14 +116,14 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) fwd_f32_kernel(const F32P
 #pragma unroll
   for (int u = 0; u < kPerLane; ++u) {
     const int c = lane + 32 * u;
-    if (c < d) o_row[c] = acc[u] * inv;
+    if (c < dv) o_row[c] = acc[u] * inv;
   }
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_f32(const F32Params& p, cudaStream_t stream, LaunchInfo* info) {
-  if (p.d < 1 || p.d > kMaxD) return cudaErrorInvalidValue;
+  if (p.d < 1 || p.d > kMaxD || p.dv < 1 || p.dv > kMaxD) return cudaErrorInvalidValue;
   const long long rows = static_cast<long long>(p.B) * p.H * p.Lq;
   const long long blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const int smem = kWarpsPerBlock * p.d * static_cast<int>(sizeof(float));

@@ -117,13 +117,14 @@ def generate(w: Workload, seed: int | None = None, batch: slice | None = None):
 
 def random_case(seed: int, B: int, H: int, Lq: int, Lk: int, d_k: int,
                 dtype=torch.bfloat16, input_scale: float = 1.0,
-                key_lens_range: tuple[int, int] | None = None):
-    """Ad-hoc seeded case with the same recipe (for parity sweeps)."""
+                key_lens_range: tuple[int, int] | None = None, d_v: int | None = None):
+    """Ad-hoc seeded case with the same recipe (for parity sweeps); v rows have
+    width ``d_v`` (default d_k)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
     out = {}
-    for name, L in (("q", Lq), ("k", Lk), ("v", Lk)):
-        x = torch.randn((B, L, H, d_k), generator=g, dtype=torch.float32)
+    for name, L, w in (("q", Lq, d_k), ("k", Lk, d_k), ("v", Lk, d_v or d_k)):
+        x = torch.randn((B, L, H, w), generator=g, dtype=torch.float32)
         if input_scale != 1.0:
             x.mul_(input_scale)
         out[name] = x.to(dtype)
