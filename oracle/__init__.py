@@ -10,7 +10,9 @@ time): score s_j = scale * q.k_j, weights a_j = e^{s_j} / sum_i e^{s_i},
 output o = sum_j a_j v_j ("Attention Is All You Need", Section 3.2.1,
 Equation (1); formula page transformer-attention, section 証明), with the
 causal and key-padding masks removing keys before the softmax.  This module
-only compiles that file with gcc, loads it with ctypes and marshals arrays.
+compiles that file with gcc, loads it with ctypes and marshals arrays; its one
+piece of arithmetic of its own is ``mha_layer``: the multi-head layer of
+Section 3.2.2 as float64 matrix products (numpy) around that attention.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 (the pages' worked examples, closed-form invariants, brute force on tiny
@@ -199,3 +201,33 @@ def mha(q, k, v, mask_kind: int = MASK_NONE, key_lens=None, scale=None,
     """Attention over all heads with the default build (see ``Oracle.mha``)."""
     return _get().mha(q, k, v, mask_kind=mask_kind, key_lens=key_lens, scale=scale,
                       threads=threads, return_lse=return_lse)
+
+
+def mha_layer(x, w_qkv, w_o, H: int, mem=None, mask_kind: int = MASK_NONE, key_lens=None,
+              scale=None, threads: int | None = None):
+    """The multi-head attention layer ("Attention Is All You Need", Section
+    3.2.2): MultiHead(Q, K, V) = Concat(head_1, ..., head_H) W^O with
+    head_h = Attention(Q W_h^Q, K W_h^K, V W_h^V), queries from x [B, Lq,
+    d_model] and keys and values from ``mem`` [B, Lk, d_model] (x itself when
+    None: self-attention).  w_qkv [d_model, 3 H d_k] holds W^Q, W^K, W^V side by
+    side, head h at columns h d_k .. h d_k + d_k - 1 of each; w_o [H d_k,
+    d_model].  All float64: the three projections, the attention of the C
+    oracle over all heads, then the output projection of the heads'
+    concatenation.  Returns y [B, Lq, d_model]."""
+    x = _as_f64(x)
+    mem = x if mem is None else _as_f64(mem)
+    w_qkv = _as_f64(w_qkv)
+    w_o = _as_f64(w_o)
+    B, Lq, d_model = x.shape
+    Lk = mem.shape[1]
+    hd = w_qkv.shape[1] // 3
+    if w_qkv.shape != (d_model, 3 * hd) or hd % H != 0 or w_o.shape != (hd, d_model):
+        raise ValueError("w_qkv must be [d_model, 3 H d_k] and w_o [H d_k, d_model]")
+    if mem.shape != (B, Lk, d_model):
+        raise ValueError("mem must be [B, Lk, d_model]")
+    d_k = hd // H
+    q = (x @ w_qkv[:, :hd]).reshape(B, Lq, H, d_k)
+    k = (mem @ w_qkv[:, hd:2 * hd]).reshape(B, Lk, H, d_k)
+    v = (mem @ w_qkv[:, 2 * hd:]).reshape(B, Lk, H, d_k)
+    o = mha(q, k, v, mask_kind, key_lens=key_lens, scale=scale, threads=threads)
+    return o.reshape(B, Lq, hd) @ w_o

@@ -196,3 +196,93 @@ def generate_decode(w: DecodeWorkload, seed: int | None = None):
     out["cache_lens"] = per_source.repeat_interleave(w.beams).to(torch.int32)
     return out
 
+
+
+# ---------------------------------------------------------------------------
+# the multi-head attention layer: projections around the attention
+# ---------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class LayerWorkload:
+    """One multi-head attention layer ("Attention Is All You Need", section
+    3.2.2): queries from x [B, Lq, d_model], keys and values from x itself
+    (self-attention, ``cross`` False, Lk = Lq) or from an encoder memory
+    [B, Lk, d_model] (cross-attention); H heads of width d_k (d_v = d_k).
+    Random weights (no trained ones exist here)."""
+    name: str
+    B: int
+    Lq: int
+    Lk: int
+    d_model: int
+    H: int
+    d_k: int
+    mask_kind: int
+    cross: bool = False
+    len_lo: int = 0          # key padding: key_lens ~ U[len_lo, len_hi]
+    len_hi: int = 0
+    note: str = ""
+
+    @property
+    def seed(self) -> int:
+        return 3000 + LAYER_INDEX[self.name]
+
+    def flops(self, key_lens=None) -> float:
+        """Algorithmic flops: the Q, K, V and output projections (2 per
+        multiply-add) plus the attention's 4*d_k per visible (query, key) pair."""
+        hd = self.H * self.d_k
+        proj = 2.0 * self.B * (self.Lq * self.d_model * hd + self.Lk * self.d_model * 2 * hd +
+                               self.Lq * hd * self.d_model)
+        if self.mask_kind == MASK_CAUSAL:
+            pairs = self.B * self.H * self.Lq * (self.Lq + 1) / 2
+        elif self.mask_kind & MASK_KEY_PADDING and key_lens is not None:
+            lens = key_lens.clamp(0, self.Lk).to(torch.int64)
+            if self.mask_kind & MASK_CAUSAL:
+                i = torch.arange(self.Lq, dtype=torch.int64)
+                pairs = float(self.H * torch.minimum(i[None, :] + 1, lens[:, None]).sum().item())
+            else:
+                pairs = float(self.H * self.Lq * lens.sum().item())
+        else:
+            pairs = float(self.B * self.H * self.Lq * self.Lk)
+        return proj + 4.0 * self.d_k * pairs
+
+
+LAYER_WORKLOADS = [
+    LayerWorkload("base_layer_decoder", 32, 128, 128, 512, 8, 64, MASK_CAUSAL,
+                  note="base model (d_model 512, 8 heads of 64): decoder self-attention layer"),
+    LayerWorkload("base_layer_cross", 32, 128, 160, 512, 8, 64, MASK_KEY_PADDING, cross=True,
+                  len_lo=64, len_hi=160,
+                  note="base model: encoder-decoder attention over padded encoder outputs"),
+    LayerWorkload("gpt3_layer", 4, 2048, 2048, 12288, 96, 128, MASK_CAUSAL,
+                  note="GPT-3-like: d_model 12288, 96 heads of 128, 2048 context, causal"),
+    LayerWorkload("gpt3_layer_b1", 1, 2048, 2048, 12288, 96, 128, MASK_CAUSAL,
+                  note="GPT-3-like, one sequence"),
+]
+LAYER_INDEX = {w.name: i for i, w in enumerate(LAYER_WORKLOADS)}
+LAYER_BY_NAME = {w.name: w for w in LAYER_WORKLOADS}
+
+
+def generate_layer(w: LayerWorkload, seed: int | None = None):
+    """Return dict(x [B, Lq, d_model], mem [B, Lk, d_model] or None, w_qkv
+    [d_model, 3 H d_k], w_o [H d_k, d_model], key_lens [B] int32 or None) in
+    bf16 on the CPU.  Draw order: x, (mem), w_qkv, w_o, (key_lens).  x and mem
+    are N(0, 1); w_qkv is N(0, 1/d_model) and w_o N(0, 1/(H d_k)) (Xavier-like:
+    the projections come out near N(0, 1) again).  w_qkv's columns are W^Q,
+    W^K, W^V in that order, head h at columns h d_k .. h d_k + d_k - 1 of each."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed if seed is None else seed)
+    hd = w.H * w.d_k
+
+    def draw(shape, std=1.0):
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        if std != 1.0:
+            x.mul_(std)
+        return x.to(torch.bfloat16)
+
+    out = {"x": draw((w.B, w.Lq, w.d_model))}
+    out["mem"] = draw((w.B, w.Lk, w.d_model)) if w.cross else None
+    out["w_qkv"] = draw((w.d_model, 3 * hd), w.d_model ** -0.5)
+    out["w_o"] = draw((hd, w.d_model), hd ** -0.5)
+    out["key_lens"] = None
+    if w.mask_kind & MASK_KEY_PADDING:
+        out["key_lens"] = torch.randint(w.len_lo, w.len_hi + 1, (w.B,), generator=g,
+                                        dtype=torch.int64).to(torch.int32)
+    return out
