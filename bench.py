@@ -691,6 +691,183 @@ def timed_steps(step, args, dev, stream, rank):
     return step_ms, max_total_ms, (sampler.summary(t_wall0, t_wall1) if rank == 0 else None)
 
 
+# ---------------------------------------------------------------------------
+# the multi-head layer (projections around the attention)
+# ---------------------------------------------------------------------------
+LAYER_METRIC = ("multi-head attention layer TFLOP/s (bf16 Q/K/V and W^O projections on cuBLASLt "
+                "+ the attention kernel, 1 GB300) and % of measured dense bf16 peak")
+
+
+def layer_sample(w, case, rows):
+    """An exact sub-problem of the layer for the CPU oracle: sequence 0, and
+    under the causal mask only its first ``rows`` query rows (they depend on
+    x rows 0 .. rows-1 alone); otherwise the whole sequence."""
+    n = min(rows, w.Lq) if (w.mask_kind & inputs.MASK_CAUSAL and not w.cross) else w.Lq
+    sub = {"x": case["x"][:1, :n], "w_qkv": case["w_qkv"], "w_o": case["w_o"],
+           "mem": case["mem"][:1] if case["mem"] is not None else None,
+           "key_lens": case["key_lens"][:1] if case["key_lens"] is not None else None}
+    one = inputs.LayerWorkload(w.name, 1, n, n if not w.cross else w.Lk, w.d_model, w.H, w.d_k,
+                               w.mask_kind, cross=w.cross)
+    return sub, one
+
+
+def layer_oracle_baseline(w, case, budget_s=10.0):
+    """The float64 layer oracle on growing exact samples within a budget."""
+    import oracle
+    rows = 64
+    best = None
+    t_all = time.perf_counter()
+    while True:
+        sub, one = layer_sample(w, case, rows)
+        lens = sub["key_lens"].numpy() if sub["key_lens"] is not None else None
+        t0 = time.perf_counter()
+        oracle.mha_layer(sub["x"], sub["w_qkv"], sub["w_o"], w.H, mem=sub["mem"],
+                         mask_kind=w.mask_kind, key_lens=lens)
+        dt = time.perf_counter() - t0
+        best = (one.flops(sub["key_lens"]) / dt / 1e12, dt, one.Lq)
+        if one.Lq >= w.Lq or time.perf_counter() - t_all + 4 * dt > budget_s:
+            break
+        rows *= 2
+    value, dt, n = best
+    return {"value": value, "unit": UNIT, "cores": oracle.default_threads(), "kind": "oracle",
+            "seconds": dt, "rows": n,
+            "sample": f"sequence 0 of {w.name}, query rows 0..{n - 1} (an exact sub-problem: "
+                      f"{'causal prefix' if w.mask_kind & inputs.MASK_CAUSAL else 'whole sequence'}), "
+                      f"float64 numpy projections + the C attention oracle, {dt:.1f} s wall"}
+
+
+def run_layer(args):
+    rank, world = mdist.init("nccl")
+    _, _, local_rank = mdist.env_rank_world()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from transformer_head_scaled_sdpa_gb300 import binding, build
+    if rank == 0:
+        build.build()
+    mdist.barrier(dev)
+    build.build()
+    w = inputs.LAYER_BY_NAME[args.workload]
+    case = inputs.generate_layer(w, seed=mdist.rank_seed(w.seed, rank))
+    g = {n: (t.to(dev) if t is not None else None) for n, t in case.items()}
+    flops_alg = w.flops(case["key_lens"])
+    y = torch.empty_like(g["x"])
+    ws = torch.empty(max(1, binding.layer_workspace_bytes(w.B, w.Lq, w.Lk, w.d_model, w.H, w.d_k)),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    in_bytes = sum(t.numel() * 2 for n, t in g.items() if t is not None and n != "key_lens")
+
+    def step():
+        binding.mha_layer_fwd(g["x"], g["w_qkv"], g["w_o"], w.H, mem=g["mem"], mask_kind=w.mask_kind,
+                              key_lens=g["key_lens"], y=y, workspace=ws, stream=stream)
+
+    step_ms, max_total_ms, clocks = timed_steps(step, args, dev, stream, rank)
+    rc = binding.mha_sync_status(stream)
+    if rc != 0:
+        raise binding.MhaError(rc, "timed region")
+    launches_per_step = binding.last_launch_info()["kernels"]
+    total_flops = mdist.sum_over_ranks(flops_alg * args.steps, dev)
+    # end to end: x (and mem) from pinned host memory, y back; weights resident
+    hx = case["x"].pin_memory()
+    hm = case["mem"].pin_memory() if case["mem"] is not None else None
+    hy = torch.empty_like(hx).pin_memory()
+    dx = torch.empty_like(g["x"])
+    dm = torch.empty_like(g["mem"]) if g["mem"] is not None else None
+    n_e2e = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        if dm is not None:
+            dm.copy_(hm, non_blocking=True)
+        binding.mha_layer_fwd(dx, g["w_qkv"], g["w_o"], w.H, mem=dm, mask_kind=w.mask_kind,
+                              key_lens=g["key_lens"], y=y, workspace=ws, stream=stream)
+        hy.copy_(y, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+    mdist.barrier(dev)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = mdist.max_over_ranks(e0.elapsed_time(e1) / n_e2e, dev)
+    e2e_flops = mdist.sum_over_ranks(flops_alg, dev)
+    if rank != 0:
+        mdist.finish()
+        return
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    value = total_flops / (max_total_ms * 1e-3) / 1e12
+    achieved = flops_alg / (step_ms * 1e-3) / 1e12
+    cfg = {"workload": w.name, "B": w.B, "Lq": w.Lq, "Lk": w.Lk, "d_model": w.d_model, "H": w.H,
+           "d_k": w.d_k, "mask": inputs.MASK_NAMES[w.mask_kind], "cross": w.cross,
+           "seed": w.seed, "weights": "random (Xavier-scaled N(0, 1/fan_in), bf16)",
+           "parallelism": f"replicas x{world} (no collective)",
+           "inputs_exceed_l2": in_bytes > L2_BYTES, "l2_flush": False,
+           "flops_per_step_per_gpu": flops_alg}
+    line = {
+        "metric": LAYER_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) x, random weights, no dataset or trained model)",
+        "config": cfg,
+        "pct_of_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_src} dense bf16 (burst)",
+                     "kernel": "cuBLASLt projection GEMMs + fwd_bf16_kernel (whole step)",
+                     "kernel_ms": step_ms},
+        "clocks": clocks,
+        "e2e": {"value": e2e_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": int(hx.numel() * 2 + (hm.numel() * 2 if hm is not None else 0)),
+                "d2h_bytes_per_step": int(hy.numel() * 2), "steps": n_e2e, "ms_per_step": e2e_ms,
+                "path": "pinned host x (and mem) -> device, mha_layer_fwd with resident weights, "
+                        "y -> host"},
+        # this library's own kernels: the attention (the GEMMs are cuBLASLt's)
+        "gpu_launches": int(launches_per_step * args.steps),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = layer_oracle_baseline(w, case)
+    print(json.dumps(line), flush=True)
+    mdist.finish()
+
+
+def run_reference_layer(args):
+    rank, world, _ = mdist.env_rank_world()
+    if rank != 0:
+        return
+    w = inputs.LAYER_BY_NAME[args.workload]
+    case = inputs.generate_layer(w)
+    base = layer_oracle_baseline(w, case, budget_s=min(30.0, 120.0 / max(1, args.steps)))
+    import oracle
+    sub, one = layer_sample(w, case, base["rows"])
+    lens = sub["key_lens"].numpy() if sub["key_lens"] is not None else None
+    for _ in range(min(args.warmup, 3)):
+        oracle.mha_layer(sub["x"], sub["w_qkv"], sub["w_o"], w.H, mem=sub["mem"],
+                         mask_kind=w.mask_kind, key_lens=lens)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.mha_layer(sub["x"], sub["w_qkv"], sub["w_o"], w.H, mem=sub["mem"],
+                         mask_kind=w.mask_kind, key_lens=lens)
+    dt = time.perf_counter() - t0
+    value = one.flops(sub["key_lens"]) * args.steps / dt / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": LAYER_METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, random weights)",
+        "config": {"workload": w.name, "B": w.B, "Lq": w.Lq, "Lk": w.Lk, "d_model": w.d_model,
+                   "H": w.H, "d_k": w.d_k, "mask": inputs.MASK_NAMES[w.mask_kind],
+                   "parallelism": "host cores"},
+        "cpu_baseline": dict(base, value=value),
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def run_bwd(args):
     rank, world = mdist.init("nccl")
     _, _, local_rank = mdist.env_rank_world()
@@ -849,7 +1026,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="gpt3_causal",
-                    choices=sorted(inputs.BY_NAME) + sorted(inputs.DECODE_BY_NAME))
+                    choices=sorted(inputs.BY_NAME) + sorted(inputs.DECODE_BY_NAME) +
+                    sorted(inputs.LAYER_BY_NAME))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -859,6 +1037,11 @@ def main():
     if args.steps < 1:
         ap.error("--steps must be >= 1")
     decode = args.workload in inputs.DECODE_BY_NAME
+    if args.workload in inputs.LAYER_BY_NAME:
+        if args.pass_ == "bwd":
+            ap.error("--pass bwd applies to the attention workloads")
+        (run_reference_layer if args.impl == "reference" else run_layer)(args)
+        return
     if args.pass_ == "bwd":
         if decode:
             ap.error("--pass bwd applies to the forward workloads")

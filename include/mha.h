@@ -254,6 +254,39 @@ int mha_decode_static(const void* q, const void* k_cache, const void* v_cache, v
 size_t mha_decode_static_scratch_bytes(void);
 
 /*
+ * mha_layer_fwd -- one multi-head attention layer ("Attention Is All You
+ * Need", Section 3.2.2):
+ *     y = MultiHead(x, m, m) = Concat(head_1, ..., head_H) W^O,
+ *     head_h = Attention(x W_h^Q, m W_h^K, m W_h^V)
+ * with m = x (self-attention) when mem is NULL, else the encoder memory
+ * (encoder-decoder attention).  The projections are plain GEMMs on cuBLASLt
+ * (bf16 operands, float32 accumulation, bf16 results); the attention is
+ * mha_fwd's kernel reading the projection output in place (no transposed or
+ * split copies: the tensor maps take the packed rows' stride) and writing the
+ * heads' concatenation that the W^O GEMM reads.
+ *   x       device bf16 [B, Lq, d_model], 16-byte aligned.
+ *   mem     device bf16 [B, Lk, d_model] or NULL (then Lk must equal Lq).
+ *   w_qkv   device bf16 [d_model, 3 H d_k]: W^Q, W^K, W^V side by side, head h
+ *           at columns h d_k .. h d_k + d_k - 1 of each block.
+ *   w_o     device bf16 [H d_k, d_model].
+ *   y       device bf16 [B, Lq, d_model]; overlaps none of the others.
+ *   d_model a multiple of 8; d_k as mha_fwd (a multiple of 8 up to 128);
+ *           d_v = d_k.  mask_kind, key_lens, scale as mha_fwd.
+ *   workspace  device, mha_layer_workspace_bytes(...) bytes, 256-byte
+ *           aligned, owned by the caller (projections, the heads' output and
+ *           the GEMM workspace); overlaps no argument.
+ * Errors as mha_fwd, MHA_ERR_WORKSPACE for a missing or short workspace,
+ * MHA_ERR_LAUNCH when cuBLASLt refuses a GEMM.  Lk == 0 writes zeros.
+ */
+int mha_layer_fwd(const void* x, const void* mem, const void* w_qkv, const void* w_o, void* y,
+                  int B, int Lq, int Lk, int d_model, int H, int d_k, int mask_kind,
+                  const int32_t* key_lens, float scale, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/* mha_layer_workspace_bytes -- workspace mha_layer_fwd needs; 0 on bad sizes. */
+size_t mha_layer_workspace_bytes(int B, int Lq, int Lk, int d_model, int H, int d_k);
+
+/*
  * mha_fwd_host_workspace_bytes -- device workspace mha_fwd_host needs for
  * these sizes (elem_bytes 2 for bf16, 4 for float32).  0 on bad sizes.
  */

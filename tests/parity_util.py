@@ -126,3 +126,28 @@ def assert_f32_close(out, ref, what=""):
     max_abs, rel = errors(out, ref)
     assert max_abs <= F32_MAX_ABS, f"{what}: max_abs {max_abs:.3e} (<= {F32_MAX_ABS})"
     return max_abs, rel
+
+
+# The multi-head layer (mha_layer_fwd) against the float64 layer oracle on the
+# same bf16 inputs and weights, relative to the reference's Frobenius norm and
+# largest magnitude.  Beyond the attention's own roundings (P and O to bf16)
+# the layer rounds the Q, K, V projections and the output y to bf16: five
+# roundings of unit roundoff u = 2^-9 on the path, each a random relative
+# error of about u / sqrt(3) per element (Q and K errors reach y through the
+# scores, scaled by |s| ~ 1 on these Xavier-scaled inputs), about 1.3u in all;
+# the bounds allow 4u (Frobenius) and 8u (largest element).  A wrong head
+# slice, a swapped K/V block or a dropped scale errs by O(1).
+LAYER_REL_FRO = 4 * 2.0 ** -9
+LAYER_REL_MAX = 8 * 2.0 ** -9
+
+
+def assert_layer_close(y, ref, what=""):
+    g = y.to(torch.float64).numpy() if hasattr(y, "numpy") else np.asarray(y, dtype=np.float64)
+    scale = float(np.abs(ref).max()) or 1.0
+    fro = float(np.linalg.norm(ref)) or 1.0
+    rel_max = float(np.abs(g - ref).max()) / scale
+    rel_fro = float(np.linalg.norm(g - ref)) / fro
+    assert rel_fro <= LAYER_REL_FRO and rel_max <= LAYER_REL_MAX, \
+        f"{what}: relative Frobenius {rel_fro:.3e} (bound {LAYER_REL_FRO:.3e}), " \
+        f"relative max {rel_max:.3e} (bound {LAYER_REL_MAX:.3e})"
+    return rel_fro, rel_max

@@ -186,3 +186,39 @@ def test_bwd_entry_errors(lib):
     assert bwd(lib, ws=None) == WORKSPACE
     assert lib.mha_bwd_workspace_bytes(2, 3, 64, 64, 96) > 0
     assert lib.mha_bwd_workspace_bytes(2, 3, 64, 64, 12) == 0
+
+
+XL, ML, WQ, WO, YL = 0x100000000, 0x110000000, 0x120000000, 0x130000000, 0x140000000
+WSL = 0x150000000
+
+
+def layer(lib, x=XL, mem=None, wq=WQ, wo=WO, y=YL, B=2, Lq=64, Lk=64, dm=512, H=8, dk=64,
+          mask=0, lens=None, scale=0.0, ws=WSL, wsb=None):
+    if wsb is None:
+        wsb = lib.mha_layer_workspace_bytes(B, Lq, Lk, dm, H, dk)
+    return lib.mha_layer_fwd(x, mem, wq, wo, y, B, Lq, Lk, dm, H, dk, mask, lens, scale, ws, wsb,
+                             None)
+
+
+def test_layer_entry_errors(lib):
+    # every call below fails its checks before any device is touched
+    assert layer(lib, B=-1) == SHAPE
+    assert layer(lib, dm=0) == SHAPE
+    assert layer(lib, Lk=65) == SHAPE                  # self-attention: Lk == Lq
+    assert layer(lib, mem=ML, mask=1, Lk=65) == SHAPE  # causal: Lq == Lk
+    assert layer(lib, mask=4) == MASK
+    assert layer(lib, mask=2) == MASK                  # key padding needs key_lens
+    assert layer(lib, scale=math.nan) == SCALE
+    assert layer(lib, dk=12) == UNSUP
+    assert layer(lib, dm=100) == UNSUP                 # d_model a multiple of 8
+    assert layer(lib, x=XL + 8) == UNSUP
+    assert layer(lib, x=None) == NULL
+    assert layer(lib, wo=None) == NULL
+    assert layer(lib, ws=None) == WORKSPACE
+    assert layer(lib, ws=WSL + 16) == WORKSPACE
+    assert layer(lib, wsb=1024) == WORKSPACE
+    assert layer(lib, y=XL + 64) == ALIAS              # y overlaps x
+    assert layer(lib, ws=WQ) == ALIAS                  # workspace overlaps the weights
+    assert layer(lib, B=0) == OK
+    assert lib.mha_layer_workspace_bytes(2, 64, 64, 512, 8, 64) > 32 << 20
+    assert lib.mha_layer_workspace_bytes(2, 64, 64, 512, 8, 12) == 0

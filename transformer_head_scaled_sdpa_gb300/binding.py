@@ -64,6 +64,11 @@ def lib():
             h.mha_fwd_lse.argtypes = _FWD_LSE_ARGS
             h.mha_fwd_f32_lse.restype = _c_i
             h.mha_fwd_f32_lse.argtypes = _FWD_LSE_ARGS
+            h.mha_layer_fwd.restype = _c_i
+            h.mha_layer_fwd.argtypes = [_c_p] * 5 + [_c_i] * 7 + [_c_p, ctypes.c_float, _c_p,
+                                                                   ctypes.c_size_t, _c_p]
+            h.mha_layer_workspace_bytes.restype = ctypes.c_size_t
+            h.mha_layer_workspace_bytes.argtypes = [_c_i] * 6
             for name in ("mha_fwd_dv", "mha_fwd_f32_dv"):
                 getattr(h, name).restype = _c_i
                 getattr(h, name).argtypes = [_c_p] * 5 + [_c_i] * 7 + [_c_p, ctypes.c_float, _c_p]
@@ -236,6 +241,55 @@ def mha_bwd(q, k, v, out, dout, lse, mask_kind: int = 0, key_lens=None, scale: f
     if rc != MHA_OK:
         raise MhaError(rc, "mha_bwd")
     return dq, dk, dv
+
+
+def layer_workspace_bytes(B, Lq, Lk, d_model, H, d_k) -> int:
+    return int(lib().mha_layer_workspace_bytes(B, Lq, Lk, d_model, H, d_k))
+
+
+def mha_layer_fwd(x, w_qkv, w_o, H: int, mem=None, mask_kind: int = 0, key_lens=None,
+                  scale: float = 0.0, y=None, workspace=None, stream=None):
+    """One multi-head attention layer (bf16): y = Concat(heads) W^O with
+    head_h = Attention(x W_h^Q, m W_h^K, m W_h^V), m = ``mem`` or x.
+    x [B, Lq, d_model], mem [B, Lk, d_model] or None, w_qkv [d_model, 3 H d_k],
+    w_o [H d_k, d_model]; returns y [B, Lq, d_model]."""
+    if x.dim() != 3 or w_qkv.dim() != 2 or w_o.dim() != 2:
+        raise ValueError("x must be [B, Lq, d_model], w_qkv and w_o matrices")
+    B, Lq, d_model = x.shape
+    hd3 = w_qkv.shape[1]
+    if hd3 % (3 * H) != 0 or tuple(w_qkv.shape) != (d_model, hd3):
+        raise ValueError("w_qkv must be [d_model, 3 H d_k]")
+    d_k = hd3 // (3 * H)
+    if tuple(w_o.shape) != (H * d_k, d_model):
+        raise ValueError("w_o must be [H d_k, d_model]")
+    Lk = Lq if mem is None else mem.shape[1]
+    tensors = [(x, "x"), (w_qkv, "w_qkv"), (w_o, "w_o")]
+    if mem is not None:
+        if mem.dim() != 3 or mem.shape[0] != B or mem.shape[2] != d_model:
+            raise ValueError("mem must be [B, Lk, d_model]")
+        tensors.append((mem, "mem"))
+    for t, n in tensors:
+        _check_tensor(t, n, torch.bfloat16, "cuda")
+    if y is None:
+        y = torch.empty_like(x)
+    _check_tensor(y, "y", torch.bfloat16, "cuda")
+    if tuple(y.shape) != tuple(x.shape):
+        raise ValueError("y must have x's shape")
+    lens_ptr = None
+    if key_lens is not None:
+        _check_tensor(key_lens, "key_lens", torch.int32, "cuda")
+        lens_ptr = key_lens.data_ptr()
+    need = layer_workspace_bytes(B, Lq, Lk, d_model, H, d_k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    _check_tensor(workspace, "workspace", torch.uint8, "cuda")
+    rc = lib().mha_layer_fwd(x.data_ptr(), mem.data_ptr() if mem is not None else None,
+                             w_qkv.data_ptr(), w_o.data_ptr(), y.data_ptr(), B, Lq, Lk, d_model,
+                             H, d_k, int(mask_kind), lens_ptr, float(scale), workspace.data_ptr(),
+                             workspace.numel(), _stream_handle(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "mha_layer_fwd")
+    return y
 
 
 def decode_workspace_bytes(B, H, Lk, d_k) -> int:

@@ -116,4 +116,11 @@ cudaError_t launch_fwd_bf16(const Bf16Params& p, int d, cudaStream_t stream, Lau
 // Launches the float32 SIMT forward (1 <= d <= 256).
 cudaError_t launch_fwd_f32(const F32Params& p, cudaStream_t stream, LaunchInfo* info);
 
+// Row-major bf16 GEMM with float32 accumulation on cuBLASLt (mha_gemm.cu):
+// C[M x N] = A[M x K] B[K x N], leading dimensions in elements.  False when
+// cuBLASLt refuses the call.
+bool gemm_bf16_rowmajor(int M, int N, int K, const void* A, long long lda, const void* B,
+                        long long ldb, void* C, long long ldc, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream);
+
 }  // namespace mha

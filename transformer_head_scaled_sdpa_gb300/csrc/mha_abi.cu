@@ -148,12 +148,17 @@ int bf16_kernel_width(int d_k, int d_v) { return (d_k <= 64 && d_v <= 64) ? 64 :
 // rows (128 for the forward's tiles, 64 for the decode step's) x 1 sequence,
 // 128-byte swizzle (the tcgen05 operand layout).  Features past d read as 0
 // and are not written by stores.
-bool encode_map(CUtensorMap* m, const void* base, int B, int L, int H, int d, int rows = 128) {
+// row_elems: elements between consecutive positions of one head (H*d for a
+// dense tensor; more when the rows interleave other tensors, as the packed
+// Q|K|V projection output does).
+bool encode_map(CUtensorMap* m, const void* base, int B, int L, int H, int d, int rows = 128,
+                long long row_elems = -1) {
+  if (row_elems < 0) row_elems = static_cast<long long>(H) * d;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,
-                                 static_cast<cuuint64_t>(H) * d * 2,
-                                 static_cast<cuuint64_t>(L) * H * d * 2};
+                                 static_cast<cuuint64_t>(row_elems) * 2,
+                                 static_cast<cuuint64_t>(L) * row_elems * 2};
   const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(rows), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
@@ -219,6 +224,11 @@ float effective_scale(float scale, int d_k) {
   return scale == 0.f ? 1.f / std::sqrt(static_cast<float>(d_k)) : scale;
 }
 
+int attention_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
+                   long long q_row, long long k_row, long long v_row, int B, int H, int Lq,
+                   int Lk, int d_k, int d_v, int mask_kind, const int32_t* key_lens, float scale,
+                   DeviceState* dev, cudaStream_t s);
+
 int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse, bool want_lse,
              int B, int H, int Lq, int Lk, int d_k, int d_v, int mask_kind,
              const int32_t* key_lens, float scale, void* stream) {
@@ -237,12 +247,26 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
   if (rc != MHA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (Lk == 0) return no_keys(out, sz.o_elems * 2, lse, static_cast<size_t>(rows_q), s);
+  return attention_bf16(q, k, v, out, lse, static_cast<long long>(H) * d_k,
+                        static_cast<long long>(H) * d_k, static_cast<long long>(H) * d_v, B, H,
+                        Lq, Lk, d_k, d_v, mask_kind, key_lens, scale, dev, s);
+}
+
+// The bf16 attention launch on checked arguments (Lq, Lk > 0).  q_row, k_row,
+// v_row: elements between consecutive positions of one head in q, k, v; out is
+// dense [B, Lq, H, d_v].
+int attention_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
+                   long long q_row, long long k_row, long long v_row, int B, int H, int Lq,
+                   int Lk, int d_k, int d_v, int mask_kind, const int32_t* key_lens, float scale,
+                   DeviceState* dev, cudaStream_t s) {
   const long long n_qtiles = (Lq + mha::kUnitRows - 1) / mha::kUnitRows;
   if (n_qtiles * B * H > 0x7fffffffll) return MHA_ERR_SHAPE;
   mha::Bf16Params p;
   std::memset(&p, 0, sizeof(p));
-  if (!encode_map(&p.tm_q, q, B, Lq, H, d_k) || !encode_map(&p.tm_k, k, B, Lk, H, d_k) ||
-      !encode_map(&p.tm_v, v, B, Lk, H, d_v) || !encode_map(&p.tm_o, out, B, Lq, H, d_v))
+  if (!encode_map(&p.tm_q, q, B, Lq, H, d_k, 128, q_row) ||
+      !encode_map(&p.tm_k, k, B, Lk, H, d_k, 128, k_row) ||
+      !encode_map(&p.tm_v, v, B, Lk, H, d_v, 128, v_row) ||
+      !encode_map(&p.tm_o, out, B, Lq, H, d_v))
     return MHA_ERR_UNSUPPORTED;
   p.out = out;
   p.lse = lse;
@@ -533,6 +557,112 @@ int mha_bwd(const void* q, const void* k, const void* v, const void* out, const 
   return mha::launch_bwd(p, bf16_kernel_width(d_k, d_k), s, &t_info) == cudaSuccess
              ? MHA_OK
              : MHA_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// The multi-head layer: projections (cuBLASLt) around the attention kernel.
+// ---------------------------------------------------------------------------
+static constexpr size_t kLayerGemmWorkspaceBytes = size_t(32) << 20;
+
+// workspace: [Q|K|V projections][O (heads concatenated)][GEMM workspace]
+static size_t layer_proj_bytes(int B, int Lq, int Lk, size_t hd) {
+  return align256((static_cast<size_t>(B) * Lq * hd + static_cast<size_t>(B) * Lk * 2 * hd) * 2);
+}
+
+size_t mha_layer_workspace_bytes(int B, int Lq, int Lk, int d_model, int H, int d_k) {
+  if (B < 0 || Lq < 0 || Lk < 0 || d_model < 1 || H < 1 || !bf16_width_ok(d_k)) return 0;
+  const size_t hd = static_cast<size_t>(H) * d_k;
+  return layer_proj_bytes(B, Lq, Lk, hd) + align256(static_cast<size_t>(B) * Lq * hd * 2) +
+         kLayerGemmWorkspaceBytes;
+}
+
+int mha_layer_fwd(const void* x, const void* mem, const void* w_qkv, const void* w_o, void* y,
+                  int B, int Lq, int Lk, int d_model, int H, int d_k, int mask_kind,
+                  const int32_t* key_lens, float scale, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+  t_info = mha::LaunchInfo{};
+  if (B < 0 || Lq < 0 || Lk < 0 || d_model < 1 || H < 1 || d_k < 1) return MHA_ERR_SHAPE;
+  if (!mask_known(mask_kind)) return MHA_ERR_MASK;
+  if (has_causal(mask_kind) && Lq != Lk) return MHA_ERR_SHAPE;
+  if (!mem && Lk != Lq) return MHA_ERR_SHAPE;  // self-attention: keys are the query rows
+  if (!std::isfinite(scale) || scale < 0.f) return MHA_ERR_SCALE;
+  if (!bf16_width_ok(d_k) || d_model % 8 != 0) return MHA_ERR_UNSUPPORTED;
+  const long long hd = static_cast<long long>(H) * d_k;
+  const long long rows_q = static_cast<long long>(B) * Lq, rows_k = static_cast<long long>(B) * Lk;
+  if (rows_q > 0x7fffffffll || rows_k > 0x7fffffffll || hd * 3 > 0x7fffffffll ||
+      (rows_q + rows_k) * (3 * hd + d_model) > (1ll << 40))
+    return MHA_ERR_SHAPE;
+  if (rows_q == 0) return MHA_OK;
+  if (!x || !w_qkv || !w_o || !y) return MHA_ERR_NULL;
+  if (has_padding(mask_kind) && !key_lens) return MHA_ERR_MASK;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(mem) |
+       reinterpret_cast<uintptr_t>(w_qkv) | reinterpret_cast<uintptr_t>(w_o) |
+       reinterpret_cast<uintptr_t>(y)) & 15u)
+    return MHA_ERR_UNSUPPORTED;
+  const size_t need = mha_layer_workspace_bytes(B, Lq, Lk, d_model, H, d_k);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MHA_ERR_WORKSPACE;
+  const size_t xb = static_cast<size_t>(rows_q) * d_model * 2;
+  const size_t mb = mem ? static_cast<size_t>(rows_k) * d_model * 2 : 0;
+  const size_t wqb = static_cast<size_t>(d_model) * 3 * hd * 2, wob = static_cast<size_t>(hd) * d_model * 2;
+  const void* ins[4] = {x, mem, w_qkv, w_o};
+  const size_t ins_b[4] = {xb, mb, wqb, wob};
+  for (int i = 0; i < 4; ++i)
+    if (overlaps(y, xb, ins[i], ins_b[i]) || overlaps(workspace, need, ins[i], ins_b[i]))
+      return MHA_ERR_ALIAS;
+  if (overlaps(y, xb, workspace, need)) return MHA_ERR_ALIAS;
+  DeviceState* dev = nullptr;
+  int rc = device_state(&dev);
+  if (rc != MHA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (Lk == 0) {  // every head's output is 0, and so is its projection
+    return cudaMemsetAsync(y, 0, xb, s) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
+  }
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  uint16_t* proj = reinterpret_cast<uint16_t*>(w);
+  uint16_t* o = reinterpret_cast<uint16_t*>(w + layer_proj_bytes(B, Lq, Lk, hd));
+  void* gws = w + layer_proj_bytes(B, Lq, Lk, hd) + align256(static_cast<size_t>(rows_q) * hd * 2);
+  const uint16_t* wq = static_cast<const uint16_t*>(w_qkv);
+  const void *q, *k, *v;
+  long long q_row, kv_row;
+  if (!mem) {
+    // one GEMM: [Q | K | V] = x [W^Q | W^K | W^V], rows of 3 H d_k
+    if (!mha::gemm_bf16_rowmajor(static_cast<int>(rows_q), static_cast<int>(3 * hd), d_model, x,
+                                 d_model, w_qkv, 3 * hd, proj, 3 * hd, gws,
+                                 kLayerGemmWorkspaceBytes, s))
+      return MHA_ERR_LAUNCH;
+    q = proj;
+    k = proj + hd;
+    v = proj + 2 * hd;
+    q_row = kv_row = 3 * hd;
+  } else {
+    // Q = x W^Q (rows of H d_k) and [K | V] = mem [W^K | W^V] (rows of 2 H d_k),
+    // reading the weight's column blocks in place (leading dimension 3 H d_k)
+    uint16_t* kv = proj + rows_q * hd;
+    if (!mha::gemm_bf16_rowmajor(static_cast<int>(rows_q), static_cast<int>(hd), d_model, x,
+                                 d_model, wq, 3 * hd, proj, hd, gws, kLayerGemmWorkspaceBytes, s) ||
+        !mha::gemm_bf16_rowmajor(static_cast<int>(rows_k), static_cast<int>(2 * hd), d_model, mem,
+                                 d_model, wq + hd, 3 * hd, kv, 2 * hd, gws,
+                                 kLayerGemmWorkspaceBytes, s))
+      return MHA_ERR_LAUNCH;
+    q = proj;
+    k = kv;
+    v = kv + hd;
+    q_row = hd;
+    kv_row = 2 * hd;
+  }
+  // the heads' attention, read in place from the projections; O comes out as
+  // [B, Lq, H, d_k] = the heads' concatenation, rows of H d_k
+  rc = attention_bf16(q, k, v, o, nullptr, q_row, kv_row, kv_row, B, H, Lq, Lk, d_k, d_k,
+                      mask_kind, key_lens, scale, dev, s);
+  if (rc != MHA_OK) return rc;
+  const mha::LaunchInfo attn = t_info;
+  // y = Concat(heads) W^O
+  if (!mha::gemm_bf16_rowmajor(static_cast<int>(rows_q), d_model, static_cast<int>(hd), o, hd,
+                               w_o, d_model, y, d_model, gws, kLayerGemmWorkspaceBytes, s))
+    return MHA_ERR_LAUNCH;
+  t_info = attn;
+  return MHA_OK;
 }
 
 size_t mha_fwd_host_workspace_bytes(int B, int H, int Lq, int Lk, int d_k, int elem_bytes) {
