@@ -702,6 +702,9 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
       // p = 2^(s*c2 - m_ref): packed scale-subtract, ex2 on the SFU, packed sums
       const float nm = -m_ref;
       float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      // (each pair is packed to bf16 as soon as it exists, so the float32
+      // values die at once and the row never holds 128 floats and 64 words)
+      uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 128; c += 2) {
         fma2(x[c], x[c + 1], x[c], x[c + 1], c2, c2, nm, nm);
@@ -709,14 +712,12 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
         x[c + 1] = ex2_approx(x[c + 1]);
         const int q = (c >> 1) & 3;
         add2(sa[q], sb[q], sa[q], sb[q], x[c], x[c + 1]);
+        pk[c >> 1] = pack_bf16x2(x[c], x[c + 1]);
       }
       add2(sa[0], sb[0], sa[0], sb[0], sa[1], sb[1]);
       add2(sa[2], sb[2], sa[2], sb[2], sa[3], sb[3]);
       l += (sa[0] + sb[0]) + (sa[2] + sb[2]);
       if (j < n_turns && (g == 0 || j + 1 < n_turns)) mbar_arrive(cx.bar(tok_pass));
-      uint32_t pk[64];
-#pragma unroll
-      for (int i = 0; i < 64; ++i) pk[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
       if constexpr (C::SEPARATE_P) {
         // PV_g of the previous tile must be done before P_g is rewritten and
         // O_g rescaled
