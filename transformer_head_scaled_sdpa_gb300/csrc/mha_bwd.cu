@@ -362,38 +362,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
           dvc[4 * v4] = dv.x, dvc[4 * v4 + 1] = dv.y, dvc[4 * v4 + 2] = dv.z, dvc[4 * v4 + 3] = dv.w;
         }
         tmem_ld_wait();
-        uint32_t pk[16], dk[16];
+        float pf[32];
         // (the mask test stays outside the element loops, which then have no
         // branches and interleave their 32 independent chains)
         if (all_visible) {
 #pragma unroll
-          for (int t = 0; t < 32; t += 2) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -l2c[t]));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[t + 1]), c2, -l2c[t + 1]));
-            pk[t >> 1] = pack_bf16x2(p0, p1);
-          }
+          for (int t = 0; t < 32; ++t)
+            pf[t] = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -l2c[t]));
         } else {
 #pragma unroll
-          for (int t = 0; t < 32; t += 2) {
-            float pp[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int qi = q0 + col0 + t + u;
-              const bool vis = key < kv_len && qi < p.Lq &&
-                               !(masks_causal(p.mask_kind) && key > qi) &&
-                               l2c[t + u] != -INFINITY;
-              const float e = ex2_approx(fmaf(__uint_as_float(sr[t + u]), c2, -l2c[t + u]));
-              pp[u] = vis ? e : 0.f;
-            }
-            pk[t >> 1] = pack_bf16x2(pp[0], pp[1]);
+          for (int t = 0; t < 32; ++t) {
+            const int qi = q0 + col0 + t;
+            const bool vis = key < kv_len && qi < p.Lq &&
+                             !(masks_causal(p.mask_kind) && key > qi) && l2c[t] != -INFINITY;
+            const float e = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -l2c[t]));
+            pf[t] = vis ? e : 0.f;
           }
         }
-        // dS = P (dP - D) with P as rounded to bf16 for the dV product
+        // P^T in bf16 for the dV product; dS = P (dP - D) from the float32 P
+        uint32_t pk[16], dk[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
-          const float d0 = bf_lo(pk[t >> 1]) * (__uint_as_float(pr[t]) - dvc[t]);
-          const float d1 = bf_hi(pk[t >> 1]) * (__uint_as_float(pr[t + 1]) - dvc[t + 1]);
-          dk[t >> 1] = pack_bf16x2(d0, d1);
+          pk[t >> 1] = pack_bf16x2(pf[t], pf[t + 1]);
+          dk[t >> 1] = pack_bf16x2(pf[t] * (__uint_as_float(pr[t]) - dvc[t]),
+                                   pf[t + 1] * (__uint_as_float(pr[t + 1]) - dvc[t + 1]));
         }
         // P^T over the first 16 of the chunk's S^T columns, dS^T over the first
         // 16 of its dP^T columns (this thread has read them; no other has)
@@ -650,31 +642,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         tmem_ld32(ts, sr);
         tmem_ld32(ts + C::TM_DP, pr);
         tmem_ld_wait();
-        uint32_t pw[16], dk[16];
+        float pf[32];
         if (all_visible) {
 #pragma unroll
-          for (int t = 0; t < 32; t += 2)
-            pw[t >> 1] = pack_bf16x2(ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -l2)),
-                                     ex2_approx(fmaf(__uint_as_float(sr[t + 1]), c2, -l2)));
+          for (int t = 0; t < 32; ++t) pf[t] = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -l2));
         } else {
 #pragma unroll
-          for (int t = 0; t < 32; t += 2) {
-            float pp[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int key = k0 + 64 * hf + 32 * cq + t + u;
-              const bool vis = row_ok && key < kv_len && !(masks_causal(p.mask_kind) && key > qi);
-              const float e = ex2_approx(fmaf(__uint_as_float(sr[t + u]), c2, -l2));
-              pp[u] = vis ? e : 0.f;
-            }
-            pw[t >> 1] = pack_bf16x2(pp[0], pp[1]);
+          for (int t = 0; t < 32; ++t) {
+            const int key = k0 + 64 * hf + 32 * cq + t;
+            const bool vis = row_ok && key < kv_len && !(masks_causal(p.mask_kind) && key > qi);
+            const float e = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -l2));
+            pf[t] = vis ? e : 0.f;
           }
         }
-        // dS = P (dP - D) with P rounded to bf16 (as the dK/dV kernel uses it)
+        // dS = P (dP - D) from the float32 P (no product here takes P itself)
+        uint32_t dk[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2)
-          dk[t >> 1] = pack_bf16x2(bf_lo(pw[t >> 1]) * (__uint_as_float(pr[t]) - dvv),
-                                   bf_hi(pw[t >> 1]) * (__uint_as_float(pr[t + 1]) - dvv));
+          dk[t >> 1] = pack_bf16x2(pf[t] * (__uint_as_float(pr[t]) - dvv),
+                                   pf[t + 1] * (__uint_as_float(pr[t + 1]) - dvv));
         // dS over the first 16 of the chunk's S columns (read by this thread only)
         tmem_st16(ts, dk);
         tmem_st_wait();
