@@ -331,7 +331,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         ok = false;
         break;
       }
-      *v_dst = v_lse ? vn * 1.4426950408889634f : (vn == -INFINITY ? 0.f : vn);
+      // stored negated, for packed fma / add below: -lse (log2 units), -D
+      *v_dst = v_lse ? -(vn * 1.4426950408889634f) : (vn == -INFINITY ? 0.f : -vn);
       named_barrier(1, kGradThreads);
       if (*abort_flag) {
         ok = false;
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         uint32_t sr[32], pr[32];
         tmem_ld32(ts, sr);
         tmem_ld32(ts + C::TM_DP, pr);
-        float l2c[32], dvc[32];
+        float l2c[32], dvc[32];  // negated: -lse (log2 units), -D
 #pragma unroll
         for (int v4 = 0; v4 < 8; ++v4) {
           const float4 lv = reinterpret_cast<const float4*>(lse2_s + col0)[v4];
@@ -364,18 +365,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         tmem_ld_wait();
         float pf[32];
         // (the mask test stays outside the element loops, which then have no
-        // branches and interleave their 32 independent chains)
+        // branches and interleave their 32 independent chains; packed f32x2
+        // arithmetic halves the issue slots of the float math)
         if (all_visible) {
 #pragma unroll
-          for (int t = 0; t < 32; ++t)
-            pf[t] = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -l2c[t]));
+          for (int t = 0; t < 32; t += 2) {
+            fma2(pf[t], pf[t + 1], __uint_as_float(sr[t]), __uint_as_float(sr[t + 1]), c2, c2,
+                 l2c[t], l2c[t + 1]);
+            pf[t] = ex2_approx(pf[t]);
+            pf[t + 1] = ex2_approx(pf[t + 1]);
+          }
         } else {
 #pragma unroll
           for (int t = 0; t < 32; ++t) {
             const int qi = q0 + col0 + t;
             const bool vis = key < kv_len && qi < p.Lq &&
-                             !(masks_causal(p.mask_kind) && key > qi) && l2c[t] != -INFINITY;
-            const float e = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -l2c[t]));
+                             !(masks_causal(p.mask_kind) && key > qi) && l2c[t] != INFINITY;
+            const float e = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, l2c[t]));
             pf[t] = vis ? e : 0.f;
           }
         }
@@ -384,8 +390,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
           pk[t >> 1] = pack_bf16x2(pf[t], pf[t + 1]);
-          dk[t >> 1] = pack_bf16x2(pf[t] * (__uint_as_float(pr[t]) - dvc[t]),
-                                   pf[t + 1] * (__uint_as_float(pr[t + 1]) - dvc[t + 1]));
+          float g0, g1;
+          add2(g0, g1, __uint_as_float(pr[t]), __uint_as_float(pr[t + 1]), dvc[t], dvc[t + 1]);
+          mul2(g0, g1, pf[t], pf[t + 1], g0, g1);
+          dk[t >> 1] = pack_bf16x2(g0, g1);
         }
         // P^T over the first 16 of the chunk's S^T columns, dS^T over the first
         // 16 of its dP^T columns (this thread has read them; no other has)
@@ -645,7 +653,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         float pf[32];
         if (all_visible) {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) pf[t] = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -l2));
+          for (int t = 0; t < 32; t += 2) {
+            fma2(pf[t], pf[t + 1], __uint_as_float(sr[t]), __uint_as_float(sr[t + 1]), c2, c2,
+                 -l2, -l2);
+            pf[t] = ex2_approx(pf[t]);
+            pf[t + 1] = ex2_approx(pf[t + 1]);
+          }
         } else {
 #pragma unroll
           for (int t = 0; t < 32; ++t) {
@@ -658,9 +671,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         // dS = P (dP - D) from the float32 P (no product here takes P itself)
         uint32_t dk[16];
 #pragma unroll
-        for (int t = 0; t < 32; t += 2)
-          dk[t >> 1] = pack_bf16x2(pf[t] * (__uint_as_float(pr[t]) - dvv),
-                                   pf[t + 1] * (__uint_as_float(pr[t + 1]) - dvv));
+        for (int t = 0; t < 32; t += 2) {
+          float g0, g1;
+          add2(g0, g1, __uint_as_float(pr[t]), __uint_as_float(pr[t + 1]), -dvv, -dvv);
+          mul2(g0, g1, pf[t], pf[t + 1], g0, g1);
+          dk[t >> 1] = pack_bf16x2(g0, g1);
+        }
         // dS over the first 16 of the chunk's S columns (read by this thread only)
         tmem_st16(ts, dk);
         tmem_st_wait();
