@@ -472,7 +472,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
 
   const int n_qt = (p.Lq + 127) / 128;
   const int unit = static_cast<int>(blockIdx.x);
-  const int qt = unit % n_qt;
+  // last query tile first: under the causal mask it sees the most key tiles,
+  // so the heavy CTAs start early and the grid's tail is light
+  const int qt = n_qt - 1 - unit % n_qt;
   const int bh = unit / n_qt;
   const int b = bh / p.H, h = bh % p.H;
   const int q0 = qt * 128;
