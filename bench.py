@@ -955,7 +955,7 @@ def run_bwd(args):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "traffic": None,
                      "peak_source": f"{peak_src} dense bf16 (burst)",
-                     "kernel": "bwd_prep_kernel + bwd_dkdv_kernel + bwd_dq_kernel (whole step)",
+                     "kernel": "bwd_dq_kernel + bwd_dkdv_kernel (whole step)",
                      "kernel_ms": step_ms, "algorithmic_bytes": bytes_alg},
         "clocks": clocks,
         "e2e": {"value": e2e_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,

@@ -8,8 +8,11 @@
 //   dS_ij = a_ij (g_ij - D_i),   D_i = sum_j a_ij g_ij = dO_i . O_i
 //   dV_j  = sum_i a_ij dO_i,     dK_j = scale sum_i dS_ij q_i,
 //   dQ_i  = scale sum_j dS_ij k_j.
-// Three kernels:
-//   bwd_prep_kernel   D_i = dO_i . O_i (float32; a group of lanes per row).
+// Two kernels, in this order on the stream:
+//   bwd_dq_kernel     one CTA per (b, h, 128-query tile); first forms D_i for
+//                     its rows (stored for the next kernel), then the key
+//                     tiles it sees stream through a two-stage ring: S = Q K^T
+//                     and dP = dO V^T, then dS (bf16, over S), then dQ += dS K.
 //   bwd_dkdv_kernel   one CTA per (b, h, 128-key tile); the query tiles that
 //                     see the keys stream through a two-stage ring.  Per query
 //                     tile: S^T = K Q^T and dP^T = V dO^T on the tensor cores
@@ -17,9 +20,6 @@
 //                     into P^T and dS^T (bf16, written over S^T and dP^T in
 //                     TMEM), and dV += P^T dO, dK += dS^T Q accumulate in TMEM
 //                     (A operands from TMEM).
-//   bwd_dq_kernel     one CTA per (b, h, 128-query tile); the key tiles it
-//                     sees stream through a two-stage ring.  S = Q K^T and
-//                     dP = dO V^T, then dS (bf16, over S), then dQ += dS K.
 // Both take each streamed tile in two halves of 64 rows with TMEM regions of
 // their own: the tensor cores run one half's products (and the next tile's
 // scores) while the gradient warps turn the other half's scores into P, dS.
@@ -47,7 +47,7 @@ struct BwdCfg {
   static constexpr int OFF_A0 = 0;
   static constexpr int OFF_A1 = TILE;
   static constexpr int OFF_RING = 2 * TILE;    // stage s: pair at OFF_RING + s * 2 * TILE
-  static constexpr int OFF_VEC = OFF_RING + 4 * TILE;  // lse2[128], D[128] (dK/dV kernel)
+  static constexpr int OFF_VEC = OFF_RING + 4 * TILE;  // dK/dV: lse2[128], D[128]; dQ: D halves [2][128]
   static constexpr int OFF_BAR = OFF_VEC + 2 * 128 * 4;
   static constexpr int NBAR = 11;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;  // tmem slot, abort flag
@@ -74,44 +74,6 @@ __device__ __forceinline__ constexpr uint32_t a_col(int ks) {
 // bf16 halves of a packed pair -> float (exact)
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-// ---------------------------------------------------------------------------
-// D_i = dO_i . O_i for every row (b, i, h) of [B, Lq, H, d]; stored [B, H, Lq].
-// A group of G lanes (a power of two, G >= d / 8 up to 16) takes one row, each
-// lane 16-byte pieces of O and dO, so a warp reads 32 / G consecutive rows.
-// ---------------------------------------------------------------------------
-__host__ __device__ __forceinline__ int prep_group(int d) {
-  const int pieces = d / 8;
-  return pieces <= 1 ? 1 : pieces <= 2 ? 2 : pieces <= 4 ? 4 : pieces <= 8 ? 8 : 16;
-}
-
-__global__ void __launch_bounds__(256) bwd_prep_kernel(const __grid_constant__ BwdParams p) {
-  const long long rows = static_cast<long long>(p.B) * p.H * p.Lq;
-  const int lane = static_cast<int>(threadIdx.x & 31);
-  const int G = prep_group(p.d);
-  const int pieces = p.d / 8;
-  const int piece = lane % G;
-  const long long row = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * (32 / G) +
-                        lane / G;
-  float acc = 0.f;
-  if (row < rows) {
-    const uint4* o = reinterpret_cast<const uint4*>(p.out) + row * pieces;
-    const uint4* g = reinterpret_cast<const uint4*>(p.dout) + row * pieces;
-    for (int c = piece; c < pieces; c += G) {
-      const uint4 ov = o[c], gv = g[c];
-      acc += bf_lo(ov.x) * bf_lo(gv.x) + bf_hi(ov.x) * bf_hi(gv.x) + bf_lo(ov.y) * bf_lo(gv.y) +
-             bf_hi(ov.y) * bf_hi(gv.y) + bf_lo(ov.z) * bf_lo(gv.z) + bf_hi(ov.z) * bf_hi(gv.z) +
-             bf_lo(ov.w) * bf_lo(gv.w) + bf_hi(ov.w) * bf_hi(gv.w);
-    }
-  }
-  for (int s = G / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (piece == 0 && row < rows) {
-    const int h = static_cast<int>(row % p.H);
-    const int i = static_cast<int>((row / p.H) % p.Lq);
-    const int b = static_cast<int>(row / (static_cast<long long>(p.H) * p.Lq));
-    p.dvec[(static_cast<size_t>(b) * p.H + h) * p.Lq + i] = acc;
-  }
-}
 
 // Visible keys of sequence b (key padding), all keys otherwise.
 __device__ __forceinline__ int kv_len_of(const BwdParams& p, int b) {
@@ -627,12 +589,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     const int qi = q0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c2 = p.scale_log2;
-    float l2 = -INFINITY, dvv = 0.f;
+    // D_i = dO_i . O_i of this row, the two warps of the lane quarter taking
+    // alternate 16-byte pieces and adding their halves in shared memory; it
+    // is also written to the workspace for the dK/dV kernel, which runs next
+    float l2 = -INFINITY, part = 0.f;
+    const size_t idx = (static_cast<size_t>(b) * p.H + h) * p.Lq + qi;
     if (qi < p.Lq) {
-      const size_t idx = (static_cast<size_t>(b) * p.H + h) * p.Lq + qi;
       l2 = p.lse[idx] * 1.4426950408889634f;
-      dvv = p.dvec[idx];
+      const int pieces = p.d / 8;
+      const size_t row_elems = (static_cast<size_t>(b) * p.Lq + qi) * p.H + h;
+      const uint4* o = reinterpret_cast<const uint4*>(p.out) + row_elems * pieces;
+      const uint4* g = reinterpret_cast<const uint4*>(p.dout) + row_elems * pieces;
+      for (int c = cq; c < pieces; c += 2) {
+        const uint4 ov = o[c], gv = g[c];
+        part += bf_lo(ov.x) * bf_lo(gv.x) + bf_hi(ov.x) * bf_hi(gv.x) + bf_lo(ov.y) * bf_lo(gv.y) +
+                bf_hi(ov.y) * bf_hi(gv.y) + bf_lo(ov.z) * bf_lo(gv.z) + bf_hi(ov.z) * bf_hi(gv.z) +
+                bf_lo(ov.w) * bf_lo(gv.w) + bf_hi(ov.w) * bf_hi(gv.w);
+      }
     }
+    float* d_part = reinterpret_cast<float*>(smem + C::OFF_VEC);  // [2][128]
+    d_part[cq * 128 + r] = part;
+    named_barrier(1, kGradThreads);  // (no wait precedes it: every gradient warp gets here)
+    const float dvv = d_part[r] + d_part[128 + r];
+    if (cq == 0 && qi < p.Lq) p.dvec[idx] = dvv;
     const bool row_ok = qi < p.Lq && l2 != -INFINITY;
     bool ok = true;
     for (int it = 0; ok && it < n_iter; ++it) {
@@ -741,22 +720,18 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, LaunchInfo* in
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const long long rows = static_cast<long long>(p.B) * p.H * p.Lq;
-  const long long rows_per_block = 8ll * (32 / prep_group(p.d));
-  bwd_prep_kernel<<<static_cast<unsigned>((rows + rows_per_block - 1) / rows_per_block), 256, 0,
-                    stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   const long long bh = static_cast<long long>(p.B) * p.H;
   const long long kv_units = bh * ((p.Lk + 127) / 128);
   const long long q_units = bh * ((p.Lq + 127) / 128);
-  bwd_dkdv_kernel<D><<<static_cast<unsigned>(kv_units), kBwdThreads, C::SMEM, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  // the dQ kernel forms D = dO . O for its rows and stores it; the dK/dV
+  // kernel, next on the stream, reads it
   bwd_dq_kernel<D><<<static_cast<unsigned>(q_units), kBwdThreads, C::SMEM, stream>>>(p);
   e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bwd_dkdv_kernel<D><<<static_cast<unsigned>(kv_units), kBwdThreads, C::SMEM, stream>>>(p);
+  e = cudaGetLastError();
   if (info) {
-    info->kernels = 3;
+    info->kernels = 2;
     info->grid = static_cast<int>(kv_units + q_units);
     info->block = kBwdThreads;
     info->smem = C::SMEM;
