@@ -61,6 +61,9 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+F32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
 def visible_pairs(w, key_lens) -> float:
     """(query, visible key) pairs: the algorithmic work unit."""
     if w.mask_kind == inputs.MASK_CAUSAL:
@@ -256,11 +259,12 @@ def run_ours(args):
                               for _ in range(n_sets - 1)]
     cur = [0]
 
+    fwd = binding.mha_fwd if w.dtype == torch.bfloat16 else binding.mha_fwd_f32
+
     def step():
         qq, kk, vv, oo = sets[cur[0] % n_sets]
         cur[0] += 1
-        binding.mha_fwd(qq, kk, vv, out=oo, mask_kind=w.mask_kind, key_lens=lens,
-                        stream=stream)
+        fwd(qq, kk, vv, out=oo, mask_kind=w.mask_kind, key_lens=lens, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -310,7 +314,8 @@ def run_ours(args):
         hq, hk, hv = (case[n].pin_memory() for n in ("q", "k", "v"))
         hout = torch.empty_like(hq).pin_memory()
         hlens = case["key_lens"].pin_memory() if case["key_lens"] is not None else None
-        ws = torch.empty(binding.host_workspace_bytes(w.B, w.H, w.Lq, w.Lk, w.d_k, 2),
+        ws = torch.empty(binding.host_workspace_bytes(w.B, w.H, w.Lq, w.Lk, w.d_k,
+                                                      q.element_size()),
                          dtype=torch.uint8, device=dev)
         n_e2e = max(3, min(args.steps, 10))
         for _ in range(2):
@@ -346,7 +351,8 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, no dataset)",
+        "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded N(0,1) inputs, no dataset)",
         "config": workload_config(w, {
             "parallelism": f"replicas x{world} (no collective)",
             "inputs_exceed_l2": bytes_in * n_sets > L2_BYTES, "l2_flush": False,
@@ -355,12 +361,21 @@ def run_ours(args):
         "pct_of_peak": 100.0 * value / world / peak,
         "pct_of_sustained_peak": 100.0 * value / world / float(
             peaks.get("bf16_tflops_sustained", peak)),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} dense bf16 (burst)",
-                     "kernel": "fwd_bf16_kernel", "kernel_ms": kernel_ms,
-                     "algorithmic_bytes": bytes_alg,
-                     "achieved_gbs": bytes_alg / (kernel_ms * 1e-3) / 1e9},
+        "roofline": ({"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                      "frac": achieved / peak, "traffic": traffic,
+                      "peak_source": f"{peak_src} dense bf16 (burst)",
+                      "kernel": "fwd_bf16_kernel", "kernel_ms": kernel_ms,
+                      "algorithmic_bytes": bytes_alg,
+                      "achieved_gbs": bytes_alg / (kernel_ms * 1e-3) / 1e9}
+                     if w.dtype == torch.bfloat16 else
+                     # the float32 kernel runs on the CUDA cores: 152 SMs x 128
+                     # FMA lanes x 2 flops x 2070 MHz (nominal)
+                     {"bound": "alu", "achieved": achieved, "peak": F32_ALU_TFLOPS, "unit": UNIT,
+                      "frac": achieved / F32_ALU_TFLOPS, "traffic": None,
+                      "peak_source": "nominal fp32 FMA rate (152 x 128 x 2 x 2.07 GHz)",
+                      "kernel": "fwd_f32_kernel", "kernel_ms": kernel_ms,
+                      "algorithmic_bytes": bytes_alg,
+                      "achieved_gbs": bytes_alg / (kernel_ms * 1e-3) / 1e9}),
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": int(launches_per_step * args.steps),
