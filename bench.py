@@ -166,6 +166,71 @@ class ClockSampler:
                 "samples_in_timed_region": len(inside)}
 
 
+def timed_steps(step, args, dev, stream, rank, warm=True):
+    """args.steps steps between a barrier + synchronize on both sides (after
+    args.warmup untimed ones when ``warm``), clocks sampled meanwhile.
+
+    By default the steps are captured once into a CUDA graph (each step's
+    launches, through the same C-ABI calls) and the graph is replayed once
+    untimed and once timed, so the device runs the launches back to back and
+    the host's per-call argument marshalling (tens of microseconds of Python)
+    is not on the clock; the mean time per step is then the graph's time over
+    args.steps.  With ``--eager`` the steps are issued one by one with CUDA
+    events around each.  Returns (mean ms per step, total ms max over ranks,
+    clock summary or None)."""
+    if warm:
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                step()
+    torch.cuda.synchronize(dev)
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+            for _ in range(args.steps):
+                step()
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+    sampler = ClockSampler(gpu_id(dev))
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps if graph is None else 0)]
+    all_start = torch.cuda.Event(enable_timing=True)
+    all_end = torch.cuda.Event(enable_timing=True)
+    mdist.barrier(dev)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        all_start.record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(args.steps):
+                ev[i][0].record(stream)
+                step()
+                ev[i][1].record(stream)
+        all_end.record(stream)
+    torch.cuda.synchronize(dev)
+    mdist.barrier(dev)
+    t_wall1 = time.time()
+    total_ms = all_start.elapsed_time(all_end)
+    step_ms = (total_ms if graph is not None else sum(a.elapsed_time(b) for a, b in ev)) / args.steps
+    max_total_ms = mdist.max_over_ranks(total_ms, dev)
+    if rank == 0:
+        time.sleep(0.3)
+        sampler.stop()
+    del graph
+    return step_ms, max_total_ms, (sampler.summary(t_wall0, t_wall1) if rank == 0 else None)
+
+
+def timing_config(args):
+    return ({"timing": "eager: one C-ABI call per step, CUDA events around each"} if args.eager
+            else {"timing": "CUDA graph of the steps' C-ABI launches, replayed once timed"})
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -274,39 +339,11 @@ def run_ours(args):
         raise binding.MhaError(rc, "warm-up")
     launches_per_step = binding.last_launch_info()["kernels"]
 
-    sampler = ClockSampler(gpu_id(dev))
-    if rank == 0:
-        sampler.start()
-        time.sleep(0.3)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    all_start = torch.cuda.Event(enable_timing=True)
-    all_end = torch.cuda.Event(enable_timing=True)
-    mdist.barrier(dev)
-    torch.cuda.synchronize(dev)
-    t_wall0 = time.time()
-    with torch.cuda.stream(stream):
-        all_start.record(stream)
-        for i in range(args.steps):
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
-        all_end.record(stream)
-    torch.cuda.synchronize(dev)
-    mdist.barrier(dev)
-    t_wall1 = time.time()
+    kernel_ms, max_total_ms, clocks = timed_steps(step, args, dev, stream, rank, warm=False)
     rc = binding.mha_sync_status(stream)
     if rc != 0:
         raise binding.MhaError(rc, "timed region")
-    per_launch_ms = [a.elapsed_time(b) for a, b in ev]
-    kernel_ms = sum(per_launch_ms) / len(per_launch_ms)
-    total_ms = all_start.elapsed_time(all_end)
-    max_total_ms = mdist.max_over_ranks(total_ms, dev)
     total_flops = mdist.sum_over_ranks(flops_alg * args.steps, dev)
-    if rank == 0:
-        time.sleep(0.3)
-        sampler.stop()
-    clocks = sampler.summary(t_wall0, t_wall1) if rank == 0 else None
 
     # end to end: pinned host buffers through the C ABI's host entry
     e2e = None
@@ -357,7 +394,8 @@ def run_ours(args):
             "parallelism": f"replicas x{world} (no collective)",
             "inputs_exceed_l2": bytes_in * n_sets > L2_BYTES, "l2_flush": False,
             "input_sets_rotated": n_sets,
-            "flops_per_step_per_gpu": flops_alg, "flops_nominal_per_step_per_gpu": flops_nominal}),
+            "flops_per_step_per_gpu": flops_alg, "flops_nominal_per_step_per_gpu": flops_nominal,
+            **timing_config(args)}),
         "pct_of_peak": 100.0 * value / world / peak,
         "pct_of_sustained_peak": 100.0 * value / world / float(
             peaks.get("bf16_tflops_sustained", peak)),
@@ -515,38 +553,11 @@ def run_decode(args):
     if rc != 0:
         raise binding.MhaError(rc, "warm-up")
     launches_per_step = binding.last_launch_info()["kernels"]
-    sampler = ClockSampler(gpu_id(dev))
-    if rank == 0:
-        sampler.start()
-        time.sleep(0.3)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    all_start = torch.cuda.Event(enable_timing=True)
-    all_end = torch.cuda.Event(enable_timing=True)
-    mdist.barrier(dev)
-    torch.cuda.synchronize(dev)
-    t_wall0 = time.time()
-    with torch.cuda.stream(stream):
-        all_start.record(stream)
-        for i in range(args.steps):
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
-        all_end.record(stream)
-    torch.cuda.synchronize(dev)
-    mdist.barrier(dev)
-    t_wall1 = time.time()
+    step_ms, max_total_ms, clocks = timed_steps(step, args, dev, stream, rank, warm=False)
     rc = binding.mha_sync_status(stream)
     if rc != 0:
         raise binding.MhaError(rc, "timed region")
-    step_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
-    total_ms = all_start.elapsed_time(all_end)
-    max_total_ms = mdist.max_over_ranks(total_ms, dev)
     total_bytes = mdist.sum_over_ranks(bytes_alg * args.steps, dev)
-    if rank == 0:
-        time.sleep(0.3)
-        sampler.stop()
-    clocks = sampler.summary(t_wall0, t_wall1) if rank == 0 else None
 
     # end to end through the public API: each step brings q (and the cache
     # lengths) from pinned host memory, runs the step on the resident cache and
@@ -596,7 +607,7 @@ def run_decode(args):
             "parallelism": f"replicas x{world} (no collective)",
             "inputs_exceed_l2": cache_bytes * n_sets > L2_BYTES, "l2_flush": False,
             "input_sets_rotated": n_sets, "bytes_per_step_per_gpu": bytes_alg,
-            "splits": binding.last_launch_info()["kernels"] > 1}),
+            "splits": binding.last_launch_info()["kernels"] > 1, **timing_config(args)}),
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": DEC_UNIT,
                      "frac": achieved / peak,
@@ -667,43 +678,6 @@ def run_reference_decode(args):
 # backward pass
 # ---------------------------------------------------------------------------
 BWD_METRIC = "attention bwd TFLOP/s (bf16, 1 GB300; 2.5x forward flops) and % of dense BF16 tensor peak"
-
-
-def timed_steps(step, args, dev, stream, rank):
-    """Warm-up, then args.steps steps between a barrier + synchronize, CUDA
-    events per step and around all; clocks sampled meanwhile.  Returns
-    (mean ms per step, total ms max over ranks, clock summary or None)."""
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
-    torch.cuda.synchronize(dev)
-    sampler = ClockSampler(gpu_id(dev))
-    if rank == 0:
-        sampler.start()
-        time.sleep(0.3)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    all_start = torch.cuda.Event(enable_timing=True)
-    all_end = torch.cuda.Event(enable_timing=True)
-    mdist.barrier(dev)
-    torch.cuda.synchronize(dev)
-    t_wall0 = time.time()
-    with torch.cuda.stream(stream):
-        all_start.record(stream)
-        for i in range(args.steps):
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
-        all_end.record(stream)
-    torch.cuda.synchronize(dev)
-    mdist.barrier(dev)
-    t_wall1 = time.time()
-    step_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
-    max_total_ms = mdist.max_over_ranks(all_start.elapsed_time(all_end), dev)
-    if rank == 0:
-        time.sleep(0.3)
-        sampler.stop()
-    return step_ms, max_total_ms, (sampler.summary(t_wall0, t_wall1) if rank == 0 else None)
 
 
 # ---------------------------------------------------------------------------
@@ -823,7 +797,7 @@ def run_layer(args):
            "seed": w.seed, "weights": "random (Xavier-scaled N(0, 1/fan_in), bf16)",
            "parallelism": f"replicas x{world} (no collective)",
            "inputs_exceed_l2": in_bytes > L2_BYTES, "l2_flush": False,
-           "flops_per_step_per_gpu": flops_alg}
+           "flops_per_step_per_gpu": flops_alg, **timing_config(args)}
     line = {
         "metric": LAYER_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_total_ms / args.steps,
@@ -965,7 +939,8 @@ def run_bwd(args):
         "data": "synthetic (seeded N(0,1) inputs and dout, no dataset)",
         "config": workload_config(w, {"pass": "bwd", "parallelism": f"replicas x{world} (no collective)",
                                       "inputs_exceed_l2": bytes_alg > L2_BYTES, "l2_flush": False,
-                                      "flops_per_step_per_gpu": flops_alg}),
+                                      "flops_per_step_per_gpu": flops_alg,
+                                      **timing_config(args)}),
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "traffic": None,
@@ -1046,6 +1021,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="issue the timed steps one by one instead of replaying a CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
