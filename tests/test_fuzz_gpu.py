@@ -64,6 +64,27 @@ def test_fuzz_forward_bf16(mha, i):
     pu.assert_lse_close(lse.cpu(), ref_lse, f"fuzz bf16 lse {desc}")
 
 
+@pytest.mark.parametrize("i", range(8))
+def test_fuzz_forward_paired(mha, i):
+    """At most 128 query rows per head, head widths up to 64 and more heads
+    than SMs: the launch pairs two heads per unit."""
+    r = np.random.default_rng(21000 + i)
+    mask = int(r.integers(0, 4))
+    B = int(r.integers(1, 6))
+    H = int(r.integers(160 // B, 400 // B + 1))
+    Lq = int(r.integers(1, 129))
+    Lk = Lq if mask & CAUSAL else int(r.integers(1, 1200))
+    d = int(r.choice([16, 32, 48, 64]))
+    case = inputs.random_case(22000 + i, B, H, Lq, Lk, d)
+    if mask & KEYPAD:
+        case["key_lens"] = torch.tensor(r.integers(0, Lk + 1, size=B), dtype=torch.int32)
+    out, lse = pu.gpu_run_lse(mha, case, mask)
+    ref, ref_lse = pu.oracle_run(case, mask, return_lse=True)
+    desc = (B, H, Lq, Lk, d, mask)
+    pu.assert_bf16_close_rounding_aware(out.cpu(), ref, f"fuzz paired {desc}")
+    pu.assert_lse_close(lse.cpu(), ref_lse, f"fuzz paired lse {desc}")
+
+
 @pytest.mark.parametrize("i", range(0, N_CASES, 3))
 def test_fuzz_forward_f32(mha, i):
     case, mask, desc = _case(i, torch.float32)

@@ -92,6 +92,17 @@ SHAPES = [
     # unit's second tile empty; ragged Lk masks the last key tile)
     (2, 3, 300, 700, 64, NONE, None),
     (3, 2, 256, 1024, 64, KEYPAD, [1024, 513, 0]),
+    # d 64 with at most 128 query rows and more heads than SMs: a unit pairs
+    # two heads, each query tile with its own key tiles (odd head counts leave
+    # the last unit's second tile empty; key lengths differ between the
+    # paired heads)
+    (1, 157, 100, 700, 64, NONE, None),
+    (3, 53, 128, 1024, 64, KEYPAD, [1024, 0, 385]),
+    (5, 33, 128, 300, 64, KEYPAD, [300, 1, 129, 256, 0]),
+    (3, 55, 128, 128, 64, CAUSAL, None),
+    (2, 77, 77, 77, 64, CAUSAL | KEYPAD, [77, 40]),
+    (7, 23, 1, 1000, 64, NONE, None),
+    (33, 8, 128, 128, 64, NONE, None),
 ]
 
 
@@ -296,6 +307,21 @@ def test_launch_shape(mha):
     # one CTA per (b, h, block of 256 query rows)
     assert info["kernels"] == 1 and info["grid"] == 3 * 5 * 2
     assert mha.mha_sync_status() == 0
+
+
+@pytest.mark.parametrize("B,H,Lq,d", [(33, 8, 128, 64), (3, 55, 100, 32), (1, 100, 128, 64),
+                                      (1, 300, 129, 64), (3, 55, 128, 128)])
+def test_paired_launch_shape(mha, B, H, Lq, d):
+    """Heads are paired (one CTA per two heads and 128-row query tile) only at
+    widths up to 64, with at most 128 query rows and more heads than SMs."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    case = pu.to_cuda(inputs.random_case(11, B, H, Lq, 200, d))
+    mha.mha_fwd(case["q"], case["k"], case["v"])
+    info = mha.last_launch_info()
+    assert mha.mha_sync_status() == 0
+    paired = d <= 64 and Lq <= 128 and B * H > sms
+    expect = (B * H + 1) // 2 if paired else B * H * ((Lq + 255) // 256)
+    assert info["grid"] == expect, (info, paired, sms)
 
 
 # --------------------------------------------------------------------------

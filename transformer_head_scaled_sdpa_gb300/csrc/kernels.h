@@ -33,7 +33,11 @@ struct Bf16Params {
   DeviceStatus* status;
   int B, H, Lq, Lk;
   int mask_kind;
-  int n_qtiles;      // query blocks per head: ceil(Lq / kUnitRows)
+  int n_qtiles;      // query blocks per head: ceil(Lq / kUnitRows); the launch
+                     // sets ceil(Lq / kBlockM) when it pairs heads
+  int paired;        // set by the launch: 0 = a unit is two query tiles of one
+                     // head sharing every K/V tile; 1 (d_k = 64) = a unit is the
+                     // same query tile of two heads, each with its own K/V tiles
   float scale_log2;  // scale * log2(e)
   int withhold_p;    // test hook: softmax 0 withholds its first P arrival (0 = off)
 };

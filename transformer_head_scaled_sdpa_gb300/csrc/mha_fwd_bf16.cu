@@ -24,6 +24,10 @@
 // set-up, tensor memory and pipelines carry over from unit to unit, the next
 // unit's Q is loaded while the current one finishes, and the hardware's
 // launch order (heavy causal blocks first) still balances the load.
+// Paired units (d_k = 64, at most 128 query rows, more heads than SMs): a
+// unit is instead one 128-row query tile of two heads, Q0 of one and Q1 of
+// the next, each with its own K/V tiles in the ring, so no softmax warpgroup
+// idles for want of a second query tile and the grid halves.
 //
 // 384 threads (three warpgroups) in five roles:
 //   warps 0-3   softmax + epilogue for Q0 (thread r owns row r = TMEM lane r)
@@ -137,42 +141,127 @@ struct Bars {
 // role ids for the status "site" field
 constexpr int kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleScheduler = 4;
 
-struct Unit {
+// A shared unit: (b, h, 256-row block), two query tiles of one head sharing
+// every K/V tile; ring slot j holds key tile j for both.
+struct SharedUnit {
   int b, h;
   int q0;       // first query row of Q0
   int n[2];     // key tiles for Q0, Q1
   int kv_len;   // keys visible before the causal limit
+  __device__ __forceinline__ int seq(int) const { return b; }
+  __device__ __forceinline__ int head(int) const { return h; }
+  __device__ __forceinline__ int qstart(int g) const { return q0 + g * kBlockM; }
+  __device__ __forceinline__ int keys(int) const { return kv_len; }
 };
 
-__device__ __forceinline__ Unit decode_unit(const Bf16Params& p, int unit) {
-  // Units are ordered in groups of kHeadGroup heads, so a group's K/V stay in
-  // L2 while all of its query blocks run; inside a group the causal blocks go
-  // heaviest first.
-  const int bh_count = p.B * p.H;
-  const int n_pairs = p.n_qtiles;  // query blocks of 256 rows
-  const int group = unit / (kHeadGroup * n_pairs);
-  const int within = unit - group * kHeadGroup * n_pairs;
-  const int heads_here = min(kHeadGroup, bh_count - group * kHeadGroup);
-  const int pair_idx = within / heads_here;
-  const int bh = group * kHeadGroup + within % heads_here;
-  const int t = masks_causal(p.mask_kind) ? (n_pairs - 1 - pair_idx) : pair_idx;
-  Unit u;
-  u.b = bh / p.H;
-  u.h = bh % p.H;
-  u.q0 = t * kUnitRows;
-  int kv_len = p.Lk;
-  if (masks_padding(p.mask_kind)) {
-    const int len = __ldg(p.key_lens + u.b);
-    kv_len = len < 0 ? 0 : (len > p.Lk ? p.Lk : len);
+// A paired unit: (two consecutive heads, 128-row query tile), Q_g from head
+// 2i + g with key tiles of its own.  The heads' tiles alternate in the ring
+// (Q0's tile j, Q1's tile j, ...) while both have tiles, then the longer list
+// goes on alone.  Per-tile fields are read by select, not by index: g is
+// often not a compile-time constant, and an indexed struct would live in
+// local memory.
+struct PairedUnit {
+  int b[2], h[2];
+  int qs[2];        // first query row of Q_g (Lq: no such tile)
+  int n[2];         // key tiles of Q_g
+  int kv_len[2];
+  int m;            // min(n[0], n[1])
+  __device__ __forceinline__ int seq(int g) const { return g ? b[1] : b[0]; }
+  __device__ __forceinline__ int head(int g) const { return g ? h[1] : h[0]; }
+  __device__ __forceinline__ int qstart(int g) const { return g ? qs[1] : qs[0]; }
+  __device__ __forceinline__ int keys(int g) const { return g ? kv_len[1] : kv_len[0]; }
+  __device__ __forceinline__ int slots() const { return n[0] + n[1]; }
+  // ring slot (within the unit) of Q_g's key tile j
+  __device__ __forceinline__ int slot_of(int g, int j) const {
+    return j < m ? 2 * j + g : 2 * m + (j - m);
   }
-  u.kv_len = kv_len;
-  const int n_kv = (kv_len + kBlockN - 1) / kBlockN;
+  // query tile owning a slot (returned) and its key tile *j
+  __device__ __forceinline__ int owner(int slot, int* j) const {
+    if (slot < 2 * m) {
+      *j = slot >> 1;
+      return slot & 1;
+    }
+    *j = m + (slot - 2 * m);
+    return n[0] > n[1] ? 0 : 1;
+  }
+};
+
+template <bool PAIRED>
+struct UnitSel {
+  using T = SharedUnit;
+};
+template <>
+struct UnitSel<true> {
+  using T = PairedUnit;
+};
+
+__device__ __forceinline__ int visible_keys(const Bf16Params& p, int b) {
+  if (!masks_padding(p.mask_kind)) return p.Lk;
+  const int len = __ldg(p.key_lens + b);
+  return len < 0 ? 0 : (len > p.Lk ? p.Lk : len);
+}
+
+// key tiles of the 128-row query tile starting at qs
+__device__ __forceinline__ int tiles_for(const Bf16Params& p, int qs, int kv_len) {
+  int n = (qs < p.Lq) ? (kv_len + kBlockN - 1) / kBlockN : 0;
+  if (masks_causal(p.mask_kind) && n > qs / kBlockN + 1) n = qs / kBlockN + 1;
+  return n;
+}
+
+// Units are ordered in groups of kHeadGroup heads, so a group's K/V stay in
+// L2 while all of its query blocks run; inside a group the causal blocks go
+// heaviest first.
+template <bool PAIRED>
+__device__ __forceinline__ typename UnitSel<PAIRED>::T decode_unit(const Bf16Params& p,
+                                                                   int unit) {
+  const int bh_count = p.B * p.H;
+  const int n_blocks = p.n_qtiles;
+  typename UnitSel<PAIRED>::T u;
+  if constexpr (!PAIRED) {
+    const int group = unit / (kHeadGroup * n_blocks);
+    const int within = unit - group * kHeadGroup * n_blocks;
+    const int heads_here = min(kHeadGroup, bh_count - group * kHeadGroup);
+    const int pair_idx = within / heads_here;
+    const int bh = group * kHeadGroup + within % heads_here;
+    const int t = masks_causal(p.mask_kind) ? (n_blocks - 1 - pair_idx) : pair_idx;
+    u.b = bh / p.H;
+    u.h = bh % p.H;
+    u.q0 = t * kUnitRows;
+    int kv_len = p.Lk;
+    if (masks_padding(p.mask_kind)) {
+      const int len = __ldg(p.key_lens + u.b);
+      kv_len = len < 0 ? 0 : (len > p.Lk ? p.Lk : len);
+    }
+    u.kv_len = kv_len;
+    const int n_kv = (kv_len + kBlockN - 1) / kBlockN;
 #pragma unroll
-  for (int g = 0; g < 2; ++g) {
-    const int qs = u.q0 + g * kBlockM;
-    int n = (qs < p.Lq) ? n_kv : 0;
-    if (masks_causal(p.mask_kind) && n > qs / kBlockN + 1) n = qs / kBlockN + 1;
-    u.n[g] = n;
+    for (int g = 0; g < 2; ++g) {
+      const int qs = u.q0 + g * kBlockM;
+      int n = (qs < p.Lq) ? n_kv : 0;
+      if (masks_causal(p.mask_kind) && n > qs / kBlockN + 1) n = qs / kBlockN + 1;
+      u.n[g] = n;
+    }
+  } else {
+    constexpr int kPairGroup = kHeadGroup / 2;
+    const int n_pairs = (bh_count + 1) / 2;
+    const int group = unit / (kPairGroup * n_blocks);
+    const int within = unit - group * kPairGroup * n_blocks;
+    const int pairs_here = min(kPairGroup, n_pairs - group * kPairGroup);
+    const int tile_idx = within / pairs_here;
+    const int pair = group * kPairGroup + within % pairs_here;
+    const int t = masks_causal(p.mask_kind) ? (n_blocks - 1 - tile_idx) : tile_idx;
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      int bh = 2 * pair + g;
+      const bool exists = bh < bh_count;  // an odd head count leaves the last Q1 empty
+      if (!exists) bh = 2 * pair;
+      u.b[g] = bh / p.H;
+      u.h[g] = bh % p.H;
+      u.qs[g] = exists ? t * kBlockM : p.Lq;
+      u.kv_len[g] = visible_keys(p, u.b[g]);
+      u.n[g] = tiles_for(p, u.qs[g], u.kv_len[g]);
+    }
+    u.m = min(u.n[0], u.n[1]);
   }
   return u;
 }
@@ -253,7 +342,7 @@ __device__ __forceinline__ void producer_role(const Bf16Params& p, const Ctx& cx
   for (int k = 0; ok; ++k) {
     const int unit = next_unit<NS>(p, cx, k, kRoleProducer, cx.lane == 0);
     if (unit < 0) break;
-    const Unit u = decode_unit(p, unit);
+    const auto u = decode_unit<false>(p, unit);
     const int n_max = max(u.n[0], u.n[1]);
     auto load_q = [&](int g) {
       // the previous unit's last S_g must be done with the Q_g buffer
@@ -322,6 +411,92 @@ __device__ __forceinline__ void producer_role(const Bf16Params& p, const Ctx& cx
   }
 }
 
+// TMA producer for paired units: Q0 with its first K and V, Q1 with its
+// first K and V, then the unit's ring slots in order.
+template <int D>
+__device__ __forceinline__ void producer_role_paired(const Bf16Params& p, const Ctx& cx) {
+  using C = Cfg<D>;
+  using BA = Bars<C::NS>;
+  constexpr int NS = C::NS;
+  int q_cnt[2] = {0, 0};  // Q_g loads so far
+  int kv_cnt = 0;         // ring slots of the units before the current one
+  int kv_issued = 0;      // K tile loads issued
+  int v_issued = 0;       // V tile loads issued
+  bool ok = true;
+  for (int k = 0; ok; ++k) {
+    const int unit = next_unit<NS>(p, cx, k, kRoleProducer, cx.lane == 0);
+    if (unit < 0) break;
+    const auto u = decode_unit<true>(p, unit);
+    auto load_q = [&](int g) {
+      // the previous unit's last S_g must be done with the Q_g buffer
+      if (q_cnt[g] > 0 && !mbar_wait(cx.bar(BA::Q_FREE + g), (q_cnt[g] - 1) & 1, cx.abort_flag,
+                                     p.status, kRoleProducer * 64 + BA::Q_FREE + g))
+        return false;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(cx.bar(BA::Q_FULL + g), C::TILE);
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d(cx.sQ + g * C::TILE + c * C::CHUNK, &p.tm_q, cx.bar(BA::Q_FULL + g), 64 * c,
+                      u.head(g), u.qstart(g), u.seq(g));
+      }
+      __syncwarp();
+      ++q_cnt[g];
+      return true;
+    };
+    // key tile j of query tile g's head into ring slot `slot` of the unit
+    auto load_kv = [&](int slot, int g, int j, bool is_v) {
+      const int t = kv_cnt + slot;
+      const int s = t % NS;
+      const uint32_t dst = (is_v ? cx.sV : cx.sK) + s * C::TILE;
+      const uint32_t full = cx.bar((is_v ? BA::V_FULL : BA::K_FULL) + s);
+      // the stage's previous K (or V) tile must be done with
+      const int empty = (is_v ? BA::V_EMPTY : BA::K_EMPTY) + s;
+      if (t >= NS && (!is_v || C::SPLIT_RELEASE) &&
+          !mbar_wait(cx.bar(empty), ((t / NS) - 1) & 1, cx.abort_flag, p.status,
+                     kRoleProducer * 64 + empty))
+        return false;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(full, C::TILE);
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_4d(dst + c * C::CHUNK, is_v ? &p.tm_v : &p.tm_k, full, 64 * c, u.head(g),
+                      j * kBlockN, u.seq(g));
+      }
+      __syncwarp();
+      if (is_v) {
+        ++v_issued;
+      } else {
+        ++kv_issued;
+      }
+      return true;
+    };
+    const int n_slots = u.slots();
+    for (int slot = 0; ok && slot < n_slots; ++slot) {
+      int j = 0;
+      const int g = u.owner(slot, &j);
+      ok = (j > 0 || load_q(g)) && load_kv(slot, g, j, false) && load_kv(slot, g, j, true);
+    }
+    kv_cnt += n_slots;
+  }
+  // Leave only when every copy this warp started has landed (the normal path
+  // finds them complete already): the last Q_g and the last load of each
+  // stage.  These waits ignore the abort flag: a copy still in flight must not
+  // land in the shared memory of a CTA that has exited.
+  volatile int never = 0;
+  for (int g = 0; g < 2; ++g)
+    if (q_cnt[g] > 0)
+      mbar_wait(cx.bar(BA::Q_FULL + g), (q_cnt[g] - 1) & 1, &never, p.status,
+                kRoleProducer * 64 + BA::Q_FULL + g);
+  for (int t = (kv_issued > NS ? kv_issued - NS : 0); t < kv_issued; ++t) {
+    const int s = t % NS;
+    mbar_wait(cx.bar(BA::K_FULL + s), (t / NS) & 1, &never, p.status,
+              kRoleProducer * 64 + BA::K_FULL + s);
+    if (t < v_issued)
+      mbar_wait(cx.bar(BA::V_FULL + s), (t / NS) & 1, &never, p.status,
+                kRoleProducer * 64 + BA::V_FULL + s);
+  }
+}
+
 // MMA issuer for one query tile, used with separate P (d_k = 64): warp 8
 // serves Q0 and warp 11 Q1 (GSEL 0 and 1), each following only its own tile's
 // chain so neither waits on the other's softmax; both release every K/V stage
@@ -330,7 +505,7 @@ __device__ __forceinline__ void producer_role(const Bf16Params& p, const Ctx& cx
 // whole warp runs the loop and the waits; one elected lane issues every
 // tcgen05.mma and tcgen05.commit, with descriptors built once and stepped by
 // constants.
-template <int D, int GSEL>
+template <int D, int GSEL, bool PAIRED>
 __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx) {
   using C = Cfg<D>;
   using BA = Bars<C::NS>;
@@ -416,45 +591,85 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx) {
   static_assert(GSEL == 0 || GSEL == 1, "one query tile per warp");
   static_assert(C::SEPARATE_P && !C::SPLIT_RELEASE,
                 "one MMA warp per query tile: P apart from S, one release per stage");
-  constexpr int g_lo = GSEL;
-  constexpr int g_hi = GSEL;
-  for (int k = 0; ok; ++k) {
-    const int unit = next_unit<NS>(p, cx, k, kRoleMma, cx.lane == 0);
-    if (unit < 0) break;
-    const Unit u = decode_unit(p, unit);
-    const int n_max = max(u.n[0], u.n[1]);
-    if (n_max == 0) continue;
-    // prologue: S_g(0)
+  if constexpr (!PAIRED) {
+    constexpr int g_lo = GSEL;
+    constexpr int g_hi = GSEL;
+    for (int k = 0; ok; ++k) {
+      const int unit = next_unit<NS>(p, cx, k, kRoleMma, cx.lane == 0);
+      if (unit < 0) break;
+      const auto u = decode_unit<PAIRED>(p, unit);
+      const int n_max = max(u.n[0], u.n[1]);
+      if (n_max == 0) continue;
+      // prologue: S_g(0)
 #pragma unroll
-    for (int g = g_lo; g <= g_hi; ++g)
-      if (ok && u.n[g] > 0)
+      for (int g = g_lo; g <= g_hi; ++g)
+        if (ok && u.n[g] > 0)
+          ok = mbar_wait(cx.bar(BA::Q_FULL + g), q_cnt[g] & 1, cx.abort_flag, p.status,
+                         site + BA::Q_FULL + g) &&
+               next_s(g, kv_cnt, 0, u.n[g]);
+      for (int j = 0; ok && j < n_max; ++j) {
+        const int t = kv_cnt + j;
+        bool used = false;
+#pragma unroll
+        for (int g = g_lo; g <= g_hi; ++g) {
+          const int n = u.n[g];
+          if (!ok || j >= n) continue;
+          used = true;
+          // S_g(j+1) first: it only needs the softmax to have read S_g(j)
+          ok = (j + 1 >= n || next_s(g, t + 1, j + 1, n)) && next_pv(g, t, j, n);
+        }
+        if (ok && !used) {
+          // A tile none of this warp's query tiles uses: release its stage only
+          // once it was loaded, so each release phase gets one arrival per MMA
+          // warp (a warp running ahead would complete a phase on its own).
+          ok = mbar_wait(cx.bar(BA::K_FULL + t % NS), (t / NS) & 1, cx.abort_flag, p.status,
+                         site + BA::K_FULL + t % NS);
+        }
+        if (!ok) break;
+        // the stage's K and V tiles are both done with (one release per stage)
+        commit(BA::K_EMPTY + t % NS);
+      }
+      for (int g = 0; g < 2; ++g) q_cnt[g] += (u.n[g] > 0);
+      kv_cnt += n_max;
+    }
+  } else {
+    constexpr int g = GSEL;
+    for (int k = 0; ok; ++k) {
+      const int unit = next_unit<NS>(p, cx, k, kRoleMma, cx.lane == 0);
+      if (unit < 0) break;
+      const auto u = decode_unit<PAIRED>(p, unit);
+      const int n_slots = u.slots();
+      if (n_slots == 0) continue;
+      const int n = u.n[g];
+      // prologue: S_g(0)
+      if (n > 0)
         ok = mbar_wait(cx.bar(BA::Q_FULL + g), q_cnt[g] & 1, cx.abort_flag, p.status,
                        site + BA::Q_FULL + g) &&
-             next_s(g, kv_cnt, 0, u.n[g]);
-    for (int j = 0; ok && j < n_max; ++j) {
-      const int t = kv_cnt + j;
-      bool used = false;
-#pragma unroll
-      for (int g = g_lo; g <= g_hi; ++g) {
-        const int n = u.n[g];
-        if (!ok || j >= n) continue;
-        used = true;
-        // S_g(j+1) first: it only needs the softmax to have read S_g(j)
-        ok = (j + 1 >= n || next_s(g, t + 1, j + 1, n)) && next_pv(g, t, j, n);
+             next_s(g, kv_cnt + u.slot_of(g, 0), 0, n);
+      // Every slot of the unit, in load order: this warp's own key tiles get
+      // S_g(j+1) (it only needs the softmax to have read S_g(j)) and then
+      // PV_g(j); every slot, own or not, gets this warp's release.
+      int j = 0;  // this warp's next key tile
+      for (int slot = 0; ok && slot < n_slots; ++slot) {
+        const int t = kv_cnt + slot;
+        if (j < n && u.slot_of(g, j) == slot) {
+          ok = (j + 1 >= n || next_s(g, kv_cnt + u.slot_of(g, j + 1), j + 1, n)) &&
+               next_pv(g, t, j, n);
+          ++j;
+        } else {
+          // A slot none of this warp's work uses: release it only once it was
+          // loaded, so each release phase gets one arrival per MMA warp (a warp
+          // running ahead would complete a phase on its own).
+          ok = mbar_wait(cx.bar(BA::K_FULL + t % NS), (t / NS) & 1, cx.abort_flag, p.status,
+                         site + BA::K_FULL + t % NS);
+        }
+        if (!ok) break;
+        // the stage's K and V tiles are both done with (one release per stage)
+        commit(BA::K_EMPTY + t % NS);
       }
-      if (ok && !used) {
-        // A tile none of this warp's query tiles uses: release its stage only
-        // once it was loaded, so each release phase gets one arrival per MMA
-        // warp (a warp running ahead would complete a phase on its own).
-        ok = mbar_wait(cx.bar(BA::K_FULL + t % NS), (t / NS) & 1, cx.abort_flag, p.status,
-                       site + BA::K_FULL + t % NS);
-      }
-      if (!ok) break;
-      // the stage's K and V tiles are both done with (one release per stage)
-      commit(BA::K_EMPTY + t % NS);
+      q_cnt[g] += (n > 0);
+      kv_cnt += n_slots;
     }
-    for (int g = 0; g < 2; ++g) q_cnt[g] += (u.n[g] > 0);
-    kv_cnt += n_max;
   }
   // Every MMA this warp issued completes before TMEM is released.
   constexpr int dr = BA::DRAIN + (GSEL == 1 ? 1 : 0);
@@ -564,7 +779,7 @@ __device__ __forceinline__ void mma_role_pair(const Bf16Params& p, const Ctx& cx
   for (int k = 0; ok; ++k) {
     const int unit = next_unit<NS>(p, cx, k, kRoleMma, cx.lane == 0);
     if (unit < 0) break;
-    const Unit u = decode_unit(p, unit);
+    const auto u = decode_unit<false>(p, unit);
     const int n_max = max(u.n[0], u.n[1]);
     if (n_max == 0) continue;
     // prologue: S0(0), S1(0); then K_0 is done with
@@ -601,7 +816,7 @@ __device__ __forceinline__ void mma_role_pair(const Bf16Params& p, const Ctx& cx
 // pair.  That keeps their SFU-bound phases apart, so each runs at the full SFU
 // rate while the other does its loads, maxima and stores (d_k = 64 without the
 // causal mask, where the SFU work per score equals the tensor work: +5 %).
-template <int D, bool TOK>
+template <int D, bool TOK, bool PAIRED>
 __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx) {
   using C = Cfg<D>;
   using BA = Bars<C::NS>;
@@ -628,10 +843,13 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
   for (int k = 0; ok; ++k) {
     const int unit = next_unit<C::NS>(p, cx, k, kRoleSoftmax, lane == 0);
     if (unit < 0) break;
-    const Unit u = decode_unit(p, unit);
-    const int q_start = u.q0 + g * kBlockM;
+    const auto u = decode_unit<PAIRED>(p, unit);
+    const int q_start = u.qstart(g);
     const int qi = q_start + row;
-    const int n_tiles = u.n[g];
+    const int n_tiles = PAIRED ? (g ? u.n[1] : u.n[0]) : u.n[g];
+    const int kv_len = u.keys(g);
+    const int seq = u.seq(g);
+    const int head = u.head(g);
     // Turns alternate Q0, Q1, Q0, ... over the key tiles both query tiles
     // have; Q1's warp hands Q0's the first turn of each unit.  Each side
     // passes only after it has waited for the other's pass, so no turn
@@ -661,7 +879,7 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
       for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(r[c]);
       // per-element mask on the diagonal tile and a ragged last tile
       const int kbase = j * kBlockN;
-      int lim = u.kv_len - kbase;                                  // keys c < lim exist
+      int lim = kv_len - kbase;                                    // keys c < lim exist
       if (masks_causal(p.mask_kind) && qi - kbase + 1 < lim) lim = qi - kbase + 1;
       if (lim < kBlockN) {
 #pragma unroll
@@ -769,7 +987,7 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
     if (p.lse && qi < p.Lq) {
       // log of the softmax denominator, natural units: m_ref and the
       // exponents are in log2 units of the scaled scores
-      p.lse[(static_cast<size_t>(u.b) * p.H + u.h) * p.Lq + qi] =
+      p.lse[(static_cast<size_t>(seq) * p.H + head) * p.Lq + qi] =
           (l > 0.f) ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
 #pragma unroll
@@ -807,7 +1025,7 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
       fence_proxy_async_smem();
       named_barrier(1 + g, 128);
       if (store_thread) {
-        tma_store_4d(&p.tm_o, stage, 64 * c, u.h, q_start, u.b);
+        tma_store_4d(&p.tm_o, stage, 64 * c, head, q_start, seq);
         tma_store_commit();
       }
       __syncwarp();
@@ -819,7 +1037,7 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
   __syncwarp();
 }
 
-template <int D, bool TOK>
+template <int D, bool TOK, bool PAIRED>
 __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_constant__ Bf16Params p) {
   using C = Cfg<D>;
   using BA = Bars<C::NS>;
@@ -889,19 +1107,23 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
 
   if (cx.warp < kSoftmaxWarp0 + 8) {
     regs_increase<C::REGS_SOFTMAX>();
-    softmax_role<D, TOK>(p, cx);
+    softmax_role<D, TOK, PAIRED>(p, cx);
   } else {
     regs_decrease<C::REGS_OTHER>();
     if (cx.warp == kMmaWarp) {
       if constexpr (C::SEPARATE_P) {
-        mma_role<D, 0>(p, cx);
+        mma_role<D, 0, PAIRED>(p, cx);
       } else {
         mma_role_pair<D>(p, cx);
       }
     } else if (cx.warp == kMma1Warp) {
-      if constexpr (C::SEPARATE_P) mma_role<D, 1>(p, cx);
+      if constexpr (C::SEPARATE_P) mma_role<D, 1, PAIRED>(p, cx);
     } else if (cx.warp == kProducerWarp) {
-      producer_role<D>(p, cx);
+      if constexpr (PAIRED) {
+        producer_role_paired<D>(p, cx);
+      } else {
+        producer_role<D>(p, cx);
+      }
     } else {
       scheduler_role<D>(p, cx);
     }
@@ -916,8 +1138,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   }
 }
 
-template <int D, bool TOK>
+template <int D, bool TOK, bool PAIRED>
 cudaError_t launch_d(const Bf16Params& p, cudaStream_t stream, LaunchInfo* info) {
+  static_assert(!PAIRED || D == 64, "heads are paired only with one MMA warp per query tile");
   using C = Cfg<D>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -925,14 +1148,17 @@ cudaError_t launch_d(const Bf16Params& p, cudaStream_t stream, LaunchInfo* info)
   static bool attr_set[64] = {};  // the attribute is per device and function
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(fwd_bf16_kernel<D, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fwd_bf16_kernel<D, TOK, PAIRED>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const long long units = static_cast<long long>(p.n_qtiles) * p.B * p.H;
+  const long long units = static_cast<long long>(p.n_qtiles) *
+                          (PAIRED ? (static_cast<long long>(p.B) * p.H + 1) / 2
+                                  : static_cast<long long>(p.B) * p.H);
   const dim3 grid(static_cast<unsigned>(units));
-  fwd_bf16_kernel<D, TOK><<<grid, kThreads, C::SMEM, stream>>>(p);
+  fwd_bf16_kernel<D, TOK, PAIRED><<<grid, kThreads, C::SMEM, stream>>>(p);
   if (info) {
     info->kernels = 1;
     info->grid = static_cast<int>(units);
@@ -944,15 +1170,40 @@ cudaError_t launch_d(const Bf16Params& p, cudaStream_t stream, LaunchInfo* info)
 
 }  // namespace
 
-cudaError_t launch_fwd_bf16(const Bf16Params& p, int d, cudaStream_t stream, LaunchInfo* info) {
+cudaError_t launch_fwd_bf16(const Bf16Params& params, int d, cudaStream_t stream,
+                            LaunchInfo* info) {
+  Bf16Params p = params;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidDevice;
+  // Pairing heads (d_k = 64 only, where each query tile has its own MMA
+  // warp).  With a single query tile per head a shared unit leaves its second
+  // tile, and half of the softmax warps, idle; pairing halves the units and
+  // runs two heads per SM at once, which pays when the shared units would
+  // take more than one wave of the SMs (measured: 256 heads of 128 rows
+  // 9.1 -> 7.4 us; 128 heads of one query row against 4096 keys 33 -> 57 us,
+  // where pairing leaves half of the SMs idle).  With two or more query tiles
+  // per head, sharing each K/V tile between them is faster.
+  p.paired = (d == 64 && p.Lq <= kBlockM && static_cast<long long>(p.B) * p.H > sms) ? 1 : 0;
+  if (p.paired) {
+    const long long units = static_cast<long long>((p.Lq + kBlockM - 1) / kBlockM) *
+                            ((static_cast<long long>(p.B) * p.H + 1) / 2);
+    if (units > 0x7fffffffll) return cudaErrorInvalidValue;
+    p.n_qtiles = (p.Lq + kBlockM - 1) / kBlockM;
+  }
   // (the exponential turn-taking pays off at d_k = 64 without the causal
   // mask once units span several key tiles; with one or two key tiles the
   // hand-over at the start of each unit costs more than it saves)
-  if (d == 64)
-    return (!masks_causal(p.mask_kind) && p.Lk >= 4 * kBlockN)
-               ? launch_d<64, true>(p, stream, info)
-               : launch_d<64, false>(p, stream, info);
-  if (d == 128) return launch_d<128, false>(p, stream, info);
+  if (d == 64) {
+    const bool tok = !masks_causal(p.mask_kind) && p.Lk >= 4 * kBlockN;
+    if (p.paired)
+      return tok ? launch_d<64, true, true>(p, stream, info)
+                 : launch_d<64, false, true>(p, stream, info);
+    return tok ? launch_d<64, true, false>(p, stream, info)
+               : launch_d<64, false, false>(p, stream, info);
+  }
+  if (d == 128) return launch_d<128, false, false>(p, stream, info);
   return cudaErrorInvalidValue;
 }
 
