@@ -117,6 +117,26 @@ cudaError_t launch_bwd(const BwdParams& p, int d, cudaStream_t stream, LaunchInf
 // Launches the bf16 tcgen05 forward for d in {64, 128}.
 cudaError_t launch_fwd_bf16(const Bf16Params& p, int d, cudaStream_t stream, LaunchInfo* info);
 
+// Launches a kernel with programmatic stream serialization: its grid may be
+// scheduled while the previous kernel on the stream drains, so its set-up
+// overlaps that kernel's tail.  The kernel must call griddep_wait() before
+// its first global memory access.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_serialized(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Launches the float32 SIMT forward (1 <= d <= 256).
 cudaError_t launch_fwd_f32(const F32Params& p, cudaStream_t stream, LaunchInfo* info);
 

@@ -108,11 +108,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
   const int bh = static_cast<int>(blockIdx.x);
   const int split = static_cast<int>(blockIdx.y);
   const int b = bh / p.H, h = bh % p.H;
-  int n = __ldg(p.cache_lens + b);
-  n = n < 0 ? 0 : (n > p.Lk ? p.Lk : n);
-  const int k_begin = split * p.chunk;
-  const int k_end = min(n, k_begin + p.chunk);
-  const int n_tiles = (k_end > k_begin) ? (k_end - k_begin + kDecTile - 1) / kDecTile : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -123,6 +118,14 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
     fence_mbar_init();
   }
   __syncthreads();
+  // global memory only from here on (the set-up may overlap the previous
+  // kernel on the stream)
+  griddep_wait();
+  int n = __ldg(p.cache_lens + b);
+  n = n < 0 ? 0 : (n > p.Lk ? p.Lk : n);
+  const int k_begin = split * p.chunk;
+  const int k_end = min(n, k_begin + p.chunk);
+  const int n_tiles = (k_end > k_begin) ? (k_end - k_begin + kDecTile - 1) / kDecTile : 0;
 
   if (warp == kDecWarps) {
     // ---- TMA warp: K and V tiles of this split into the ring
@@ -292,6 +295,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
   const int lane = static_cast<int>(threadIdx.x & 31);
   const long long bh = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const long long BH = static_cast<long long>(p.B) * p.H;
+  griddep_wait();  // the split kernel's partials are complete and visible
   if (bh >= BH) return;
   float M = -INFINITY;
   for (int s = 0; s < p.n_splits; ++s) M = fmaxf(M, p.part_m[s * BH + bh]);
@@ -330,14 +334,13 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream, LaunchIn
     attr_set[dev] = true;
   }
   const dim3 grid(static_cast<unsigned>(p.B * p.H), static_cast<unsigned>(p.n_splits));
-  decode_split_kernel<D><<<grid, kDecThreads, C::SMEM, stream>>>(p);
-  e = cudaGetLastError();
+  e = launch_serialized(decode_split_kernel<D>, grid, dim3(kDecThreads), C::SMEM, stream, p);
   if (e != cudaSuccess) return e;
   int kernels = 1;
   if (p.n_splits > 1) {
     const long long bh = static_cast<long long>(p.B) * p.H;
-    decode_combine_kernel<D><<<static_cast<unsigned>((bh + 7) / 8), 256, 0, stream>>>(p);
-    e = cudaGetLastError();
+    e = launch_serialized(decode_combine_kernel<D>, dim3(static_cast<unsigned>((bh + 7) / 8)),
+                          dim3(256), 0, stream, p);
     kernels = 2;
   }
   if (info) {

@@ -152,6 +152,14 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream finishes.
+// griddep_wait blocks until the grids it depends on have completed and their
+// memory operations are visible (it returns at once when there are none), so
+// every global access must come after it.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // cluster launch control: a running CTA cancels a CTA of the same grid that
 // has not started yet and takes over its work.  The 16-byte response lands in
 // shared memory at `resp`, counted in bytes on the mbarrier.
