@@ -84,10 +84,12 @@ struct Cfg {
   static constexpr int OFF_BAR = OFF_STAGE + 2 * CHUNK;
   static constexpr int NBAR = 31 + 4 * NS;
   // tmem slot (+0), abort flag (+4), unit queue (+8, +12), CLC response (+16,
-  // 16 bytes, must be 16-byte aligned)
+  // 16 bytes, must be 16-byte aligned), then the queue's two decoded units
+  // (64 bytes each)
   static constexpr int OFF_MISC = (OFF_BAR + 8 * NBAR + 63) / 64 * 64;
   static constexpr int OFF_CLC = OFF_MISC + 16;
-  static constexpr int SMEM = OFF_MISC + 64 + 1024;    // + slack to align the base to 1024
+  static constexpr int OFF_UNITS = OFF_MISC + 64;
+  static constexpr int SMEM = OFF_UNITS + 128 + 1024;  // + slack to align the base to 1024
   // TMEM columns.  With d_k = 64 P has columns of its own (S0 | S1 | O0 | O1 |
   // P0 | P1), so S_g(j+1) can be computed while softmax g still works on tile
   // j; with d_k = 128 the 512 columns hold only S0 | S1 | O0 | O1 and P_g is
@@ -152,6 +154,12 @@ struct SharedUnit {
   __device__ __forceinline__ int head(int) const { return h; }
   __device__ __forceinline__ int qstart(int g) const { return q0 + g * kBlockM; }
   __device__ __forceinline__ int keys(int) const { return kv_len; }
+  __device__ __forceinline__ void store(volatile int* w) const {
+    w[0] = b; w[1] = h; w[2] = q0; w[3] = n[0]; w[4] = n[1]; w[5] = kv_len;
+  }
+  __device__ __forceinline__ void load(const volatile int* w) {
+    b = w[0]; h = w[1]; q0 = w[2]; n[0] = w[3]; n[1] = w[4]; kv_len = w[5];
+  }
 };
 
 // A paired unit: (two consecutive heads, 128-row query tile), Q_g from head
@@ -170,6 +178,14 @@ struct PairedUnit {
   __device__ __forceinline__ int head(int g) const { return g ? h[1] : h[0]; }
   __device__ __forceinline__ int qstart(int g) const { return g ? qs[1] : qs[0]; }
   __device__ __forceinline__ int keys(int g) const { return g ? kv_len[1] : kv_len[0]; }
+  __device__ __forceinline__ void store(volatile int* w) const {
+    w[0] = b[0]; w[1] = b[1]; w[2] = h[0]; w[3] = h[1]; w[4] = qs[0]; w[5] = qs[1];
+    w[6] = n[0]; w[7] = n[1]; w[8] = kv_len[0]; w[9] = kv_len[1]; w[10] = m;
+  }
+  __device__ __forceinline__ void load(const volatile int* w) {
+    b[0] = w[0]; b[1] = w[1]; h[0] = w[2]; h[1] = w[3]; qs[0] = w[4]; qs[1] = w[5];
+    n[0] = w[6]; n[1] = w[7]; kv_len[0] = w[8]; kv_len[1] = w[9]; m = w[10];
+  }
   __device__ __forceinline__ int slots() const { return n[0] + n[1]; }
   // ring slot (within the unit) of Q_g's key tile j
   __device__ __forceinline__ int slot_of(int g, int j) const {
@@ -273,6 +289,7 @@ struct Ctx {
   uint32_t clc_resp;           // 16-byte cancellation response
   volatile int* abort_flag;
   volatile int* unit_slot;     // [2]
+  volatile int* unit_data;     // [2][16]: the queued units, decoded
   int warp, lane;
   __device__ __forceinline__ uint32_t bar(int id) const {
     return s_bar + 8u * static_cast<uint32_t>(id);
@@ -280,26 +297,36 @@ struct Ctx {
 };
 
 // Waits for the k-th unit of this CTA from the queue; returns its index, or
-// -1 at the end of the work (or when the CTA gave up).  Every consumer calls
-// it once per unit, in the same order.
-template <int NS>
+// -1 at the end of the work (or when the CTA gave up), and copies the unit,
+// decoded by the scheduler, into u.  Every consumer calls it once per unit,
+// in the same order.
+template <int NS, typename UnitT>
 __device__ __forceinline__ int next_unit(const Bf16Params& p, const Ctx& cx, int k, int role,
-                                         bool arrive) {
+                                         bool arrive, UnitT& u) {
   using BA = Bars<NS>;
   const int slot = k & 1;
   if (!mbar_wait(cx.bar(BA::UNIT_FULL + slot), (k >> 1) & 1, cx.abort_flag, p.status,
                  role * 64 + BA::UNIT_FULL + slot))
     return -1;
   const int unit = cx.unit_slot[slot];
+  if (unit >= 0) u.load(cx.unit_data + 16 * slot);
   __syncwarp();
   if (arrive) mbar_arrive(cx.bar(BA::UNIT_EMPTY + slot));
   return unit;
 }
 
+// For a consumer that decodes the unit itself.
+struct UnitIndexOnly {
+  __device__ __forceinline__ void load(const volatile int*) {}
+};
+
 // Scheduler (warp 10, one lane): publishes the CTA's own unit, then keeps one
 // unit of look-ahead by cancelling not-yet-launched CTAs and taking their
-// units, until no CTA is left to cancel.
-template <int D>
+// units, until no CTA is left to cancel.  It also decodes each unit for the
+// other roles, off their critical paths (measured: the decode, with its
+// integer divisions, took the MMA warp about 1200 cycles at each unit
+// boundary, being issued between busy softmax warps).
+template <int D, bool PAIRED>
 __device__ __forceinline__ void scheduler_role(const Bf16Params& p, const Ctx& cx) {
   using BA = Bars<Cfg<D>::NS>;
   if (cx.lane != 0) return;
@@ -309,6 +336,7 @@ __device__ __forceinline__ void scheduler_role(const Bf16Params& p, const Ctx& c
     if (k >= 2 && !mbar_wait(cx.bar(BA::UNIT_EMPTY + slot), ((k >> 1) - 1) & 1, cx.abort_flag,
                              p.status, kRoleScheduler * 64 + BA::UNIT_EMPTY + slot))
       unit = -1;
+    if (unit >= 0) decode_unit<PAIRED>(p, unit).store(cx.unit_data + 16 * slot);
     cx.unit_slot[slot] = unit;
     mbar_arrive(cx.bar(BA::UNIT_FULL + slot));
     if (unit < 0) break;
@@ -340,9 +368,9 @@ __device__ __forceinline__ void producer_role(const Bf16Params& p, const Ctx& cx
   int v_issued = 0;       // V tile loads issued
   bool ok = true;
   for (int k = 0; ok; ++k) {
-    const int unit = next_unit<NS>(p, cx, k, kRoleProducer, cx.lane == 0);
+    typename UnitSel<false>::T u;
+    const int unit = next_unit<NS>(p, cx, k, kRoleProducer, cx.lane == 0, u);
     if (unit < 0) break;
-    const auto u = decode_unit<false>(p, unit);
     const int n_max = max(u.n[0], u.n[1]);
     auto load_q = [&](int g) {
       // the previous unit's last S_g must be done with the Q_g buffer
@@ -424,9 +452,9 @@ __device__ __forceinline__ void producer_role_paired(const Bf16Params& p, const 
   int v_issued = 0;       // V tile loads issued
   bool ok = true;
   for (int k = 0; ok; ++k) {
-    const int unit = next_unit<NS>(p, cx, k, kRoleProducer, cx.lane == 0);
+    typename UnitSel<true>::T u;
+    const int unit = next_unit<NS>(p, cx, k, kRoleProducer, cx.lane == 0, u);
     if (unit < 0) break;
-    const auto u = decode_unit<true>(p, unit);
     auto load_q = [&](int g) {
       // the previous unit's last S_g must be done with the Q_g buffer
       if (q_cnt[g] > 0 && !mbar_wait(cx.bar(BA::Q_FREE + g), (q_cnt[g] - 1) & 1, cx.abort_flag,
@@ -595,9 +623,9 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx) {
     constexpr int g_lo = GSEL;
     constexpr int g_hi = GSEL;
     for (int k = 0; ok; ++k) {
-      const int unit = next_unit<NS>(p, cx, k, kRoleMma, cx.lane == 0);
+      typename UnitSel<PAIRED>::T u;
+      const int unit = next_unit<NS>(p, cx, k, kRoleMma, cx.lane == 0, u);
       if (unit < 0) break;
-      const auto u = decode_unit<PAIRED>(p, unit);
       const int n_max = max(u.n[0], u.n[1]);
       if (n_max == 0) continue;
       // prologue: S_g(0)
@@ -635,9 +663,9 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx) {
   } else {
     constexpr int g = GSEL;
     for (int k = 0; ok; ++k) {
-      const int unit = next_unit<NS>(p, cx, k, kRoleMma, cx.lane == 0);
+      typename UnitSel<PAIRED>::T u;
+      const int unit = next_unit<NS>(p, cx, k, kRoleMma, cx.lane == 0, u);
       if (unit < 0) break;
-      const auto u = decode_unit<PAIRED>(p, unit);
       const int n_slots = u.slots();
       if (n_slots == 0) continue;
       const int n = u.n[g];
@@ -777,9 +805,9 @@ __device__ __forceinline__ void mma_role_pair(const Bf16Params& p, const Ctx& cx
     return true;
   };
   for (int k = 0; ok; ++k) {
-    const int unit = next_unit<NS>(p, cx, k, kRoleMma, cx.lane == 0);
+    typename UnitSel<false>::T u;
+    const int unit = next_unit<NS>(p, cx, k, kRoleMma, cx.lane == 0, u);
     if (unit < 0) break;
-    const auto u = decode_unit<false>(p, unit);
     const int n_max = max(u.n[0], u.n[1]);
     if (n_max == 0) continue;
     // prologue: S0(0), S1(0); then K_0 is done with
@@ -841,9 +869,19 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
   const int tok_pass = (g ? BA::TOK_A : BA::TOK_B) + quarter;
   bool ok = true;
   for (int k = 0; ok; ++k) {
-    const int unit = next_unit<C::NS>(p, cx, k, kRoleSoftmax, lane == 0);
+    // With the exponential turns the softmax decodes its unit itself
+    // (measured: reading the scheduler's copy made those kernels 1-2 %
+    // slower, while it makes the others 2-3 % faster).
+    typename UnitSel<PAIRED>::T u;
+    int unit;
+    if constexpr (TOK) {
+      UnitIndexOnly none;
+      unit = next_unit<C::NS>(p, cx, k, kRoleSoftmax, lane == 0, none);
+      if (unit >= 0) u = decode_unit<PAIRED>(p, unit);
+    } else {
+      unit = next_unit<C::NS>(p, cx, k, kRoleSoftmax, lane == 0, u);
+    }
     if (unit < 0) break;
-    const auto u = decode_unit<PAIRED>(p, unit);
     const int q_start = u.qstart(g);
     const int qi = q_start + row;
     const int n_tiles = PAIRED ? (g ? u.n[1] : u.n[0]) : u.n[g];
@@ -1058,6 +1096,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   cx.abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   cx.unit_slot = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+  cx.unit_data = reinterpret_cast<volatile int*>(smem + C::OFF_UNITS);
   cx.clc_resp = s_base + C::OFF_CLC;
 
   // ---- setup ---------------------------------------------------------------
@@ -1132,7 +1171,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
         producer_role<D>(p, cx);
       }
     } else {
-      scheduler_role<D>(p, cx);
+      scheduler_role<D, PAIRED>(p, cx);
     }
   }
 
