@@ -75,6 +75,20 @@ __device__ __forceinline__ constexpr uint32_t a_col(int ks) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// CTA order: groups of kBwdHeadGroup heads, so the tiles a group's CTAs all
+// stream (Q and dO, or K and V) stay in L2 while the group runs; inside a group
+// the tile index t runs over all of the group's heads before moving on, which
+// puts the heavy causal tiles of every head first and leaves the grid a light
+// tail.  Returns t (0 = the first launched) and sets *bh.
+constexpr int kBwdHeadGroup = 32;
+__device__ __forceinline__ int bwd_unit(int unit, int n_t, int bh_count, int* bh) {
+  const int group = unit / (kBwdHeadGroup * n_t);
+  const int within = unit - group * kBwdHeadGroup * n_t;
+  const int here = min(kBwdHeadGroup, bh_count - group * kBwdHeadGroup);
+  *bh = group * kBwdHeadGroup + within % here;
+  return within / here;
+}
+
 // Visible keys of sequence b (key padding), all keys otherwise.
 __device__ __forceinline__ int kv_len_of(const BwdParams& p, int b) {
   int n = p.Lk;
@@ -103,16 +117,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
 
   const int n_kt = (p.Lk + 127) / 128;
-  const int unit = static_cast<int>(blockIdx.x);
-  const int kt = unit % n_kt;
-  const int bh = unit / n_kt;
+  int bh = 0;
+  // first key tile first: under the causal mask it sees the most query tiles
+  const int kt = bwd_unit(static_cast<int>(blockIdx.x), n_kt, p.B * p.H, &bh);
   const int b = bh / p.H, h = bh % p.H;
   const int k0 = kt * 128;
-  const int kv_len = kv_len_of(p, b);
   const int n_qt = (p.Lq + 127) / 128;
   // query tiles that see a key of this tile (causal: from the diagonal on)
   const int qt_begin = masks_causal(p.mask_kind) ? kt : 0;
-  const int n_iter = (k0 < kv_len) ? (n_qt - qt_begin) : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kFixFull), 1);
@@ -137,6 +149,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // global memory only from here on (the set-up may overlap the previous
+  // kernel on the stream, which for this kernel writes D)
+  griddep_wait();
+  const int kv_len = kv_len_of(p, b);
+  const int n_iter = (k0 < kv_len) ? (n_qt - qt_begin) : 0;
 
   if (warp == kTmaWarp) {
     // ---- TMA: K and V of this key tile once, then Q_i, dO_i per query tile
@@ -433,17 +450,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
 
   const int n_qt = (p.Lq + 127) / 128;
-  const int unit = static_cast<int>(blockIdx.x);
-  // last query tile first: under the causal mask it sees the most key tiles,
-  // so the heavy CTAs start early and the grid's tail is light
-  const int qt = n_qt - 1 - unit % n_qt;
-  const int bh = unit / n_qt;
+  int bh = 0;
+  // last query tile first: under the causal mask it sees the most key tiles
+  const int qt = n_qt - 1 - bwd_unit(static_cast<int>(blockIdx.x), n_qt, p.B * p.H, &bh);
   const int b = bh / p.H, h = bh % p.H;
   const int q0 = qt * 128;
-  const int kv_len = kv_len_of(p, b);
-  int n_kt = (kv_len + 127) / 128;
-  if (masks_causal(p.mask_kind) && n_kt > qt + 1) n_kt = qt + 1;
-  const int n_iter = n_kt;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kFixFull), 1);
@@ -468,6 +479,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // global memory only from here on (the set-up may overlap the previous
+  // kernel on the stream)
+  griddep_wait();
+  const int kv_len = kv_len_of(p, b);
+  int n_kt = (kv_len + 127) / 128;
+  if (masks_causal(p.mask_kind) && n_kt > qt + 1) n_kt = qt + 1;
+  const int n_iter = n_kt;
 
   if (warp == kTmaWarp) {
     // ---- TMA: Q_i and dO_i once, then K_j, V_j per key tile
@@ -725,11 +743,11 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, LaunchInfo* in
   const long long q_units = bh * ((p.Lq + 127) / 128);
   // the dQ kernel forms D = dO . O for its rows and stores it; the dK/dV
   // kernel, next on the stream, reads it
-  bwd_dq_kernel<D><<<static_cast<unsigned>(q_units), kBwdThreads, C::SMEM, stream>>>(p);
-  e = cudaGetLastError();
+  e = launch_serialized(bwd_dq_kernel<D>, dim3(static_cast<unsigned>(q_units)), dim3(kBwdThreads),
+                        C::SMEM, stream, p);
   if (e != cudaSuccess) return e;
-  bwd_dkdv_kernel<D><<<static_cast<unsigned>(kv_units), kBwdThreads, C::SMEM, stream>>>(p);
-  e = cudaGetLastError();
+  e = launch_serialized(bwd_dkdv_kernel<D>, dim3(static_cast<unsigned>(kv_units)),
+                        dim3(kBwdThreads), C::SMEM, stream, p);
   if (info) {
     info->kernels = 2;
     info->grid = static_cast<int>(kv_units + q_units);
