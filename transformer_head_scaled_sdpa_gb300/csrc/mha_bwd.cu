@@ -34,9 +34,12 @@ namespace mha {
 namespace {
 
 constexpr int kBwdThreads = 320;  // warps 0-7 gradient, 8 MMA, 9 TMA
+constexpr int kDkdvThreads = 352; // the dK/dV kernel adds warp 10, its scheduler
 constexpr int kGradThreads = 256;
-constexpr int kMmaWarp = 8, kTmaWarp = 9;
-constexpr int kRoleBwdProducer = 8, kRoleBwdMma = 9, kRoleBwdGrad = 10;
+constexpr int kMmaWarp = 8, kTmaWarp = 9, kSchedWarp = 10;
+// unit-queue readers of the dK/dV kernel: 8 gradient warps, the MMA warp, the TMA lane
+constexpr int kDkdvUnitConsumers = 10;
+constexpr int kRoleBwdProducer = 8, kRoleBwdMma = 9, kRoleBwdGrad = 10, kRoleBwdSched = 11;
 
 template <int D>
 struct BwdCfg {
@@ -49,9 +52,11 @@ struct BwdCfg {
   static constexpr int OFF_RING = 2 * TILE;    // stage s: pair at OFF_RING + s * 2 * TILE
   static constexpr int OFF_VEC = OFF_RING + 4 * TILE;  // dK/dV: lse2[128], D[128]; dQ: D halves [2][128]
   static constexpr int OFF_BAR = OFF_VEC + 2 * 128 * 4;
-  static constexpr int NBAR = 11;
-  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;  // tmem slot, abort flag
-  static constexpr int SMEM = OFF_MISC + 16 + 1024;
+  static constexpr int NBAR = 18;
+  // tmem slot (+0), abort flag (+4), unit queue (+8, +12), cancellation
+  // response (+16, 16 bytes, 16-byte aligned)
+  static constexpr int OFF_MISC = (OFF_BAR + 8 * NBAR + 15) / 16 * 16;
+  static constexpr int SMEM = OFF_MISC + 32 + 1024;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   // TMEM: a tile's score-shaped matrices in two halves of 64 columns, half
   // hf at columns 128 hf (S or S^T) and 128 hf + 64 (dP or dP^T); then the
@@ -63,7 +68,10 @@ struct BwdCfg {
 // barrier ids.  kScores + hf: the score products of half hf are in TMEM;
 // kGrads + hf: the gradient warps have written P and dS of half hf.
 enum { kFixFull = 0, kRingFull = 1, kRingEmpty = 3, kScores = 5, kGrads = 7, kAccDone = 9,
-       kDrain = 10 };
+       kDrain = 10,
+       // the persistent dK/dV kernel: the unit's last score products are done
+       // with K and V; the epilogue has read the accumulators; the unit queue
+       kFixFree = 11, kAccFree = 12, kUnitFull = 13, kUnitEmpty = 15, kClc = 17 };
 
 // TMEM column of the 16 rows of K16 step ks (0..3) of a half, packed as bf16
 // pairs: chunk ks / 2 (32 rows) keeps them in the first 16 of its 32 columns
@@ -100,10 +108,17 @@ __device__ __forceinline__ int kv_len_of(const BwdParams& p, int b) {
 }
 
 // ---------------------------------------------------------------------------
-// dK, dV: one CTA per (b, h, key tile)
+// dK, dV: units (b, h, key tile), persistent CTAs
 // ---------------------------------------------------------------------------
+// The grid has one CTA per unit, but a running CTA cancels CTAs that have not
+// started (cluster launch control) and takes their units, as the forward
+// does: the TMA warp loads the next unit's K and V as soon as the current
+// unit's last score products are done with them, and the next unit's first
+// score products are issued while the gradient warps still write the current
+// unit's dK and dV, so the per-CTA set-up, the K/V load latency and the
+// pipeline fill leave the critical path.
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kDkdvThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -112,25 +127,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
   auto bar = [&](int id) { return s_base + C::OFF_BAR + 8u * id; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* unit_slot = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+  const uint32_t clc_resp = s_base + C::OFF_MISC + 16;
   float* lse2_s = reinterpret_cast<float*>(smem + C::OFF_VEC);
   float* dvec_s = lse2_s + 128;
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
 
   const int n_kt = (p.Lk + 127) / 128;
-  int bh = 0;
-  // first key tile first: under the causal mask it sees the most query tiles
-  const int kt = bwd_unit(static_cast<int>(blockIdx.x), n_kt, p.B * p.H, &bh);
-  const int b = bh / p.H, h = bh % p.H;
-  const int k0 = kt * 128;
   const int n_qt = (p.Lq + 127) / 128;
-  // query tiles that see a key of this tile (causal: from the diagonal on)
-  const int qt_begin = masks_causal(p.mask_kind) ? kt : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kFixFull), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kRingFull + s), 1);
       mbar_init(bar(kRingEmpty + s), 1);
+      mbar_init(bar(kUnitFull + s), 1);
+      mbar_init(bar(kUnitEmpty + s), kDkdvUnitConsumers);
     }
     for (int hf = 0; hf < 2; ++hf) {
       mbar_init(bar(kScores + hf), 1);
@@ -138,6 +150,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     }
     mbar_init(bar(kAccDone), 1);
     mbar_init(bar(kDrain), 1);
+    mbar_init(bar(kFixFree), 1);
+    mbar_init(bar(kAccFree), kGradThreads);
+    mbar_init(bar(kClc), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -152,35 +167,105 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
   // global memory only from here on (the set-up may overlap the previous
   // kernel on the stream, which for this kernel writes D)
   griddep_wait();
-  const int kv_len = kv_len_of(p, b);
-  const int n_iter = (k0 < kv_len) ? (n_qt - qt_begin) : 0;
 
-  if (warp == kTmaWarp) {
-    // ---- TMA: K and V of this key tile once, then Q_i, dO_i per query tile
-    if (lane == 0 && n_iter > 0) {
-      mbar_arrive_expect_tx(bar(kFixFull), 2 * C::TILE);
-      for (int c = 0; c < C::KCH; ++c) {
-        tma_load_4d(s_base + C::OFF_A0 + c * C::CHUNK, &p.tm_k, bar(kFixFull), 64 * c, h, k0, b);
-        tma_load_4d(s_base + C::OFF_A1 + c * C::CHUNK, &p.tm_v, bar(kFixFull), 64 * c, h, k0, b);
+  // a unit's geometry: first key tile first (under the causal mask it sees
+  // the most query tiles)
+  struct KvUnit {
+    int b, h, k0, qt_begin, n_iter, kv_len;
+  };
+  auto decode = [&](int unit) {
+    KvUnit u;
+    int bh = 0;
+    const int kt = bwd_unit(unit, n_kt, p.B * p.H, &bh);
+    u.b = bh / p.H;
+    u.h = bh % p.H;
+    u.k0 = kt * 128;
+    u.kv_len = kv_len_of(p, u.b);
+    // query tiles that see a key of this tile (causal: from the diagonal on)
+    u.qt_begin = masks_causal(p.mask_kind) ? kt : 0;
+    u.n_iter = (u.k0 < u.kv_len) ? (n_qt - u.qt_begin) : 0;
+    return u;
+  };
+  // the k-th unit of this CTA from the queue (-1: no more, or gave up)
+  auto take = [&](int k, int role) {
+    const int slot = k & 1;
+    if (!mbar_wait(bar(kUnitFull + slot), (k >> 1) & 1, abort_flag, p.status,
+                   role * 64 + kUnitFull + slot))
+      return -1;
+    return static_cast<int>(unit_slot[slot]);
+  };
+  auto release = [&](int k) { mbar_arrive(bar(kUnitEmpty + (k & 1))); };
+
+  if (warp == kSchedWarp) {
+    // ---- scheduler (one lane): publishes the CTA's own unit, then keeps one
+    // unit of look-ahead by cancelling CTAs that have not started
+    if (lane == 0) {
+      int unit = static_cast<int>(blockIdx.x);
+      for (int k = 0;; ++k) {
+        const int slot = k & 1;
+        if (k >= 2 && !mbar_wait(bar(kUnitEmpty + slot), ((k >> 1) - 1) & 1, abort_flag, p.status,
+                                 kRoleBwdSched * 64 + kUnitEmpty + slot))
+          unit = -1;
+        unit_slot[slot] = unit;
+        mbar_arrive(bar(kUnitFull + slot));
+        if (unit < 0) break;
+        mbar_arrive_expect_tx(bar(kClc), 16);
+        clc_try_cancel(clc_resp, bar(kClc));
+        // the response is written asynchronously: wait for it even when the
+        // CTA is giving up, so nothing lands in shared memory after exit
+        volatile int never = 0;
+        if (!mbar_wait(bar(kClc), k & 1, &never, p.status, kRoleBwdSched * 64 + kClc) ||
+            *abort_flag)
+          unit = -1;
+        else
+          unit = clc_query_first_ctaid_x(clc_resp);
       }
-      int it = 0;
-      for (; it < n_iter; ++it) {
-        const int s = it & 1;
-        if (it >= 2 && !mbar_wait(bar(kRingEmpty + s), ((it >> 1) - 1) & 1, abort_flag, p.status,
-                                  kRoleBwdProducer * 64 + s))
+    }
+    __syncwarp();
+  } else if (warp == kTmaWarp) {
+    // ---- TMA (one lane): per unit K and V (once the previous unit's last
+    // score products are done with them), then Q_i, dO_i per query tile
+    if (lane == 0) {
+      int ring_t = 0;  // query tiles issued so far, over all units
+      int fix_n = 0;   // units whose K and V were loaded
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int unit = take(k, kRoleBwdProducer);
+        if (unit >= 0) release(k);
+        if (unit < 0) break;
+        const KvUnit u = decode(unit);
+        if (u.n_iter == 0) continue;
+        if (fix_n > 0 && !mbar_wait(bar(kFixFree), (fix_n - 1) & 1, abort_flag, p.status,
+                                    kRoleBwdProducer * 64 + kFixFree))
           break;
-        const int q0 = (qt_begin + it) * 128;
-        const uint32_t dst = s_base + C::OFF_RING + s * 2 * C::TILE;
-        mbar_arrive_expect_tx(bar(kRingFull + s), 2 * C::TILE);
+        mbar_arrive_expect_tx(bar(kFixFull), 2 * C::TILE);
         for (int c = 0; c < C::KCH; ++c) {
-          tma_load_4d(dst + c * C::CHUNK, &p.tm_q, bar(kRingFull + s), 64 * c, h, q0, b);
-          tma_load_4d(dst + C::TILE + c * C::CHUNK, &p.tm_do, bar(kRingFull + s), 64 * c, h, q0, b);
+          tma_load_4d(s_base + C::OFF_A0 + c * C::CHUNK, &p.tm_k, bar(kFixFull), 64 * c, u.h, u.k0, u.b);
+          tma_load_4d(s_base + C::OFF_A1 + c * C::CHUNK, &p.tm_v, bar(kFixFull), 64 * c, u.h, u.k0, u.b);
+        }
+        ++fix_n;
+        for (int it = 0; it < u.n_iter; ++it, ++ring_t) {
+          const int s = ring_t & 1;
+          if (ring_t >= 2 && !mbar_wait(bar(kRingEmpty + s), ((ring_t >> 1) - 1) & 1, abort_flag,
+                                        p.status, kRoleBwdProducer * 64 + s)) {
+            ok = false;
+            break;
+          }
+          const int q0 = (u.qt_begin + it) * 128;
+          const uint32_t dst = s_base + C::OFF_RING + s * 2 * C::TILE;
+          mbar_arrive_expect_tx(bar(kRingFull + s), 2 * C::TILE);
+          for (int c = 0; c < C::KCH; ++c) {
+            tma_load_4d(dst + c * C::CHUNK, &p.tm_q, bar(kRingFull + s), 64 * c, u.h, q0, u.b);
+            tma_load_4d(dst + C::TILE + c * C::CHUNK, &p.tm_do, bar(kRingFull + s), 64 * c, u.h, q0,
+                        u.b);
+          }
         }
       }
       // every copy started lands before the CTA exits
       volatile int never = 0;
-      mbar_wait(bar(kFixFull), 0, &never, p.status, kRoleBwdProducer * 64 + 8);
-      for (int t = (it > 2 ? it - 2 : 0); t < it; ++t)
+      if (fix_n > 0)
+        mbar_wait(bar(kFixFull), (fix_n - 1) & 1, &never, p.status, kRoleBwdProducer * 64 + 8);
+      for (int t = (ring_t > 2 ? ring_t - 2 : 0); t < ring_t; ++t)
         mbar_wait(bar(kRingFull + (t & 1)), (t >> 1) & 1, &never, p.status,
                   kRoleBwdProducer * 64 + 9);
     }
@@ -189,7 +274,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     // ---- MMA issuer.  A query tile is taken in two halves of 64 queries with
     // score regions of their own, so the tensor cores work on one half while
     // the gradient warps work on the other: per half, dV/dK of this tile, then
-    // S^T/dP^T of the next tile into the region just consumed.
+    // S^T/dP^T of the next tile into the region just consumed.  Across units
+    // the next unit's first score products follow the current unit's last
+    // accumulating products the same way; only its first accumulating product
+    // waits for the epilogue to have read dK and dV.
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);   // K-major A and B
     constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);     // B MN-major
     const uint64_t dA0 = smem_desc_sw128(s_base + C::OFF_A0, 16, 1024);   // K tile, K-major
@@ -219,7 +307,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     // dV += P^T dO, dK += dS^T Q over half hf.  The 16 queries of step ks are
     // 8 packed TMEM columns: chunk ks / 2 of the half keeps its 32 queries in
     // the first 16 columns of its own 32.
-    auto issue_grads = [&](int t, int hf) {
+    auto issue_grads = [&](int t, int hf, bool first) {
       const uint32_t rows = half_rows(t, hf);
       const uint64_t dQm = smem_desc_sw128(rows, C::CHUNK, 1024);
       const uint64_t dDm = smem_desc_sw128(rows + C::TILE, C::CHUNK, 1024);
@@ -227,52 +315,78 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         umma_ts(tmem + C::TM_ACC0, ts + a_col(ks), dDm + static_cast<uint64_t>((ks * 2048) >> 4),
-                idesc_o, (ks > 0 || t > 0 || hf > 0) ? 1u : 0u);
+                idesc_o, (ks > 0 || !first) ? 1u : 0u);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         umma_ts(tmem + C::TM_ACC1, ts + C::TM_DP + a_col(ks), dQm + static_cast<uint64_t>((ks * 2048) >> 4),
-                idesc_o, (ks > 0 || t > 0 || hf > 0) ? 1u : 0u);
+                idesc_o, (ks > 0 || !first) ? 1u : 0u);
     };
     bool ok = true;
-    if (n_iter > 0) {
-      ok = mbar_wait(bar(kFixFull), 0, abort_flag, p.status, kRoleBwdMma * 64 + kFixFull) &&
-           mbar_wait(bar(kRingFull), 0, abort_flag, p.status, kRoleBwdMma * 64 + kRingFull);
-      if (ok) {
-        tc_fence_after();
-        if (elect_one()) {
-          issue_scores(0, 0);
-          issue_scores(0, 1);
-        }
-        __syncwarp();
+    int ring_t = 0;  // query tiles of the units before the current one
+    int fix_n = 0;   // units with work so far
+    for (int k = 0; ok; ++k) {
+      const int unit = take(k, kRoleBwdMma);
+      __syncwarp();
+      if (unit >= 0 && lane == 0) release(k);
+      if (unit < 0) break;
+      const KvUnit u = decode(unit);
+      if (u.n_iter == 0) continue;
+      ok = mbar_wait(bar(kFixFull), fix_n & 1, abort_flag, p.status, kRoleBwdMma * 64 + kFixFull) &&
+           mbar_wait(bar(kRingFull + (ring_t & 1)), (ring_t >> 1) & 1, abort_flag, p.status,
+                     kRoleBwdMma * 64 + kRingFull);
+      if (!ok) break;
+      tc_fence_after();
+      if (elect_one()) {
+        issue_scores(ring_t, 0);
+        issue_scores(ring_t, 1);
+        // a one-tile unit's score products are its last use of K and V
+        if (u.n_iter == 1) umma_commit(bar(kFixFree));
       }
-    }
-    for (int it = 0; ok && it < n_iter; ++it) {
-      const bool more = it + 1 < n_iter;
-      for (int hf = 0; hf < 2; ++hf) {
-        if (!mbar_wait(bar(kGrads + hf), it & 1, abort_flag, p.status, kRoleBwdMma * 64 + kGrads + hf)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (elect_one()) {
-          issue_grads(it, hf);
-          if (hf == 1) {
-            umma_commit(bar(kRingEmpty + (it & 1)));
-            if (!more) umma_commit(bar(kAccDone));
+      __syncwarp();
+      for (int it = 0; ok && it < u.n_iter; ++it) {
+        const int t = ring_t + it;
+        const bool more = it + 1 < u.n_iter;
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!mbar_wait(bar(kGrads + hf), t & 1, abort_flag, p.status,
+                         kRoleBwdMma * 64 + kGrads + hf)) {
+            ok = false;
+            break;
           }
+          // the unit's first accumulating product overwrites dK and dV: the
+          // previous unit's epilogue must have read them
+          if (it == 0 && hf == 0 && fix_n > 0 &&
+              !mbar_wait(bar(kAccFree), (fix_n - 1) & 1, abort_flag, p.status,
+                         kRoleBwdMma * 64 + kAccFree)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            issue_grads(t, hf, it == 0 && hf == 0);
+            if (hf == 1) {
+              umma_commit(bar(kRingEmpty + (t & 1)));
+              if (!more) umma_commit(bar(kAccDone));
+            }
+          }
+          __syncwarp();
+          if (!more) continue;
+          const int sn = (t + 1) & 1;
+          if (hf == 0 && !mbar_wait(bar(kRingFull + sn), ((t + 1) >> 1) & 1, abort_flag, p.status,
+                                    kRoleBwdMma * 64 + kRingFull + sn)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            issue_scores(t + 1, hf);
+            // the last tile's score products are the unit's last use of K, V
+            if (hf == 1 && it + 2 == u.n_iter) umma_commit(bar(kFixFree));
+          }
+          __syncwarp();
         }
-        __syncwarp();
-        if (!more) continue;
-        const int sn = (it + 1) & 1;
-        if (hf == 0 && !mbar_wait(bar(kRingFull + sn), ((it + 1) >> 1) & 1, abort_flag, p.status,
-                                  kRoleBwdMma * 64 + kRingFull + sn)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (elect_one()) issue_scores(it + 1, hf);
-        __syncwarp();
       }
+      ring_t += u.n_iter;
+      ++fix_n;
     }
     if (elect_one()) umma_commit(bar(kDrain));
     __syncwarp();
@@ -283,7 +397,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     // lane quarter) and, of each half tile, the 32 queries of chunk w / 4
     const int quarter = warp & 3, cq = warp >> 2;
     const int r = quarter * 32 + lane;
-    const int key = k0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c2 = p.scale_log2;
     // one entry of a query tile's lse (threads 0-127) or D (128-255), loaded
@@ -292,116 +405,142 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     const bool v_lse = threadIdx.x < 128;
     const float* v_src = v_lse ? p.lse : p.dvec;
     float* v_dst = (v_lse ? lse2_s : dvec_s) + vi;
-    float vn = 0.f;
-    auto fetch = [&](int t) {
-      const int qi = (qt_begin + t) * 128 + vi;
-      vn = qi < p.Lq ? v_src[(static_cast<size_t>(b) * p.H + h) * p.Lq + qi] : -INFINITY;
-    };
-    if (n_iter > 0) fetch(0);
     bool ok = true;
-    for (int it = 0; ok && it < n_iter; ++it) {
-      const int q0 = (qt_begin + it) * 128;
-      // the tile's lse (log2 units) and D into shared memory once the previous
-      // tile's readers are past the barrier.  (A named barrier cannot time out:
-      // after each one the abort flag is checked, and a warp that gives up
-      // arrives once on it on its way out.)
-      named_barrier(1, kGradThreads);
-      if (*abort_flag) {
-        ok = false;
+    int ring_t = 0;  // query tiles of the units before the current one
+    int unit_n = 0;  // units with work so far
+    for (int k = 0; ok; ++k) {
+      const int unit = take(k, kRoleBwdGrad);
+      __syncwarp();
+      if (unit >= 0 && lane == 0) release(k);
+      if (unit < 0) {
+        ok = unit == -1 && !*abort_flag;
         break;
       }
-      // stored negated, for packed fma / add below: -lse (log2 units), -D
-      *v_dst = v_lse ? -(vn * 1.4426950408889634f) : (vn == -INFINITY ? 0.f : -vn);
-      named_barrier(1, kGradThreads);
-      if (*abort_flag) {
-        ok = false;
-        break;
-      }
-      if (it + 1 < n_iter) fetch(it + 1);
-      // Every (key, query) pair of the tile is visible unless the tile holds
-      // keys past the key length, queries past Lq, or the causal diagonal.
-      const bool all_visible = k0 + 127 < kv_len && q0 + 127 < p.Lq &&
-                               !(masks_causal(p.mask_kind) && q0 < k0 + 127);
-      for (int hf = 0; hf < 2; ++hf) {
-        if (!mbar_wait(bar(kScores + hf), it & 1, abort_flag, p.status, kRoleBwdGrad * 64 + kScores + hf)) {
+      const KvUnit u = decode(unit);
+      const int b = u.b, h = u.h, k0 = u.k0, qt_begin = u.qt_begin, n_iter = u.n_iter;
+      const int kv_len = u.kv_len;
+      const int key = k0 + r;
+      float vn = 0.f;
+      auto fetch = [&](int t) {
+        const int qi = (qt_begin + t) * 128 + vi;
+        vn = qi < p.Lq ? v_src[(static_cast<size_t>(b) * p.H + h) * p.Lq + qi] : -INFINITY;
+      };
+      if (n_iter > 0) fetch(0);
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const int t_all = ring_t + it;  // barrier phases run over all units
+        const int q0 = (qt_begin + it) * 128;
+        // the tile's lse (log2 units) and D into shared memory once the previous
+        // tile's readers are past the barrier.  (A named barrier cannot time out:
+        // after each one the abort flag is checked, and a warp that gives up
+        // arrives once on it on its way out.)
+        named_barrier(1, kGradThreads);
+        if (*abort_flag) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t ts = tmem + C::TM_HALF * hf + lane_off + 32u * cq;
-        const int col0 = 64 * hf + 32 * cq;  // first query column of the chunk
-        uint32_t sr[32], pr[32];
-        tmem_ld32(ts, sr);
-        tmem_ld32(ts + C::TM_DP, pr);
-        float l2c[32], dvc[32];  // negated: -lse (log2 units), -D
-#pragma unroll
-        for (int v4 = 0; v4 < 8; ++v4) {
-          const float4 lv = reinterpret_cast<const float4*>(lse2_s + col0)[v4];
-          const float4 dv = reinterpret_cast<const float4*>(dvec_s + col0)[v4];
-          l2c[4 * v4] = lv.x, l2c[4 * v4 + 1] = lv.y, l2c[4 * v4 + 2] = lv.z, l2c[4 * v4 + 3] = lv.w;
-          dvc[4 * v4] = dv.x, dvc[4 * v4 + 1] = dv.y, dvc[4 * v4 + 2] = dv.z, dvc[4 * v4 + 3] = dv.w;
+        // stored negated, for packed fma / add below: -lse (log2 units), -D
+        *v_dst = v_lse ? -(vn * 1.4426950408889634f) : (vn == -INFINITY ? 0.f : -vn);
+        named_barrier(1, kGradThreads);
+        if (*abort_flag) {
+          ok = false;
+          break;
         }
-        tmem_ld_wait();
-        float pf[32];
-        // (the mask test stays outside the element loops, which then have no
-        // branches and interleave their 32 independent chains; packed f32x2
-        // arithmetic halves the issue slots of the float math)
-        if (all_visible) {
+        if (it + 1 < n_iter) fetch(it + 1);
+        // Every (key, query) pair of the tile is visible unless the tile holds
+        // keys past the key length, queries past Lq, or the causal diagonal.
+        const bool all_visible = k0 + 127 < kv_len && q0 + 127 < p.Lq &&
+                                 !(masks_causal(p.mask_kind) && q0 < k0 + 127);
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!mbar_wait(bar(kScores + hf), t_all & 1, abort_flag, p.status,
+                         kRoleBwdGrad * 64 + kScores + hf)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ts = tmem + C::TM_HALF * hf + lane_off + 32u * cq;
+          const int col0 = 64 * hf + 32 * cq;  // first query column of the chunk
+          uint32_t sr[32], pr[32];
+          tmem_ld32(ts, sr);
+          tmem_ld32(ts + C::TM_DP, pr);
+          float l2c[32], dvc[32];  // negated: -lse (log2 units), -D
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4) {
+            const float4 lv = reinterpret_cast<const float4*>(lse2_s + col0)[v4];
+            const float4 dv = reinterpret_cast<const float4*>(dvec_s + col0)[v4];
+            l2c[4 * v4] = lv.x, l2c[4 * v4 + 1] = lv.y, l2c[4 * v4 + 2] = lv.z, l2c[4 * v4 + 3] = lv.w;
+            dvc[4 * v4] = dv.x, dvc[4 * v4 + 1] = dv.y, dvc[4 * v4 + 2] = dv.z, dvc[4 * v4 + 3] = dv.w;
+          }
+          tmem_ld_wait();
+          float pf[32];
+          // (the mask test stays outside the element loops, which then have no
+          // branches and interleave their 32 independent chains; packed f32x2
+          // arithmetic halves the issue slots of the float math)
+          if (all_visible) {
+#pragma unroll
+            for (int t = 0; t < 32; t += 2) {
+              fma2(pf[t], pf[t + 1], __uint_as_float(sr[t]), __uint_as_float(sr[t + 1]), c2, c2,
+                   l2c[t], l2c[t + 1]);
+              pf[t] = ex2_approx(pf[t]);
+              pf[t + 1] = ex2_approx(pf[t + 1]);
+            }
+          } else {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+              const int qi = q0 + col0 + t;
+              const bool vis = key < kv_len && qi < p.Lq &&
+                               !(masks_causal(p.mask_kind) && key > qi) && l2c[t] != INFINITY;
+              const float e = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, l2c[t]));
+              pf[t] = vis ? e : 0.f;
+            }
+          }
+          // P^T in bf16 for the dV product; dS = P (dP - D) from the float32 P
+          uint32_t pk[16], dk[16];
 #pragma unroll
           for (int t = 0; t < 32; t += 2) {
-            fma2(pf[t], pf[t + 1], __uint_as_float(sr[t]), __uint_as_float(sr[t + 1]), c2, c2,
-                 l2c[t], l2c[t + 1]);
-            pf[t] = ex2_approx(pf[t]);
-            pf[t + 1] = ex2_approx(pf[t + 1]);
+            pk[t >> 1] = pack_bf16x2(pf[t], pf[t + 1]);
+            float g0, g1;
+            add2(g0, g1, __uint_as_float(pr[t]), __uint_as_float(pr[t + 1]), dvc[t], dvc[t + 1]);
+            mul2(g0, g1, pf[t], pf[t + 1], g0, g1);
+            dk[t >> 1] = pack_bf16x2(g0, g1);
           }
-        } else {
-#pragma unroll
-          for (int t = 0; t < 32; ++t) {
-            const int qi = q0 + col0 + t;
-            const bool vis = key < kv_len && qi < p.Lq &&
-                             !(masks_causal(p.mask_kind) && key > qi) && l2c[t] != INFINITY;
-            const float e = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, l2c[t]));
-            pf[t] = vis ? e : 0.f;
-          }
+          // P^T over the first 16 of the chunk's S^T columns, dS^T over the first
+          // 16 of its dP^T columns (this thread has read them; no other has)
+          tmem_st16(ts, pk);
+          tmem_st16(ts + C::TM_DP, dk);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(kGrads + hf));
         }
-        // P^T in bf16 for the dV product; dS = P (dP - D) from the float32 P
-        uint32_t pk[16], dk[16];
-#pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          pk[t >> 1] = pack_bf16x2(pf[t], pf[t + 1]);
-          float g0, g1;
-          add2(g0, g1, __uint_as_float(pr[t]), __uint_as_float(pr[t + 1]), dvc[t], dvc[t + 1]);
-          mul2(g0, g1, pf[t], pf[t + 1], g0, g1);
-          dk[t >> 1] = pack_bf16x2(g0, g1);
-        }
-        // P^T over the first 16 of the chunk's S^T columns, dS^T over the first
-        // 16 of its dP^T columns (this thread has read them; no other has)
-        tmem_st16(ts, pk);
-        tmem_st16(ts + C::TM_DP, dk);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(kGrads + hf));
       }
-    }
-    // ---- epilogue: dV and scale * dK rows to global (rows past Lk skipped);
-    // warp w takes the 32-column chunks c with c % 2 == w / 4
-    if (ok && n_iter > 0)
-      ok = mbar_wait(bar(kAccDone), 0, abort_flag, p.status, kRoleBwdGrad * 64 + kAccDone);
-    if (ok) {
-      tc_fence_after();
+      if (!ok) break;
+      // ---- epilogue: dV and scale * dK rows to global (rows past Lk skipped);
+      // warp w takes the 32-column chunks c with c % 2 == w / 4.  The
+      // accumulators are read first, then released to the next unit.
+      if (n_iter > 0) {
+        ok = mbar_wait(bar(kAccDone), unit_n & 1, abort_flag, p.status,
+                       kRoleBwdGrad * 64 + kAccDone);
+        if (!ok) break;
+        tc_fence_after();
+      }
       const size_t row_off = ((static_cast<size_t>(b) * p.Lk + key) * p.H + h) * p.d;
       __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(p.dv) + row_off;
       __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(p.dk) + row_off;
 #pragma unroll 1
       for (int c32 = cq; c32 < D / 32; c32 += 2) {
-        uint32_t a[32], k[32];
+        uint32_t a[32], kk[32];
         if (n_iter > 0) {
           tmem_ld32(tmem + C::TM_ACC0 + lane_off + 32u * c32, a);
-          tmem_ld32(tmem + C::TM_ACC1 + lane_off + 32u * c32, k);
+          tmem_ld32(tmem + C::TM_ACC1 + lane_off + 32u * c32, kk);
           tmem_ld_wait();
+          if (c32 + 2 >= D / 32) {
+            // this thread's last accumulator columns are read: the next unit
+            // may overwrite them
+            tc_fence_before();
+            mbar_arrive(bar(kAccFree));
+          }
         } else {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) a[t] = k[t] = 0u;
+          for (int t = 0; t < 32; ++t) a[t] = kk[t] = 0u;
         }
         if (key < p.Lk) {
 #pragma unroll
@@ -412,18 +551,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             wa.y = pack_bf16x2(__uint_as_float(a[8 * v4 + 2]), __uint_as_float(a[8 * v4 + 3]));
             wa.z = pack_bf16x2(__uint_as_float(a[8 * v4 + 4]), __uint_as_float(a[8 * v4 + 5]));
             wa.w = pack_bf16x2(__uint_as_float(a[8 * v4 + 6]), __uint_as_float(a[8 * v4 + 7]));
-            wk.x = pack_bf16x2(__uint_as_float(k[8 * v4 + 0]) * p.scale, __uint_as_float(k[8 * v4 + 1]) * p.scale);
-            wk.y = pack_bf16x2(__uint_as_float(k[8 * v4 + 2]) * p.scale, __uint_as_float(k[8 * v4 + 3]) * p.scale);
-            wk.z = pack_bf16x2(__uint_as_float(k[8 * v4 + 4]) * p.scale, __uint_as_float(k[8 * v4 + 5]) * p.scale);
-            wk.w = pack_bf16x2(__uint_as_float(k[8 * v4 + 6]) * p.scale, __uint_as_float(k[8 * v4 + 7]) * p.scale);
+            wk.x = pack_bf16x2(__uint_as_float(kk[8 * v4 + 0]) * p.scale, __uint_as_float(kk[8 * v4 + 1]) * p.scale);
+            wk.y = pack_bf16x2(__uint_as_float(kk[8 * v4 + 2]) * p.scale, __uint_as_float(kk[8 * v4 + 3]) * p.scale);
+            wk.z = pack_bf16x2(__uint_as_float(kk[8 * v4 + 4]) * p.scale, __uint_as_float(kk[8 * v4 + 5]) * p.scale);
+            wk.w = pack_bf16x2(__uint_as_float(kk[8 * v4 + 6]) * p.scale, __uint_as_float(kk[8 * v4 + 7]) * p.scale);
             *reinterpret_cast<uint4*>(dv_row + 32 * c32 + 8 * v4) = wa;
             *reinterpret_cast<uint4*>(dk_row + 32 * c32 + 8 * v4) = wk;
           }
         }
       }
-    } else {
-      named_barrier_arrive(1, kGradThreads);  // release gradient warps blocked on the barrier
+      if (n_iter > 0) {
+        ring_t += n_iter;
+        ++unit_n;
+      }
     }
+    if (!ok) named_barrier_arrive(1, kGradThreads);  // release gradient warps blocked on the barrier
   }
 
   tc_fence_before();
@@ -747,7 +889,7 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, LaunchInfo* in
                         C::SMEM, stream, p);
   if (e != cudaSuccess) return e;
   e = launch_serialized(bwd_dkdv_kernel<D>, dim3(static_cast<unsigned>(kv_units)),
-                        dim3(kBwdThreads), C::SMEM, stream, p);
+                        dim3(kDkdvThreads), C::SMEM, stream, p);
   if (info) {
     info->kernels = 2;
     info->grid = static_cast<int>(kv_units + q_units);
