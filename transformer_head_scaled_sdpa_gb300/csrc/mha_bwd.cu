@@ -33,12 +33,11 @@
 namespace mha {
 namespace {
 
-constexpr int kBwdThreads = 320;  // warps 0-7 gradient, 8 MMA, 9 TMA
-constexpr int kDkdvThreads = 352; // the dK/dV kernel adds warp 10, its scheduler
+constexpr int kBwdThreads = 352;  // warps 0-7 gradient, 8 MMA, 9 TMA, 10 scheduler
 constexpr int kGradThreads = 256;
 constexpr int kMmaWarp = 8, kTmaWarp = 9, kSchedWarp = 10;
-// unit-queue readers of the dK/dV kernel: 8 gradient warps, the MMA warp, the TMA lane
-constexpr int kDkdvUnitConsumers = 10;
+// unit-queue readers: 8 gradient warps, the MMA warp, the TMA lane
+constexpr int kBwdUnitConsumers = 10;
 constexpr int kRoleBwdProducer = 8, kRoleBwdMma = 9, kRoleBwdGrad = 10, kRoleBwdSched = 11;
 
 template <int D>
@@ -118,7 +117,7 @@ __device__ __forceinline__ int kv_len_of(const BwdParams& p, int b) {
 // unit's dK and dV, so the per-CTA set-up, the K/V load latency and the
 // pipeline fill leave the critical path.
 template <int D>
-__global__ void __launch_bounds__(kDkdvThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -142,7 +141,7 @@ __global__ void __launch_bounds__(kDkdvThreads, 1) bwd_dkdv_kernel(const __grid_
       mbar_init(bar(kRingFull + s), 1);
       mbar_init(bar(kRingEmpty + s), 1);
       mbar_init(bar(kUnitFull + s), 1);
-      mbar_init(bar(kUnitEmpty + s), kDkdvUnitConsumers);
+      mbar_init(bar(kUnitEmpty + s), kBwdUnitConsumers);
     }
     for (int hf = 0; hf < 2; ++hf) {
       mbar_init(bar(kScores + hf), 1);
@@ -577,8 +576,12 @@ __global__ void __launch_bounds__(kDkdvThreads, 1) bwd_dkdv_kernel(const __grid_
 }
 
 // ---------------------------------------------------------------------------
-// dQ: one CTA per (b, h, query tile)
+// dQ: units (b, h, query tile), persistent CTAs
 // ---------------------------------------------------------------------------
+// Persistent like the dK/dV kernel: the TMA warp loads the next unit's Q and
+// dO as soon as the current unit's last score products are done with them,
+// and the next unit's first score products are issued while the gradient
+// warps still write the current unit's dQ.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
@@ -589,20 +592,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
   auto bar = [&](int id) { return s_base + C::OFF_BAR + 8u * id; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* unit_slot = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+  const uint32_t clc_resp = s_base + C::OFF_MISC + 16;
+  float* d_part = reinterpret_cast<float*>(smem + C::OFF_VEC);  // [2][128]
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
 
   const int n_qt = (p.Lq + 127) / 128;
-  int bh = 0;
-  // last query tile first: under the causal mask it sees the most key tiles
-  const int qt = n_qt - 1 - bwd_unit(static_cast<int>(blockIdx.x), n_qt, p.B * p.H, &bh);
-  const int b = bh / p.H, h = bh % p.H;
-  const int q0 = qt * 128;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kFixFull), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kRingFull + s), 1);
       mbar_init(bar(kRingEmpty + s), 1);
+      mbar_init(bar(kUnitFull + s), 1);
+      mbar_init(bar(kUnitEmpty + s), kBwdUnitConsumers);
     }
     for (int hf = 0; hf < 2; ++hf) {
       mbar_init(bar(kScores + hf), 1);
@@ -610,6 +613,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     }
     mbar_init(bar(kAccDone), 1);
     mbar_init(bar(kDrain), 1);
+    mbar_init(bar(kFixFree), 1);
+    mbar_init(bar(kAccFree), kGradThreads);
+    mbar_init(bar(kClc), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -624,36 +630,105 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
   // global memory only from here on (the set-up may overlap the previous
   // kernel on the stream)
   griddep_wait();
-  const int kv_len = kv_len_of(p, b);
-  int n_kt = (kv_len + 127) / 128;
-  if (masks_causal(p.mask_kind) && n_kt > qt + 1) n_kt = qt + 1;
-  const int n_iter = n_kt;
 
-  if (warp == kTmaWarp) {
-    // ---- TMA: Q_i and dO_i once, then K_j, V_j per key tile
-    if (lane == 0 && n_iter > 0) {
-      mbar_arrive_expect_tx(bar(kFixFull), 2 * C::TILE);
-      for (int c = 0; c < C::KCH; ++c) {
-        tma_load_4d(s_base + C::OFF_A0 + c * C::CHUNK, &p.tm_q, bar(kFixFull), 64 * c, h, q0, b);
-        tma_load_4d(s_base + C::OFF_A1 + c * C::CHUNK, &p.tm_do, bar(kFixFull), 64 * c, h, q0, b);
+  // a unit's geometry: last query tile first (under the causal mask it sees
+  // the most key tiles)
+  struct QUnit {
+    int b, h, q0, qt, n_iter, kv_len;
+  };
+  auto decode = [&](int unit) {
+    QUnit u;
+    int bh = 0;
+    u.qt = n_qt - 1 - bwd_unit(unit, n_qt, p.B * p.H, &bh);
+    u.b = bh / p.H;
+    u.h = bh % p.H;
+    u.q0 = u.qt * 128;
+    u.kv_len = kv_len_of(p, u.b);
+    int n = (u.kv_len + 127) / 128;
+    if (masks_causal(p.mask_kind) && n > u.qt + 1) n = u.qt + 1;
+    u.n_iter = n;
+    return u;
+  };
+  // the k-th unit of this CTA from the queue (-1: no more, or gave up)
+  auto take = [&](int k, int role) {
+    const int slot = k & 1;
+    if (!mbar_wait(bar(kUnitFull + slot), (k >> 1) & 1, abort_flag, p.status,
+                   role * 64 + kUnitFull + slot))
+      return -1;
+    return static_cast<int>(unit_slot[slot]);
+  };
+  auto release = [&](int k) { mbar_arrive(bar(kUnitEmpty + (k & 1))); };
+
+  if (warp == kSchedWarp) {
+    // ---- scheduler (one lane): publishes the CTA's own unit, then keeps one
+    // unit of look-ahead by cancelling CTAs that have not started
+    if (lane == 0) {
+      int unit = static_cast<int>(blockIdx.x);
+      for (int k = 0;; ++k) {
+        const int slot = k & 1;
+        if (k >= 2 && !mbar_wait(bar(kUnitEmpty + slot), ((k >> 1) - 1) & 1, abort_flag, p.status,
+                                 kRoleBwdSched * 64 + kUnitEmpty + slot))
+          unit = -1;
+        unit_slot[slot] = unit;
+        mbar_arrive(bar(kUnitFull + slot));
+        if (unit < 0) break;
+        mbar_arrive_expect_tx(bar(kClc), 16);
+        clc_try_cancel(clc_resp, bar(kClc));
+        // the response is written asynchronously: wait for it even when the
+        // CTA is giving up, so nothing lands in shared memory after exit
+        volatile int never = 0;
+        if (!mbar_wait(bar(kClc), k & 1, &never, p.status, kRoleBwdSched * 64 + kClc) ||
+            *abort_flag)
+          unit = -1;
+        else
+          unit = clc_query_first_ctaid_x(clc_resp);
       }
-      int it = 0;
-      for (; it < n_iter; ++it) {
-        const int s = it & 1;
-        if (it >= 2 && !mbar_wait(bar(kRingEmpty + s), ((it >> 1) - 1) & 1, abort_flag, p.status,
-                                  kRoleBwdProducer * 64 + 16 + s))
+    }
+    __syncwarp();
+  } else if (warp == kTmaWarp) {
+    // ---- TMA (one lane): per unit Q and dO (once the previous unit's last
+    // score products are done with them), then K_j, V_j per key tile
+    if (lane == 0) {
+      int ring_t = 0;  // key tiles issued so far, over all units
+      int fix_n = 0;   // units whose Q and dO were loaded
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int unit = take(k, kRoleBwdProducer);
+        if (unit >= 0) release(k);
+        if (unit < 0) break;
+        const QUnit u = decode(unit);
+        if (u.n_iter == 0) continue;
+        if (fix_n > 0 && !mbar_wait(bar(kFixFree), (fix_n - 1) & 1, abort_flag, p.status,
+                                    kRoleBwdProducer * 64 + 16 + kFixFree))
           break;
-        const int k0 = it * 128;
-        const uint32_t dst = s_base + C::OFF_RING + s * 2 * C::TILE;
-        mbar_arrive_expect_tx(bar(kRingFull + s), 2 * C::TILE);
+        mbar_arrive_expect_tx(bar(kFixFull), 2 * C::TILE);
         for (int c = 0; c < C::KCH; ++c) {
-          tma_load_4d(dst + c * C::CHUNK, &p.tm_k, bar(kRingFull + s), 64 * c, h, k0, b);
-          tma_load_4d(dst + C::TILE + c * C::CHUNK, &p.tm_v, bar(kRingFull + s), 64 * c, h, k0, b);
+          tma_load_4d(s_base + C::OFF_A0 + c * C::CHUNK, &p.tm_q, bar(kFixFull), 64 * c, u.h, u.q0, u.b);
+          tma_load_4d(s_base + C::OFF_A1 + c * C::CHUNK, &p.tm_do, bar(kFixFull), 64 * c, u.h, u.q0,
+                      u.b);
+        }
+        ++fix_n;
+        for (int it = 0; it < u.n_iter; ++it, ++ring_t) {
+          const int s = ring_t & 1;
+          if (ring_t >= 2 && !mbar_wait(bar(kRingEmpty + s), ((ring_t >> 1) - 1) & 1, abort_flag,
+                                        p.status, kRoleBwdProducer * 64 + 16 + s)) {
+            ok = false;
+            break;
+          }
+          const int k0 = it * 128;
+          const uint32_t dst = s_base + C::OFF_RING + s * 2 * C::TILE;
+          mbar_arrive_expect_tx(bar(kRingFull + s), 2 * C::TILE);
+          for (int c = 0; c < C::KCH; ++c) {
+            tma_load_4d(dst + c * C::CHUNK, &p.tm_k, bar(kRingFull + s), 64 * c, u.h, k0, u.b);
+            tma_load_4d(dst + C::TILE + c * C::CHUNK, &p.tm_v, bar(kRingFull + s), 64 * c, u.h, k0,
+                        u.b);
+          }
         }
       }
       volatile int never = 0;
-      mbar_wait(bar(kFixFull), 0, &never, p.status, kRoleBwdProducer * 64 + 24);
-      for (int t = (it > 2 ? it - 2 : 0); t < it; ++t)
+      if (fix_n > 0)
+        mbar_wait(bar(kFixFull), (fix_n - 1) & 1, &never, p.status, kRoleBwdProducer * 64 + 24);
+      for (int t = (ring_t > 2 ? ring_t - 2 : 0); t < ring_t; ++t)
         mbar_wait(bar(kRingFull + (t & 1)), (t >> 1) & 1, &never, p.status,
                   kRoleBwdProducer * 64 + 25);
     }
@@ -687,55 +762,81 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       umma_commit(bar(kScores + hf));
     };
     // dQ += dS K over half hf (16 keys = 8 packed TMEM columns of A per step)
-    auto issue_grads = [&](int t, int hf) {
+    auto issue_grads = [&](int t, int hf, bool first) {
       const uint64_t dKm = smem_desc_sw128(half_rows(t, hf), C::CHUNK, 1024);  // K, MN-major
       const uint32_t ts = tmem + C::TM_HALF * hf;
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         umma_ts(tmem + C::TM_ACC0, ts + a_col(ks), dKm + static_cast<uint64_t>((ks * 2048) >> 4),
-                idesc_o, (ks > 0 || t > 0 || hf > 0) ? 1u : 0u);
+                idesc_o, (ks > 0 || !first) ? 1u : 0u);
     };
     bool ok = true;
-    if (n_iter > 0) {
-      ok = mbar_wait(bar(kFixFull), 0, abort_flag, p.status, kRoleBwdMma * 64 + 16 + kFixFull) &&
-           mbar_wait(bar(kRingFull), 0, abort_flag, p.status, kRoleBwdMma * 64 + 16 + kRingFull);
-      if (ok) {
-        tc_fence_after();
-        if (elect_one()) {
-          issue_scores(0, 0);
-          issue_scores(0, 1);
-        }
-        __syncwarp();
+    int ring_t = 0;  // key tiles of the units before the current one
+    int fix_n = 0;   // units with work so far
+    for (int k = 0; ok; ++k) {
+      const int unit = take(k, kRoleBwdMma);
+      __syncwarp();
+      if (unit >= 0 && lane == 0) release(k);
+      if (unit < 0) break;
+      const QUnit u = decode(unit);
+      if (u.n_iter == 0) continue;
+      ok = mbar_wait(bar(kFixFull), fix_n & 1, abort_flag, p.status,
+                     kRoleBwdMma * 64 + 16 + kFixFull) &&
+           mbar_wait(bar(kRingFull + (ring_t & 1)), (ring_t >> 1) & 1, abort_flag, p.status,
+                     kRoleBwdMma * 64 + 16 + kRingFull);
+      if (!ok) break;
+      tc_fence_after();
+      if (elect_one()) {
+        issue_scores(ring_t, 0);
+        issue_scores(ring_t, 1);
+        // a one-tile unit's score products are its last use of Q and dO
+        if (u.n_iter == 1) umma_commit(bar(kFixFree));
       }
-    }
-    for (int it = 0; ok && it < n_iter; ++it) {
-      const bool more = it + 1 < n_iter;
-      for (int hf = 0; hf < 2; ++hf) {
-        if (!mbar_wait(bar(kGrads + hf), it & 1, abort_flag, p.status,
-                       kRoleBwdMma * 64 + 16 + kGrads + hf)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (elect_one()) {
-          issue_grads(it, hf);
-          if (hf == 1) {
-            umma_commit(bar(kRingEmpty + (it & 1)));
-            if (!more) umma_commit(bar(kAccDone));
+      __syncwarp();
+      for (int it = 0; ok && it < u.n_iter; ++it) {
+        const int t = ring_t + it;
+        const bool more = it + 1 < u.n_iter;
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!mbar_wait(bar(kGrads + hf), t & 1, abort_flag, p.status,
+                         kRoleBwdMma * 64 + 16 + kGrads + hf)) {
+            ok = false;
+            break;
           }
+          // the unit's first accumulating product overwrites dQ: the previous
+          // unit's epilogue must have read it
+          if (it == 0 && hf == 0 && fix_n > 0 &&
+              !mbar_wait(bar(kAccFree), (fix_n - 1) & 1, abort_flag, p.status,
+                         kRoleBwdMma * 64 + 16 + kAccFree)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            issue_grads(t, hf, it == 0 && hf == 0);
+            if (hf == 1) {
+              umma_commit(bar(kRingEmpty + (t & 1)));
+              if (!more) umma_commit(bar(kAccDone));
+            }
+          }
+          __syncwarp();
+          if (!more) continue;
+          const int sn = (t + 1) & 1;
+          if (hf == 0 && !mbar_wait(bar(kRingFull + sn), ((t + 1) >> 1) & 1, abort_flag, p.status,
+                                    kRoleBwdMma * 64 + 16 + kRingFull + sn)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (elect_one()) {
+            issue_scores(t + 1, hf);
+            // the last tile's score products are the unit's last use of Q, dO
+            if (hf == 1 && it + 2 == u.n_iter) umma_commit(bar(kFixFree));
+          }
+          __syncwarp();
         }
-        __syncwarp();
-        if (!more) continue;
-        const int sn = (it + 1) & 1;
-        if (hf == 0 && !mbar_wait(bar(kRingFull + sn), ((it + 1) >> 1) & 1, abort_flag, p.status,
-                                  kRoleBwdMma * 64 + 16 + kRingFull + sn)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (elect_one()) issue_scores(it + 1, hf);
-        __syncwarp();
       }
+      ring_t += u.n_iter;
+      ++fix_n;
     }
     if (elect_one()) umma_commit(bar(kDrain));
     __syncwarp();
@@ -746,89 +847,119 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     // each half tile, the 32 keys of chunk w / 4
     const int quarter = warp & 3, cq = warp >> 2;
     const int r = quarter * 32 + lane;
-    const int qi = q0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c2 = p.scale_log2;
-    // D_i = dO_i . O_i of this row, the two warps of the lane quarter taking
-    // alternate 16-byte pieces and adding their halves in shared memory; it
-    // is also written to the workspace for the dK/dV kernel, which runs next
-    float l2 = -INFINITY, part = 0.f;
-    const size_t idx = (static_cast<size_t>(b) * p.H + h) * p.Lq + qi;
-    if (qi < p.Lq) {
-      l2 = p.lse[idx] * 1.4426950408889634f;
-      const int pieces = p.d / 8;
-      const size_t row_elems = (static_cast<size_t>(b) * p.Lq + qi) * p.H + h;
-      const uint4* o = reinterpret_cast<const uint4*>(p.out) + row_elems * pieces;
-      const uint4* g = reinterpret_cast<const uint4*>(p.dout) + row_elems * pieces;
-      for (int c = cq; c < pieces; c += 2) {
-        const uint4 ov = o[c], gv = g[c];
-        part += bf_lo(ov.x) * bf_lo(gv.x) + bf_hi(ov.x) * bf_hi(gv.x) + bf_lo(ov.y) * bf_lo(gv.y) +
-                bf_hi(ov.y) * bf_hi(gv.y) + bf_lo(ov.z) * bf_lo(gv.z) + bf_hi(ov.z) * bf_hi(gv.z) +
-                bf_lo(ov.w) * bf_lo(gv.w) + bf_hi(ov.w) * bf_hi(gv.w);
-      }
-    }
-    float* d_part = reinterpret_cast<float*>(smem + C::OFF_VEC);  // [2][128]
-    d_part[cq * 128 + r] = part;
-    named_barrier(1, kGradThreads);  // (no wait precedes it: every gradient warp gets here)
-    const float dvv = d_part[r] + d_part[128 + r];
-    if (cq == 0 && qi < p.Lq) p.dvec[idx] = dvv;
-    const bool row_ok = qi < p.Lq && l2 != -INFINITY;
     bool ok = true;
-    for (int it = 0; ok && it < n_iter; ++it) {
-      const int k0 = it * 128;
-      // every key of the tile visible to every query of the CTA's tile?
-      const bool all_visible = k0 + 127 < kv_len && q0 + 127 < p.Lq &&
-                               !(masks_causal(p.mask_kind) && q0 < k0 + 127);
-      for (int hf = 0; hf < 2; ++hf) {
-        if (!mbar_wait(bar(kScores + hf), it & 1, abort_flag, p.status,
-                       kRoleBwdGrad * 64 + 16 + kScores + hf)) {
-          ok = false;
-          break;
+    int ring_t = 0;  // key tiles of the units before the current one
+    int unit_n = 0;  // units with work so far
+    for (int k = 0; ok; ++k) {
+      const int unit = take(k, kRoleBwdGrad);
+      __syncwarp();
+      if (unit >= 0 && lane == 0) release(k);
+      if (unit < 0) {
+        ok = unit == -1 && !*abort_flag;
+        break;
+      }
+      const QUnit u = decode(unit);
+      const int b = u.b, h = u.h, q0 = u.q0, n_iter = u.n_iter, kv_len = u.kv_len;
+      const int qi = q0 + r;
+      // D_i = dO_i . O_i of this row, the two warps of the lane quarter taking
+      // alternate 16-byte pieces and adding their halves in shared memory; it
+      // is also written to the workspace for the dK/dV kernel, which runs next
+      float l2 = -INFINITY, part = 0.f;
+      const size_t idx = (static_cast<size_t>(b) * p.H + h) * p.Lq + qi;
+      if (qi < p.Lq) {
+        l2 = p.lse[idx] * 1.4426950408889634f;
+        const int pieces = p.d / 8;
+        const size_t row_elems = (static_cast<size_t>(b) * p.Lq + qi) * p.H + h;
+        const uint4* o = reinterpret_cast<const uint4*>(p.out) + row_elems * pieces;
+        const uint4* g = reinterpret_cast<const uint4*>(p.dout) + row_elems * pieces;
+        for (int c = cq; c < pieces; c += 2) {
+          const uint4 ov = o[c], gv = g[c];
+          part += bf_lo(ov.x) * bf_lo(gv.x) + bf_hi(ov.x) * bf_hi(gv.x) + bf_lo(ov.y) * bf_lo(gv.y) +
+                  bf_hi(ov.y) * bf_hi(gv.y) + bf_lo(ov.z) * bf_lo(gv.z) + bf_hi(ov.z) * bf_hi(gv.z) +
+                  bf_lo(ov.w) * bf_lo(gv.w) + bf_hi(ov.w) * bf_hi(gv.w);
         }
-        tc_fence_after();
-        const uint32_t ts = tmem + C::TM_HALF * hf + lane_off + 32u * cq;
-        uint32_t sr[32], pr[32];
-        tmem_ld32(ts, sr);
-        tmem_ld32(ts + C::TM_DP, pr);
-        tmem_ld_wait();
-        float pf[32];
-        if (all_visible) {
+      }
+      d_part[cq * 128 + r] = part;
+      // (the second barrier keeps the next unit's halves from overwriting
+      // this one's before both warps of the quarter have read them.  A named
+      // barrier cannot time out: after each one the abort flag is checked,
+      // and a warp that gives up arrives once on it on its way out.)
+      named_barrier(1, kGradThreads);
+      if (*abort_flag) {
+        ok = false;
+        break;
+      }
+      const float dvv = d_part[r] + d_part[128 + r];
+      named_barrier(1, kGradThreads);
+      if (*abort_flag) {
+        ok = false;
+        break;
+      }
+      if (cq == 0 && qi < p.Lq) p.dvec[idx] = dvv;
+      const bool row_ok = qi < p.Lq && l2 != -INFINITY;
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const int t_all = ring_t + it;  // barrier phases run over all units
+        const int k0 = it * 128;
+        // every key of the tile visible to every query of the unit's tile?
+        const bool all_visible = k0 + 127 < kv_len && q0 + 127 < p.Lq &&
+                                 !(masks_causal(p.mask_kind) && q0 < k0 + 127);
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!mbar_wait(bar(kScores + hf), t_all & 1, abort_flag, p.status,
+                         kRoleBwdGrad * 64 + 16 + kScores + hf)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ts = tmem + C::TM_HALF * hf + lane_off + 32u * cq;
+          uint32_t sr[32], pr[32];
+          tmem_ld32(ts, sr);
+          tmem_ld32(ts + C::TM_DP, pr);
+          tmem_ld_wait();
+          float pf[32];
+          if (all_visible) {
+#pragma unroll
+            for (int t = 0; t < 32; t += 2) {
+              fma2(pf[t], pf[t + 1], __uint_as_float(sr[t]), __uint_as_float(sr[t + 1]), c2, c2,
+                   -l2, -l2);
+              pf[t] = ex2_approx(pf[t]);
+              pf[t + 1] = ex2_approx(pf[t + 1]);
+            }
+          } else {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+              const int key = k0 + 64 * hf + 32 * cq + t;
+              const bool vis = row_ok && key < kv_len && !(masks_causal(p.mask_kind) && key > qi);
+              const float e = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -l2));
+              pf[t] = vis ? e : 0.f;
+            }
+          }
+          // dS = P (dP - D) from the float32 P (no product here takes P itself)
+          uint32_t dk[16];
 #pragma unroll
           for (int t = 0; t < 32; t += 2) {
-            fma2(pf[t], pf[t + 1], __uint_as_float(sr[t]), __uint_as_float(sr[t + 1]), c2, c2,
-                 -l2, -l2);
-            pf[t] = ex2_approx(pf[t]);
-            pf[t + 1] = ex2_approx(pf[t + 1]);
+            float g0, g1;
+            add2(g0, g1, __uint_as_float(pr[t]), __uint_as_float(pr[t + 1]), -dvv, -dvv);
+            mul2(g0, g1, pf[t], pf[t + 1], g0, g1);
+            dk[t >> 1] = pack_bf16x2(g0, g1);
           }
-        } else {
-#pragma unroll
-          for (int t = 0; t < 32; ++t) {
-            const int key = k0 + 64 * hf + 32 * cq + t;
-            const bool vis = row_ok && key < kv_len && !(masks_causal(p.mask_kind) && key > qi);
-            const float e = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -l2));
-            pf[t] = vis ? e : 0.f;
-          }
+          // dS over the first 16 of the chunk's S columns (read by this thread only)
+          tmem_st16(ts, dk);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(kGrads + hf));
         }
-        // dS = P (dP - D) from the float32 P (no product here takes P itself)
-        uint32_t dk[16];
-#pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          float g0, g1;
-          add2(g0, g1, __uint_as_float(pr[t]), __uint_as_float(pr[t + 1]), -dvv, -dvv);
-          mul2(g0, g1, pf[t], pf[t + 1], g0, g1);
-          dk[t >> 1] = pack_bf16x2(g0, g1);
-        }
-        // dS over the first 16 of the chunk's S columns (read by this thread only)
-        tmem_st16(ts, dk);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(kGrads + hf));
       }
-    }
-    if (ok && n_iter > 0)
-      ok = mbar_wait(bar(kAccDone), 0, abort_flag, p.status, kRoleBwdGrad * 64 + 16 + kAccDone);
-    if (ok) {
-      tc_fence_after();
+      if (!ok) break;
+      // ---- epilogue: the accumulator is read first, then released to the
+      // next unit
+      if (n_iter > 0) {
+        ok = mbar_wait(bar(kAccDone), unit_n & 1, abort_flag, p.status,
+                       kRoleBwdGrad * 64 + 16 + kAccDone);
+        if (!ok) break;
+        tc_fence_after();
+      }
       __nv_bfloat16* dq_row = reinterpret_cast<__nv_bfloat16*>(p.dq) +
                               ((static_cast<size_t>(b) * p.Lq + qi) * p.H + h) * p.d;
 #pragma unroll 1
@@ -837,6 +968,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         if (n_iter > 0) {
           tmem_ld32(tmem + C::TM_ACC0 + lane_off + 32u * c32, a);
           tmem_ld_wait();
+          if (c32 + 2 >= D / 32) {
+            // this thread's last accumulator columns are read
+            tc_fence_before();
+            mbar_arrive(bar(kAccFree));
+          }
         } else {
 #pragma unroll
           for (int t = 0; t < 32; ++t) a[t] = 0u;
@@ -854,7 +990,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
           }
         }
       }
+      if (n_iter > 0) {
+        ring_t += n_iter;
+        ++unit_n;
+      }
     }
+    if (!ok) named_barrier_arrive(1, kGradThreads);  // release gradient warps blocked on the barrier
   }
 
   tc_fence_before();
@@ -889,7 +1030,7 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, LaunchInfo* in
                         C::SMEM, stream, p);
   if (e != cudaSuccess) return e;
   e = launch_serialized(bwd_dkdv_kernel<D>, dim3(static_cast<unsigned>(kv_units)),
-                        dim3(kDkdvThreads), C::SMEM, stream, p);
+                        dim3(kBwdThreads), C::SMEM, stream, p);
   if (info) {
     info->kernels = 2;
     info->grid = static_cast<int>(kv_units + q_units);
