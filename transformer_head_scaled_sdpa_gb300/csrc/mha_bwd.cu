@@ -9,11 +9,11 @@
 //   dV_j  = sum_i a_ij dO_i,     dK_j = scale sum_i dS_ij q_i,
 //   dQ_i  = scale sum_j dS_ij k_j.
 // Two kernels, in this order on the stream:
-//   bwd_dq_kernel     one CTA per (b, h, 128-query tile); first forms D_i for
+//   bwd_dq_kernel     units (b, h, 128-query tile); first forms D_i for
 //                     its rows (stored for the next kernel), then the key
 //                     tiles it sees stream through a two-stage ring: S = Q K^T
 //                     and dP = dO V^T, then dS (bf16, over S), then dQ += dS K.
-//   bwd_dkdv_kernel   one CTA per (b, h, 128-key tile); the query tiles that
+//   bwd_dkdv_kernel   units (b, h, 128-key tile); the query tiles that
 //                     see the keys stream through a two-stage ring.  Per query
 //                     tile: S^T = K Q^T and dP^T = V dO^T on the tensor cores
 //                     (keys on TMEM lanes), the eight gradient warps turn them
@@ -23,6 +23,9 @@
 // Both take each streamed tile in two halves of 64 rows with TMEM regions of
 // their own: the tensor cores run one half's products (and the next tile's
 // scores) while the gradient warps turn the other half's scores into P, dS.
+// Both are persistent: one CTA per SM runs unit after unit (cluster launch
+// control), loading the next unit's fixed tiles and issuing its first scores
+// while the current unit's epilogue drains.
 // Every operand reuses the forward's shared-memory layout (128-row tiles of
 // 64-feature, 128-byte swizzled chunks): K-major as an operand whose
 // reduction runs over d, MN-major where it runs over the rows.
