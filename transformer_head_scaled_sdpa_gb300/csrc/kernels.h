@@ -94,6 +94,7 @@ cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream, Lau
 // Gradient of the bf16 forward.
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // [B, L, H, d] bf16, box {64, 1, 128, 1}, 128-byte swizzle
+  CUtensorMap tm_o;                      // [B, Lq, H, d] the forward output, same box
   const void* out;    // [B, Lq, H, d] bf16 forward output
   const void* dout;   // [B, Lq, H, d] bf16 dL/dO
   const float* lse;   // [B, H, Lq] forward row log-sum-exp (natural log)
@@ -111,7 +112,7 @@ struct BwdParams {
   float scale_log2;   // scale * log2(e)
 };
 
-// Launches the gradient: the D pre-pass, the dK/dV kernel and the dQ kernel.
+// Launches the gradient: the dQ kernel (which also forms D) and the dK/dV kernel.
 cudaError_t launch_bwd(const BwdParams& p, int d, cudaStream_t stream, LaunchInfo* info);
 
 // Launches the bf16 tcgen05 forward for d in {64, 128}.

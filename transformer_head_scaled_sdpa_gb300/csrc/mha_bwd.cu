@@ -54,11 +54,15 @@ struct BwdCfg {
   static constexpr int OFF_RING = 2 * TILE;    // stage s: pair at OFF_RING + s * 2 * TILE
   static constexpr int OFF_VEC = OFF_RING + 4 * TILE;  // dK/dV: lse2[128], D[128]; dQ: D halves [2][128]
   static constexpr int OFF_BAR = OFF_VEC + 2 * 128 * 4;
-  static constexpr int NBAR = 18;
+  static constexpr int NBAR = 19;
   // tmem slot (+0), abort flag (+4), unit queue (+8, +12), cancellation
   // response (+16, 16 bytes, 16-byte aligned)
   static constexpr int OFF_MISC = (OFF_BAR + 8 * NBAR + 15) / 16 * 16;
   static constexpr int SMEM = OFF_MISC + 32 + 1024;
+  // the dQ kernel also stages the forward output O (for D = dO . O)
+  static constexpr int OFF_O = (OFF_MISC + 32 + 1023) / 1024 * 1024;
+  static constexpr int SMEM_DQ = OFF_O + TILE + 1024;
+  static_assert(SMEM_DQ <= 227 * 1024, "shared memory budget (dQ)");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   // TMEM: a tile's score-shaped matrices in two halves of 64 columns, half
   // hf at columns 128 hf (S or S^T) and 128 hf + 64 (dP or dP^T); then the
@@ -73,7 +77,9 @@ enum { kFixFull = 0, kRingFull = 1, kRingEmpty = 3, kScores = 5, kGrads = 7, kAc
        kDrain = 10,
        // the persistent dK/dV kernel: the unit's last score products are done
        // with K and V; the epilogue has read the accumulators; the unit queue
-       kFixFree = 11, kAccFree = 12, kUnitFull = 13, kUnitEmpty = 15, kClc = 17 };
+       kFixFree = 11, kAccFree = 12, kUnitFull = 13, kUnitEmpty = 15, kClc = 17,
+       // the dQ kernel: the gradient warps have read the unit's O tile
+       kOFree = 18 };
 
 // TMEM column of the 16 rows of K16 step ks (0..3) of a half, packed as bf16
 // pairs: chunk ks / 2 (32 rows) keeps them in the first 16 of its 32 columns
@@ -410,10 +416,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     bool ok = true;
     int ring_t = 0;  // query tiles of the units before the current one
     int unit_n = 0;  // units with work so far
+    // The next unit is taken from the queue at the current unit's last tile,
+    // and its first tile's lse / D loaded then, so that load's latency is not
+    // paid at the unit boundary.
+    int next_unit_idx = -2;  // -2: not taken early
+    float vn = 0.f;
+    bool vn_ready = false;   // vn holds the current unit's first value
+    auto fetch_of = [&](const KvUnit& w, int t) {
+      const int qi = (w.qt_begin + t) * 128 + vi;
+      vn = qi < p.Lq ? v_src[(static_cast<size_t>(w.b) * p.H + w.h) * p.Lq + qi] : -INFINITY;
+    };
     for (int k = 0; ok; ++k) {
-      const int unit = take(k, kRoleBwdGrad);
-      __syncwarp();
-      if (unit >= 0 && lane == 0) release(k);
+      int unit;
+      if (next_unit_idx != -2) {
+        unit = next_unit_idx;
+        next_unit_idx = -2;
+      } else {
+        unit = take(k, kRoleBwdGrad);
+        __syncwarp();
+        if (unit >= 0 && lane == 0) release(k);
+        vn_ready = false;
+      }
       if (unit < 0) {
         ok = unit == -1 && !*abort_flag;
         break;
@@ -422,12 +445,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       const int b = u.b, h = u.h, k0 = u.k0, qt_begin = u.qt_begin, n_iter = u.n_iter;
       const int kv_len = u.kv_len;
       const int key = k0 + r;
-      float vn = 0.f;
-      auto fetch = [&](int t) {
-        const int qi = (qt_begin + t) * 128 + vi;
-        vn = qi < p.Lq ? v_src[(static_cast<size_t>(b) * p.H + h) * p.Lq + qi] : -INFINITY;
-      };
-      if (n_iter > 0) fetch(0);
+      if (n_iter > 0 && !vn_ready) fetch_of(u, 0);
+      vn_ready = false;
       for (int it = 0; ok && it < n_iter; ++it) {
         const int t_all = ring_t + it;  // barrier phases run over all units
         const int q0 = (qt_begin + it) * 128;
@@ -447,7 +466,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
           ok = false;
           break;
         }
-        if (it + 1 < n_iter) fetch(it + 1);
+        if (it + 1 < n_iter) {
+          fetch_of(u, it + 1);
+        } else {
+          // last tile: the next unit and its first lse / D now
+          next_unit_idx = take(k + 1, kRoleBwdGrad);
+          __syncwarp();
+          if (next_unit_idx >= 0) {
+            if (lane == 0) release(k + 1);
+            const KvUnit w = decode(next_unit_idx);
+            if (w.n_iter > 0) {
+              fetch_of(w, 0);
+              vn_ready = true;
+            }
+          }
+        }
         // Every (key, query) pair of the tile is visible unless the tile holds
         // keys past the key length, queries past Lq, or the causal diagonal.
         const bool all_visible = k0 + 127 < kv_len && q0 + 127 < p.Lq &&
@@ -619,6 +652,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     mbar_init(bar(kFixFree), 1);
     mbar_init(bar(kAccFree), kGradThreads);
     mbar_init(bar(kClc), 1);
+    mbar_init(bar(kOFree), kGradThreads);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -701,14 +735,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         if (unit < 0) break;
         const QUnit u = decode(unit);
         if (u.n_iter == 0) continue;
-        if (fix_n > 0 && !mbar_wait(bar(kFixFree), (fix_n - 1) & 1, abort_flag, p.status,
-                                    kRoleBwdProducer * 64 + 16 + kFixFree))
+        // the previous unit's Q and dO (last score products) and O (the
+        // gradient warps' D) must be done with
+        if (fix_n > 0 && (!mbar_wait(bar(kFixFree), (fix_n - 1) & 1, abort_flag, p.status,
+                                     kRoleBwdProducer * 64 + 16 + kFixFree) ||
+                          !mbar_wait(bar(kOFree), (fix_n - 1) & 1, abort_flag, p.status,
+                                     kRoleBwdProducer * 64 + 16 + kOFree)))
           break;
-        mbar_arrive_expect_tx(bar(kFixFull), 2 * C::TILE);
+        mbar_arrive_expect_tx(bar(kFixFull), 3 * C::TILE);
         for (int c = 0; c < C::KCH; ++c) {
           tma_load_4d(s_base + C::OFF_A0 + c * C::CHUNK, &p.tm_q, bar(kFixFull), 64 * c, u.h, u.q0, u.b);
           tma_load_4d(s_base + C::OFF_A1 + c * C::CHUNK, &p.tm_do, bar(kFixFull), 64 * c, u.h, u.q0,
                       u.b);
+          tma_load_4d(s_base + C::OFF_O + c * C::CHUNK, &p.tm_o, bar(kFixFull), 64 * c, u.h, u.q0, u.b);
         }
         ++fix_n;
         for (int it = 0; it < u.n_iter; ++it, ++ring_t) {
@@ -866,23 +905,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       const QUnit u = decode(unit);
       const int b = u.b, h = u.h, q0 = u.q0, n_iter = u.n_iter, kv_len = u.kv_len;
       const int qi = q0 + r;
-      // D_i = dO_i . O_i of this row, the two warps of the lane quarter taking
-      // alternate 16-byte pieces and adding their halves in shared memory; it
-      // is also written to the workspace for the dK/dV kernel, which runs next
+      // D_i = dO_i . O_i of this row from the staged dO and O tiles (128-byte
+      // swizzled rows), the two warps of the lane quarter taking alternate
+      // 16-byte pieces and adding their halves in shared memory; it is also
+      // written to the workspace for the dK/dV kernel, which runs next.  (A
+      // unit without keys has no tiles and needs no D.)
       float l2 = -INFINITY, part = 0.f;
       const size_t idx = (static_cast<size_t>(b) * p.H + h) * p.Lq + qi;
-      if (qi < p.Lq) {
-        l2 = p.lse[idx] * 1.4426950408889634f;
-        const int pieces = p.d / 8;
-        const size_t row_elems = (static_cast<size_t>(b) * p.Lq + qi) * p.H + h;
-        const uint4* o = reinterpret_cast<const uint4*>(p.out) + row_elems * pieces;
-        const uint4* g = reinterpret_cast<const uint4*>(p.dout) + row_elems * pieces;
+      if (qi < p.Lq) l2 = p.lse[idx] * 1.4426950408889634f;
+      if (n_iter > 0) {
+        ok = mbar_wait(bar(kFixFull), unit_n & 1, abort_flag, p.status,
+                       kRoleBwdGrad * 64 + 16 + kFixFull);
+        if (!ok) break;
+        const int pieces = p.d / 8;  // the tiles hold zeros past d
         for (int c = cq; c < pieces; c += 2) {
-          const uint4 ov = o[c], gv = g[c];
+          const uint32_t off = static_cast<uint32_t>((c >> 3) * C::CHUNK + r * 128 +
+                                                     (((c & 7) ^ (r & 7)) << 4));
+          const uint4 ov = ld_shared_v4(s_base + C::OFF_O + off);
+          const uint4 gv = ld_shared_v4(s_base + C::OFF_A1 + off);
           part += bf_lo(ov.x) * bf_lo(gv.x) + bf_hi(ov.x) * bf_hi(gv.x) + bf_lo(ov.y) * bf_lo(gv.y) +
                   bf_hi(ov.y) * bf_hi(gv.y) + bf_lo(ov.z) * bf_lo(gv.z) + bf_hi(ov.z) * bf_hi(gv.z) +
                   bf_lo(ov.w) * bf_lo(gv.w) + bf_hi(ov.w) * bf_hi(gv.w);
         }
+        mbar_arrive(bar(kOFree));
       }
       d_part[cq * 128 + r] = part;
       // (the second barrier keeps the next unit's halves from overwriting
@@ -1020,7 +1065,7 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, LaunchInfo* in
   if (!attr_set[dev]) {
     e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_DQ);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -1030,7 +1075,7 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, LaunchInfo* in
   // the dQ kernel forms D = dO . O for its rows and stores it; the dK/dV
   // kernel, next on the stream, reads it
   e = launch_serialized(bwd_dq_kernel<D>, dim3(static_cast<unsigned>(q_units)), dim3(kBwdThreads),
-                        C::SMEM, stream, p);
+                        C::SMEM_DQ, stream, p);
   if (e != cudaSuccess) return e;
   e = launch_serialized(bwd_dkdv_kernel<D>, dim3(static_cast<unsigned>(kv_units)),
                         dim3(kBwdThreads), C::SMEM, stream, p);
