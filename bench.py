@@ -1,9 +1,17 @@
 """Benchmark of the multi-head attention forward on GB300.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                [--pass fwd|bwd] [--eager] [--no-cpu-baseline]
 
 One step = one mha_fwd call over the whole workload (every sequence, head and
 query tile), inputs resident in HBM.  Prints ONE JSON line (rank 0).
+
+Timing: after W warm-up steps the K timed steps' C-ABI calls are captured once
+into a CUDA graph, which is replayed once untimed and once between CUDA events
+on the launching stream (barrier + synchronize on both sides), so the device
+runs the launches back to back; ``--eager`` issues them one by one with events
+around each instead.  Consecutive steps rotate over enough input copies that
+no step finds its inputs in L2.
 
 Metric: attention forward TFLOP/s, FLOPs = 4*B*H*Lq*Lk*d_k (halved under the
 causal mask), bf16 inputs, float32 accumulation; also reported as a fraction
