@@ -95,6 +95,7 @@ cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream, Lau
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // [B, L, H, d] bf16, box {64, 1, 128, 1}, 128-byte swizzle
   CUtensorMap tm_o;                      // [B, Lq, H, d] the forward output, same box
+  CUtensorMap tm_dk, tm_dv;              // [B, Lk, H, d] the key gradients (stored), same box
   const void* out;    // [B, Lq, H, d] bf16 forward output
   const void* dout;   // [B, Lq, H, d] bf16 dL/dO
   const float* lse;   // [B, H, Lq] forward row log-sum-exp (natural log)

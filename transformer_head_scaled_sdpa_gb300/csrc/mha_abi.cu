@@ -536,7 +536,8 @@ int mha_bwd(const void* q, const void* k, const void* v, const void* out, const 
   std::memset(&p, 0, sizeof(p));
   if (!encode_map(&p.tm_q, q, B, Lq, H, d_k) || !encode_map(&p.tm_k, k, B, Lk, H, d_k) ||
       !encode_map(&p.tm_v, v, B, Lk, H, d_k) || !encode_map(&p.tm_do, dout, B, Lq, H, d_k) ||
-      !encode_map(&p.tm_o, out, B, Lq, H, d_k))
+      !encode_map(&p.tm_o, out, B, Lq, H, d_k) || !encode_map(&p.tm_dk, dk, B, Lk, H, d_k) ||
+      !encode_map(&p.tm_dv, dv, B, Lk, H, d_k))
     return MHA_ERR_UNSUPPORTED;
   p.out = out;
   p.dout = dout;

@@ -54,7 +54,7 @@ struct BwdCfg {
   static constexpr int OFF_RING = 2 * TILE;    // stage s: pair at OFF_RING + s * 2 * TILE
   static constexpr int OFF_VEC = OFF_RING + 4 * TILE;  // dK/dV: lse2[128], D[128]; dQ: D halves [2][128]
   static constexpr int OFF_BAR = OFF_VEC + 2 * 128 * 4;
-  static constexpr int NBAR = 19;
+  static constexpr int NBAR = 21;
   // tmem slot (+0), abort flag (+4), unit queue (+8, +12), cancellation
   // response (+16, 16 bytes, 16-byte aligned)
   static constexpr int OFF_MISC = (OFF_BAR + 8 * NBAR + 15) / 16 * 16;
@@ -63,6 +63,11 @@ struct BwdCfg {
   static constexpr int OFF_O = (OFF_MISC + 32 + 1023) / 1024 * 1024;
   static constexpr int SMEM_DQ = OFF_O + TILE + 1024;
   static_assert(SMEM_DQ <= 227 * 1024, "shared memory budget (dQ)");
+  // the dK/dV kernel stages one 64-column chunk of dV and of dK there for
+  // its TMA stores
+  static constexpr int OFF_STG = OFF_O;
+  static constexpr int SMEM_DKDV = OFF_STG + 2 * CHUNK + 1024;
+  static_assert(SMEM_DKDV <= 227 * 1024, "shared memory budget (dK/dV)");
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   // TMEM: a tile's score-shaped matrices in two halves of 64 columns, half
   // hf at columns 128 hf (S or S^T) and 128 hf + 64 (dP or dP^T); then the
@@ -79,7 +84,10 @@ enum { kFixFull = 0, kRingFull = 1, kRingEmpty = 3, kScores = 5, kGrads = 7, kAc
        // with K and V; the epilogue has read the accumulators; the unit queue
        kFixFree = 11, kAccFree = 12, kUnitFull = 13, kUnitEmpty = 15, kClc = 17,
        // the dQ kernel: the gradient warps have read the unit's O tile
-       kOFree = 18 };
+       kOFree = 18,
+       // the dK/dV epilogue: a chunk is staged (256 arrivals); its TMA stores
+       // have read the staging buffers
+       kStgFull = 19, kStgFree = 20 };
 
 // TMEM column of the 16 rows of K16 step ks (0..3) of a half, packed as bf16
 // pairs: chunk ks / 2 (32 rows) keeps them in the first 16 of its 32 columns
@@ -161,6 +169,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     mbar_init(bar(kFixFree), 1);
     mbar_init(bar(kAccFree), kGradThreads);
     mbar_init(bar(kClc), 1);
+    mbar_init(bar(kStgFull), kGradThreads);
+    mbar_init(bar(kStgFree), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -416,6 +426,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     bool ok = true;
     int ring_t = 0;  // query tiles of the units before the current one
     int unit_n = 0;  // units with work so far
+    int stg_n = 0;   // epilogue chunks staged so far
+    const uint32_t stg_v = s_base + C::OFF_STG, stg_k = stg_v + C::CHUNK;
     // The next unit is taken from the queue at the current unit's last tile,
     // and its first tile's lse / D loaded then, so that load's latency is not
     // paid at the unit boundary.
@@ -557,17 +569,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         if (!ok) break;
         tc_fence_after();
       }
-      const size_t row_off = ((static_cast<size_t>(b) * p.Lk + key) * p.H + h) * p.d;
-      __nv_bfloat16* dv_row = reinterpret_cast<__nv_bfloat16*>(p.dv) + row_off;
-      __nv_bfloat16* dk_row = reinterpret_cast<__nv_bfloat16*>(p.dk) + row_off;
+      // Per 64-column chunk: the accumulators to bf16 (dK scaled) in the
+      // two staging buffers (128-byte swizzle, this thread's row and 32 of
+      // the columns), then one thread stores both with TMA (rows past Lk and
+      // columns past d are not written).  Row-wise global stores from each
+      // thread cost this kernel about 9 % at d 128.
 #pragma unroll 1
-      for (int c32 = cq; c32 < D / 32; c32 += 2) {
+      for (int c64 = 0; c64 < C::KCH; ++c64) {
+        const int c32 = 2 * c64 + cq;
         uint32_t a[32], kk[32];
         if (n_iter > 0) {
           tmem_ld32(tmem + C::TM_ACC0 + lane_off + 32u * c32, a);
           tmem_ld32(tmem + C::TM_ACC1 + lane_off + 32u * c32, kk);
           tmem_ld_wait();
-          if (c32 + 2 >= D / 32) {
+          if (c64 + 1 == C::KCH) {
             // this thread's last accumulator columns are read: the next unit
             // may overwrite them
             tc_fence_before();
@@ -577,24 +592,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
 #pragma unroll
           for (int t = 0; t < 32; ++t) a[t] = kk[t] = 0u;
         }
-        if (key < p.Lk) {
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            if (32 * c32 + 8 * v4 >= p.d) break;  // columns past d are padding
-            uint4 wa, wk;
-            wa.x = pack_bf16x2(__uint_as_float(a[8 * v4 + 0]), __uint_as_float(a[8 * v4 + 1]));
-            wa.y = pack_bf16x2(__uint_as_float(a[8 * v4 + 2]), __uint_as_float(a[8 * v4 + 3]));
-            wa.z = pack_bf16x2(__uint_as_float(a[8 * v4 + 4]), __uint_as_float(a[8 * v4 + 5]));
-            wa.w = pack_bf16x2(__uint_as_float(a[8 * v4 + 6]), __uint_as_float(a[8 * v4 + 7]));
-            wk.x = pack_bf16x2(__uint_as_float(kk[8 * v4 + 0]) * p.scale, __uint_as_float(kk[8 * v4 + 1]) * p.scale);
-            wk.y = pack_bf16x2(__uint_as_float(kk[8 * v4 + 2]) * p.scale, __uint_as_float(kk[8 * v4 + 3]) * p.scale);
-            wk.z = pack_bf16x2(__uint_as_float(kk[8 * v4 + 4]) * p.scale, __uint_as_float(kk[8 * v4 + 5]) * p.scale);
-            wk.w = pack_bf16x2(__uint_as_float(kk[8 * v4 + 6]) * p.scale, __uint_as_float(kk[8 * v4 + 7]) * p.scale);
-            *reinterpret_cast<uint4*>(dv_row + 32 * c32 + 8 * v4) = wa;
-            *reinterpret_cast<uint4*>(dk_row + 32 * c32 + 8 * v4) = wk;
-          }
+        // the previous chunk's stores must have read the staging buffers
+        if (stg_n > 0 && !mbar_wait(bar(kStgFree), (stg_n - 1) & 1, abort_flag, p.status,
+                                    kRoleBwdGrad * 64 + kStgFree)) {
+          ok = false;
+          break;
         }
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) {
+          const uint32_t off = static_cast<uint32_t>(r * 128 + (((4 * cq + v4) ^ (r & 7)) << 4));
+          st_shared_v4(stg_v + off,
+                       pack_bf16x2(__uint_as_float(a[8 * v4 + 0]), __uint_as_float(a[8 * v4 + 1])),
+                       pack_bf16x2(__uint_as_float(a[8 * v4 + 2]), __uint_as_float(a[8 * v4 + 3])),
+                       pack_bf16x2(__uint_as_float(a[8 * v4 + 4]), __uint_as_float(a[8 * v4 + 5])),
+                       pack_bf16x2(__uint_as_float(a[8 * v4 + 6]), __uint_as_float(a[8 * v4 + 7])));
+          st_shared_v4(stg_k + off,
+                       pack_bf16x2(__uint_as_float(kk[8 * v4 + 0]) * p.scale, __uint_as_float(kk[8 * v4 + 1]) * p.scale),
+                       pack_bf16x2(__uint_as_float(kk[8 * v4 + 2]) * p.scale, __uint_as_float(kk[8 * v4 + 3]) * p.scale),
+                       pack_bf16x2(__uint_as_float(kk[8 * v4 + 4]) * p.scale, __uint_as_float(kk[8 * v4 + 5]) * p.scale),
+                       pack_bf16x2(__uint_as_float(kk[8 * v4 + 6]) * p.scale, __uint_as_float(kk[8 * v4 + 7]) * p.scale));
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kStgFull));
+        if (threadIdx.x == 0) {
+          if (!mbar_wait(bar(kStgFull), stg_n & 1, abort_flag, p.status,
+                         kRoleBwdGrad * 64 + kStgFull)) {
+            ok = false;
+            break;
+          }
+          tma_store_4d(&p.tm_dv, stg_v, 64 * c64, h, k0, b);
+          tma_store_4d(&p.tm_dk, stg_k, 64 * c64, h, k0, b);
+          tma_store_commit();
+          tma_store_wait_read();
+          mbar_arrive(bar(kStgFree));
+        }
+        ++stg_n;
       }
+      if (!ok) break;
       if (n_iter > 0) {
         ring_t += n_iter;
         ++unit_n;
@@ -1063,7 +1097,8 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, LaunchInfo* in
   static bool attr_set[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_DKDV);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_DQ);
     if (e != cudaSuccess) return e;
@@ -1078,7 +1113,7 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, LaunchInfo* in
                         C::SMEM_DQ, stream, p);
   if (e != cudaSuccess) return e;
   e = launch_serialized(bwd_dkdv_kernel<D>, dim3(static_cast<unsigned>(kv_units)),
-                        dim3(kBwdThreads), C::SMEM, stream, p);
+                        dim3(kBwdThreads), C::SMEM_DKDV, stream, p);
   if (info) {
     info->kernels = 2;
     info->grid = static_cast<int>(kv_units + q_units);
