@@ -928,6 +928,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     bool ok = true;
     int ring_t = 0;  // key tiles of the units before the current one
     int unit_n = 0;  // units with work so far
+    // dQ rows in whole 32-byte sectors: rows of a multiple of 16 elements
+    // from a 32-byte aligned base
+    const bool whole_sectors =
+        p.d % 16 == 0 && (reinterpret_cast<uintptr_t>(p.dq) & 31u) == 0;
     for (int k = 0; ok; ++k) {
       const int unit = take(k, kRoleBwdGrad);
       __syncwarp();
@@ -1060,15 +1064,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
           for (int t = 0; t < 32; ++t) a[t] = 0u;
         }
         if (qi < p.Lq) {
+          uint4 w[4];
 #pragma unroll
           for (int v4 = 0; v4 < 4; ++v4) {
-            if (32 * c32 + 8 * v4 >= p.d) break;  // columns past d are padding
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(a[8 * v4 + 0]) * p.scale, __uint_as_float(a[8 * v4 + 1]) * p.scale);
-            w.y = pack_bf16x2(__uint_as_float(a[8 * v4 + 2]) * p.scale, __uint_as_float(a[8 * v4 + 3]) * p.scale);
-            w.z = pack_bf16x2(__uint_as_float(a[8 * v4 + 4]) * p.scale, __uint_as_float(a[8 * v4 + 5]) * p.scale);
-            w.w = pack_bf16x2(__uint_as_float(a[8 * v4 + 6]) * p.scale, __uint_as_float(a[8 * v4 + 7]) * p.scale);
-            *reinterpret_cast<uint4*>(dq_row + 32 * c32 + 8 * v4) = w;
+            w[v4].x = pack_bf16x2(__uint_as_float(a[8 * v4 + 0]) * p.scale, __uint_as_float(a[8 * v4 + 1]) * p.scale);
+            w[v4].y = pack_bf16x2(__uint_as_float(a[8 * v4 + 2]) * p.scale, __uint_as_float(a[8 * v4 + 3]) * p.scale);
+            w[v4].z = pack_bf16x2(__uint_as_float(a[8 * v4 + 4]) * p.scale, __uint_as_float(a[8 * v4 + 5]) * p.scale);
+            w[v4].w = pack_bf16x2(__uint_as_float(a[8 * v4 + 6]) * p.scale, __uint_as_float(a[8 * v4 + 7]) * p.scale);
+          }
+          if (whole_sectors && 32 * c32 + 32 <= p.d) {
+            // whole 32-byte sectors, two stores instead of four
+            st_global_v8(dq_row + 32 * c32, w[0], w[1]);
+            st_global_v8(dq_row + 32 * c32 + 16, w[2], w[3]);
+          } else {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              if (32 * c32 + 8 * v4 >= p.d) break;  // columns past d are padding
+              *reinterpret_cast<uint4*>(dq_row + 32 * c32 + 8 * v4) = w[v4];
+            }
           }
         }
       }
