@@ -63,6 +63,14 @@ SHAPES = [
     (2, 3, 200, 333, 32, NONE, None),
     (3, 2, 300, 300, 96, CAUSAL, None),
     (2, 2, 130, 257, 8, KEYPAD, [257, 40]),
+    # more units than SMs, so every CTA runs several units back to back (the
+    # kernels are persistent), with units without keys between them, rows
+    # past Lk clipped by the dK/dV tensor-map stores, and dQ rows on both
+    # store paths (whole 32-byte sectors at d 128, 16-byte stores at d 40)
+    (5, 40, 256, 256, 64, KEYPAD, [256, 0, 130, 1, 255]),
+    (3, 60, 300, 300, 128, 3, [300, 0, 129]),
+    (2, 80, 200, 333, 128, NONE, None),
+    (4, 40, 150, 150, 40, CAUSAL, None),
 ]
 
 
