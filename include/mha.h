@@ -297,8 +297,13 @@ size_t mha_fwd_host_workspace_bytes(int B, int H, int Lq, int Lk, int d_k,
  * mha_fwd_host -- the same operation on HOST buffers: copies q, k, v (and
  * key_lens) into the caller's device workspace, runs mha_fwd (elem_bytes 2)
  * or mha_fwd_f32 (elem_bytes 4) there, copies the output back into out and
- * waits for the stream.  Host buffers should be page-locked for the copies to
- * be asynchronous.  Returns the argument check's code, MHA_ERR_WORKSPACE,
+ * waits for the stream.  The batch goes in up to four chunks of whole
+ * sequences over two internal streams, so the copies in, the kernels and the
+ * copies out of consecutive chunks overlap; the internal streams start after
+ * the work already queued on `stream`, which waits for them.  The first call
+ * on a device creates those two streams and three events, kept for the
+ * process.  Host buffers should be page-locked for the copies to be
+ * asynchronous.  Returns the argument check's code, MHA_ERR_WORKSPACE,
  * MHA_ERR_LAUNCH, or the device status (as mha_sync_status).
  */
 int mha_fwd_host(const void* q, const void* k, const void* v, void* out,

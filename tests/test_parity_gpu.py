@@ -442,6 +442,35 @@ def test_host_entry_matches_device_entry(mha):
     assert torch.equal(out, dev)
 
 
+@pytest.mark.parametrize("shape", [
+    # B, H, Lq, Lk, d, mask, key_lens, dtype.  Below 16 MiB of inputs one
+    # chunk; then 8 MiB or more per chunk, up to four: three uneven chunks of
+    # five sequences, four of seven (with key padding), two in float32
+    (1, 3, 200, 300, 64, NONE, None, torch.bfloat16),
+    (5, 2, 33, 90, 40, KEYPAD, [90, 1, 0, 45, 89], torch.float32),
+    (5, 16, 512, 512, 128, CAUSAL, None, torch.bfloat16),
+    (7, 16, 300, 600, 128, KEYPAD, [600, 0, 1, 128, 129, 300, 599], torch.bfloat16),
+    (6, 8, 512, 700, 64, KEYPAD, [700, 1, 0, 350, 699, 128], torch.float32),
+], ids=lambda s: "x".join(map(str, s[:5])) + f"-m{s[5]}-{str(s[7])[6:]}")
+def test_host_entry_chunks(mha, shape):
+    """The host entry runs the batch in chunks of sequences over two streams:
+    every sequence's output equals the device entry's, bit for bit."""
+    B, H, Lq, Lk, d, mask, lens, dtype = shape
+    case = inputs.random_case(zlib.crc32(repr(shape).encode()) & 0xFFFF, B, H, Lq, Lk, d,
+                              dtype=dtype)
+    if lens is not None:
+        case["key_lens"] = torch.tensor(lens, dtype=torch.int32)
+    dev = pu.gpu_run(mha, case, mask).cpu()
+    host = {n: case[n].pin_memory() for n in ("q", "k", "v")}
+    out = torch.full_like(host["q"], 7.0).pin_memory()
+    eb = 2 if dtype == torch.bfloat16 else 4
+    ws = torch.empty(mha.host_workspace_bytes(B, H, Lq, Lk, d, eb), dtype=torch.uint8,
+                     device="cuda")
+    mha.mha_fwd_host(host["q"], host["k"], host["v"], out, ws, mask_kind=mask,
+                     key_lens=case["key_lens"])
+    assert torch.equal(out, dev)
+
+
 def test_attention_kernel_timeout_path(mha):
     """With one pipeline signal withheld, every CTA's bounded wait runs out
     (about a second), the kernel aborts, drains and frees its tensor memory,

@@ -37,6 +37,37 @@ struct DeviceState {
 std::mutex g_mutex;
 int g_withhold_p = 0;  // test hook of mha_debug_withhold_p
 DeviceState g_dev[kMaxDevices];
+
+// The host entry's two streams and its events, created on the device's
+// first mha_fwd_host call and kept for the process.
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t st[2] = {nullptr, nullptr};
+  cudaEvent_t start = nullptr, done[2] = {nullptr, nullptr};
+};
+HostPipe g_pipe[kMaxDevices];
+
+int host_pipe(HostPipe** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_LAUNCH;
+  if (dev < 0 || dev >= kMaxDevices) return MHA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  HostPipe& hp = g_pipe[dev];
+  if (!hp.ready) {
+    for (int i = 0; i < 2; ++i) {
+      if (!hp.st[i] && cudaStreamCreateWithFlags(&hp.st[i], cudaStreamNonBlocking) != cudaSuccess)
+        return MHA_ERR_LAUNCH;
+      if (!hp.done[i] &&
+          cudaEventCreateWithFlags(&hp.done[i], cudaEventDisableTiming) != cudaSuccess)
+        return MHA_ERR_LAUNCH;
+    }
+    if (!hp.start && cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) != cudaSuccess)
+      return MHA_ERR_LAUNCH;
+    hp.ready = true;
+  }
+  *out = &hp;
+  return MHA_OK;
+}
 thread_local mha::LaunchInfo t_info;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -688,6 +719,8 @@ int mha_fwd_host(const void* q, const void* k, const void* v, void* out, int B, 
   if (!q || !out || (kb > 0 && (!k || !v))) return MHA_ERR_NULL;
   if (!mask_known(mask_kind)) return MHA_ERR_MASK;
   if (has_padding(mask_kind) && !key_lens) return MHA_ERR_MASK;
+  HostPipe* pipe = nullptr;
+  if (host_pipe(&pipe) != MHA_OK) return MHA_ERR_LAUNCH;
   uint8_t* w = static_cast<uint8_t*>(workspace);
   uint8_t* dq = w;
   uint8_t* dk = dq + align256(qb);
@@ -695,12 +728,6 @@ int mha_fwd_host(const void* q, const void* k, const void* v, void* out, int B, 
   uint8_t* dout = dv + align256(kb);
   int32_t* dlens = reinterpret_cast<int32_t*>(dout + align256(qb));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(dq, q, qb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MHA_ERR_LAUNCH;
-  if (kb > 0) {
-    if (cudaMemcpyAsync(dk, k, kb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(dv, v, kb, cudaMemcpyHostToDevice, s) != cudaSuccess)
-      return MHA_ERR_LAUNCH;
-  }
   const int32_t* lens = nullptr;
   if (has_padding(mask_kind)) {
     if (cudaMemcpyAsync(dlens, key_lens, static_cast<size_t>(B) * 4, cudaMemcpyHostToDevice, s) !=
@@ -708,17 +735,59 @@ int mha_fwd_host(const void* q, const void* k, const void* v, void* out, int B, 
       return MHA_ERR_LAUNCH;
     lens = dlens;
   }
-  const int rc = (elem_bytes == 2)
-                     ? mha_fwd(dq, kb ? dk : nullptr, kb ? dv : nullptr, dout, B, H, Lq, Lk, d_k,
-                               mask_kind, lens, scale, stream)
-                     : mha_fwd_f32(dq, kb ? dk : nullptr, kb ? dv : nullptr, dout, B, H, Lq, Lk,
-                                   d_k, mask_kind, lens, scale, stream);
+  // Sequences are independent and each one's rows are contiguous in every
+  // tensor, so the batch goes in chunks of sequences over two streams: the
+  // copies in of one chunk, the kernel of the one before and the copy out of
+  // the one before that overlap.  Both streams start after the work already
+  // on the caller's stream, which waits for both at the end.  Chunks carry at
+  // least 8 MiB of inputs: below that a chunk's own launch costs more than
+  // the overlap saves (measured: 32 sequences of 128 rows, 12.6 MB, took
+  // 168 us in four chunks against 128 us in one).
+  const size_t in_bytes = qb + 2 * kb;
+  long long chunks = static_cast<long long>(in_bytes >> 23);
+  if (chunks > 4) chunks = 4;
+  if (chunks > B) chunks = B;
+  const int n_chunks = chunks < 1 ? 1 : static_cast<int>(chunks);
+  const size_t q_seq = qb / B, k_seq = kb / B;
+  if (cudaEventRecord(pipe->start, s) != cudaSuccess ||
+      cudaStreamWaitEvent(pipe->st[0], pipe->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(pipe->st[1], pipe->start, 0) != cudaSuccess)
+    return MHA_ERR_LAUNCH;
+  int rc = MHA_OK;
+  for (int c = 0; c < n_chunks && rc == MHA_OK; ++c) {
+    const int b0 = static_cast<int>(static_cast<long long>(B) * c / n_chunks);
+    const int b1 = static_cast<int>(static_cast<long long>(B) * (c + 1) / n_chunks);
+    const int nb = b1 - b0;
+    cudaStream_t x = pipe->st[c & 1];
+    const size_t qo = q_seq * b0, ko = k_seq * b0;
+    if (cudaMemcpyAsync(dq + qo, static_cast<const uint8_t*>(q) + qo, q_seq * nb,
+                        cudaMemcpyHostToDevice, x) != cudaSuccess ||
+        (kb > 0 && (cudaMemcpyAsync(dk + ko, static_cast<const uint8_t*>(k) + ko, k_seq * nb,
+                                    cudaMemcpyHostToDevice, x) != cudaSuccess ||
+                    cudaMemcpyAsync(dv + ko, static_cast<const uint8_t*>(v) + ko, k_seq * nb,
+                                    cudaMemcpyHostToDevice, x) != cudaSuccess))) {
+      rc = MHA_ERR_LAUNCH;
+      break;
+    }
+    rc = (elem_bytes == 2)
+             ? mha_fwd(dq + qo, kb ? dk + ko : nullptr, kb ? dv + ko : nullptr, dout + qo, nb, H, Lq,
+                       Lk, d_k, mask_kind, lens ? lens + b0 : nullptr, scale, x)
+             : mha_fwd_f32(dq + qo, kb ? dk + ko : nullptr, kb ? dv + ko : nullptr, dout + qo, nb,
+                           H, Lq, Lk, d_k, mask_kind, lens ? lens + b0 : nullptr, scale, x);
+    if (rc != MHA_OK) break;
+    if (cudaMemcpyAsync(static_cast<uint8_t*>(out) + qo, dout + qo, q_seq * nb,
+                        cudaMemcpyDeviceToHost, x) != cudaSuccess)
+      rc = MHA_ERR_LAUNCH;
+  }
+  for (int i = 0; i < 2; ++i) {
+    if (cudaEventRecord(pipe->done[i], pipe->st[i]) != cudaSuccess ||
+        cudaStreamWaitEvent(s, pipe->done[i], 0) != cudaSuccess)
+      rc = rc == MHA_OK ? MHA_ERR_LAUNCH : rc;
+  }
   if (rc != MHA_OK) {
     cudaStreamSynchronize(s);
     return rc;
   }
-  if (cudaMemcpyAsync(out, dout, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return MHA_ERR_LAUNCH;
   return mha_sync_status(stream);
 }
 
