@@ -58,7 +58,6 @@ struct BwdCfg {
   // tmem slot (+0), abort flag (+4), unit queue (+8, +12), cancellation
   // response (+16, 16 bytes, 16-byte aligned)
   static constexpr int OFF_MISC = (OFF_BAR + 8 * NBAR + 15) / 16 * 16;
-  static constexpr int SMEM = OFF_MISC + 32 + 1024;
   // the dQ kernel also stages the forward output O (for D = dO . O)
   static constexpr int OFF_O = (OFF_MISC + 32 + 1023) / 1024 * 1024;
   static constexpr int SMEM_DQ = OFF_O + TILE + 1024;
@@ -68,7 +67,6 @@ struct BwdCfg {
   static constexpr int OFF_STG = OFF_O;
   static constexpr int SMEM_DKDV = OFF_STG + 2 * CHUNK + 1024;
   static_assert(SMEM_DKDV <= 227 * 1024, "shared memory budget (dK/dV)");
-  static_assert(SMEM <= 227 * 1024, "shared memory budget");
   // TMEM: a tile's score-shaped matrices in two halves of 64 columns, half
   // hf at columns 128 hf (S or S^T) and 128 hf + 64 (dP or dP^T); then the
   // d-wide accumulators
@@ -1131,7 +1129,7 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, LaunchInfo* in
     info->kernels = 2;
     info->grid = static_cast<int>(kv_units + q_units);
     info->block = kBwdThreads;
-    info->smem = C::SMEM;
+    info->smem = C::SMEM_DKDV > C::SMEM_DQ ? C::SMEM_DKDV : C::SMEM_DQ;
   }
   return e;
 }
