@@ -35,7 +35,7 @@
 //   warp 8      TMEM allocator and MMA issuer (for Q0 only with d_k = 64)
 //   warp 11     MMA issuer for Q1 (d_k = 64; idle with d_k = 128)
 //   warp 9      TMA producer: Q0, Q1, then K_j / V_j into an NS-stage ring
-//   warp 10     scheduler: feeds a two-slot queue of units to the others
+//   warp 10     scheduler: feeds a two-slot queue of decoded units to the others
 // The third warpgroup gives registers to the softmax warpgroups, which hold
 // a whole 128-score row per thread: launched at 168 per thread, it drops to
 // 112 and they rise to 192 (256*192 + 128*112 = 63488 <= 384*168 registers).
