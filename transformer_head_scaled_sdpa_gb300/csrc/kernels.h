@@ -35,6 +35,8 @@ struct Bf16Params {
   int mask_kind;
   int n_qtiles;      // query blocks per head: ceil(Lq / kUnitRows); the launch
                      // sets ceil(Lq / kBlockM) when it pairs heads
+  int head_group;    // set by the launch: heads whose units are dispatched
+                     // together (their K/V stay in L2); even
   int paired;        // set by the launch: 0 = a unit is two query tiles of one
                      // head sharing every K/V tile; 1 (d_k = 64) = a unit is the
                      // same query tile of two heads, each with its own K/V tiles
@@ -111,6 +113,7 @@ struct BwdParams {
   int mask_kind;
   float scale;        // multiplier of q . k
   float scale_log2;   // scale * log2(e)
+  int head_group;     // set by the launch: heads whose units are dispatched together
 };
 
 // Launches the gradient: the dQ kernel (which also forms D) and the dK/dV kernel.

@@ -97,17 +97,20 @@ __device__ __forceinline__ constexpr uint32_t a_col(int ks) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// CTA order: groups of kBwdHeadGroup heads, so the tiles a group's CTAs all
+// CTA order: groups of p.head_group heads, so the tiles a group's CTAs all
 // stream (Q and dO, or K and V) stay in L2 while the group runs; inside a group
 // the tile index t runs over all of the group's heads before moving on, which
 // puts the heavy causal tiles of every head first and leaves the grid a light
 // tail.  Returns t (0 = the first launched) and sets *bh.
-constexpr int kBwdHeadGroup = 32;
-__device__ __forceinline__ int bwd_unit(int unit, int n_t, int bh_count, int* bh) {
-  const int group = unit / (kBwdHeadGroup * n_t);
-  const int within = unit - group * kBwdHeadGroup * n_t;
-  const int here = min(kBwdHeadGroup, bh_count - group * kBwdHeadGroup);
-  *bh = group * kBwdHeadGroup + within % here;
+// The group holds about kBwdHeadGroupBytes of the streamed tiles (measured:
+// 32 heads suit the GPT-3-like gradient and 64 big16 L 2048, 1 MiB and
+// 512 KiB of Q and dO per head).
+constexpr long long kBwdHeadGroupBytes = 32ll << 20;
+__device__ __forceinline__ int bwd_unit(int unit, int n_t, int bh_count, int hg, int* bh) {
+  const int group = unit / (hg * n_t);
+  const int within = unit - group * hg * n_t;
+  const int here = min(hg, bh_count - group * hg);
+  *bh = group * hg + within % here;
   return within / here;
 }
 
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
   auto decode = [&](int unit) {
     KvUnit u;
     int bh = 0;
-    const int kt = bwd_unit(unit, n_kt, p.B * p.H, &bh);
+    const int kt = bwd_unit(unit, n_kt, p.B * p.H, p.head_group, &bh);
     u.b = bh / p.H;
     u.h = bh % p.H;
     u.k0 = kt * 128;
@@ -708,7 +711,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
   auto decode = [&](int unit) {
     QUnit u;
     int bh = 0;
-    u.qt = n_qt - 1 - bwd_unit(unit, n_qt, p.B * p.H, &bh);
+    u.qt = n_qt - 1 - bwd_unit(unit, n_qt, p.B * p.H, p.head_group, &bh);
     u.b = bh / p.H;
     u.h = bh % p.H;
     u.q0 = u.qt * 128;
@@ -1136,7 +1139,18 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream, LaunchInfo* in
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdParams& p, int d, cudaStream_t stream, LaunchInfo* info) {
+cudaError_t launch_bwd(const BwdParams& params, int d, cudaStream_t stream, LaunchInfo* info) {
+  BwdParams p = params;
+  {
+    // bytes of the two tiles a head streams (Q and dO, or K and V)
+    const long long L = p.Lq > p.Lk ? p.Lq : p.Lk;
+    const long long per_head = 2ll * L * d * 2 > 0 ? 2ll * L * d * 2 : 1;
+    long long hg = kBwdHeadGroupBytes / per_head;
+    const long long bh = static_cast<long long>(p.B) * p.H;
+    if (hg > bh) hg = bh;
+    if (hg < 1) hg = 1;
+    p.head_group = static_cast<int>(hg);
+  }
   if (d == 64) return launch_bwd_d<64>(p, stream, info);
   if (d == 128) return launch_bwd_d<128>(p, stream, info);
   return cudaErrorInvalidValue;
