@@ -67,11 +67,12 @@ constexpr int kSoftmaxWarp0 = 0;
 constexpr int kMmaWarp = 8, kProducerWarp = 9, kMma1Warp = 11;  // warp 10: scheduler
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p stays <= 2^8
 // Heads dispatched together are chosen by their K/V bytes, about this much
-// per group, so a group's K/V stay in L2 while its query blocks run.
-// (Measured against a fixed 32 heads: 64 MiB made the GPT-3-like causal
-// forward 2 % and big16 L 2048 causal 13 % faster; 128 MiB another 2 % on the
-// GPT-3-like workload and 1 % slower on base8 L 4096 without the mask.)
-constexpr long long kHeadGroupBytes = 128ll << 20;
+// per group, so a group's K/V stay in L2 while its query blocks run (32 heads
+// of the GPT-3-like shape, 64 of big16 L 2048, every head of the base-model
+// shapes).  Larger groups were faster in short runs (128 MiB: GPT-3-like +4 %
+// at full clock) but doubled that kernel's DRAM reads, and under the power cap
+// a 2000-step run lost 5 % to the lower clock.
+constexpr long long kHeadGroupBytes = 32ll << 20;
 // unit-queue readers: 8 softmax warps, the producer and 1 or 2 MMA warps
 template <int D>
 constexpr int unit_consumers() { return D == 64 ? 11 : 10; }
