@@ -171,7 +171,8 @@ int mha_fwd_f32_dv(const void* q, const void* k, const void* v, void* out, float
  *     dq_i = scale sum_j dS_ij k_j
  * over the visible (query, key) pairs of mask_kind / key_lens; keys no query
  * sees get zero gradient.
- *   q, k, v, out  the forward's inputs and output (bf16, layouts of mha_fwd).
+ *   q, k, v, out  the forward's inputs and output (bf16, layouts of mha_fwd),
+ *                 16-byte aligned (out is read by TMA to form D).
  *   dout          device bf16 [B, Lq, H, d_k], 16-byte aligned.
  *   lse           device float32 [B, H, Lq] from mha_fwd_lse on the same inputs.
  *   dq, dk, dv    device bf16 in the layouts of q, k, v, 16-byte aligned;
