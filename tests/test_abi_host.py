@@ -172,8 +172,8 @@ def test_decode_entry_errors(lib):
 DOUT, DQ, DK, DVG = 0x80000000, 0x90000000, 0xA0000000, 0xB0000000
 
 
-def bwd(lib, d=64, mask=0, lens=None, lse=LSE, ws=WS, ws_bytes=1 << 20):
-    return lib.mha_bwd(Q, K, V, O, DOUT, lse, DQ, DK, DVG, 2, 3, 64, 64, d, mask, lens, 0.0, ws,
+def bwd(lib, d=64, mask=0, lens=None, lse=LSE, ws=WS, ws_bytes=1 << 20, out=O, dk=DK):
+    return lib.mha_bwd(Q, K, V, out, DOUT, lse, DQ, dk, DVG, 2, 3, 64, 64, d, mask, lens, 0.0, ws,
                        ws_bytes, None)
 
 
@@ -184,6 +184,8 @@ def test_bwd_entry_errors(lib):
     assert bwd(lib, mask=3) == MASK           # both masks need key_lens
     assert bwd(lib, lse=None) == NULL
     assert bwd(lib, ws=None) == WORKSPACE
+    assert bwd(lib, out=O + 8) == UNSUP       # out and dk/dv are read / written by TMA
+    assert bwd(lib, dk=DK + 8) == UNSUP
     assert lib.mha_bwd_workspace_bytes(2, 3, 64, 64, 96) > 0
     assert lib.mha_bwd_workspace_bytes(2, 3, 64, 64, 12) == 0
 
