@@ -178,7 +178,8 @@ int mha_fwd_f32_dv(const void* q, const void* k, const void* v, void* out, float
  *   dq, dk, dv    device bf16 in the layouts of q, k, v, 16-byte aligned;
  *                 overlapping no input and each other (MHA_ERR_ALIAS).
  *   workspace     device scratch of mha_bwd_workspace_bytes(...) bytes
- *                 (D_i, float32), 16-byte aligned, owned by the caller.
+ *                 (D_i, float32), 16-byte aligned, owned by the caller;
+ *                 overlaps no other argument (MHA_ERR_ALIAS).
  *   Other arguments as mha_fwd (d_v = d_k, any mask kind); d_k a multiple of
  *   8 from 8 to 128.
  * Products on the tensor cores in float32; the weights and dS are rounded to
@@ -242,7 +243,8 @@ size_t mha_decode_workspace_bytes(int B, int H, int Lk, int d_k);
  *   sizes would need more than the array holds (never for d_k <= 128: the
  *   split count keeps the partials under 1215 rows of d_k + 2 floats).
  *   Nothing in the array has to start at zero: each call's split kernel
- *   writes every partial its combine kernel reads.
+ *   writes every partial its combine kernel reads (a split that gives up on
+ *   a time-out writes an empty partial, which the combine skips).
  *   Every call on a device shares the one array: calls that overlap in time
  *   (on different streams or host threads) race and give undefined results;
  *   serialise them, or use mha_decode with a workspace per stream.
@@ -303,7 +305,11 @@ size_t mha_fwd_host_workspace_bytes(int B, int H, int Lq, int Lk, int d_k,
  * copies out of consecutive chunks overlap; the internal streams start after
  * the work already queued on `stream`, which waits for them.  The first call
  * on a device creates those two streams and three events, kept for the
- * process.  Host buffers should be page-locked for the copies to be
+ * process.  Calls from several host threads at once are safe: each call
+ * holds a per-device lock while it queues its work on the shared internal
+ * streams, so concurrent calls run one after the other on the device (use
+ * mha_fwd on streams of your own to overlap them).  Each call needs its own
+ * workspace.  Host buffers should be page-locked for the copies to be
  * asynchronous.  Returns the argument check's code, MHA_ERR_WORKSPACE,
  * MHA_ERR_LAUNCH, or the device status (as mha_sync_status).
  */

@@ -186,6 +186,8 @@ def test_bwd_entry_errors(lib):
     assert bwd(lib, ws=None) == WORKSPACE
     assert bwd(lib, out=O + 8) == UNSUP       # out and dk/dv are read / written by TMA
     assert bwd(lib, dk=DK + 8) == UNSUP
+    assert bwd(lib, ws=Q) == ALIAS            # the workspace overlaps an input
+    assert bwd(lib, ws=DQ + 256) == ALIAS     # ... or a gradient
     assert lib.mha_bwd_workspace_bytes(2, 3, 64, 64, 96) > 0
     assert lib.mha_bwd_workspace_bytes(2, 3, 64, 64, 12) == 0
 

@@ -39,11 +39,16 @@ int g_withhold_p = 0;  // test hook of mha_debug_withhold_p
 DeviceState g_dev[kMaxDevices];
 
 // The host entry's two streams and its events, created on the device's
-// first mha_fwd_host call and kept for the process.
+// first mha_fwd_host call and kept for the process.  `order` is held while a
+// call records `start` and queues its chunks, so two host threads calling at
+// once cannot re-record each other's start event (the internal streams would
+// then wait on the other caller's stream) or interleave chunks on the shared
+// streams.
 struct HostPipe {
   bool ready = false;
   cudaStream_t st[2] = {nullptr, nullptr};
   cudaEvent_t start = nullptr, done[2] = {nullptr, nullptr};
+  std::mutex order;
 };
 HostPipe g_pipe[kMaxDevices];
 
@@ -549,6 +554,13 @@ int mha_bwd(const void* q, const void* k, const void* v, const void* out, const 
   if (Lq > 0 && Lk > 0 && (!workspace || workspace_bytes < need ||
                             (reinterpret_cast<uintptr_t>(workspace) & 15u)))
     return MHA_ERR_WORKSPACE;
+  // the workspace (D_i, written by the first kernel) overlaps no argument
+  if (Lq > 0 && Lk > 0) {
+    for (int i = 0; i < 6; ++i)
+      if (overlaps(workspace, need, ins[i], ins_b[i])) return MHA_ERR_ALIAS;
+    for (int o = 0; o < 3; ++o)
+      if (overlaps(workspace, need, outs[o], outs_b[o])) return MHA_ERR_ALIAS;
+  }
   DeviceState* dev = nullptr;
   rc = device_state(&dev);
   if (rc != MHA_OK) return rc;
@@ -749,6 +761,7 @@ int mha_fwd_host(const void* q, const void* k, const void* v, void* out, int B, 
   if (chunks > B) chunks = B;
   const int n_chunks = chunks < 1 ? 1 : static_cast<int>(chunks);
   const size_t q_seq = qb / B, k_seq = kb / B;
+  std::unique_lock<std::mutex> queued(pipe->order);
   if (cudaEventRecord(pipe->start, s) != cudaSuccess ||
       cudaStreamWaitEvent(pipe->st[0], pipe->start, 0) != cudaSuccess ||
       cudaStreamWaitEvent(pipe->st[1], pipe->start, 0) != cudaSuccess)
@@ -784,6 +797,7 @@ int mha_fwd_host(const void* q, const void* k, const void* v, void* out, int B, 
         cudaStreamWaitEvent(s, pipe->done[i], 0) != cudaSuccess)
       rc = rc == MHA_OK ? MHA_ERR_LAUNCH : rc;
   }
+  queued.unlock();
   if (rc != MHA_OK) {
     cudaStreamSynchronize(s);
     return rc;

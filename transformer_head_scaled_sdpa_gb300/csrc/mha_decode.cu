@@ -234,9 +234,20 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
     if (lane == 0) mbar_arrive(empty(s));
   }
 
+  // A CTA that gives up still marks its split's partial as empty (maximum
+  // -inf, sum 0), so the combine kernel skips it instead of blending in
+  // whatever an earlier call left in the workspace; the status word records
+  // the time-out and the output is undefined.
+  auto mark_empty = [&]() {
+    if (p.n_splits > 1 && lane == 0) {
+      p.part_m[static_cast<size_t>(split) * p.B * p.H + bh] = -INFINITY;
+      p.part_l[static_cast<size_t>(split) * p.B * p.H + bh] = 0.f;
+    }
+  };
   // ---- merge the four warps (named barrier 1 over the compute warps only)
   if (!ok) {
-    // giving up: let the other compute warps pass the barrier; nothing is stored
+    // giving up: let the other compute warps pass the barrier; no output
+    mark_empty();
     named_barrier_arrive(1, 32 * kDecWarps);
     return;
   }
@@ -249,7 +260,10 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
 #pragma unroll
   for (int e = 0; e < EPL; ++e) red[2 * kDecWarps + warp * D + EPL * lane + e] = acc[e];
   named_barrier(1, 32 * kDecWarps);
-  if (*abort_flag) return;
+  if (*abort_flag) {
+    mark_empty();
+    return;
+  }
   float M = -INFINITY;
 #pragma unroll
   for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, red[w]);
