@@ -15,7 +15,15 @@ no step finds its inputs in L2.
 
 Metric: attention forward TFLOP/s, FLOPs = 4*B*H*Lq*Lk*d_k (halved under the
 causal mask), bf16 inputs, float32 accumulation; also reported as a fraction
-of the measured dense bf16 tensor peak.  The default workload is the GPT-3-like
+of the measured dense bf16 tensor peak.  The roofline fraction counts the
+(query, visible key) pairs (L(L+1)/2 per head under the causal mask, the drawn
+key lengths under key padding), reported beside as ``value_algorithmic``.
+
+The default forward run also times every configuration of the target
+specification and the supplementary d_k = 64, L >= 2048 shapes (``configs``:
+TFLOP/s, fraction of the tensor peak, GB/s of algorithmic bytes and fraction of
+the HBM bandwidth, and the oracle's rate on all host cores and, for the three
+smallest, on one core); ``--no-sweep`` skips it.  The default workload is the GPT-3-like
 causal self-attention (B 4, H 96, d_k 128, L 2048): the only L >= 2048 shape of
 the five the pages suggest, and the one the throughput target is quoted on.
 
@@ -276,23 +284,26 @@ def kernel_fingerprint(kernel: str = "fwd_bf16_kernel") -> str:
     return h.hexdigest()
 
 
-def cpu_baseline(w, case, budget_s=12.0):
+def cpu_baseline(w, case, budget_s=12.0, threads=None, min_s=0.0):
     """The oracle, as it stands, on a bounded sample of whole heads of the
-    workload; returns TFLOP/s of algorithmic work and the sample description."""
+    workload (cycling over the heads again while less than ``min_s`` seconds
+    have passed, for workloads that take microseconds); returns TFLOP/s of
+    algorithmic work and the sample description.  ``threads`` None: every
+    core the process may use."""
     import oracle
-    cores = oracle.default_threads()
+    cores = oracle.default_threads() if threads is None else threads
     done_pairs = 0.0
     heads = 0
     t0 = time.perf_counter()
     b_h = [(b, h) for b in range(w.B) for h in range(w.H)]
-    while heads < len(b_h):
-        b, h = b_h[heads]
+    one = inputs.Workload(w.name, 1, 1, w.d_k, w.Lq, w.Lk, w.mask_kind, w.dtype)
+    while heads < len(b_h) or time.perf_counter() - t0 < min_s:
+        b, h = b_h[heads % len(b_h)]
         sub = {n: case[n][b:b + 1, :, h:h + 1] for n in ("q", "k", "v")}
         lens = case["key_lens"][b:b + 1] if case["key_lens"] is not None else None
         oracle.mha(sub["q"], sub["k"], sub["v"], w.mask_kind,
-                   key_lens=lens.numpy() if lens is not None else None)
+                   key_lens=lens.numpy() if lens is not None else None, threads=threads)
         heads += 1
-        one = inputs.Workload(w.name, 1, 1, w.d_k, w.Lq, w.Lk, w.mask_kind, w.dtype)
         done_pairs += visible_pairs(one, lens)
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -300,8 +311,144 @@ def cpu_baseline(w, case, budget_s=12.0):
     flops = 4.0 * w.d_k * done_pairs
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{heads} whole (b, h) heads of {w.name} ({w.Lq}x{w.Lk}, d_k {w.d_k}, "
-                      f"{inputs.MASK_NAMES[w.mask_kind]}) in float64, {dt:.1f} s wall",
-            "seconds": dt}
+                      f"{inputs.MASK_NAMES[w.mask_kind]}) in float64, {dt:.2f} s wall",
+            "seconds": dt, "seconds_per_step": dt * w.B * w.H / heads}
+
+
+def forward_sets(w, case, dev):
+    """The workload's inputs on the device, rotated over enough copies that
+    consecutive steps never find their inputs in L2 (when one set fits)."""
+    q, k, v = (case[n].to(dev) for n in ("q", "k", "v"))
+    out = torch.empty_like(q)
+    bytes_in = sum(t.numel() * t.element_size() for t in (q, k, v))
+    n_sets = 1 if bytes_in > L2_BYTES else -(-2 * L2_BYTES // bytes_in)
+    sets = [(q, k, v, out)] + [tuple(t.clone() for t in (q, k, v, out))
+                              for _ in range(n_sets - 1)]
+    return sets, bytes_in
+
+
+def measure_forward(w, case, args, dev, stream, rank, steps, warmup):
+    """Time `steps` forward calls of the workload (after `warmup`), inputs
+    resident; returns (kernel ms per step, max-over-ranks total ms, clocks,
+    launches per step, input bytes, sets rotated)."""
+    from transformer_head_scaled_sdpa_gb300 import binding
+    lens = case["key_lens"].to(dev) if case["key_lens"] is not None else None
+    sets, bytes_in = forward_sets(w, case, dev)
+    cur = [0]
+    fwd = binding.mha_fwd if w.dtype == torch.bfloat16 else binding.mha_fwd_f32
+
+    def step():
+        qq, kk, vv, oo = sets[cur[0] % len(sets)]
+        cur[0] += 1
+        fwd(qq, kk, vv, out=oo, mask_kind=w.mask_kind, key_lens=lens, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    rc = binding.mha_sync_status(stream)
+    if rc != 0:
+        raise binding.MhaError(rc, f"warm-up of {w.name}")
+    launches = binding.last_launch_info()["kernels"]
+    timing = argparse.Namespace(steps=steps, warmup=0, eager=args.eager)
+    kernel_ms, max_total_ms, clocks = timed_steps(step, timing, dev, stream, rank, warm=False)
+    rc = binding.mha_sync_status(stream)
+    if rc != 0:
+        raise binding.MhaError(rc, f"timed region of {w.name}")
+    del sets
+    return kernel_ms, max_total_ms, clocks, launches, bytes_in
+
+
+def host_link(dev, stream, nbytes=256 << 20, reps=3):
+    """Pinned host <-> device copy bandwidth (GB/s): each direction alone and
+    both at once (two streams), best of `reps`; the ceiling of the e2e path."""
+    h_src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_dst = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_b = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    other = torch.cuda.Stream(device=dev)
+
+    def best(fn):
+        t = []
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(dev)
+            t.append(time.perf_counter() - t0)
+        return min(t)
+
+    def h2d():
+        with torch.cuda.stream(stream):
+            d_a.copy_(h_src, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(stream):
+            h_dst.copy_(d_b, non_blocking=True)
+
+    def both():
+        with torch.cuda.stream(stream):
+            d_a.copy_(h_src, non_blocking=True)
+        with torch.cuda.stream(other):
+            h_dst.copy_(d_b, non_blocking=True)
+
+    h2d()
+    d2h()
+    r = {"h2d_gbs": nbytes / best(h2d) / 1e9, "d2h_gbs": nbytes / best(d2h) / 1e9,
+         "both_gbs": 2 * nbytes / best(both) / 1e9, "bytes": nbytes,
+         "how": "pinned torch copies on two streams, wall clock after synchronize, best of 3"}
+    del h_src, h_dst, d_a, d_b
+    return r
+
+
+# Every configuration of the target specification plus the supplementary
+# d_k = 64, L >= 2048 shapes, with and without the causal mask: the default
+# run times each one (the headline workload is measured once, above).
+SWEEP = ["toy_cross_f32", "base_encoder_self", "base_decoder_causal", "base_cross_keypad",
+         "gpt3_causal", "big16_L2048", "big16_L2048_causal", "base8_L4096",
+         "base8_L4096_causal"]
+# the configurations whose oracle is also timed on a single core
+ONE_CORE = {"toy_cross_f32", "base_encoder_self", "base_decoder_causal"}
+
+
+def config_record(w, case, kernel_ms, launches, peaks, with_oracle):
+    """One sweep row: nominal and algorithmic TFLOP/s, fractions of the
+    measured tensor and HBM peaks, and the oracle's rate on the host cores."""
+    pairs = visible_pairs(w, case["key_lens"])
+    flops_alg = 4.0 * w.d_k * pairs
+    flops_nom = w.flops()
+    elem = 2 if w.dtype == torch.bfloat16 else 4
+    # Q and O once, K and V once over the keys any query sees
+    if w.mask_kind & inputs.MASK_KEY_PADDING:
+        kv_rows = float(case["key_lens"].clamp(0, w.Lk).sum().item())
+    else:
+        kv_rows = float(w.B * w.Lk)
+    bytes_alg = elem * w.H * w.d_k * (2.0 * w.B * w.Lq + 2.0 * kv_rows)
+    tensor_peak = float(peaks["bf16_tflops"])
+    hbm = float(peaks["hbm_gbs"])
+    sec = kernel_ms * 1e-3
+    rec = {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d_k": w.d_k,
+           "mask": inputs.MASK_NAMES[w.mask_kind],
+           "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+           "us_per_step": kernel_ms * 1e3, "launches_per_step": launches,
+           "tflops": flops_nom / sec / 1e12,
+           "tflops_algorithmic": flops_alg / sec / 1e12,
+           "frac_tensor_peak": (flops_alg / sec / 1e12 / tensor_peak
+                                if w.dtype == torch.bfloat16 else None),
+           "gbs": bytes_alg / sec / 1e9, "frac_hbm": bytes_alg / sec / 1e9 / hbm,
+           "algorithmic_bytes": bytes_alg,
+           "bound": ("alu" if w.dtype != torch.bfloat16 else
+                     "tensor" if flops_alg / bytes_alg > tensor_peak * 1e3 / hbm else "hbm")}
+    if w.dtype != torch.bfloat16:
+        rec["frac_alu_peak"] = flops_alg / sec / 1e12 / F32_ALU_TFLOPS
+    if with_oracle:
+        o = cpu_baseline(w, case, budget_s=2.0, min_s=0.5)
+        rec["oracle_all_cores"] = {k: o[k] for k in ("value", "unit", "cores", "sample",
+                                                     "seconds_per_step")}
+        if w.name in ONE_CORE:
+            o1 = cpu_baseline(w, case, budget_s=2.0, threads=1, min_s=0.5)
+            rec["oracle_one_core"] = {k: o1[k] for k in ("value", "unit", "cores", "sample",
+                                                         "seconds_per_step")}
+    return rec
 
 
 def run_ours(args):
@@ -316,42 +463,18 @@ def run_ours(args):
     build.build()  # no-op once built; loads on every rank
     w = inputs.BY_NAME[args.workload]
     case = inputs.generate(w, seed=mdist.rank_seed(w.seed, rank))
-    q, k, v = (case[n].to(dev) for n in ("q", "k", "v"))
-    lens = case["key_lens"].to(dev) if case["key_lens"] is not None else None
-    out = torch.empty_like(q)
     stream = torch.cuda.Stream(device=dev)
     pairs = visible_pairs(w, case["key_lens"])
     flops_alg = 4.0 * w.d_k * pairs                 # per launch, this rank
-    flops_nominal = w.flops()
-    bytes_in = sum(t.numel() * t.element_size() for t in (q, k, v))
-    bytes_alg = bytes_in + out.numel() * out.element_size()
-    # Consecutive steps must not find their inputs in L2: when one set of
-    # inputs fits in L2, steps rotate over enough copies to exceed it twice.
+    flops_nominal = w.flops()                       # 4 B H Lq Lk d_k, halved if causal
+    elem = 2 if w.dtype == torch.bfloat16 else 4
+    bytes_alg = elem * w.B * w.H * w.d_k * (2 * w.Lq + 2 * w.Lk)
+
+    kernel_ms, max_total_ms, clocks, launches_per_step, bytes_in = measure_forward(
+        w, case, args, dev, stream, rank, args.steps, args.warmup)
     n_sets = 1 if bytes_in > L2_BYTES else -(-2 * L2_BYTES // bytes_in)
-    sets = [(q, k, v, out)] + [tuple(t.clone() for t in (q, k, v, out))
-                              for _ in range(n_sets - 1)]
-    cur = [0]
-
-    fwd = binding.mha_fwd if w.dtype == torch.bfloat16 else binding.mha_fwd_f32
-
-    def step():
-        qq, kk, vv, oo = sets[cur[0] % n_sets]
-        cur[0] += 1
-        fwd(qq, kk, vv, out=oo, mask_kind=w.mask_kind, key_lens=lens, stream=stream)
-
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
-    rc = binding.mha_sync_status(stream)
-    if rc != 0:
-        raise binding.MhaError(rc, "warm-up")
-    launches_per_step = binding.last_launch_info()["kernels"]
-
-    kernel_ms, max_total_ms, clocks = timed_steps(step, args, dev, stream, rank, warm=False)
-    rc = binding.mha_sync_status(stream)
-    if rc != 0:
-        raise binding.MhaError(rc, "timed region")
-    total_flops = mdist.sum_over_ranks(flops_alg * args.steps, dev)
+    total_flops = mdist.sum_over_ranks(flops_nominal * args.steps, dev)
+    total_flops_alg = mdist.sum_over_ranks(flops_alg * args.steps, dev)
 
     # end to end: pinned host buffers through the C ABI's host entry
     e2e = None
@@ -359,8 +482,7 @@ def run_ours(args):
         hq, hk, hv = (case[n].pin_memory() for n in ("q", "k", "v"))
         hout = torch.empty_like(hq).pin_memory()
         hlens = case["key_lens"].pin_memory() if case["key_lens"] is not None else None
-        ws = torch.empty(binding.host_workspace_bytes(w.B, w.H, w.Lq, w.Lk, w.d_k,
-                                                      q.element_size()),
+        ws = torch.empty(binding.host_workspace_bytes(w.B, w.H, w.Lq, w.Lk, w.d_k, elem),
                          dtype=torch.uint8, device=dev)
         n_e2e = max(3, min(args.steps, 10))
         for _ in range(2):
@@ -377,12 +499,19 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = mdist.max_over_ranks(e0.elapsed_time(e1) / n_e2e, dev)
-        e2e_flops = mdist.sum_over_ranks(flops_alg, dev)
+        e2e_flops = mdist.sum_over_ranks(flops_nominal, dev)
         h2d = bytes_in + (hlens.numel() * 4 if hlens is not None else 0)
         e2e = {"value": e2e_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * 2),
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * elem),
                "steps": n_e2e, "ms_per_step": e2e_ms,
                "path": "mha_fwd_host (C ABI): pinned host q,k,v -> device, kernel, out -> host"}
+        del ws
+        if rank == 0:
+            link = host_link(dev, stream)
+            e2e["host_link"] = link
+            moved = (h2d + hout.numel() * elem) / (e2e_ms * 1e-3) / 1e9
+            e2e["host_gbs"] = moved
+            e2e["frac_host_link_both"] = moved / link["both_gbs"]
 
     if rank != 0:
         mdist.finish()
@@ -402,8 +531,12 @@ def run_ours(args):
             "parallelism": f"replicas x{world} (no collective)",
             "inputs_exceed_l2": bytes_in * n_sets > L2_BYTES, "l2_flush": False,
             "input_sets_rotated": n_sets,
-            "flops_per_step_per_gpu": flops_alg, "flops_nominal_per_step_per_gpu": flops_nominal,
+            "flops": "value: nominal 4*B*H*Lq*Lk*d_k (halved under the causal mask); "
+                     "roofline: the (query, visible key) pairs",
+            "flops_nominal_per_step_per_gpu": flops_nominal,
+            "flops_algorithmic_per_step_per_gpu": flops_alg,
             **timing_config(args)}),
+        "value_algorithmic": total_flops_alg / (max_total_ms * 1e-3) / 1e12,
         "pct_of_peak": 100.0 * value / world / peak,
         "pct_of_sustained_peak": 100.0 * value / world / float(
             peaks.get("bf16_tflops_sustained", peak)),
@@ -428,6 +561,22 @@ def run_ours(args):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, case)
+    if world == 1 and not args.no_sweep:
+        # every configuration, each timed the same way (graph of >= 50 steps)
+        rows = []
+        sweep_steps = max(args.steps, 50)
+        for name in SWEEP:
+            wc = inputs.BY_NAME[name]
+            if name == w.name:
+                rows.append(config_record(wc, case, kernel_ms, launches_per_step, peaks,
+                                          not args.no_cpu_baseline))
+                continue
+            c = inputs.generate(wc)
+            k_ms, _, _, launches, _ = measure_forward(wc, c, args, dev, stream, rank,
+                                                      sweep_steps, args.warmup)
+            rows.append(config_record(wc, c, k_ms, launches, peaks, not args.no_cpu_baseline))
+            del c
+        line["configs"] = rows
     print(json.dumps(line), flush=True)
     mdist.finish()
 
@@ -1029,6 +1178,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the per-configuration sweep of the default forward run")
     ap.add_argument("--eager", action="store_true",
                     help="issue the timed steps one by one instead of replaying a CUDA graph")
     args = ap.parse_args()
