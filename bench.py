@@ -840,8 +840,9 @@ BWD_METRIC = "attention bwd TFLOP/s (bf16, 1 GB300; 2.5x forward flops) and % of
 # ---------------------------------------------------------------------------
 # the multi-head layer (projections around the attention)
 # ---------------------------------------------------------------------------
-LAYER_METRIC = ("multi-head attention layer TFLOP/s (bf16 Q/K/V and W^O projections on cuBLASLt "
-                "+ the attention kernel, 1 GB300) and % of measured dense bf16 peak")
+LAYER_METRIC = ("multi-head attention layer TFLOP/s (bf16 Q/K/V and W^O projections on the "
+                "library's tcgen05 GEMM + the attention kernel, 1 GB300) and % of measured dense "
+                "bf16 peak")
 
 
 def layer_sample(w, case, rows):
@@ -965,7 +966,7 @@ def run_layer(args):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "traffic": None,
                      "peak_source": f"{peak_src} dense bf16 (burst)",
-                     "kernel": "cuBLASLt projection GEMMs + fwd_bf16_kernel (whole step)",
+                     "kernel": "gemm_bf16_kernel projections + fwd_bf16_kernel (whole step)",
                      "kernel_ms": step_ms},
         "clocks": clocks,
         "e2e": {"value": e2e_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
@@ -973,7 +974,7 @@ def run_layer(args):
                 "d2h_bytes_per_step": int(hy.numel() * 2), "steps": n_e2e, "ms_per_step": e2e_ms,
                 "path": "pinned host x (and mem) -> device, mha_layer_fwd with resident weights, "
                         "y -> host"},
-        # this library's own kernels: the attention (the GEMMs are cuBLASLt's)
+        # this library's own kernels: the projection GEMMs and the attention
         "gpu_launches": int(launches_per_step * args.steps),
     }
     if world == 1 and not args.no_cpu_baseline:

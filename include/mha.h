@@ -88,10 +88,13 @@ typedef enum {
  *             even from float32 accumulators.
  *   B, H, Lq, Lk   sizes >= 0.  B*H*Lq == 0 is a no-op returning MHA_OK;
  *             Lk == 0 writes zeros.  k and v may be NULL when Lk == 0.
- *   d_k       a multiple of 8 from 8 to 128 (64 and 128 are the kernels'
- *             widths; other sizes run on the next wider kernel, the tensor
- *             maps reading the missing features as 0 and writing only d_k
- *             output columns).
+ *   d_k       a multiple of 8 from 8 to 256 ("Attention Is All You Need",
+ *             Section 3.2.1, fixes no width).  Heads up to 64 and up to 128
+ *             run on the 64- and 128-wide kernels, which issue only the
+ *             head's own ceil(d_k / 16) K steps and output columns (the
+ *             tensor maps read the missing features as 0 and write only d_k
+ *             columns); wider heads (to 256) run on a kernel of their own
+ *             with 64-key tiles and Q held in tensor memory.
  *   mask_kind one of mha_mask_kind.
  *   key_lens  device pointer to B int32 values, read only when the mask
  *             includes key padding (may be NULL otherwise).
@@ -149,7 +152,7 @@ int mha_fwd_f32_lse(const void* q, const void* k, const void* v, void* out, floa
  *   [B, Lq, H, d_v]; scores use the d_k columns of q and k, the output is the
  *   weighted mean of the d_v columns of v.  scale 0 selects 1/sqrt(d_k).
  *   lse   as mha_fwd_lse, or NULL for none.
- *   bf16: d_k and d_v multiples of 8 from 8 to 128 (both run on the kernel
+ *   bf16: d_k and d_v multiples of 8 from 8 to 256 (both run on the kernel
  *   wide enough for the larger); float32: 1 to 256 each.
  * Other arguments, errors and behaviour as mha_fwd / mha_fwd_f32.
  */
@@ -216,7 +219,9 @@ size_t mha_bwd_workspace_bytes(int B, int H, int Lq, int Lk, int d_k);
  *              log-sum-exp (-inf when cache_lens[b] <= 0).
  *   cache_lens device int32 [B], clamped to [0, Lk]; required (MHA_ERR_MASK
  *              when NULL).  A sequence with no key gets output 0.
- *   d_k        64 or 128.   scale as in mha_fwd (0 selects 1/sqrt(d_k)).
+ *   d_k        a multiple of 8 from 8 to 256 (a head narrower than 64, 128
+ *              or 256 runs on the kernel of that width with the rest of each
+ *              row read as zero).  scale as in mha_fwd (0 selects 1/sqrt(d_k)).
  *   workspace  device scratch of at least mha_decode_workspace_bytes(B, H, Lk,
  *              d_k) bytes, 16-byte aligned, owned by the caller (NULL allowed
  *              when that is 0); not shared with a concurrent call.
@@ -235,13 +240,14 @@ size_t mha_decode_workspace_bytes(int B, int H, int Lk, int d_k);
 
 /*
  * mha_decode_static -- mha_decode without a workspace argument: the split
- * partials go to a fixed device array inside the library (1 MiB per device,
+ * partials go to a fixed device array inside the library (2 MiB per device,
  * mha_decode_static_scratch_bytes()), so the call allocates nothing and needs
  * no scratch from the caller.  Not from the pages: they have no counterpart;
  * it exists for callers that cannot hand over device memory.
  *   Arguments, results and errors as mha_decode; MHA_ERR_WORKSPACE when the
- *   sizes would need more than the array holds (never for d_k <= 128: the
- *   split count keeps the partials under 1215 rows of d_k + 2 floats).
+ *   sizes would need more than the array holds (never for any d_k the decode
+ *   accepts: the split count keeps the partials under 1215 rows of at most
+ *   256 + 2 floats).
  *   Nothing in the array has to start at zero: each call's split kernel
  *   writes every partial its combine kernel reads (a split that gives up on
  *   a time-out writes an empty partial, which the combine skips).
@@ -262,24 +268,25 @@ size_t mha_decode_static_scratch_bytes(void);
  *     y = MultiHead(x, m, m) = Concat(head_1, ..., head_H) W^O,
  *     head_h = Attention(x W_h^Q, m W_h^K, m W_h^V)
  * with m = x (self-attention) when mem is NULL, else the encoder memory
- * (encoder-decoder attention).  The projections are plain GEMMs on cuBLASLt
- * (bf16 operands, float32 accumulation, bf16 results); the attention is
- * mha_fwd's kernel reading the projection output in place (no transposed or
- * split copies: the tensor maps take the packed rows' stride) and writing the
- * heads' concatenation that the W^O GEMM reads.
+ * (encoder-decoder attention).  The projections run on this library's
+ * tensor-core GEMM (mha_gemm_bf16: bf16 operands, float32 accumulation,
+ * bf16 results); the attention is mha_fwd's kernel reading the projection
+ * output in place (no transposed or split copies: the tensor maps take the
+ * packed rows' stride) and writing the heads' concatenation that the W^O
+ * GEMM reads.  Every kernel the layer launches is this library's.
  *   x       device bf16 [B, Lq, d_model], 16-byte aligned.
  *   mem     device bf16 [B, Lk, d_model] or NULL (then Lk must equal Lq).
  *   w_qkv   device bf16 [d_model, 3 H d_k]: W^Q, W^K, W^V side by side, head h
  *           at columns h d_k .. h d_k + d_k - 1 of each block.
  *   w_o     device bf16 [H d_k, d_model].
  *   y       device bf16 [B, Lq, d_model]; overlaps none of the others.
- *   d_model a multiple of 8; d_k as mha_fwd (a multiple of 8 up to 128);
+ *   d_model a multiple of 8; d_k as mha_fwd (a multiple of 8 up to 256);
  *           d_v = d_k.  mask_kind, key_lens, scale as mha_fwd.
  *   workspace  device, mha_layer_workspace_bytes(...) bytes, 256-byte
- *           aligned, owned by the caller (projections, the heads' output and
- *           the GEMM workspace); overlaps no argument.
- * Errors as mha_fwd, MHA_ERR_WORKSPACE for a missing or short workspace,
- * MHA_ERR_LAUNCH when cuBLASLt refuses a GEMM.  Lk == 0 writes zeros.
+ *           aligned, owned by the caller (the projections and the heads'
+ *           output); overlaps no argument.
+ * Errors as mha_fwd, MHA_ERR_WORKSPACE for a missing or short workspace.
+ * Lk == 0 writes zeros.
  */
 int mha_layer_fwd(const void* x, const void* mem, const void* w_qkv, const void* w_o, void* y,
                   int B, int Lq, int Lk, int d_model, int H, int d_k, int mask_kind,
@@ -288,6 +295,20 @@ int mha_layer_fwd(const void* x, const void* mem, const void* w_qkv, const void*
 
 /* mha_layer_workspace_bytes -- workspace mha_layer_fwd needs; 0 on bad sizes. */
 size_t mha_layer_workspace_bytes(int B, int Lq, int Lk, int d_model, int H, int d_k);
+
+/*
+ * mha_gemm_bf16 -- the layer's projection product on the tensor cores
+ * ("Attention Is All You Need", Section 3.2.2: Q W^Q, K W^K, V W^V and
+ * Concat(heads) W^O are plain matrix products):
+ *     c[M x N] = a[M x K] b[K x N]
+ * all row-major bf16 in device memory, float32 accumulation, c rounded to
+ * bf16 (RNE).  lda, ldb, ldc: elements between consecutive rows (>= K, N, N;
+ * multiples of 8); a, b, c 16-byte aligned; c overlaps neither a nor b.
+ * K == 0 writes zeros.  Returns MHA_OK once enqueued, MHA_ERR_SHAPE,
+ * MHA_ERR_NULL, MHA_ERR_UNSUPPORTED (alignment) or MHA_ERR_ALIAS.
+ */
+int mha_gemm_bf16(const void* a, const void* b, void* c, int M, int N, int K, long long lda,
+                  long long ldb, long long ldc, void* stream);
 
 /*
  * mha_fwd_host_workspace_bytes -- device workspace mha_fwd_host needs for

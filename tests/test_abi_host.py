@@ -82,7 +82,8 @@ def test_argument_errors(lib, fn):
 def test_bf16_specific_errors(lib):
     assert fwd(lib, d=12) == UNSUP          # bf16 path: d_k a multiple of 8 ...
     assert fwd(lib, d=4) == UNSUP
-    assert fwd(lib, d=136) == UNSUP         # ... up to 128
+    assert fwd(lib, d=264) == UNSUP         # ... up to 256
+    assert fwd(lib, d=260) == UNSUP
     assert fwd(lib, q=Q + 8) == UNSUP       # TMA needs 16-byte aligned bases
     assert fwd(lib, fn="mha_fwd_f32", d=257) == UNSUP
     assert fwd(lib, fn="mha_fwd_f32", q=Q + 2) == UNSUP
@@ -118,7 +119,7 @@ def test_dv_entry_errors(lib, fn):
 
 def test_dv_width_limits(lib):
     assert fwd_dv(lib, d_v=12) == UNSUP       # bf16: multiples of 8 ...
-    assert fwd_dv(lib, d_v=136) == UNSUP      # ... up to 128
+    assert fwd_dv(lib, d_v=264) == UNSUP      # ... up to 256
     assert fwd_dv(lib, d_k=20) == UNSUP
     assert fwd_dv(lib, fn="mha_fwd_f32_dv", d_v=257) == UNSUP
 
@@ -148,7 +149,8 @@ def dec(lib, q=Q, k=K, v=V, o=O, lse=None, B=2, H=3, Lk=64, d=64, lens=LENS_D, s
 def test_decode_entry_errors(lib):
     assert dec(lib, B=-1) == SHAPE
     assert dec(lib, Lk=-1) == SHAPE
-    assert dec(lib, d=96) == UNSUP
+    assert dec(lib, d=100) == UNSUP                        # multiples of 8 up to 256
+    assert dec(lib, d=264) == UNSUP
     assert dec(lib, scale=math.nan) == SCALE
     assert dec(lib, q=None) == NULL
     assert dec(lib, k=None) == NULL
@@ -224,5 +226,23 @@ def test_layer_entry_errors(lib):
     assert layer(lib, y=XL + 64) == ALIAS              # y overlaps x
     assert layer(lib, ws=WQ) == ALIAS                  # workspace overlaps the weights
     assert layer(lib, B=0) == OK
-    assert lib.mha_layer_workspace_bytes(2, 64, 64, 512, 8, 64) > 32 << 20
+    # the Q|K|V projections and the heads' output, bf16: (3 + 1) x 2 x 64 x 512 x 2 bytes
+    assert lib.mha_layer_workspace_bytes(2, 64, 64, 512, 8, 64) == 4 * 2 * 64 * 512 * 2
     assert lib.mha_layer_workspace_bytes(2, 64, 64, 512, 8, 12) == 0
+
+
+AG, BG, CG = 0x160000000, 0x170000000, 0x180000000
+
+
+def test_gemm_entry_errors(lib):
+    f = lib.mha_gemm_bf16
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_longlong] * 3 + [ctypes.c_void_p]
+    assert f(AG, BG, CG, -1, 8, 8, 8, 8, 8, None) == SHAPE
+    assert f(AG, BG, CG, 8, 8, 16, 8, 8, 8, None) == SHAPE       # lda < K
+    assert f(AG, BG, CG, 8, 16, 8, 8, 8, 16, None) == SHAPE      # ldb < N
+    assert f(None, BG, CG, 8, 8, 8, 8, 8, 8, None) == NULL
+    assert f(AG, BG, CG, 8, 8, 12, 12, 8, 8, None) == UNSUP      # rows not a multiple of 8
+    assert f(AG + 8, BG, CG, 8, 8, 8, 8, 8, 8, None) == UNSUP    # base not 16-byte aligned
+    assert f(AG, BG, AG + 16, 8, 8, 8, 8, 8, 8, None) == ALIAS   # c overlaps a
+    assert f(AG, BG, CG, 0, 8, 8, 8, 8, 8, None) == OK           # nothing to compute

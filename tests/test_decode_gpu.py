@@ -4,8 +4,9 @@ A decode step is the forward with one query row per sequence and key
 lengths = cache lengths, so the oracle is evaluated on q as [B, 1, H, d]
 under key padding.  Covers the single-pass and the split (two-kernel) paths,
 cache lengths of 0, 1, exact multiples of the 64-key tile and ragged ones,
-splits that hold no key, both head sizes, the row log-sum-exp, and the
-decode workloads at full size on sampled heads.
+splits that hold no key, head widths from 8 to 256 (each on the kernel of
+the next width up: 64, 128 or 256), the row log-sum-exp, and the decode
+workloads at full size on sampled heads.
 """
 import zlib
 
@@ -63,6 +64,15 @@ CASES = [
     (4, 8, 1, 64, [1, 0, 1, 1]),
     (3, 2, 8192, 64, [8192, 100, 5000]),                       # 32 splits
     (2, 3, 77, 128, [77, 13]),
+    # other head widths: the next kernel width up (64, 128, 256) with the
+    # rest of each row read as zero
+    (8, 4, 300, 32, [300, 0, 1, 64, 65, 128, 299, 200]),     # split in 2
+    (4, 3, 1000, 96, [1000, 999, 64, 3]),                    # split
+    (64, 16, 256, 96, None),                                  # one pass
+    (2, 4, 3000, 256, [3000, 1234]),                          # split, widest
+    (48, 16, 300, 256, None),                                 # one pass, widest
+    (3, 5, 130, 8, [130, 129, 0]),                            # narrowest
+    (2, 2, 640, 200, [640, 577]),                             # ragged last chunk
 ]
 
 

@@ -1,5 +1,6 @@
-"""The multi-head layer (mha_layer_fwd: cuBLASLt projections around the
-attention kernel) against the float64 layer oracle, through the C ABI."""
+"""The multi-head layer (mha_layer_fwd: the library's tensor-core GEMM for
+the projections around the attention kernel) against the float64 layer
+oracle, through the C ABI."""
 import numpy as np
 import pytest
 import torch

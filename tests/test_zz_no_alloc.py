@@ -3,7 +3,8 @@ instead of a caller workspace.
 
 On the GPU it must give exactly what mha_decode gives, call after call (two
 consecutive calls of each, on a split and a one-pass case).  On the host,
-every size the decode accepts at d_k <= 128 must fit the fixed array.
+every size the decode accepts (head widths up to 256) must fit the fixed
+array.
 """
 import pytest
 import torch
@@ -22,11 +23,11 @@ def test_static_scratch_covers_every_decode_size(lib):
     against the fixed array for every head count that splits and cache
     lengths up to far past any context."""
     cap = lib.mha_decode_static_scratch_bytes()
-    assert cap == 1 << 20
+    assert cap == 2 << 20
     worst = 0
     for bh in range(1, 700):
         for lk in (1, 255, 256, 257, 1000, 4096, 16384, 1 << 20):
-            for d in (64, 128):
+            for d in (8, 64, 96, 128, 200, 256):
                 worst = max(worst, lib.mha_decode_workspace_bytes(1, bh, lk, d))
     assert 0 < worst <= cap
 
@@ -42,8 +43,10 @@ def make(seed, B, H, Lk, d, lens):
 @pytest.mark.gpu
 @pytest.mark.parametrize("shape", [(1, 8, 4096, 128, [3001]),          # split: 16 chunks
                                    (2, 3, 700, 64, [700, 129]),        # split: 3 chunks
-                                   (64, 16, 256, 128, [200] * 64)],    # one pass
-                         ids=["split16", "split3", "onepass"])
+                                   (64, 16, 256, 128, [200] * 64),     # one pass
+                                   (3, 5, 1500, 256, [1500, 7, 700]),  # split, d_k 256
+                                   (4, 2, 900, 40, [900, 1, 5, 333])],  # split, d_k 40
+                         ids=["split16", "split3", "onepass", "split_d256", "split_d40"])
 def test_static_matches_workspace_entry(lib, shape):
     if not torch.cuda.is_available():
         pytest.fail("CUDA device required for gpu tests")

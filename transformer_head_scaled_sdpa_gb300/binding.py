@@ -69,6 +69,8 @@ def lib():
                                                                    ctypes.c_size_t, _c_p]
             h.mha_layer_workspace_bytes.restype = ctypes.c_size_t
             h.mha_layer_workspace_bytes.argtypes = [_c_i] * 6
+            h.mha_gemm_bf16.restype = _c_i
+            h.mha_gemm_bf16.argtypes = [_c_p] * 3 + [_c_i] * 3 + [ctypes.c_longlong] * 3 + [_c_p]
             for name in ("mha_fwd_dv", "mha_fwd_f32_dv"):
                 getattr(h, name).restype = _c_i
                 getattr(h, name).argtypes = [_c_p] * 5 + [_c_i] * 7 + [_c_p, ctypes.c_float, _c_p]
@@ -290,6 +292,30 @@ def mha_layer_fwd(x, w_qkv, w_o, H: int, mem=None, mask_kind: int = 0, key_lens=
     if rc != MHA_OK:
         raise MhaError(rc, "mha_layer_fwd")
     return y
+
+
+def mha_gemm_bf16(a, b, c=None, stream=None):
+    """c = a @ b on the library's tensor-core GEMM: a [M, K], b [K, N] bf16
+    CUDA matrices whose rows may be strided (stride(1) == 1, stride(0) a
+    multiple of 8 elements, e.g. column blocks of a wider matrix); c [M, N]
+    (allocated when not given, else written in place, same row rules)."""
+    for t, n in ((a, "a"), (b, "b")):
+        if t.dim() != 2 or t.dtype != torch.bfloat16 or not t.is_cuda or t.stride(1) != 1:
+            raise ValueError(f"{n} must be a row-major bf16 CUDA matrix")
+    M, K = a.shape
+    if b.shape[0] != K:
+        raise ValueError(f"inner sizes differ: a {tuple(a.shape)}, b {tuple(b.shape)}")
+    N = b.shape[1]
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    if c.dim() != 2 or tuple(c.shape) != (M, N) or c.dtype != torch.bfloat16 or c.stride(1) != 1:
+        raise ValueError("c must be a row-major bf16 [M, N] matrix")
+    rc = lib().mha_gemm_bf16(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K,
+                             max(a.stride(0), K), max(b.stride(0), N), max(c.stride(0), N),
+                             _stream_handle(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "mha_gemm_bf16")
+    return c
 
 
 def decode_workspace_bytes(B, H, Lk, d_k) -> int:

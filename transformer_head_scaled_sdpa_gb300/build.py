@@ -21,8 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libmha.so")
 
-SOURCES = ["mha_abi.cu", "mha_fwd_bf16.cu", "mha_fwd_f32.cu", "mha_decode.cu", "mha_bwd.cu",
-           "mha_gemm.cu"]
+SOURCES = ["mha_abi.cu", "mha_fwd_bf16.cu", "mha_fwd_wide.cu", "mha_fwd_f32.cu", "mha_decode.cu",
+           "mha_bwd.cu", "mha_gemm.cu"]
 HEADERS = [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "kernels.h"),
            os.path.join(INCLUDE, "mha.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -73,11 +73,9 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    # cuBLASLt (the layer's projection GEMMs), found next to the toolkit that
-    # compiled the library
-    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc)), "lib64")
-    r = subprocess.run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs +
-                       ["-L", cuda_lib, "-lcublasLt", "-Xlinker", f"-rpath={cuda_lib}"],
+    # (the CUDA driver API entry for tensor maps is looked up at run time: no
+    # library beyond the CUDA runtime is linked)
+    r = subprocess.run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs,
                        capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

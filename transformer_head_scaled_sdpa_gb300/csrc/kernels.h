@@ -41,6 +41,8 @@ struct Bf16Params {
                      // head sharing every K/V tile; 1 (d_k = 64) = a unit is the
                      // same query tile of two heads, each with its own K/V tiles
   float scale_log2;  // scale * log2(e)
+  int dk_steps;      // K16 steps of S = Q K^T: ceil(d_k / 16) <= D / 16
+  int dv_n;          // N of the P.V products: d_v rounded up to 16, <= D
   int withhold_p;    // test hook: softmax 0 withholds its first P arrival (0 = off)
 };
 
@@ -72,11 +74,13 @@ struct DecodeParams {
   void* out;         // [B, H, d] bf16
   float* lse;        // [B, H] or null
   const int32_t* cache_lens;  // [B] keys per sequence (clamped to [0, Lk])
-  float* part_o;     // [n_splits, B*H, d]  (n_splits > 1)
+  float* part_o;     // [n_splits, B*H, kernel width]  (n_splits > 1)
   float* part_m;     // [n_splits, B*H]
   float* part_l;     // [n_splits, B*H]
   DeviceStatus* status;
   int B, H, Lk;
+  int d;             // head width d_k: a multiple of 8 up to 256 (the kernel's
+                     // width, 64, 128 or 256, is the next one up)
   int chunk;         // keys per split, a multiple of 64
   int n_splits;
   float scale_log2;  // scale * log2(e)
@@ -89,9 +93,12 @@ constexpr int kDecMaxSplits = 64;
 // partial results unless it is 1).
 int decode_splits(int B, int H, int Lk);
 
-// Launches the decode step (d in {64, 128}): the split kernel and, with more
-// than one split, the combine kernel.
-cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream, LaunchInfo* info);
+// Width of the decode kernel a head of d features runs on (64, 128 or 256).
+int decode_kernel_width(int d);
+
+// Launches the decode step (p.d a multiple of 8 up to 256): the split kernel
+// and, with more than one split, the combine kernel.
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream, LaunchInfo* info);
 
 // Gradient of the bf16 forward.
 struct BwdParams {
@@ -122,6 +129,11 @@ cudaError_t launch_bwd(const BwdParams& p, int d, cudaStream_t stream, LaunchInf
 // Launches the bf16 tcgen05 forward for d in {64, 128}.
 cudaError_t launch_fwd_bf16(const Bf16Params& p, int d, cudaStream_t stream, LaunchInfo* info);
 
+// Launches the bf16 tcgen05 forward for heads wider than 128 (d_k, d_v up to
+// 256; mha_fwd_wide.cu): tm_q box {64, 1, 128, 1}, tm_k and tm_v box
+// {64, 1, 64, 1}, tm_o box {64, 1, 32, 1}; sets n_qtiles and head_group.
+cudaError_t launch_fwd_wide(const Bf16Params& p, cudaStream_t stream, LaunchInfo* info);
+
 // Launches a kernel with programmatic stream serialization: its grid may be
 // scheduled while the previous kernel on the stream drains, so its set-up
 // overlaps that kernel's tail.  The kernel must call griddep_wait() before
@@ -145,11 +157,25 @@ inline cudaError_t launch_serialized(void (*kernel)(Params...), dim3 grid, dim3 
 // Launches the float32 SIMT forward (1 <= d <= 256).
 cudaError_t launch_fwd_f32(const F32Params& p, cudaStream_t stream, LaunchInfo* info);
 
-// Row-major bf16 GEMM with float32 accumulation on cuBLASLt (mha_gemm.cu):
-// C[M x N] = A[M x K] B[K x N], leading dimensions in elements.  False when
-// cuBLASLt refuses the call.
-bool gemm_bf16_rowmajor(int M, int N, int K, const void* A, long long lda, const void* B,
-                        long long ldb, void* C, long long ldc, void* workspace,
-                        size_t workspace_bytes, cudaStream_t stream);
+// Row-major bf16 GEMM on the tensor cores (mha_gemm.cu): C[M x N] =
+// A[M x K] B[K x N], float32 accumulation, bf16 result.
+struct GemmParams {
+  CUtensorMap tm_a;  // A [M, K] (row stride lda), box {64 k, 128 rows}, 128-byte swizzle
+  CUtensorMap tm_b;  // B [K, N] (row stride ldb), box {64 n, 64 k}, 128-byte swizzle
+  CUtensorMap tm_c;  // C [M, N] (row stride ldc), box {64 n, 32 rows}, 128-byte swizzle
+  DeviceStatus* status;
+  int M, N, K;
+  int tiles_m, tiles_n;  // ceil(M / 128), ceil(N / 256)
+  int k_blocks;          // ceil(K / 64)
+};
+
+// Tile sizes of the GEMM kernel (rows and columns of C per tile, k per step).
+int gemm_tile_rows();
+int gemm_tile_cols();
+int gemm_k_block();
+
+// Launches the GEMM (one persistent CTA per SM, or per tile when fewer);
+// adds one to info->kernels.
+cudaError_t launch_gemm(const GemmParams& p, cudaStream_t stream, LaunchInfo* info);
 
 }  // namespace mha

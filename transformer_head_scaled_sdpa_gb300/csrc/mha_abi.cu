@@ -20,9 +20,9 @@ using mha::DeviceStatus;
 __device__ DeviceStatus g_status;
 
 // Scratch of mha_decode_static (the split partials of one decode step), for
-// callers that pass no workspace: 1 MiB per device, shared by every call of
+// callers that pass no workspace: 2 MiB per device, shared by every call of
 // that entry on the device.
-constexpr size_t kDecodeStaticScratchBytes = size_t(1) << 20;
+constexpr size_t kDecodeStaticScratchBytes = size_t(2) << 20;
 static __device__ __align__(256) uint8_t g_decode_scratch[kDecodeStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -175,10 +175,14 @@ int check_args(const void* q, const void* k, const void* v, void* out, int B, in
 }
 
 // bf16 rows on the tensor-core kernels: a multiple of 8 elements (16-byte row
-// strides for the tensor maps) up to 128; narrower rows are zero-filled by the
-// tensor-map loads up to the kernel's width (64 or 128) and clipped on store.
-bool bf16_width_ok(int d) { return d >= 8 && d <= 128 && d % 8 == 0; }
-int bf16_kernel_width(int d_k, int d_v) { return (d_k <= 64 && d_v <= 64) ? 64 : 128; }
+// strides for the tensor maps) up to 256 for the forward (128 for the
+// gradient); narrower rows are zero-filled by the tensor-map loads up to the
+// kernel's width (64, 128, or 256 on the wide kernel) and clipped on store.
+bool bf16_width_ok(int d) { return d >= 8 && d <= 256 && d % 8 == 0; }
+bool bf16_bwd_width_ok(int d) { return d >= 8 && d <= 128 && d % 8 == 0; }
+int bf16_kernel_width(int d_k, int d_v) {
+  return (d_k <= 64 && d_v <= 64) ? 64 : ((d_k <= 128 && d_v <= 128) ? 128 : 256);
+}
 
 // 4-D map over a [B, L, H, d] bf16 tensor; box = 64 features x 1 head x `rows`
 // rows (128 for the forward's tiles, 64 for the decode step's) x 1 sequence,
@@ -299,10 +303,13 @@ int attention_bf16(const void* q, const void* k, const void* v, void* out, float
   if (n_qtiles * B * H > 0x7fffffffll) return MHA_ERR_SHAPE;
   mha::Bf16Params p;
   std::memset(&p, 0, sizeof(p));
+  // the wide kernel streams 64-key tiles and each epilogue warp stores its own
+  // 32 rows
+  const bool wide = bf16_kernel_width(d_k, d_v) > 128;
   if (!encode_map(&p.tm_q, q, B, Lq, H, d_k, 128, q_row) ||
-      !encode_map(&p.tm_k, k, B, Lk, H, d_k, 128, k_row) ||
-      !encode_map(&p.tm_v, v, B, Lk, H, d_v, 128, v_row) ||
-      !encode_map(&p.tm_o, out, B, Lq, H, d_v))
+      !encode_map(&p.tm_k, k, B, Lk, H, d_k, wide ? 64 : 128, k_row) ||
+      !encode_map(&p.tm_v, v, B, Lk, H, d_v, wide ? 64 : 128, v_row) ||
+      !encode_map(&p.tm_o, out, B, Lq, H, d_v, wide ? 32 : 128))
     return MHA_ERR_UNSUPPORTED;
   p.out = out;
   p.lse = lse;
@@ -315,10 +322,12 @@ int attention_bf16(const void* q, const void* k, const void* v, void* out, float
   p.mask_kind = mask_kind;
   p.n_qtiles = static_cast<int>(n_qtiles);
   p.scale_log2 = effective_scale(scale, d_k) * kLog2e;
+  p.dk_steps = (d_k + 15) / 16;
+  p.dv_n = (d_v + 15) / 16 * 16;
   p.withhold_p = g_withhold_p;
-  return mha::launch_fwd_bf16(p, bf16_kernel_width(d_k, d_v), s, &t_info) == cudaSuccess
-             ? MHA_OK
-             : MHA_ERR_LAUNCH;
+  const cudaError_t e = wide ? mha::launch_fwd_wide(p, s, &t_info)
+                             : mha::launch_fwd_bf16(p, bf16_kernel_width(d_k, d_v), s, &t_info);
+  return e == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
 }
 
 int fwd_f32(const void* q, const void* k, const void* v, void* out, float* lse, bool want_lse,
@@ -407,16 +416,21 @@ static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 // Workspace of the decode step: partial outputs, maxima and sums of every
 // split (none with a single split).
+// (partial outputs are kept at the kernel's width: 64, 128 or 256)
 static size_t decode_ws_bytes(int B, int H, int Lk, int d_k, int* splits_out) {
   const int S = mha::decode_splits(B, H, Lk);
   if (splits_out) *splits_out = S;
   if (S <= 1) return 0;
   const size_t bh = static_cast<size_t>(B) * H;
-  return align256(static_cast<size_t>(S) * bh * d_k * 4) + 2 * align256(static_cast<size_t>(S) * bh * 4);
+  const size_t w = static_cast<size_t>(mha::decode_kernel_width(d_k));
+  return align256(static_cast<size_t>(S) * bh * w * 4) + 2 * align256(static_cast<size_t>(S) * bh * 4);
 }
 
+// decode head widths: multiples of 8 from 8 to 256
+static bool decode_width_ok(int d) { return d >= 8 && d <= 256 && d % 8 == 0; }
+
 size_t mha_decode_workspace_bytes(int B, int H, int Lk, int d_k) {
-  if (B < 0 || H < 0 || Lk < 0 || (d_k != 64 && d_k != 128)) return 0;
+  if (B < 0 || H < 0 || Lk < 0 || !decode_width_ok(d_k)) return 0;
   return decode_ws_bytes(B, H, Lk, d_k, nullptr);
 }
 
@@ -429,7 +443,7 @@ static int decode_step(const void* q, const void* k_cache, const void* v_cache, 
   t_info = mha::LaunchInfo{};
   if (B < 0 || H < 0 || Lk < 0) return MHA_ERR_SHAPE;
   if (!std::isfinite(scale) || scale < 0.f) return MHA_ERR_SCALE;
-  if (d_k != 64 && d_k != 128) return MHA_ERR_UNSUPPORTED;
+  if (!decode_width_ok(d_k)) return MHA_ERR_UNSUPPORTED;
   const long long bh = static_cast<long long>(B) * H;
   const long long cache_rows = bh * Lk;
   if (bh > 0x7fffffffll || cache_rows > (1ll << 40)) return MHA_ERR_SHAPE;
@@ -481,7 +495,7 @@ static int decode_step(const void* q, const void* k_cache, const void* v_cache, 
     // maximum -inf, sum 0) before the combine reads it: nothing starts at zero
     uint8_t* w = static_cast<uint8_t*>(workspace);
     p.part_o = reinterpret_cast<float*>(w);
-    w += align256(static_cast<size_t>(S) * bh * d_k * 4);
+    w += align256(static_cast<size_t>(S) * bh * mha::decode_kernel_width(d_k) * 4);
     p.part_m = reinterpret_cast<float*>(w);
     w += align256(static_cast<size_t>(S) * bh * 4);
     p.part_l = reinterpret_cast<float*>(w);
@@ -490,11 +504,12 @@ static int decode_step(const void* q, const void* k_cache, const void* v_cache, 
   p.B = B;
   p.H = H;
   p.Lk = Lk;
+  p.d = d_k;
   p.n_splits = S;
   const int per = (Lk + S - 1) / S;
   p.chunk = (per + 63) / 64 * 64;
   p.scale_log2 = effective_scale(scale, d_k) * kLog2e;
-  return mha::launch_decode(p, d_k, s, &t_info) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
+  return mha::launch_decode(p, s, &t_info) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
 }
 
 int mha_decode(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,
@@ -514,7 +529,7 @@ int mha_decode_static(const void* q, const void* k_cache, const void* v_cache, v
 size_t mha_decode_static_scratch_bytes(void) { return kDecodeStaticScratchBytes; }
 
 size_t mha_bwd_workspace_bytes(int B, int H, int Lq, int Lk, int d_k) {
-  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || !bf16_width_ok(d_k)) return 0;
+  if (B < 0 || H < 0 || Lq < 0 || Lk < 0 || !bf16_bwd_width_ok(d_k)) return 0;
   return align256(static_cast<size_t>(B) * H * Lq * 4);
 }
 
@@ -529,7 +544,7 @@ int mha_bwd(const void* q, const void* k, const void* v, const void* out, const 
   int rc = check_args(q, k, v, const_cast<void*>(out), B, H, Lq, Lk, d_k, d_k, mask_kind,
                       key_lens, scale, 2, 16, &empty, &sz);
   if (rc != MHA_OK) return rc;
-  if (!bf16_width_ok(d_k)) return MHA_ERR_UNSUPPORTED;
+  if (!bf16_bwd_width_ok(d_k)) return MHA_ERR_UNSUPPORTED;
   const long long bh = static_cast<long long>(B) * H;
   if (bh == 0) return MHA_OK;
   const size_t qb = sz.q_elems * 2, kb = sz.kv_elems * 2;
@@ -605,11 +620,44 @@ int mha_bwd(const void* q, const void* k, const void* v, const void* out, const 
 }
 
 // ---------------------------------------------------------------------------
-// The multi-head layer: projections (cuBLASLt) around the attention kernel.
+// The multi-head layer: projections (the tcgen05 GEMM) around the attention
+// kernel.
 // ---------------------------------------------------------------------------
-static constexpr size_t kLayerGemmWorkspaceBytes = size_t(32) << 20;
+// 2-D map over a row-major bf16 matrix [rows, cols] with `ld` elements
+// between rows; box = box_cols x box_rows, 128-byte swizzle (box_cols 64).
+static bool encode_2d(CUtensorMap* m, const void* base, long long rows, long long cols,
+                      long long ld, int box_cols, int box_rows) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
-// workspace: [Q|K|V projections][O (heads concatenated)][GEMM workspace]
+// C[M x N] = A[M x K] B[K x N] (row-major bf16, leading dimensions in
+// elements: multiples of 8, bases 16-byte aligned) on the tensor cores.
+static int gemm_bf16(int M, int N, int K, const void* A, long long lda, const void* B,
+                     long long ldb, void* C, long long ldc, DeviceState* dev, cudaStream_t s,
+                     mha::LaunchInfo* info) {
+  mha::GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (!encode_2d(&p.tm_a, A, M, K, lda, 64, 128) || !encode_2d(&p.tm_b, B, K, N, ldb, 64, 64) ||
+      !encode_2d(&p.tm_c, C, M, N, ldc, 64, 32))
+    return MHA_ERR_UNSUPPORTED;
+  p.status = dev->status;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.tiles_m = (M + mha::gemm_tile_rows() - 1) / mha::gemm_tile_rows();
+  p.tiles_n = (N + mha::gemm_tile_cols() - 1) / mha::gemm_tile_cols();
+  p.k_blocks = (K + mha::gemm_k_block() - 1) / mha::gemm_k_block();
+  return mha::launch_gemm(p, s, info) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
+}
+
+// workspace: [Q|K|V projections][O (heads concatenated)]
 static size_t layer_proj_bytes(int B, int Lq, int Lk, size_t hd) {
   return align256((static_cast<size_t>(B) * Lq * hd + static_cast<size_t>(B) * Lk * 2 * hd) * 2);
 }
@@ -617,8 +665,36 @@ static size_t layer_proj_bytes(int B, int Lq, int Lk, size_t hd) {
 size_t mha_layer_workspace_bytes(int B, int Lq, int Lk, int d_model, int H, int d_k) {
   if (B < 0 || Lq < 0 || Lk < 0 || d_model < 1 || H < 1 || !bf16_width_ok(d_k)) return 0;
   const size_t hd = static_cast<size_t>(H) * d_k;
-  return layer_proj_bytes(B, Lq, Lk, hd) + align256(static_cast<size_t>(B) * Lq * hd * 2) +
-         kLayerGemmWorkspaceBytes;
+  return layer_proj_bytes(B, Lq, Lk, hd) + align256(static_cast<size_t>(B) * Lq * hd * 2);
+}
+
+int mha_gemm_bf16(const void* a, const void* b, void* c, int M, int N, int K, long long lda,
+                  long long ldb, long long ldc, void* stream) {
+  t_info = mha::LaunchInfo{};
+  if (M < 0 || N < 0 || K < 0) return MHA_ERR_SHAPE;
+  if (M == 0 || N == 0) return MHA_OK;
+  if (!a || !b || !c) return MHA_ERR_NULL;
+  if (lda < K || ldb < N || ldc < N || lda > (1ll << 40) || ldb > (1ll << 40) || ldc > (1ll << 40))
+    return MHA_ERR_SHAPE;
+  if ((lda | ldb | ldc) % 8 != 0 ||
+      ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) |
+        reinterpret_cast<uintptr_t>(c)) & 15u))
+    return MHA_ERR_UNSUPPORTED;
+  const size_t cb = (static_cast<size_t>(M - 1) * ldc + N) * 2;
+  if (overlaps(c, cb, a, K > 0 ? (static_cast<size_t>(M - 1) * lda + K) * 2 : 0) ||
+      overlaps(c, cb, b, K > 0 ? (static_cast<size_t>(K - 1) * ldb + N) * 2 : 0))
+    return MHA_ERR_ALIAS;
+  DeviceState* dev = nullptr;
+  int rc = device_state(&dev);
+  if (rc != MHA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) {  // an empty sum: C = 0, row by row
+    if (cudaMemset2DAsync(c, static_cast<size_t>(ldc) * 2, 0, static_cast<size_t>(N) * 2, M, s) !=
+        cudaSuccess)
+      return MHA_ERR_LAUNCH;
+    return MHA_OK;
+  }
+  return gemm_bf16(M, N, K, a, lda, b, ldb, c, ldc, dev, s, &t_info);
 }
 
 int mha_layer_fwd(const void* x, const void* mem, const void* w_qkv, const void* w_o, void* y,
@@ -666,16 +742,15 @@ int mha_layer_fwd(const void* x, const void* mem, const void* w_qkv, const void*
   uint8_t* w = static_cast<uint8_t*>(workspace);
   uint16_t* proj = reinterpret_cast<uint16_t*>(w);
   uint16_t* o = reinterpret_cast<uint16_t*>(w + layer_proj_bytes(B, Lq, Lk, hd));
-  void* gws = w + layer_proj_bytes(B, Lq, Lk, hd) + align256(static_cast<size_t>(rows_q) * hd * 2);
   const uint16_t* wq = static_cast<const uint16_t*>(w_qkv);
   const void *q, *k, *v;
   long long q_row, kv_row;
+  mha::LaunchInfo gemms;  // the projection launches (the attention's own info is kept apart)
   if (!mem) {
     // one GEMM: [Q | K | V] = x [W^Q | W^K | W^V], rows of 3 H d_k
-    if (!mha::gemm_bf16_rowmajor(static_cast<int>(rows_q), static_cast<int>(3 * hd), d_model, x,
-                                 d_model, w_qkv, 3 * hd, proj, 3 * hd, gws,
-                                 kLayerGemmWorkspaceBytes, s))
-      return MHA_ERR_LAUNCH;
+    rc = gemm_bf16(static_cast<int>(rows_q), static_cast<int>(3 * hd), d_model, x, d_model,
+                   w_qkv, 3 * hd, proj, 3 * hd, dev, s, &gemms);
+    if (rc != MHA_OK) return rc;
     q = proj;
     k = proj + hd;
     v = proj + 2 * hd;
@@ -684,12 +759,12 @@ int mha_layer_fwd(const void* x, const void* mem, const void* w_qkv, const void*
     // Q = x W^Q (rows of H d_k) and [K | V] = mem [W^K | W^V] (rows of 2 H d_k),
     // reading the weight's column blocks in place (leading dimension 3 H d_k)
     uint16_t* kv = proj + rows_q * hd;
-    if (!mha::gemm_bf16_rowmajor(static_cast<int>(rows_q), static_cast<int>(hd), d_model, x,
-                                 d_model, wq, 3 * hd, proj, hd, gws, kLayerGemmWorkspaceBytes, s) ||
-        !mha::gemm_bf16_rowmajor(static_cast<int>(rows_k), static_cast<int>(2 * hd), d_model, mem,
-                                 d_model, wq + hd, 3 * hd, kv, 2 * hd, gws,
-                                 kLayerGemmWorkspaceBytes, s))
-      return MHA_ERR_LAUNCH;
+    rc = gemm_bf16(static_cast<int>(rows_q), static_cast<int>(hd), d_model, x, d_model, wq,
+                   3 * hd, proj, hd, dev, s, &gemms);
+    if (rc == MHA_OK)
+      rc = gemm_bf16(static_cast<int>(rows_k), static_cast<int>(2 * hd), d_model, mem, d_model,
+                     wq + hd, 3 * hd, kv, 2 * hd, dev, s, &gemms);
+    if (rc != MHA_OK) return rc;
     q = proj;
     k = kv;
     v = kv + hd;
@@ -703,10 +778,12 @@ int mha_layer_fwd(const void* x, const void* mem, const void* w_qkv, const void*
   if (rc != MHA_OK) return rc;
   const mha::LaunchInfo attn = t_info;
   // y = Concat(heads) W^O
-  if (!mha::gemm_bf16_rowmajor(static_cast<int>(rows_q), d_model, static_cast<int>(hd), o, hd,
-                               w_o, d_model, y, d_model, gws, kLayerGemmWorkspaceBytes, s))
-    return MHA_ERR_LAUNCH;
+  rc = gemm_bf16(static_cast<int>(rows_q), d_model, static_cast<int>(hd), o, hd, w_o, d_model, y,
+                 d_model, dev, s, &gemms);
+  if (rc != MHA_OK) return rc;
+  // every launch of the layer is this library's: the GEMMs and the attention
   t_info = attn;
+  t_info.kernels = attn.kernels + gemms.kernels;
   return MHA_OK;
 }
 

@@ -45,12 +45,15 @@ constexpr int kDecThreads = 32 * (kDecWarps + 1);  // + the TMA warp
 constexpr int kDecTile = 64;                    // keys per TMA tile
 constexpr int kKeysPerWarp = kDecTile / kDecWarps;  // 16
 
+// D: the kernel's width (64, 128 or 256); a head of d_k < D features runs on
+// it with the rest of each row read as zero (the tensor maps' fill) and
+// only its own d_k output columns written.
 template <int D>
 struct DecCfg {
   static constexpr int KCH = D / 64;              // 128-byte chunks per key row
   static constexpr int CHUNK = kDecTile * 128;    // [64 keys x 128 B], 128-byte swizzle
   static constexpr int TILE = KCH * CHUNK;        // one K or V tile
-  static constexpr int NS = (D == 64) ? 4 : 3;    // ring stages
+  static constexpr int NS = (D == 64) ? 4 : 3;    // ring stages (192 KB at D = 256)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = NS * TILE;
   static constexpr int OFF_BAR = 2 * NS * TILE;   // full[NS], empty[NS]
@@ -78,7 +81,14 @@ __device__ __forceinline__ void load_row(uint32_t tile, int r, int lane, float (
   const int u = (e % 64) / 8;               // 16-byte unit within the 128-byte row
   const int within = (e % 8) * 2;           // byte offset inside the unit
   const uint32_t addr = tile + c * DecCfg<D>::CHUNK + r * 128 + ((u ^ (r & 7)) << 4) + within;
-  if constexpr (EPL == 4) {
+  if constexpr (EPL == 8) {
+    uint32_t a, b, c2, d2;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c2), "=r"(d2)
+                 : "r"(addr));
+    x[0] = bf_lo(a); x[1] = bf_hi(a); x[2] = bf_lo(b); x[3] = bf_hi(b);
+    x[4] = bf_lo(c2); x[5] = bf_hi(c2); x[6] = bf_lo(d2); x[7] = bf_hi(d2);
+  } else if constexpr (EPL == 4) {
     uint32_t a, b;
     asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
     x[0] = bf_lo(a); x[1] = bf_hi(a); x[2] = bf_lo(b); x[3] = bf_hi(b);
@@ -157,12 +167,16 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
 
   // ---- compute warps
   // q (lane's EPL elements), pre-scaled so that scores come out in log2 units
+  // (features past the head's d_k are 0: they add nothing to the scores)
   float qv[EPL];
   {
     const __nv_bfloat16* qrow =
-        reinterpret_cast<const __nv_bfloat16*>(p.q) + static_cast<size_t>(bh) * D + EPL * lane;
+        reinterpret_cast<const __nv_bfloat16*>(p.q) + static_cast<size_t>(bh) * p.d;
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) qv[e] = __bfloat162float(qrow[e]) * p.scale_log2;
+    for (int e = 0; e < EPL; ++e) {
+      const int col = EPL * lane + e;
+      qv[e] = col < p.d ? __bfloat162float(qrow[col]) * p.scale_log2 : 0.f;
+    }
   }
   float m = -INFINITY;       // running maximum of this warp's keys (warp-uniform)
   float l = 0.f;             // running sum; counted in even lanes only
@@ -278,8 +292,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const __grid_
   const int t = static_cast<int>(threadIdx.x);
   if (p.n_splits == 1) {
     const float inv = (L > 0.f) ? 1.f / L : 0.f;
-    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(bh) * D;
-    for (int e = t; e < D; e += 32 * kDecWarps) {
+    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(bh) * p.d;
+    for (int e = t; e < p.d; e += 32 * kDecWarps) {
       float o = 0.f;
 #pragma unroll
       for (int w = 0; w < kDecWarps; ++w) o = fmaf(wgt[w], red[2 * kDecWarps + w * D + e], o);
@@ -327,9 +341,10 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
     for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, po[e], o[e]);
   }
   const float inv = (L > 0.f) ? 1.f / L : 0.f;
-  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + bh * D + EPL * lane;
+  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + bh * p.d;
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) orow[e] = __float2bfloat16_rn(o[e] * inv);
+  for (int e = 0; e < EPL; ++e)
+    if (EPL * lane + e < p.d) orow[EPL * lane + e] = __float2bfloat16_rn(o[e] * inv);
   if (p.lse && lane == 0) p.lse[bh] = (L > 0.f) ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
@@ -379,10 +394,15 @@ int decode_splits(int B, int H, int Lk) {
   return s < 1 ? 1 : static_cast<int>(s);
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int d, cudaStream_t stream, LaunchInfo* info) {
-  if (d == 64) return launch_decode_d<64>(p, stream, info);
-  if (d == 128) return launch_decode_d<128>(p, stream, info);
-  return cudaErrorInvalidValue;
+int decode_kernel_width(int d) { return d <= 64 ? 64 : (d <= 128 ? 128 : 256); }
+
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream, LaunchInfo* info) {
+  if (p.d < 8 || p.d > 256 || p.d % 8 != 0) return cudaErrorInvalidValue;
+  switch (decode_kernel_width(p.d)) {
+    case 64: return launch_decode_d<64>(p, stream, info);
+    case 128: return launch_decode_d<128>(p, stream, info);
+    default: return launch_decode_d<256>(p, stream, info);
+  }
 }
 
 }  // namespace mha

@@ -66,6 +66,13 @@ constexpr int kThreads = 384;
 constexpr int kSoftmaxWarp0 = 0;
 constexpr int kMmaWarp = 8, kProducerWarp = 9, kMma1Warp = 11;  // warp 10: scheduler
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p stays <= 2^8
+#ifndef MHA_POLY_PERIOD
+#define MHA_POLY_PERIOD 0
+#endif
+// On tiles with no masked element, every kPolyPeriod-th pair of exponentials
+// is evaluated on the FMA pipe (exp2_fma2) instead of the special-function
+// unit (0: none).
+constexpr int kPolyPeriod = MHA_POLY_PERIOD;
 // Heads dispatched together are chosen by their K/V bytes, about this much
 // per group, so a group's K/V stay in L2 while its query blocks run (32 heads
 // of the GPT-3-like shape, 64 of big16 L 2048, every head of the base-model
@@ -540,13 +547,18 @@ __device__ __forceinline__ void producer_role_paired(const Bf16Params& p, const 
 // whole warp runs the loop and the waits; one elected lane issues every
 // tcgen05.mma and tcgen05.commit, with descriptors built once and stepped by
 // constants.
-template <int D, int GSEL, bool PAIRED>
+template <int D, int GSEL, bool PAIRED, bool NARROW>
 __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx) {
   using C = Cfg<D>;
   using BA = Bars<C::NS>;
   constexpr int NS = C::NS;
   constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
-  constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+  // NARROW: the head's own widths, ceil(d_k / 16) K steps for S and N = d_v
+  // rounded up to 16 for P.V (features past d_k read as zero; O columns past
+  // d_v unused); otherwise the kernel's full width, as compile-time constants
+  const int n_ks = NARROW ? p.dk_steps : D / 16;
+  const uint32_t idesc_o =
+      NARROW ? idesc_bf16_f32(128, p.dv_n, false, true) : idesc_bf16_f32(128, D, false, true);
   // K-major Q and K tiles: 8-row groups 1024 B apart; V MN-major with its
   // second 64-wide d chunk one CHUNK further.
   const uint64_t dq0 = smem_desc_sw128(cx.sQ, 16, 1024);
@@ -581,6 +593,7 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx) {
     if (elect_one()) {
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
+        if (ks >= n_ks) break;
         const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
         umma_ss(tm_s, a + off, b + off, idesc_s, ks > 0 ? 1u : 0u);
       }
@@ -717,14 +730,17 @@ __device__ __forceinline__ void mma_role(const Bf16Params& p, const Ctx& cx) {
 // PV0(j), S0(j+1), PV1(j), S1(j+1), which keeps the two softmax warpgroups
 // alternating on the tensor core.  (Measured: this fixed order is ~3 % faster
 // here than two independent issuers.)
-template <int D>
+template <int D, bool NARROW>
 __device__ __forceinline__ void mma_role_pair(const Bf16Params& p, const Ctx& cx) {
   using C = Cfg<D>;
   using BA = Bars<C::NS>;
   constexpr int NS = C::NS;
   static_assert(!C::SEPARATE_P && C::SPLIT_RELEASE, "pair order: P over S, split release");
   constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
-  constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+  // the head's own widths when NARROW (as in mma_role)
+  const int n_ks = NARROW ? p.dk_steps : D / 16;
+  const uint32_t idesc_o =
+      NARROW ? idesc_bf16_f32(128, p.dv_n, false, true) : idesc_bf16_f32(128, D, false, true);
   // K-major Q and K tiles: 8-row groups 1024 B apart; V MN-major with its
   // second 64-wide d chunk one CHUNK further.
   const uint64_t dq0 = smem_desc_sw128(cx.sQ, 16, 1024);
@@ -742,6 +758,7 @@ __device__ __forceinline__ void mma_role_pair(const Bf16Params& p, const Ctx& cx
     if (elect_one()) {
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
+        if (ks >= n_ks) break;
         const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
         umma_ss(d_tmem, a + off, b + off, idesc_s, ks > 0 ? 1u : 0u);
       }
@@ -851,7 +868,7 @@ __device__ __forceinline__ void mma_role_pair(const Bf16Params& p, const Ctx& cx
 // pair.  That keeps their SFU-bound phases apart, so each runs at the full SFU
 // rate while the other does its loads, maxima and stores (d_k = 64 without the
 // causal mask, where the SFU work per score equals the tensor work: +5 %).
-template <int D, bool TOK, bool PAIRED>
+template <int D, bool TOK, bool PAIRED, bool NARROW>
 __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx) {
   using C = Cfg<D>;
   using BA = Bars<C::NS>;
@@ -868,6 +885,8 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
   // async-groups belong to the issuing thread)
   const bool store_thread = (warp == 4 * g) && lane == 0;
   const float c2 = p.scale_log2;
+  // O columns the P.V products write (d_v rounded up to 16; D unless NARROW)
+  const int dv_n = NARROW ? p.dv_n : D;
   int s_cnt = 0;  // S_g tiles so far
   int o_cnt = 0;  // units with O_g so far
   int tok_cnt = 0;  // exponential turns taken so far
@@ -968,14 +987,29 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
       // (each pair is packed to bf16 as soon as it exists, so the float32
       // values die at once and the row never holds 128 floats and 64 words)
       uint32_t pk[64];
+      auto exps = [&](bool poly) {
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        fma2(x[c], x[c + 1], x[c], x[c + 1], c2, c2, nm, nm);
-        x[c] = ex2_approx(x[c]);
-        x[c + 1] = ex2_approx(x[c + 1]);
-        const int q = (c >> 1) & 3;
-        add2(sa[q], sb[q], sa[q], sb[q], x[c], x[c + 1]);
-        pk[c >> 1] = pack_bf16x2(x[c], x[c + 1]);
+        for (int c = 0; c < 128; c += 2) {
+          fma2(x[c], x[c + 1], x[c], x[c + 1], c2, c2, nm, nm);
+          if (kPolyPeriod > 0 && poly && (c / 2) % kPolyPeriod == kPolyPeriod - 1) {
+            x[c] = fmaxf(x[c], -125.f);
+            x[c + 1] = fmaxf(x[c + 1], -125.f);
+            exp2_fma2(x[c], x[c + 1]);
+          } else {
+            x[c] = ex2_approx(x[c]);
+            x[c + 1] = ex2_approx(x[c + 1]);
+          }
+          const int q = (c >> 1) & 3;
+          add2(sa[q], sb[q], sa[q], sb[q], x[c], x[c + 1]);
+          pk[c >> 1] = pack_bf16x2(x[c], x[c + 1]);
+        }
+      };
+      // (a masked score is -inf and must give exactly 0: those tiles stay on
+      // the special-function unit)
+      if (kPolyPeriod > 0 && D == 64 && __all_sync(0xffffffffu, lim >= kBlockN)) {
+        exps(true);
+      } else {
+        exps(false);
       }
       add2(sa[0], sb[0], sa[0], sb[0], sa[1], sb[1]);
       add2(sa[2], sb[2], sa[2], sb[2], sa[3], sb[3]);
@@ -998,6 +1032,7 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
       if (__any_sync(0xffffffffu, move)) {
 #pragma unroll
         for (int c32 = 0; c32 < D / 32; ++c32) {
+          if (32 * c32 >= dv_n) break;  // O columns past d_v are never written
           uint32_t o[32];
           tmem_ld32(tO + 32u * c32, o);
           tmem_ld_wait();
@@ -1035,18 +1070,24 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
       p.lse[(static_cast<size_t>(seq) * p.H + head) * p.Lq + qi] =
           (l > 0.f) ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
     }
+    // only the 64-column chunks that hold output columns (d_v <= 64 on the
+    // 128-wide kernel stores one), and in them only the written 32-column
+    // halves are read from TMEM
+    const int n_chunks = (dv_n + 63) / 64;
 #pragma unroll
     for (int c = 0; c < C::KCH; ++c) {
+      if (c >= n_chunks) break;
       // the previous TMA store from the staging chunk must have read it
       if (store_thread) tma_store_wait_read();
       named_barrier(1 + g, 128);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t o[32];
-        if (n_tiles > 0) {
+        const bool written = 64 * c + 32 * half < dv_n;
+        if (n_tiles > 0 && written) {
           tmem_ld32(tO + 64u * c + 32u * half, o);
           tmem_ld_wait();
-          if (c == C::KCH - 1 && half == 1) {
+          if (c == n_chunks - 1 && (half == 1 || 64 * c + 32 >= dv_n)) {
             // O_g may be overwritten by the next unit from here on
             tc_fence_before();
             mbar_arrive(cx.bar(BA::O_FREE + g));
@@ -1082,7 +1123,7 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
   __syncwarp();
 }
 
-template <int D, bool TOK, bool PAIRED>
+template <int D, bool TOK, bool PAIRED, bool NARROW>
 __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_constant__ Bf16Params p) {
   using C = Cfg<D>;
   using BA = Bars<C::NS>;
@@ -1160,17 +1201,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
 
   if (cx.warp < kSoftmaxWarp0 + 8) {
     regs_increase<C::REGS_SOFTMAX>();
-    softmax_role<D, TOK, PAIRED>(p, cx);
+    softmax_role<D, TOK, PAIRED, NARROW>(p, cx);
   } else {
     regs_decrease<C::REGS_OTHER>();
     if (cx.warp == kMmaWarp) {
       if constexpr (C::SEPARATE_P) {
-        mma_role<D, 0, PAIRED>(p, cx);
+        mma_role<D, 0, PAIRED, NARROW>(p, cx);
       } else {
-        mma_role_pair<D>(p, cx);
+        mma_role_pair<D, NARROW>(p, cx);
       }
     } else if (cx.warp == kMma1Warp) {
-      if constexpr (C::SEPARATE_P) mma_role<D, 1, PAIRED>(p, cx);
+      if constexpr (C::SEPARATE_P) mma_role<D, 1, PAIRED, NARROW>(p, cx);
     } else if (cx.warp == kProducerWarp) {
       if constexpr (PAIRED) {
         producer_role_paired<D>(p, cx);
@@ -1191,9 +1232,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_bf16_kernel(const __grid_cons
   }
 }
 
-template <int D, bool TOK, bool PAIRED>
+template <int D, bool TOK, bool PAIRED, bool NARROW>
 cudaError_t launch_d(const Bf16Params& p, cudaStream_t stream, LaunchInfo* info) {
   static_assert(!PAIRED || D == 64, "heads are paired only with one MMA warp per query tile");
+  static_assert(!(TOK && NARROW), "the narrow instantiations take no exponential turns");
   using C = Cfg<D>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1201,7 +1243,7 @@ cudaError_t launch_d(const Bf16Params& p, cudaStream_t stream, LaunchInfo* info)
   static bool attr_set[64] = {};  // the attribute is per device and function
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(fwd_bf16_kernel<D, TOK, PAIRED>,
+    e = cudaFuncSetAttribute(fwd_bf16_kernel<D, TOK, PAIRED, NARROW>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM);
     if (e != cudaSuccess) return e;
@@ -1211,7 +1253,7 @@ cudaError_t launch_d(const Bf16Params& p, cudaStream_t stream, LaunchInfo* info)
                           (PAIRED ? (static_cast<long long>(p.B) * p.H + 1) / 2
                                   : static_cast<long long>(p.B) * p.H);
   const dim3 grid(static_cast<unsigned>(units));
-  e = launch_serialized(fwd_bf16_kernel<D, TOK, PAIRED>, grid, dim3(kThreads), C::SMEM, stream, p);
+  e = launch_serialized(fwd_bf16_kernel<D, TOK, PAIRED, NARROW>, grid, dim3(kThreads), C::SMEM, stream, p);
   if (e != cudaSuccess) return e;
   if (info) {
     info->kernels = 1;
@@ -1258,15 +1300,24 @@ cudaError_t launch_fwd_bf16(const Bf16Params& params, int d, cudaStream_t stream
   // (the exponential turn-taking pays off at d_k = 64 without the causal
   // mask once units span several key tiles; with one or two key tiles the
   // hand-over at the start of each unit costs more than it saves)
+  // A head narrower than the kernel (d_k or d_v below 64 or 128) runs an
+  // instantiation that issues only its own K steps and output columns; the
+  // full-width ones keep those counts as compile-time constants.
+  const bool narrow = p.dk_steps * 16 < d || p.dv_n < d;
   if (d == 64) {
+    if (narrow)
+      return p.paired ? launch_d<64, false, true, true>(p, stream, info)
+                      : launch_d<64, false, false, true>(p, stream, info);
     const bool tok = !masks_causal(p.mask_kind) && p.Lk >= 4 * kBlockN;
     if (p.paired)
-      return tok ? launch_d<64, true, true>(p, stream, info)
-                 : launch_d<64, false, true>(p, stream, info);
-    return tok ? launch_d<64, true, false>(p, stream, info)
-               : launch_d<64, false, false>(p, stream, info);
+      return tok ? launch_d<64, true, true, false>(p, stream, info)
+                 : launch_d<64, false, true, false>(p, stream, info);
+    return tok ? launch_d<64, true, false, false>(p, stream, info)
+               : launch_d<64, false, false, false>(p, stream, info);
   }
-  if (d == 128) return launch_d<128, false, false>(p, stream, info);
+  if (d == 128)
+    return narrow ? launch_d<128, false, false, true>(p, stream, info)
+                  : launch_d<128, false, false, false>(p, stream, info);
   return cudaErrorInvalidValue;
 }
 
