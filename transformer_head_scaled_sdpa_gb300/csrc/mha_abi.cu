@@ -673,16 +673,18 @@ int mha_gemm_bf16(const void* a, const void* b, void* c, int M, int N, int K, lo
   t_info = mha::LaunchInfo{};
   if (M < 0 || N < 0 || K < 0) return MHA_ERR_SHAPE;
   if (M == 0 || N == 0) return MHA_OK;
-  if (!a || !b || !c) return MHA_ERR_NULL;
-  if (lda < K || ldb < N || ldc < N || lda > (1ll << 40) || ldb > (1ll << 40) || ldc > (1ll << 40))
+  // (with K == 0 only c is touched: a and b may be NULL, their strides unused)
+  if (!c || (K > 0 && (!a || !b))) return MHA_ERR_NULL;
+  if (ldc < N || ldc > (1ll << 40) ||
+      (K > 0 && (lda < K || ldb < N || lda > (1ll << 40) || ldb > (1ll << 40))))
     return MHA_ERR_SHAPE;
-  if ((lda | ldb | ldc) % 8 != 0 ||
-      ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) |
-        reinterpret_cast<uintptr_t>(c)) & 15u))
+  if (ldc % 8 != 0 || (reinterpret_cast<uintptr_t>(c) & 15u) ||
+      (K > 0 && ((lda | ldb) % 8 != 0 ||
+                 ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 15u))))
     return MHA_ERR_UNSUPPORTED;
   const size_t cb = (static_cast<size_t>(M - 1) * ldc + N) * 2;
-  if (overlaps(c, cb, a, K > 0 ? (static_cast<size_t>(M - 1) * lda + K) * 2 : 0) ||
-      overlaps(c, cb, b, K > 0 ? (static_cast<size_t>(K - 1) * ldb + N) * 2 : 0))
+  if (K > 0 && (overlaps(c, cb, a, (static_cast<size_t>(M - 1) * lda + K) * 2) ||
+                overlaps(c, cb, b, (static_cast<size_t>(K - 1) * ldb + N) * 2)))
     return MHA_ERR_ALIAS;
   DeviceState* dev = nullptr;
   int rc = device_state(&dev);
