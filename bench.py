@@ -401,11 +401,12 @@ def host_link(dev, stream, nbytes=256 << 20, reps=3):
 
 
 # Every configuration of the target specification plus the supplementary
-# d_k = 64, L >= 2048 shapes, with and without the causal mask: the default
-# run times each one (the headline workload is measured once, above).
+# d_k = 64, L >= 2048 shapes and the head-width-256 shapes, with and without
+# the causal mask: the default run times each one (the headline workload is
+# measured once, above).
 SWEEP = ["toy_cross_f32", "base_encoder_self", "base_decoder_causal", "base_cross_keypad",
          "gpt3_causal", "big16_L2048", "big16_L2048_causal", "base8_L4096",
-         "base8_L4096_causal"]
+         "base8_L4096_causal", "d256_L2048", "d256_L2048_causal"]
 # the configurations whose oracle is also timed on a single core
 ONE_CORE = {"toy_cross_f32", "base_encoder_self", "base_decoder_causal"}
 
@@ -543,8 +544,8 @@ def run_ours(args):
         "roofline": ({"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                       "frac": achieved / peak, "traffic": traffic,
                       "peak_source": f"{peak_src} dense bf16 (burst)",
-                      "kernel": "fwd_bf16_kernel", "kernel_ms": kernel_ms,
-                      "algorithmic_bytes": bytes_alg,
+                      "kernel": "fwd_wide_kernel" if w.d_k > 128 else "fwd_bf16_kernel",
+                      "kernel_ms": kernel_ms, "algorithmic_bytes": bytes_alg,
                       "achieved_gbs": bytes_alg / (kernel_ms * 1e-3) / 1e9}
                      if w.dtype == torch.bfloat16 else
                      # the float32 kernel runs on the CUDA cores: 152 SMs x 128

@@ -66,13 +66,6 @@ constexpr int kThreads = 384;
 constexpr int kSoftmaxWarp0 = 0;
 constexpr int kMmaWarp = 8, kProducerWarp = 9, kMma1Warp = 11;  // warp 10: scheduler
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p stays <= 2^8
-#ifndef MHA_POLY_PERIOD
-#define MHA_POLY_PERIOD 0
-#endif
-// On tiles with no masked element, every kPolyPeriod-th pair of exponentials
-// is evaluated on the FMA pipe (exp2_fma2) instead of the special-function
-// unit (0: none).
-constexpr int kPolyPeriod = MHA_POLY_PERIOD;
 // Heads dispatched together are chosen by their K/V bytes, about this much
 // per group, so a group's K/V stay in L2 while its query blocks run (32 heads
 // of the GPT-3-like shape, 64 of big16 L 2048, every head of the base-model
@@ -987,29 +980,14 @@ __device__ __forceinline__ void softmax_role(const Bf16Params& p, const Ctx& cx)
       // (each pair is packed to bf16 as soon as it exists, so the float32
       // values die at once and the row never holds 128 floats and 64 words)
       uint32_t pk[64];
-      auto exps = [&](bool poly) {
 #pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          fma2(x[c], x[c + 1], x[c], x[c + 1], c2, c2, nm, nm);
-          if (kPolyPeriod > 0 && poly && (c / 2) % kPolyPeriod == kPolyPeriod - 1) {
-            x[c] = fmaxf(x[c], -125.f);
-            x[c + 1] = fmaxf(x[c + 1], -125.f);
-            exp2_fma2(x[c], x[c + 1]);
-          } else {
-            x[c] = ex2_approx(x[c]);
-            x[c + 1] = ex2_approx(x[c + 1]);
-          }
-          const int q = (c >> 1) & 3;
-          add2(sa[q], sb[q], sa[q], sb[q], x[c], x[c + 1]);
-          pk[c >> 1] = pack_bf16x2(x[c], x[c + 1]);
-        }
-      };
-      // (a masked score is -inf and must give exactly 0: those tiles stay on
-      // the special-function unit)
-      if (kPolyPeriod > 0 && D == 64 && __all_sync(0xffffffffu, lim >= kBlockN)) {
-        exps(true);
-      } else {
-        exps(false);
+      for (int c = 0; c < 128; c += 2) {
+        fma2(x[c], x[c + 1], x[c], x[c + 1], c2, c2, nm, nm);
+        x[c] = ex2_approx(x[c]);
+        x[c + 1] = ex2_approx(x[c + 1]);
+        const int q = (c >> 1) & 3;
+        add2(sa[q], sb[q], sa[q], sb[q], x[c], x[c + 1]);
+        pk[c >> 1] = pack_bf16x2(x[c], x[c + 1]);
       }
       add2(sa[0], sb[0], sa[0], sb[0], sa[1], sb[1]);
       add2(sa[2], sb[2], sa[2], sb[2], sa[3], sb[3]);

@@ -391,41 +391,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// 2^a, 2^b on the FMA pipe (two lanes per instruction), for a share of a
-// softmax's exponentials so the special-function unit is not the only
-// pipe that takes them.  Range reduction x = n + f, n = round(x): adding
-// 1.5 * 2^23 leaves n in the low mantissa bits of t, and f = x - (t - 1.5 * 2^23)
-// lies in [-1/2, 1/2].  2^f comes from a cubic fitted by minimax in relative
-// error on that interval (linear programming over 8001 points; largest error
-// 7.5e-5 in float32 Horner form, 26x below half a bf16 unit in the last
-// place).  2^n is added to the exponent field of 2^f: t's bits times 2^23 are
-// n << 23 modulo 2^32 (the shift constant's own bits vanish), one integer
-// multiply-add.  Inputs must be finite and >= -125 (the caller clamps), so
-// the exponent field stays positive; they are <= 2^22 in magnitude.
-__device__ __forceinline__ void exp2_fma2(float& a, float& b) {
-  float ta, tb, pa, pb;
-  asm("{\n\t.reg .b64 x, k, t, f, p, c;\n\t"
-      "mov.b64 x, {%4, %5};\n\t"
-      "mov.b64 k, {%6, %6};\n\t"
-      "add.rn.f32x2 t, x, k;\n\t"
-      "sub.rn.f32x2 f, t, k;\n\t"
-      "sub.rn.f32x2 f, x, f;\n\t"
-      "mov.b64 c, {%7, %7};\n\t"
-      "mov.b64 p, {%8, %8};\n\t"
-      "fma.rn.f32x2 p, c, f, p;\n\t"
-      "mov.b64 c, {%9, %9};\n\t"
-      "fma.rn.f32x2 p, p, f, c;\n\t"
-      "mov.b64 c, {%10, %10};\n\t"
-      "fma.rn.f32x2 p, p, f, c;\n\t"
-      "mov.b64 {%0, %1}, t;\n\t"
-      "mov.b64 {%2, %3}, p;\n\t}"
-      : "=f"(ta), "=f"(tb), "=f"(pa), "=f"(pb)
-      : "f"(a), "f"(b), "f"(12582912.0f), "f"(0x1.c3f766p-5f), "f"(0x1.f0de1ep-3f),
-        "f"(0x1.62f31ap-1f), "f"(0x1.fff692p-1f));
-  a = __uint_as_float(__float_as_uint(ta) * 8388608u + __float_as_uint(pa));
-  b = __uint_as_float(__float_as_uint(tb) * 8388608u + __float_as_uint(pb));
-}
-
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;

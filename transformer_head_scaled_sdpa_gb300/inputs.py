@@ -81,6 +81,12 @@ WORKLOADS = [
     # the small case for detailed profiler captures
     Workload("gpt3_causal_b1", 1, 96, 128, 2048, 2048, MASK_CAUSAL, torch.bfloat16,
              input_scale=0.5, note="GPT-3-like, one sequence"),
+    # heads of 256 features (the pages fix no head width: keys of d_k, values
+    # of d_v), 16 heads at L 2048: the wide kernel's measurement rows
+    Workload("d256_L2048", 4, 16, 256, 2048, 2048, MASK_NONE, torch.bfloat16,
+             note="16 heads of d_k 256, L 2048"),
+    Workload("d256_L2048_causal", 4, 16, 256, 2048, 2048, MASK_CAUSAL, torch.bfloat16,
+             note="16 heads of d_k 256, L 2048, causal"),
 ]
 WORKLOAD_INDEX = {w.name: i for i, w in enumerate(WORKLOADS)}
 BY_NAME = {w.name: w for w in WORKLOADS}
