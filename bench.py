@@ -36,6 +36,10 @@ bounded sample of the same workload (rank 0 only).
 workload for a seeded dout, with the forward's output and row lse resident);
 FLOPs = 2.5x the forward's (five products over the visible pairs).
 
+``--pass gemm``: the layers' projection GEMM (mha_gemm_bf16) alone, on the
+GPT-3-like and base-model projection shapes, beside torch.matmul (cuBLAS) on
+the same operands.
+
 Decode workloads (``--workload gpt3_decode`` / ``base_decode`` /
 ``gpt3_decode_b1``): one step = one mha_decode call (every sequence's new
 query against its key/value cache); the metric is the step's algorithmic
@@ -1168,6 +1172,76 @@ def run_reference_bwd(args):
     }), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# the projection GEMM alone (mha_gemm_bf16) against torch.matmul
+# ---------------------------------------------------------------------------
+GEMM_METRIC = "projection GEMM TFLOP/s (bf16, float32 accumulation, 1 GB300)"
+# (M, N, K) of the layers' projections: GPT-3-like Q|K|V and W^O (B 4 x L 2048
+# rows), a square reference, the base model's Q|K|V and W^O (32 x 128 rows)
+GEMM_SHAPES = [(8192, 36864, 12288), (8192, 12288, 12288), (8192, 8192, 8192),
+               (4096, 1536, 512), (4096, 512, 512)]
+
+
+def run_gemm(args):
+    rank, world = mdist.init("nccl")
+    _, _, local_rank = mdist.env_rank_world()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from transformer_head_scaled_sdpa_gb300 import binding, build
+    if rank == 0:
+        build.build()
+    mdist.barrier(dev)
+    build.build()
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    rows = []
+    g = torch.Generator(device="cpu").manual_seed(4321)
+    for M, N, K in GEMM_SHAPES:
+        a = torch.randn(M, K, generator=g).to(torch.bfloat16).to(dev)
+        b = (torch.randn(K, N, generator=g) / K ** 0.5).to(torch.bfloat16).to(dev)
+        c = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        flops = 2.0 * M * N * K
+        res = {}
+        for name, fn in (("ours", lambda: binding.mha_gemm_bf16(a, b, c)),
+                         ("torch", lambda: torch.matmul(a, b, out=c))):
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize(dev)
+            n = max(3, int(2e12 / flops))
+            best = float("inf")
+            for _ in range(3):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(n):
+                    fn()
+                e1.record()
+                torch.cuda.synchronize(dev)
+                best = min(best, e0.elapsed_time(e1) / n)
+            res[name] = flops / (best * 1e-3) / 1e12
+        rc = binding.mha_sync_status()
+        if rc != 0:
+            raise binding.MhaError(rc, "gemm")
+        rows.append({"M": M, "N": N, "K": K, "tflops": res["ours"], "torch_tflops": res["torch"],
+                     "ratio_to_torch": res["ours"] / res["torch"], "frac": res["ours"] / peak})
+        del a, b, c
+    if rank == 0:
+        first = rows[0]
+        print(json.dumps({
+            "metric": GEMM_METRIC, "value": first["tflops"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) x, N(0,1/K) weights)",
+            "config": {"workload": "projection GEMMs", "shapes": GEMM_SHAPES,
+                       "timing": "CUDA events around back-to-back calls, best of 3"},
+            "roofline": {"bound": "tensor", "achieved": first["tflops"], "peak": peak,
+                         "unit": UNIT, "frac": first["frac"], "traffic": None,
+                         "peak_source": f"{peak_src} dense bf16 (burst)",
+                         "kernel": "gemm_bf16_kernel"},
+            "gemms": rows}), flush=True)
+    mdist.finish()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1178,7 +1252,7 @@ def main():
                     choices=sorted(inputs.BY_NAME) + sorted(inputs.DECODE_BY_NAME) +
                     sorted(inputs.LAYER_BY_NAME))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd"])
+    ap.add_argument("--pass", dest="pass_", default="fwd", choices=["fwd", "bwd", "gemm"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the per-configuration sweep of the default forward run")
@@ -1190,6 +1264,11 @@ def main():
     if args.steps < 1:
         ap.error("--steps must be >= 1")
     decode = args.workload in inputs.DECODE_BY_NAME
+    if args.pass_ == "gemm":
+        if args.impl == "reference":
+            ap.error("--pass gemm has no reference arm")
+        run_gemm(args)
+        return
     if args.workload in inputs.LAYER_BY_NAME:
         if args.pass_ == "bwd":
             ap.error("--pass bwd applies to the attention workloads")
