@@ -31,9 +31,15 @@
 //              run in order)
 //   warp 5     TMA producer: the next unit's Q into a staging buffer, then K_j
 //              and V_j (64 keys x 256 features) into two-stage rings
-//   warps 6-7  idle
-// Units are dispatched statically (CTA c takes units c, c + grid, ...), in
-// groups of heads whose K/V stay in L2, heaviest causal query tiles first.
+//   warp 6     scheduler: the grid has one CTA per unit, but CTAs are
+//              persistent: once a CTA runs, this warp cancels CTAs that have
+//              not started (cluster launch control) and feeds their units to
+//              the other roles through a two-slot queue, so the hardware's
+//              launch order balances the work dynamically (a static striding
+//              of the causal units left the busiest SM 24 % above the mean)
+//   warp 7     idle
+// Units are ordered in groups of heads whose K/V stay in L2, heaviest causal
+// query tiles first.
 // Causal key tiles past a query tile's last row are never loaded; the
 // diagonal tiles and a ragged last tile are masked per element.  Every wait
 // is bounded (abort flag, MHA_ERR_TIMEOUT in the status word).
@@ -45,12 +51,13 @@ namespace mha {
 namespace {
 
 constexpr int kWThreads = 256;
-constexpr int kWMmaWarp = 4, kWProducerWarp = 5;
+constexpr int kWMmaWarp = 4, kWProducerWarp = 5, kWSchedulerWarp = 6;
+constexpr int kWConsumers = 6;    // unit-queue readers: 4 softmax warps, the MMA and producer warps
 constexpr int kWKeys = 64;        // keys per K / V tile
 constexpr int kWStages = 2;       // K and V ring stages
 constexpr float kWRescaleThreshold = 8.0f;
 constexpr long long kWHeadGroupBytes = 32ll << 20;
-constexpr int kRoleWProducer = 11, kRoleWMma = 12, kRoleWSoftmax = 13;
+constexpr int kRoleWProducer = 11, kRoleWMma = 12, kRoleWSoftmax = 13, kRoleWScheduler = 14;
 
 struct WCfg {
   static constexpr int Q_CHUNK = 128 * 128;            // [128 rows x 128 B]
@@ -78,9 +85,13 @@ struct WCfg {
   static constexpr int K_EMPTY = 12 + kWStages;
   static constexpr int V_FULL = 12 + 2 * kWStages;
   static constexpr int V_EMPTY = 12 + 3 * kWStages;
-  static constexpr int NBAR = 12 + 4 * kWStages;
-  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;  // TMEM slot, abort flag
-  static constexpr int SMEM = OFF_MISC + 16 + 1024;
+  static constexpr int UNIT_FULL = 12 + 4 * kWStages;   // + slot: unit published
+  static constexpr int UNIT_EMPTY = 14 + 4 * kWStages;  // + slot: every consumer read it
+  static constexpr int CLC = 16 + 4 * kWStages;         // cancellation response landed
+  static constexpr int NBAR = 17 + 4 * kWStages;
+  // TMEM slot (+0), abort flag (+4), unit queue (+8, +12), CLC response (+16, 16 bytes)
+  static constexpr int OFF_MISC = (OFF_BAR + 8 * NBAR + 15) / 16 * 16;
+  static constexpr int SMEM = OFF_MISC + 32 + 1024;
   static constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S0 = 384, TM_S1 = 448;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
@@ -132,9 +143,22 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
   auto bar = [&](int id) { return s_base + C::OFF_BAR + 8u * static_cast<uint32_t>(id); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* unit_slot = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+  const uint32_t clc_resp = s_base + C::OFF_MISC + 16;
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
-  const int n_units = p.B * p.H * p.n_qtiles;
   constexpr int S = kWStages;
+  // The k-th unit of this CTA from the queue (every consumer warp takes every
+  // unit, in order); -1 at the end of the work or when the CTA gave up.
+  auto next_unit = [&](int k, int role) {
+    const int slot = k & 1;
+    if (!mbar_wait(bar(C::UNIT_FULL + slot), (k >> 1) & 1, abort_flag, p.status,
+                   role * 64 + C::UNIT_FULL + slot))
+      return -1;
+    const int u = unit_slot[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(C::UNIT_EMPTY + slot));
+    return u;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::Q_FULL), 1);
@@ -155,6 +179,11 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
       mbar_init(bar(C::V_FULL + s), 1);
       mbar_init(bar(C::V_EMPTY + s), 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(C::UNIT_FULL + i), 1);
+      mbar_init(bar(C::UNIT_EMPTY + i), kWConsumers);
+    }
+    mbar_init(bar(C::CLC), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -180,7 +209,9 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
     int q_cnt = 0, t = 0;  // Q loads, K/V tiles so far
     int k_issued = 0, v_issued = 0;
     bool ok = true;
-    for (int u = static_cast<int>(blockIdx.x); ok && u < n_units; u += static_cast<int>(gridDim.x)) {
+    for (int k = 0; ok; ++k) {
+      const int u = next_unit(k, kRoleWProducer);
+      if (u < 0) break;
       const WUnit w = wide_unit(p, u);
       if (w.n == 0) continue;
       // the softmax must have copied the previous unit's Q out of the staging buffer
@@ -299,7 +330,9 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
       __syncwarp();
       return true;
     };
-    for (int u = static_cast<int>(blockIdx.x); ok && u < n_units; u += static_cast<int>(gridDim.x)) {
+    for (int k = 0; ok; ++k) {
+      const int u = next_unit(k, kRoleWMma);
+      if (u < 0) break;
       const WUnit w = wide_unit(p, u);
       if (w.n == 0) continue;
       if (!mbar_wait(bar(C::Q_TMEM_FULL), u_cnt & 1, abort_flag, p.status, site + C::Q_TMEM_FULL)) {
@@ -331,7 +364,9 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
     const uint32_t out_base = sOut + static_cast<uint32_t>(warp * 2 * C::OUT_CHUNK);
     int u_cnt = 0, t = 0, chunks = 0;
     bool ok = true;
-    for (int u = static_cast<int>(blockIdx.x); ok && u < n_units; u += static_cast<int>(gridDim.x)) {
+    for (int k = 0; ok; ++k) {
+      const int u = next_unit(k, kRoleWSoftmax);
+      if (u < 0) break;
       const WUnit w = wide_unit(p, u);
       const int qi = w.q0 + row;
       if (w.n > 0) {
@@ -513,6 +548,30 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
     }
     if (lane == 0) tma_store_wait_all();
     __syncwarp();
+  } else if (warp == kWSchedulerWarp && lane == 0) {
+    // ---- scheduler: publishes this CTA's own unit, then keeps one unit of
+    // look-ahead by cancelling CTAs that have not started and taking theirs
+    int unit = static_cast<int>(blockIdx.x);
+    for (int k = 0;; ++k) {
+      const int slot = k & 1;
+      if (k >= 2 && !mbar_wait(bar(C::UNIT_EMPTY + slot), ((k >> 1) - 1) & 1, abort_flag,
+                               p.status, kRoleWScheduler * 64 + C::UNIT_EMPTY + slot))
+        unit = -1;
+      unit_slot[slot] = unit;
+      mbar_arrive(bar(C::UNIT_FULL + slot));
+      if (unit < 0) break;
+      mbar_arrive_expect_tx(bar(C::CLC), 16);
+      clc_try_cancel(clc_resp, bar(C::CLC));
+      // the response lands asynchronously: wait for it even when giving up,
+      // so nothing is written to shared memory after the CTA exits
+      volatile int never = 0;
+      if (!mbar_wait(bar(C::CLC), k & 1, &never, p.status, kRoleWScheduler * 64 + C::CLC) ||
+          *abort_flag) {
+        unit = -1;
+      } else {
+        unit = clc_query_first_ctaid_x(clc_resp);  // -1 when nothing was cancelled
+      }
+    }
   }
 
   tc_fence_before();
@@ -541,19 +600,17 @@ cudaError_t launch_fwd_wide(const Bf16Params& params, cudaStream_t stream, Launc
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   static bool attr_set[64] = {};
-  static int sms[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
     e = cudaFuncSetAttribute(fwd_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              WCfg::SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const long long units = static_cast<long long>(p.B) * p.H * p.n_qtiles;
   if (units <= 0 || units > 0x7fffffffll) return cudaErrorInvalidValue;
-  const int grid = static_cast<int>(units < sms[dev] ? units : sms[dev]);
+  // one CTA per unit; running CTAs take over the units of those not started
+  const int grid = static_cast<int>(units);
   e = launch_serialized(fwd_wide_kernel, dim3(grid), dim3(kWThreads), WCfg::SMEM, stream, p);
   if (e != cudaSuccess) return e;
   if (info) {
