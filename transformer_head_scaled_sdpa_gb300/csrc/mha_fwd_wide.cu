@@ -23,8 +23,10 @@
 //
 // 256 threads in four roles:
 //   warps 0-3  softmax + epilogue (thread r owns query row r = TMEM lane r);
-//              at the start of each unit they also copy that unit's Q tile
-//              from shared memory into TMEM (one row each)
+//              right after a unit's last weights (before its epilogue) they
+//              copy the next unit's Q tile from shared memory into TMEM (one
+//              row each), so the next unit's first scores are computed while
+//              the epilogue runs
 //   warp 4     TMEM allocator and MMA issuer: S(0), S(1), PV(0), S(2), PV(1),
 //              ..., so S(j+1) runs while the softmax works on S(j), and S(j+2)
 //              overwrites P(j) only after PV(j) read it (MMAs of one thread
@@ -362,42 +364,46 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
     const float c2 = p.scale_log2;
     const int dv_n = p.dv_n;
     const uint32_t out_base = sOut + static_cast<uint32_t>(warp * 2 * C::OUT_CHUNK);
-    int u_cnt = 0, t = 0, chunks = 0;
+    int q_copies = 0, o_cnt = 0, t = 0, chunks = 0;
     bool ok = true;
-    for (int k = 0; ok; ++k) {
-      const int u = next_unit(k, kRoleWSoftmax);
-      if (u < 0) break;
-      const WUnit w = wide_unit(p, u);
-      const int qi = w.q0 + row;
-      if (w.n > 0) {
-        // copy this row of Q (256 bf16, 128-byte swizzle) from the staging
-        // buffer into TMEM, once the previous unit's last S no longer reads it
-        if (!mbar_wait(bar(C::Q_FULL), u_cnt & 1, abort_flag, p.status, site + C::Q_FULL) ||
-            (u_cnt > 0 && !mbar_wait(bar(C::Q_TMEM_FREE), (u_cnt - 1) & 1, abort_flag, p.status,
-                                     site + C::Q_TMEM_FREE))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+    // Copies this thread's row of a unit's Q (256 bf16, 128-byte swizzle)
+    // from the staging buffer into TMEM, once the last S of the previous unit
+    // with key tiles no longer reads TMEM's Q.
+    auto copy_q = [&]() -> bool {
+      if (!mbar_wait(bar(C::Q_FULL), q_copies & 1, abort_flag, p.status, site + C::Q_FULL) ||
+          (q_copies > 0 && !mbar_wait(bar(C::Q_TMEM_FREE), (q_copies - 1) & 1, abort_flag,
+                                      p.status, site + C::Q_TMEM_FREE)))
+        return false;
+      tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            const uint4 x = ld_shared_v4(sQ + c * C::Q_CHUNK + row * 128 +
-                                         (static_cast<uint32_t>(v ^ (row & 7)) << 4));
-            r[4 * v] = x.x;
-            r[4 * v + 1] = x.y;
-            r[4 * v + 2] = x.z;
-            r[4 * v + 3] = x.w;
-          }
-          tmem_st32(tmem + lane_off + C::TM_Q + 32u * c, r);
+        for (int v = 0; v < 8; ++v) {
+          const uint4 x = ld_shared_v4(sQ + c * C::Q_CHUNK + row * 128 +
+                                       (static_cast<uint32_t>(v ^ (row & 7)) << 4));
+          r[4 * v] = x.x;
+          r[4 * v + 1] = x.y;
+          r[4 * v + 2] = x.z;
+          r[4 * v + 3] = x.w;
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(C::Q_TMEM_FULL));
-        mbar_arrive(bar(C::Q_STAGE_FREE));
+        tmem_st32(tmem + lane_off + C::TM_Q + 32u * c, r);
       }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::Q_TMEM_FULL));
+      mbar_arrive(bar(C::Q_STAGE_FREE));
+      ++q_copies;
+      return true;
+    };
+    int u = next_unit(0, kRoleWSoftmax);
+    WUnit w{};
+    if (u >= 0) {
+      w = wide_unit(p, u);
+      if (w.n > 0) ok = copy_q();
+    }
+    for (int k = 0; ok && u >= 0; ++k) {
+      const int qi = w.q0 + row;
       float m_ref = 0.f, l = 0.f;
       for (int j = 0; j < w.n; ++j, ++t) {
         const int buf = t & 1;
@@ -490,10 +496,22 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
         mbar_arrive(bar(C::P_FULL + buf));
       }
       if (!ok) break;
+      // The next unit's Q goes into TMEM now (this unit's last S is complete:
+      // its scores were read), so the MMA warp computes the next unit's first
+      // scores while this unit's epilogue runs.
+      const int u_next = next_unit(k + 1, kRoleWSoftmax);
+      WUnit w_next{};
+      if (u_next >= 0) {
+        w_next = wide_unit(p, u_next);
+        if (w_next.n > 0 && !copy_q()) {
+          ok = false;
+          break;
+        }
+      }
       // ---- epilogue: O / l to bf16, this warp's 32 rows, 64 columns at a time
       // through the warp's staging buffers and a TMA store
       if (w.n > 0) {
-        if (!mbar_wait(bar(C::O_DONE), u_cnt & 1, abort_flag, p.status, site + C::O_DONE)) {
+        if (!mbar_wait(bar(C::O_DONE), o_cnt & 1, abort_flag, p.status, site + C::O_DONE)) {
           ok = false;
           break;
         }
@@ -544,7 +562,9 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
         }
         __syncwarp();
       }
-      if (w.n > 0) ++u_cnt;
+      if (w.n > 0) ++o_cnt;
+      u = u_next;
+      w = w_next;
     }
     if (lane == 0) tma_store_wait_all();
     __syncwarp();
