@@ -357,18 +357,9 @@ int mha_sync_status(void* stream);
  */
 int mha_selftest_timeout(void* stream);
 
-/*
- * mha_debug_withhold_p -- test hook (not for production use).  While on, every
- * later mha_fwd launch withholds one internal pipeline signal (the first
- * probability tile of its first query tile), so the kernel's bounded wait runs
- * out: after about a second each CTA aborts, waits for its own copies and
- * tensor-core operations, frees its tensor memory and records
- * MHA_ERR_TIMEOUT, which mha_sync_status returns.  Outputs of such a launch
- * are undefined.  Off by default; process-wide.
- */
-void mha_debug_withhold_p(int on);
 
-/* mha_status_string -- static English text for a status code. */
+/* mha_status_string -- static English text for a status code.  (The test
+ * hooks of the library are declared apart, in mha_test_hooks.h.) */
 const char* mha_status_string(int status);
 
 /*

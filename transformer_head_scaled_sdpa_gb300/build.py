@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(BUILD_DIR, "libmha.so")
 SOURCES = ["mha_abi.cu", "mha_fwd_bf16.cu", "mha_fwd_wide.cu", "mha_fwd_f32.cu", "mha_decode.cu",
            "mha_bwd.cu", "mha_gemm.cu"]
 HEADERS = [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "kernels.h"),
-           os.path.join(INCLUDE, "mha.h")]
+           os.path.join(INCLUDE, "mha.h"), os.path.join(INCLUDE, "mha_test_hooks.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-Wall", "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -1,4 +1,5 @@
-// mha_abi.cu -- the C ABI of libmha.so (declared in include/mha.h): argument
+// mha_abi.cu -- the C ABI of libmha.so (declared in include/mha.h, its test
+// hooks in include/mha_test_hooks.h): argument
 // checks, TMA tensor-map encoding, kernel dispatch, the host-buffer entry and
 // the per-device status word.
 #include <cuda.h>
@@ -10,6 +11,7 @@
 #include <mutex>
 
 #include "../../include/mha.h"
+#include "../../include/mha_test_hooks.h"
 #include "kernels.h"
 
 namespace {
