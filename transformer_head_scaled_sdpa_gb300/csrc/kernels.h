@@ -165,17 +165,12 @@ struct GemmParams {
   CUtensorMap tm_c;  // C [M, N] (row stride ldc), box {64 n, 32 rows}, 128-byte swizzle
   DeviceStatus* status;
   int M, N, K;
-  int tiles_m, tiles_n;  // ceil(M / 128), ceil(N / 256)
-  int k_blocks;          // ceil(K / 64)
+  int tiles_m, tiles_n;  // set by the launch: row blocks (128 or 256 rows), ceil(N / 256)
+  int k_blocks;          // set by the launch: ceil(K / 64)
 };
 
-// Tile sizes of the GEMM kernel (rows and columns of C per tile, k per step).
-int gemm_tile_rows();
-int gemm_tile_cols();
-int gemm_k_block();
-
-// Launches the GEMM (one persistent CTA per SM, or per tile when fewer);
-// adds one to info->kernels.
+// Launches the GEMM (one persistent CTA per SM, or per tile when fewer; tiles
+// of 128 x 256, or 256 x 256 when K is long); adds one to info->kernels.
 cudaError_t launch_gemm(const GemmParams& p, cudaStream_t stream, LaunchInfo* info);
 
 }  // namespace mha

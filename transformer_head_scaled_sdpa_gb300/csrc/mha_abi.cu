@@ -646,6 +646,7 @@ static int gemm_bf16(int M, int N, int K, const void* A, long long lda, const vo
                      mha::LaunchInfo* info) {
   mha::GemmParams p;
   std::memset(&p, 0, sizeof(p));
+  // (A is loaded in 128-row boxes: a 256-row tile takes two)
   if (!encode_2d(&p.tm_a, A, M, K, lda, 64, 128) || !encode_2d(&p.tm_b, B, K, N, ldb, 64, 64) ||
       !encode_2d(&p.tm_c, C, M, N, ldc, 64, 32))
     return MHA_ERR_UNSUPPORTED;
@@ -653,9 +654,6 @@ static int gemm_bf16(int M, int N, int K, const void* A, long long lda, const vo
   p.M = M;
   p.N = N;
   p.K = K;
-  p.tiles_m = (M + mha::gemm_tile_rows() - 1) / mha::gemm_tile_rows();
-  p.tiles_n = (N + mha::gemm_tile_cols() - 1) / mha::gemm_tile_cols();
-  p.k_blocks = (K + mha::gemm_k_block() - 1) / mha::gemm_k_block();
   return mha::launch_gemm(p, s, info) == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
 }
 

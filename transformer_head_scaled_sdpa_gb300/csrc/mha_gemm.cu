@@ -20,6 +20,12 @@
 //              shared memory (128-byte swizzle) and writes them with a TMA
 //              store; each warp stages and stores its own rows, so the
 //              epilogue needs no barrier across warps
+// With a long K (a tile's products take far longer than its epilogue) the
+// tiles are 256 x 256 instead: two 128-row accumulators (all 512 TMEM
+// columns) share every B block, so each k step moves 64 KB through TMA for
+// 1024 tensor cycles instead of 48 KB for 512 -- two thirds of the L2 to
+// shared-memory traffic per flop -- at the cost of the epilogue no longer
+// overlapping the next tile (one accumulator pair, three 64 KB stages).
 // Rows, columns and k past the matrix edges are read as zero by the tensor
 // maps and never written.  Every wait is bounded: a role that gives up
 // raises the CTA's abort flag, the others follow, each waits for its own
@@ -32,46 +38,56 @@ namespace mha {
 namespace {
 
 constexpr int kGemmThreads = 192;
-constexpr int kGemmBM = 128, kGemmBN = 256, kGemmBK = 64;
-constexpr int kGemmStages = 4;
-constexpr int kGemmGroupM = 16;  // row blocks walked together (L2 reuse)
+constexpr int kGemmBN = 256, kGemmBK = 64;
 constexpr int kGemmProducerWarp = 0, kGemmMmaWarp = 1;
 constexpr int kRoleGemmProducer = 8, kRoleGemmMma = 9, kRoleGemmEpilogue = 10;
 
+// TALL: 256-row tiles (two 128-row accumulators, no second accumulator set);
+// otherwise 128-row tiles with two accumulators in turn.
+template <bool TALL>
 struct GemmCfg {
-  static constexpr int A_BYTES = kGemmBM * kGemmBK * 2;         // 128 rows x 128 B
+  static constexpr int BM = TALL ? 256 : 128;
+  static constexpr int HALVES = BM / 128;                        // 128-row accumulators per tile
+  static constexpr int ACC_SETS = TALL ? 1 : 2;                  // tiles in TMEM at once
+  static constexpr int STAGES = TALL ? 3 : 4;
+  static constexpr int GROUP_M = TALL ? 8 : 16;                  // row blocks walked together (L2 reuse)
+  static constexpr int A_HALF = 128 * kGemmBK * 2;               // 128 rows x 128 B
+  static constexpr int A_BYTES = HALVES * A_HALF;
   static constexpr int B_CHUNK = kGemmBK * 128;                  // 64 k rows x 64 n (128 B)
   static constexpr int B_BYTES = (kGemmBN / 64) * B_CHUNK;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;          // 48 KB
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;          // 48 KB, or 64 KB when TALL
   static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = kGemmStages * A_BYTES;
+  static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OUT_CHUNK = 32 * 128;                     // one warp's 32 rows x 64 bf16
-  static constexpr int OFF_OUT = OFF_B + kGemmStages * B_BYTES;  // 4 warps x 2 buffers
+  static constexpr int OFF_OUT = OFF_B + STAGES * B_BYTES;       // 4 warps x 2 buffers
   static constexpr int OFF_BAR = OFF_OUT + 8 * OUT_CHUNK;
-  static constexpr int FULL = 0, EMPTY = kGemmStages, ACC_FULL = 2 * kGemmStages,
-                       ACC_EMPTY = 2 * kGemmStages + 2, DRAIN = 2 * kGemmStages + 4;
-  static constexpr int NBAR = 2 * kGemmStages + 5;
+  static constexpr int FULL = 0, EMPTY = STAGES, ACC_FULL = 2 * STAGES,
+                       ACC_EMPTY = 2 * STAGES + 2, DRAIN = 2 * STAGES + 4;
+  static constexpr int NBAR = 2 * STAGES + 5;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;            // TMEM slot, abort flag
   static constexpr int SMEM = OFF_MISC + 16 + 1024;              // + slack to align to 1024
-  static constexpr uint32_t TMEM_COLS = 512;                     // two 128 x 256 accumulators
+  static constexpr uint32_t TMEM_COLS = 512;                     // 2 x 256 float32 columns
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(OFF_B % 1024 == 0 && OFF_OUT % 1024 == 0 && OFF_BAR % 8 == 0, "alignment");
 };
 
-// Output tile t: groups of kGemmGroupM row blocks, row block fastest inside a
+// Output tile t: groups of GROUP_M row blocks, row block fastest inside a
 // group, so the tiles that run at once share A row panels and B column panels.
+template <bool TALL>
 __device__ __forceinline__ void gemm_tile(const GemmParams& p, int t, int& m0, int& n0) {
-  const int per_group = kGemmGroupM * p.tiles_n;
+  constexpr int G = GemmCfg<TALL>::GROUP_M;
+  const int per_group = G * p.tiles_n;
   const int group = t / per_group;
-  const int first = group * kGemmGroupM;
-  const int rows = min(kGemmGroupM, p.tiles_m - first);
+  const int first = group * G;
+  const int rows = min(G, p.tiles_m - first);
   const int in = t - group * per_group;
-  m0 = (first + in % rows) * kGemmBM;
+  m0 = (first + in % rows) * GemmCfg<TALL>::BM;
   n0 = (in / rows) * kGemmBN;
 }
 
+template <bool TALL>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_kernel(const __grid_constant__ GemmParams p) {
-  using C = GemmCfg;
+  using C = GemmCfg<TALL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -82,14 +98,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_kernel(const __grid
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
   const int n_tiles = p.tiles_m * p.tiles_n;
-  constexpr int S = kGemmStages;
+  constexpr int S = C::STAGES;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar(C::FULL + s), 1);
       mbar_init(bar(C::EMPTY + s), 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < C::ACC_SETS; ++a) {
       mbar_init(bar(C::ACC_FULL + a), 1);
       mbar_init(bar(C::ACC_EMPTY + a), 128);
     }
@@ -121,7 +137,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_kernel(const __grid
     bool ok = true;
     for (int t = static_cast<int>(blockIdx.x); ok && t < n_tiles; t += static_cast<int>(gridDim.x)) {
       int m0, n0;
-      gemm_tile(p, t, m0, n0);
+      gemm_tile<TALL>(p, t, m0, n0);
       for (int kb = 0; kb < p.k_blocks; ++kb) {
         const int s = g % S;
         if (g >= S && !mbar_wait(bar(C::EMPTY + s), ((g / S) - 1) & 1, abort_flag, p.status,
@@ -131,7 +147,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_kernel(const __grid
         }
         if (elect_one()) {
           mbar_arrive_expect_tx(bar(C::FULL + s), C::STAGE_BYTES);
-          tma_load_2d(sA + s * C::A_BYTES, &p.tm_a, bar(C::FULL + s), kb * kGemmBK, m0);
+#pragma unroll
+          for (int hf = 0; hf < C::HALVES; ++hf)
+            tma_load_2d(sA + s * C::A_BYTES + hf * C::A_HALF, &p.tm_a, bar(C::FULL + s),
+                        kb * kGemmBK, m0 + 128 * hf);
 #pragma unroll
           for (int j = 0; j < kGemmBN / 64; ++j)
             tma_load_2d(sB + s * C::B_BYTES + j * C::B_CHUNK, &p.tm_b, bar(C::FULL + s),
@@ -151,17 +170,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_kernel(const __grid
     // step inside the 128-byte swizzle atom); B N-major (64-wide n chunks
     // B_CHUNK apart, 8-row k groups 1024 B apart, +2048 B per K16 step)
     const int site = kRoleGemmMma * 64;
-    constexpr uint32_t idesc = idesc_bf16_f32(kGemmBM, kGemmBN, false, true);
+    constexpr uint32_t idesc = idesc_bf16_f32(128, kGemmBN, false, true);
     const uint64_t da0 = smem_desc_sw128(sA, 16, 1024);
     const uint64_t db0 = smem_desc_sw128(sB, C::B_CHUNK, 1024);
     int g = 0, i = 0;
     bool ok = true;
     for (int t = static_cast<int>(blockIdx.x); ok && t < n_tiles;
          t += static_cast<int>(gridDim.x), ++i) {
-      const int a = i & 1;
-      // the epilogue must have read this accumulator's previous tile
-      if (i >= 2 && !mbar_wait(bar(C::ACC_EMPTY + a), ((i >> 1) - 1) & 1, abort_flag, p.status,
-                               site + C::ACC_EMPTY + a)) {
+      const int a = C::ACC_SETS == 2 ? (i & 1) : 0;
+      const int use = C::ACC_SETS == 2 ? (i >> 1) : i;  // earlier tiles in this accumulator set
+      // the epilogue must have read this accumulator set's previous tile
+      if (use >= 1 && !mbar_wait(bar(C::ACC_EMPTY + a), (use - 1) & 1, abort_flag, p.status,
+                                 site + C::ACC_EMPTY + a)) {
         ok = false;
         break;
       }
@@ -179,8 +199,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_kernel(const __grid
           const uint64_t db = db0 + static_cast<uint64_t>((s * C::B_BYTES) >> 4);
 #pragma unroll
           for (int ks = 0; ks < kGemmBK / 16; ++ks)
-            umma_ss(acc, da + static_cast<uint64_t>((ks * 32) >> 4),
-                    db + static_cast<uint64_t>((ks * 2048) >> 4), idesc, (kb | ks) ? 1u : 0u);
+#pragma unroll
+            for (int hf = 0; hf < C::HALVES; ++hf)
+              umma_ss(acc + static_cast<uint32_t>(hf * kGemmBN),
+                      da + static_cast<uint64_t>((hf * C::A_HALF + ks * 32) >> 4),
+                      db + static_cast<uint64_t>((ks * 2048) >> 4), idesc, (kb | ks) ? 1u : 0u);
           umma_commit(bar(C::EMPTY + s));  // the stage is free once these are done
         }
         __syncwarp();
@@ -203,21 +226,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_kernel(const __grid
     const uint32_t out_base = sOut + static_cast<uint32_t>(q * 2 * C::OUT_CHUNK);
     int i = 0, chunks = 0;
     for (int t = static_cast<int>(blockIdx.x); t < n_tiles; t += static_cast<int>(gridDim.x), ++i) {
-      const int a = i & 1;
-      if (!mbar_wait(bar(C::ACC_FULL + a), (i >> 1) & 1, abort_flag, p.status,
-                     site + C::ACC_FULL + a))
+      const int a = C::ACC_SETS == 2 ? (i & 1) : 0;
+      const int use = C::ACC_SETS == 2 ? (i >> 1) : i;
+      if (!mbar_wait(bar(C::ACC_FULL + a), use & 1, abort_flag, p.status, site + C::ACC_FULL + a))
         break;
       tc_fence_after();
       int m0, n0;
-      gemm_tile(p, t, m0, n0);
-      const uint32_t tacc = tmem + lane_off + static_cast<uint32_t>(a * kGemmBN);
+      gemm_tile<TALL>(p, t, m0, n0);
+      // chunk cc: accumulator half cc / 4 (rows 128 (cc / 4) ..), columns 64 (cc % 4) ..
 #pragma unroll 1
-      for (int c = 0; c < kGemmBN / 64; ++c, ++chunks) {
+      for (int cc = 0; cc < C::HALVES * (kGemmBN / 64); ++cc, ++chunks) {
+        const int hf = cc / (kGemmBN / 64), c = cc % (kGemmBN / 64);
+        const uint32_t tacc = tmem + lane_off + static_cast<uint32_t>((a + hf) * kGemmBN);
         uint32_t r[64];
         tmem_ld32(tacc + 64u * c, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
         tmem_ld32(tacc + 64u * c + 32u, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
         tmem_ld_wait();
-        if (c == kGemmBN / 64 - 1) {
+        if (cc == C::HALVES * (kGemmBN / 64) - 1) {
           // the accumulator may take the next tile from here on
           tc_fence_before();
           mbar_arrive(bar(C::ACC_EMPTY + a));
@@ -239,8 +264,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_kernel(const __grid
         fence_proxy_async_smem();
         __syncwarp();
         // (a box wholly past the matrix's last row or column is not stored)
-        if (lane == 0 && n0 + 64 * c < p.N && m0 + 32 * q < p.M) {
-          tma_store_2d(&p.tm_c, stage, n0 + 64 * c, m0 + 32 * q);
+        const int row0 = m0 + 128 * hf + 32 * q;
+        if (lane == 0 && n0 + 64 * c < p.N && row0 < p.M) {
+          tma_store_2d(&p.tm_c, stage, n0 + 64 * c, row0);
           tma_store_commit();
         }
         __syncwarp();
@@ -262,7 +288,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_kernel(const __grid
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmParams& p, cudaStream_t stream, LaunchInfo* info) {
+namespace {
+
+template <bool TALL>
+cudaError_t launch_gemm_t(const GemmParams& params, cudaStream_t stream, LaunchInfo* info) {
+  using C = GemmCfg<TALL>;
+  GemmParams p = params;
+  p.tiles_m = (p.M + C::BM - 1) / C::BM;
+  p.tiles_n = (p.N + kGemmBN - 1) / kGemmBN;
+  p.k_blocks = (p.K + kGemmBK - 1) / kGemmBK;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -270,8 +304,8 @@ cudaError_t launch_gemm(const GemmParams& p, cudaStream_t stream, LaunchInfo* in
   static int sms[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             GemmCfg::SMEM);
+    e = cudaFuncSetAttribute(gemm_bf16_kernel<TALL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
@@ -280,19 +314,28 @@ cudaError_t launch_gemm(const GemmParams& p, cudaStream_t stream, LaunchInfo* in
   const long long tiles = static_cast<long long>(p.tiles_m) * p.tiles_n;
   if (tiles <= 0 || tiles > 0x7fffffffll) return cudaErrorInvalidValue;
   const int grid = static_cast<int>(tiles < sms[dev] ? tiles : sms[dev]);
-  e = launch_serialized(gemm_bf16_kernel, dim3(grid), dim3(kGemmThreads), GemmCfg::SMEM, stream, p);
+  e = launch_serialized(gemm_bf16_kernel<TALL>, dim3(grid), dim3(kGemmThreads), C::SMEM, stream, p);
   if (e != cudaSuccess) return e;
   if (info) {
     info->kernels += 1;
     info->grid = grid;
     info->block = kGemmThreads;
-    info->smem = GemmCfg::SMEM;
+    info->smem = C::SMEM;
   }
   return cudaGetLastError();
 }
 
-int gemm_tile_rows() { return kGemmBM; }
-int gemm_tile_cols() { return kGemmBN; }
-int gemm_k_block() { return kGemmBK; }
+}  // namespace
+
+// The 256-row tiles when K is long enough that a tile's products (K / 64 k
+// steps of 1024 tensor cycles) dwarf its epilogue, which they do not overlap
+// (measured: +9 to +12 % at K 4096 to 12288 against the 128-row tiles, -5 %
+// at K 512).
+constexpr int kGemmTallMinK = 4096;
+
+cudaError_t launch_gemm(const GemmParams& p, cudaStream_t stream, LaunchInfo* info) {
+  return p.K >= kGemmTallMinK ? launch_gemm_t<true>(p, stream, info)
+                              : launch_gemm_t<false>(p, stream, info);
+}
 
 }  // namespace mha
