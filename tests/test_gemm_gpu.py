@@ -7,7 +7,8 @@ output rounding (half a bf16 unit, 2^-9 relative) plus float32 summation
 differences: each element within 2^-8 of its magnitude plus 2^-14 of the
 largest, and the whole within 2^-9 relative Frobenius.  Shapes cover single
 tiles, ragged edges in M, N and K, strided row views (the layer reads column
-blocks of the packed weight in place), more tiles than SMs, and K = 0.
+blocks of the packed weight in place), more tiles than SMs, K = 0, and both
+tilings (128-row tiles below K = 4096, 256-row tiles from there on).
 """
 import pytest
 import torch
@@ -45,6 +46,8 @@ def _check(got, ref, what):
 SHAPES = [
     (1, 8, 8), (128, 256, 64), (100, 200, 72), (300, 520, 200), (257, 1000, 1032),
     (1024, 768, 512), (2048, 1536, 512), (96, 4104, 40),
+    # K >= 4096: 256-row tiles (two accumulators), ragged in M, N and K
+    (300, 520, 4104), (129, 264, 4096), (513, 776, 6152),
 ]
 
 

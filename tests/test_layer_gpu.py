@@ -52,6 +52,7 @@ SHAPES = [
     (3, 150, 150, 192, 6, 32, BOTH, False, [150, 64, 1]),
     (1, 5, 9, 64, 2, 32, NONE, True, None),
     (2, 260, 260, 384, 3, 96, NONE, False, None),      # d_model != H d_k
+    (1, 256, 256, 4096, 32, 128, CAUSAL, False, None),  # K 4096: 256-row GEMM tiles
 ]
 
 
