@@ -365,6 +365,7 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
     const int dv_n = p.dv_n;
     const uint32_t out_base = sOut + static_cast<uint32_t>(warp * 2 * C::OUT_CHUNK);
     int q_copies = 0, o_cnt = 0, t = 0, chunks = 0;
+    bool prev_stored = true;  // the previous chunk issued a TMA store
     bool ok = true;
     // Copies this thread's row of a unit's Q (256 bf16, 128-byte swizzle)
     // from the staging buffer into TMEM, once the last S of the previous unit
@@ -524,7 +525,16 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
       const int n_chunks = (dv_n + 63) / 64;
       for (int c = 0; c < n_chunks; ++c, ++chunks) {
         const uint32_t stage = out_base + static_cast<uint32_t>((chunks & 1) * C::OUT_CHUNK);
-        if (lane == 0) tma_store_wait_read_1();
+        // the store issued from this buffer two chunks ago must have read it
+        // (at most one group still reading when the previous chunk stored,
+        // none when it stored nothing)
+        if (lane == 0) {
+          if (prev_stored) {
+            tma_store_wait_read_1();
+          } else {
+            tma_store_wait_read();
+          }
+        }
         __syncwarp();
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -556,7 +566,8 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
         fence_proxy_async_smem();
         __syncwarp();
         // (a warp whose 32 rows all lie past Lq stores nothing)
-        if (lane == 0 && w.q0 + 32 * warp < p.Lq) {
+        prev_stored = w.q0 + 32 * warp < p.Lq;
+        if (lane == 0 && prev_stored) {
           tma_store_4d(&p.tm_o, stage, 64 * c, w.h, w.q0 + 32 * warp, w.b);
           tma_store_commit();
         }

@@ -225,6 +225,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_kernel(const __grid
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
     const uint32_t out_base = sOut + static_cast<uint32_t>(q * 2 * C::OUT_CHUNK);
     int i = 0, chunks = 0;
+    bool prev_stored = true;  // the previous chunk issued a TMA store
     for (int t = static_cast<int>(blockIdx.x); t < n_tiles; t += static_cast<int>(gridDim.x), ++i) {
       const int a = C::ACC_SETS == 2 ? (i & 1) : 0;
       const int use = C::ACC_SETS == 2 ? (i >> 1) : i;
@@ -248,8 +249,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_kernel(const __grid
           mbar_arrive(bar(C::ACC_EMPTY + a));
         }
         const uint32_t stage = out_base + static_cast<uint32_t>((chunks & 1) * C::OUT_CHUNK);
-        // the store issued from this buffer two chunks ago must have read it
-        if (lane == 0) tma_store_wait_read_1();
+        // The store issued from this buffer two chunks ago must have read it:
+        // with the previous chunk's store committed after it, at most one
+        // group may still be reading; when the previous chunk stored nothing
+        // (its box lay wholly past the matrix), none may.
+        if (lane == 0) {
+          if (prev_stored) {
+            tma_store_wait_read_1();
+          } else {
+            tma_store_wait_read();
+          }
+        }
         __syncwarp();
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -265,7 +275,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_bf16_kernel(const __grid
         __syncwarp();
         // (a box wholly past the matrix's last row or column is not stored)
         const int row0 = m0 + 128 * hf + 32 * q;
-        if (lane == 0 && n0 + 64 * c < p.N && row0 < p.M) {
+        prev_stored = n0 + 64 * c < p.N && row0 < p.M;
+        if (lane == 0 && prev_stored) {
           tma_store_2d(&p.tm_c, stage, n0 + 64 * c, row0);
           tma_store_commit();
         }
