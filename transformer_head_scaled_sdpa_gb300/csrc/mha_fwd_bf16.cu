@@ -67,12 +67,13 @@ constexpr int kSoftmaxWarp0 = 0;
 constexpr int kMmaWarp = 8, kProducerWarp = 9, kMma1Warp = 11;  // warp 10: scheduler
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p stays <= 2^8
 // Heads dispatched together are chosen by their K/V bytes, about this much
-// per group, so a group's K/V stay in L2 while its query blocks run (32 heads
-// of the GPT-3-like shape, 64 of big16 L 2048, every head of the base-model
-// shapes).  Larger groups were faster in short runs (128 MiB: GPT-3-like +4 %
-// at full clock) but doubled that kernel's DRAM reads, and under the power cap
-// a 2000-step run lost 5 % to the lower clock.
-constexpr long long kHeadGroupBytes = 32ll << 20;
+// per group, so a group's K/V stay in L2 while its query blocks run (48 heads
+// of the GPT-3-like shape, 96 of big16 L 2048, every head of the base-model
+// shapes).  Measured against 32 MiB: GPT-3-like +2 % in short runs and +1.5 %
+// in 2000-call runs under the power cap, the d_k 64 workloads -0.3 % to +1 %;
+// 64 MiB fell in between; 128 MiB was faster still in short runs but doubled
+// the GPT-3-like kernel's DRAM reads and lost 5 % under the power cap.
+constexpr long long kHeadGroupBytes = 48ll << 20;
 // unit-queue readers: 8 softmax warps, the producer and 1 or 2 MMA warps
 template <int D>
 constexpr int unit_consumers() { return D == 64 ? 11 : 10; }
