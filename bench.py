@@ -331,6 +331,14 @@ def forward_sets(w, case, dev):
     return sets, bytes_in
 
 
+def fwd_kernel_label():
+    """The bf16 forward kernel of the library's last launch: the one-tile
+    kernel (heads wider than 128; short sequences of heads up to 64 wide) runs
+    256-thread CTAs, the two-tile kernel 384."""
+    from transformer_head_scaled_sdpa_gb300 import binding
+    return "fwd_wide_kernel" if binding.last_launch_info()["block"] == 256 else "fwd_bf16_kernel"
+
+
 def measure_forward(w, case, args, dev, stream, rank, steps, warmup):
     """Time `steps` forward calls of the workload (after `warmup`), inputs
     resident; returns (kernel ms per step, max-over-ranks total ms, clocks,
@@ -435,6 +443,7 @@ def config_record(w, case, kernel_ms, launches, peaks, with_oracle):
            "mask": inputs.MASK_NAMES[w.mask_kind],
            "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
            "us_per_step": kernel_ms * 1e3, "launches_per_step": launches,
+           "kernel": fwd_kernel_label() if w.dtype == torch.bfloat16 else "fwd_f32_kernel",
            "tflops": flops_nom / sec / 1e12,
            "tflops_algorithmic": flops_alg / sec / 1e12,
            "frac_tensor_peak": (flops_alg / sec / 1e12 / tensor_peak
@@ -548,7 +557,7 @@ def run_ours(args):
         "roofline": ({"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                       "frac": achieved / peak, "traffic": traffic,
                       "peak_source": f"{peak_src} dense bf16 (burst)",
-                      "kernel": "fwd_wide_kernel" if w.d_k > 128 else "fwd_bf16_kernel",
+                      "kernel": fwd_kernel_label(),
                       "kernel_ms": kernel_ms, "algorithmic_bytes": bytes_alg,
                       "achieved_gbs": bytes_alg / (kernel_ms * 1e-3) / 1e9}
                      if w.dtype == torch.bfloat16 else

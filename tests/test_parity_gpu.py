@@ -300,22 +300,29 @@ def test_empty_and_keyless(mha):
     assert torch.count_nonzero(out) == 0
 
 
-def test_launch_shape(mha):
-    case = pu.to_cuda(inputs.random_case(10, 3, 5, 300, 300, 64))
+@pytest.mark.parametrize("Lq,Lk,d", [(300, 300, 64), (600, 300, 64), (300, 600, 64),
+                                     (300, 300, 128), (512, 512, 40)])
+def test_launch_shape(mha, Lq, Lk, d):
+    """Heads up to 64 wide over sequences of at most 512 take the light
+    one-tile kernel (one 256-thread CTA per (b, h, 128-query tile)); the rest
+    the two-tile kernel (one 384-thread CTA per (b, h, 256 query rows))."""
+    case = pu.to_cuda(inputs.random_case(10, 3, 5, Lq, Lk, d))
     mha.mha_fwd(case["q"], case["k"], case["v"])
     info = mha.last_launch_info()
-    # one CTA per (b, h, block of 256 query rows)
-    assert info["kernels"] == 1 and info["grid"] == 3 * 5 * 2
     assert mha.mha_sync_status() == 0
+    light = d <= 64 and Lq <= 512 and Lk <= 512
+    expect = (3 * 5 * ((Lq + 127) // 128), 256) if light else (3 * 5 * ((Lq + 255) // 256), 384)
+    assert info["kernels"] == 1 and (info["grid"], info["block"]) == expect, info
 
 
 @pytest.mark.parametrize("B,H,Lq,d", [(33, 8, 128, 64), (3, 55, 100, 32), (1, 100, 128, 64),
                                       (1, 300, 129, 64), (3, 55, 128, 128)])
 def test_paired_launch_shape(mha, B, H, Lq, d):
-    """Heads are paired (one CTA per two heads and 128-row query tile) only at
-    widths up to 64, with at most 128 query rows and more heads than SMs."""
+    """Heads are paired (one CTA per two heads and 128-row query tile) only on
+    the two-tile kernel (keys past 512 at widths up to 64), with at most 128
+    query rows and more heads than SMs."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    case = pu.to_cuda(inputs.random_case(11, B, H, Lq, 200, d))
+    case = pu.to_cuda(inputs.random_case(11, B, H, Lq, 600, d))
     mha.mha_fwd(case["q"], case["k"], case["v"])
     info = mha.last_launch_info()
     assert mha.mha_sync_status() == 0
@@ -471,11 +478,14 @@ def test_host_entry_chunks(mha, shape):
     assert torch.equal(out, dev)
 
 
-def test_attention_kernel_timeout_path(mha):
+@pytest.mark.parametrize("L,d", [(256, 64), (768, 64), (768, 128), (300, 256)])
+def test_attention_kernel_timeout_path(mha, L, d):
     """With one pipeline signal withheld, every CTA's bounded wait runs out
     (about a second), the kernel aborts, drains and frees its tensor memory,
-    reports MHA_ERR_TIMEOUT, and the next launch computes correctly."""
-    case = inputs.random_case(12, 1, 2, 256, 256, 64)
+    reports MHA_ERR_TIMEOUT, and the next launch computes correctly.  Covers
+    the light one-tile kernel (L 256), the two-tile kernel at both widths and
+    the wide one-tile kernel."""
+    case = inputs.random_case(12, 1, 2, L, L, d)
     g = pu.to_cuda(case)
     mha.mha_debug_withhold_p(True)
     try:
@@ -492,7 +502,7 @@ def test_attention_kernel_timeout_path_with_turns(mha):
     """The same with the d_k = 64 kernel that passes exponential turns
     between its two query tiles (no mask): the withheld signal still ends in
     MHA_ERR_TIMEOUT, every role leaves, and the next launch is correct."""
-    case = inputs.random_case(13, 1, 2, 256, 512, 64)
+    case = inputs.random_case(13, 1, 2, 256, 1024, 64)
     g = pu.to_cuda(case)
     mha.mha_debug_withhold_p(True)
     try:

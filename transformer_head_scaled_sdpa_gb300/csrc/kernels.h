@@ -129,10 +129,12 @@ cudaError_t launch_bwd(const BwdParams& p, int d, cudaStream_t stream, LaunchInf
 // Launches the bf16 tcgen05 forward for d in {64, 128}.
 cudaError_t launch_fwd_bf16(const Bf16Params& p, int d, cudaStream_t stream, LaunchInfo* info);
 
-// Launches the bf16 tcgen05 forward for heads wider than 128 (d_k, d_v up to
-// 256; mha_fwd_wide.cu): tm_q box {64, 1, 128, 1}, tm_k and tm_v box
-// {64, 1, 64, 1}, tm_o box {64, 1, 32, 1}; sets n_qtiles and head_group.
-cudaError_t launch_fwd_wide(const Bf16Params& p, cudaStream_t stream, LaunchInfo* info);
+// Launches the one-query-tile bf16 tcgen05 forward (mha_fwd_wide.cu) at
+// width 256 (heads wider than 128, d_k and d_v up to 256) or 64 (the light
+// variant, two CTAs per SM, for short sequences of heads up to 64 wide):
+// tm_q box {64, 1, 128, 1}, tm_k and tm_v box {64, 1, 64, 1}, tm_o box
+// {64, 1, 32, 1}; sets n_qtiles and head_group.
+cudaError_t launch_fwd_wide(const Bf16Params& p, int width, cudaStream_t stream, LaunchInfo* info);
 
 // Launches a kernel with programmatic stream serialization: its grid may be
 // scheduled while the previous kernel on the stream drains, so its set-up

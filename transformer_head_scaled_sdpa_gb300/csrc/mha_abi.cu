@@ -294,6 +294,10 @@ int fwd_bf16(const void* q, const void* k, const void* v, void* out, float* lse,
                         Lq, Lk, d_k, d_v, mask_kind, key_lens, scale, dev, s);
 }
 
+// Heads up to 64 wide over short sequences take the light one-tile kernel
+// (two CTAs per SM, so one CTA's unit boundary overlaps another's tiles).
+static bool light_forward(int Lq, int Lk) { return Lq <= 512 && Lk <= 512; }
+
 // The bf16 attention launch on checked arguments (Lq, Lk > 0).  q_row, k_row,
 // v_row: elements between consecutive positions of one head in q, k, v; out is
 // dense [B, Lq, H, d_v].
@@ -305,13 +309,16 @@ int attention_bf16(const void* q, const void* k, const void* v, void* out, float
   if (n_qtiles * B * H > 0x7fffffffll) return MHA_ERR_SHAPE;
   mha::Bf16Params p;
   std::memset(&p, 0, sizeof(p));
-  // the wide kernel streams 64-key tiles and each epilogue warp stores its own
-  // 32 rows
-  const bool wide = bf16_kernel_width(d_k, d_v) > 128;
+  // the one-tile kernel (heads wider than 128; short sequences of heads up to
+  // 64 wide) streams 64-key tiles and each epilogue warp stores its own 32 rows
+  const int width = bf16_kernel_width(d_k, d_v);
+  const bool wide = width > 128;
+  const bool light = width == 64 && light_forward(Lq, Lk);
+  const bool one_tile = wide || light;
   if (!encode_map(&p.tm_q, q, B, Lq, H, d_k, 128, q_row) ||
-      !encode_map(&p.tm_k, k, B, Lk, H, d_k, wide ? 64 : 128, k_row) ||
-      !encode_map(&p.tm_v, v, B, Lk, H, d_v, wide ? 64 : 128, v_row) ||
-      !encode_map(&p.tm_o, out, B, Lq, H, d_v, wide ? 32 : 128))
+      !encode_map(&p.tm_k, k, B, Lk, H, d_k, one_tile ? 64 : 128, k_row) ||
+      !encode_map(&p.tm_v, v, B, Lk, H, d_v, one_tile ? 64 : 128, v_row) ||
+      !encode_map(&p.tm_o, out, B, Lq, H, d_v, one_tile ? 32 : 128))
     return MHA_ERR_UNSUPPORTED;
   p.out = out;
   p.lse = lse;
@@ -327,8 +334,8 @@ int attention_bf16(const void* q, const void* k, const void* v, void* out, float
   p.dk_steps = (d_k + 15) / 16;
   p.dv_n = (d_v + 15) / 16 * 16;
   p.withhold_p = g_withhold_p;
-  const cudaError_t e = wide ? mha::launch_fwd_wide(p, s, &t_info)
-                             : mha::launch_fwd_bf16(p, bf16_kernel_width(d_k, d_v), s, &t_info);
+  const cudaError_t e = one_tile ? mha::launch_fwd_wide(p, wide ? 256 : 64, s, &t_info)
+                                 : mha::launch_fwd_bf16(p, width, s, &t_info);
   return e == cudaSuccess ? MHA_OK : MHA_ERR_LAUNCH;
 }
 

@@ -61,11 +61,15 @@ constexpr float kWRescaleThreshold = 8.0f;
 constexpr long long kWHeadGroupBytes = 32ll << 20;
 constexpr int kRoleWProducer = 11, kRoleWMma = 12, kRoleWSoftmax = 13, kRoleWScheduler = 14;
 
+// W: the widest head the instantiation takes (256, or 64 for the light
+// variant whose CTAs fit two to an SM)
+template <int W>
 struct WCfg {
+  static constexpr int NCH = W / 64;                   // 64-feature chunks
   static constexpr int Q_CHUNK = 128 * 128;            // [128 rows x 128 B]
-  static constexpr int Q_BYTES = 4 * Q_CHUNK;          // 256 features
+  static constexpr int Q_BYTES = NCH * Q_CHUNK;
   static constexpr int KV_CHUNK = kWKeys * 128;        // [64 keys x 128 B]
-  static constexpr int KV_BYTES = 4 * KV_CHUNK;
+  static constexpr int KV_BYTES = NCH * KV_CHUNK;
   static constexpr int OUT_CHUNK = 32 * 128;           // one warp's 32 rows x 64 bf16
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
@@ -94,8 +98,12 @@ struct WCfg {
   // TMEM slot (+0), abort flag (+4), unit queue (+8, +12), CLC response (+16, 16 bytes)
   static constexpr int OFF_MISC = (OFF_BAR + 8 * NBAR + 15) / 16 * 16;
   static constexpr int SMEM = OFF_MISC + 32 + 1024;
-  static constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S0 = 384, TM_S1 = 448;
-  static constexpr uint32_t TMEM_COLS = 512;
+  // TMEM: O (W columns) | Q (W / 2: bf16 pairs) | S0 | S1 (64 each)
+  static constexpr uint32_t TM_O = 0, TM_Q = W, TM_S0 = W + W / 2, TM_S1 = TM_S0 + 64;
+  static constexpr uint32_t TMEM_COLS = W == 256 ? 512 : 256;
+  static_assert(TM_S1 + 64 <= TMEM_COLS, "TMEM budget");
+  // CTAs per SM the launch bounds allow
+  static constexpr int MIN_BLOCKS = W == 256 ? 1 : 2;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
   static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_OUT % 1024 == 0 && OFF_BAR % 8 == 0,
                 "alignment");
@@ -134,8 +142,10 @@ __device__ __forceinline__ WUnit wide_unit(const Bf16Params& p, int u) {
   return w;
 }
 
-__global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_constant__ Bf16Params p) {
-  using C = WCfg;
+template <int W>
+__global__ void __launch_bounds__(kWThreads, WCfg<W>::MIN_BLOCKS)
+    fwd_wide_kernel(const __grid_constant__ Bf16Params p) {
+  using C = WCfg<W>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -225,7 +235,7 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
       if (elect_one()) {
         mbar_arrive_expect_tx(bar(C::Q_FULL), C::Q_BYTES);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < C::NCH; ++c)
           tma_load_4d(sQ + c * C::Q_CHUNK, &p.tm_q, bar(C::Q_FULL), 64 * c, w.h, w.q0, w.b);
       }
       __syncwarp();
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
         if (elect_one()) {
           mbar_arrive_expect_tx(bar(C::K_FULL + s), C::KV_BYTES);
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < C::NCH; ++c)
             tma_load_4d(sK + s * C::KV_BYTES + c * C::KV_CHUNK, &p.tm_k, bar(C::K_FULL + s), 64 * c,
                         w.h, j * kWKeys, w.b);
         }
@@ -254,7 +264,7 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
         if (elect_one()) {
           mbar_arrive_expect_tx(bar(C::V_FULL + s), C::KV_BYTES);
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < C::NCH; ++c)
             tma_load_4d(sV + s * C::KV_BYTES + c * C::KV_CHUNK, &p.tm_v, bar(C::V_FULL + s), 64 * c,
                         w.h, j * kWKeys, w.b);
         }
@@ -377,7 +387,7 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
         return false;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < C::NCH; ++c) {
         uint32_t r[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
@@ -476,7 +486,7 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
           }
           tc_fence_after();
 #pragma unroll
-          for (int c32 = 0; c32 < 8; ++c32) {
+          for (int c32 = 0; c32 < W / 32; ++c32) {
             if (32 * c32 >= dv_n) break;
             uint32_t o[32];
             tmem_ld32(tmem + lane_off + C::TM_O + 32u * c32, o);
@@ -494,7 +504,9 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
         tmem_st32(tS, pk);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(C::P_FULL + buf));
+        // (test hook: the CTA's first weights are never handed over, so the
+        // MMA warp's bounded wait runs out)
+        if (!(p.withhold_p && k == 0 && j == 0)) mbar_arrive(bar(C::P_FULL + buf));
       }
       if (!ok) break;
       // The next unit's Q goes into TMEM now (this unit's last S is complete:
@@ -613,13 +625,13 @@ __global__ void __launch_bounds__(kWThreads, 1) fwd_wide_kernel(const __grid_con
   }
 }
 
-}  // namespace
-
-cudaError_t launch_fwd_wide(const Bf16Params& params, cudaStream_t stream, LaunchInfo* info) {
+template <int W>
+cudaError_t launch_wide_w(const Bf16Params& params, cudaStream_t stream, LaunchInfo* info) {
+  using C = WCfg<W>;
   Bf16Params p = params;
   {
-    // heads whose K/V (256 features) stay in L2 while their query tiles run
-    const long long per_head = 2ll * p.Lk * 256 * 2 > 0 ? 2ll * p.Lk * 256 * 2 : 1;
+    // heads whose K/V stay in L2 while their query tiles run
+    const long long per_head = 2ll * p.Lk * W * 2 > 0 ? 2ll * p.Lk * W * 2 : 1;
     long long hg = kWHeadGroupBytes / per_head;
     const long long bh = static_cast<long long>(p.B) * p.H;
     if (hg > bh) hg = bh;
@@ -633,8 +645,7 @@ cudaError_t launch_fwd_wide(const Bf16Params& params, cudaStream_t stream, Launc
   static bool attr_set[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(fwd_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             WCfg::SMEM);
+    e = cudaFuncSetAttribute(fwd_wide_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
@@ -642,15 +653,24 @@ cudaError_t launch_fwd_wide(const Bf16Params& params, cudaStream_t stream, Launc
   if (units <= 0 || units > 0x7fffffffll) return cudaErrorInvalidValue;
   // one CTA per unit; running CTAs take over the units of those not started
   const int grid = static_cast<int>(units);
-  e = launch_serialized(fwd_wide_kernel, dim3(grid), dim3(kWThreads), WCfg::SMEM, stream, p);
+  e = launch_serialized(fwd_wide_kernel<W>, dim3(grid), dim3(kWThreads), C::SMEM, stream, p);
   if (e != cudaSuccess) return e;
   if (info) {
     info->kernels = 1;
     info->grid = grid;
     info->block = kWThreads;
-    info->smem = WCfg::SMEM;
+    info->smem = C::SMEM;
   }
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_wide(const Bf16Params& params, int width, cudaStream_t stream,
+                            LaunchInfo* info) {
+  if (width == 256) return launch_wide_w<256>(params, stream, info);
+  if (width == 64) return launch_wide_w<64>(params, stream, info);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace mha
