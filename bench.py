@@ -331,11 +331,14 @@ def forward_sets(w, case, dev):
     return sets, bytes_in
 
 
-def fwd_kernel_label():
-    """The bf16 forward kernel of the library's last launch: the one-tile
-    kernel (heads wider than 128; short sequences of heads up to 64 wide) runs
-    256-thread CTAs, the two-tile kernel 384."""
+def fwd_kernel_label(w):
+    """The forward kernel of the library's last launch (call it right after
+    the workload's own launches): the float32 kernel for float32 workloads;
+    for bf16 the one-tile kernel (heads wider than 128; short sequences of
+    heads up to 64 wide) runs 256-thread CTAs, the two-tile kernel 384."""
     from transformer_head_scaled_sdpa_gb300 import binding
+    if w.dtype != torch.bfloat16:
+        return "fwd_f32_kernel"
     return "fwd_wide_kernel" if binding.last_launch_info()["block"] == 256 else "fwd_bf16_kernel"
 
 
@@ -423,7 +426,7 @@ SWEEP = ["toy_cross_f32", "base_encoder_self", "base_decoder_causal", "base_cros
 ONE_CORE = {"toy_cross_f32", "base_encoder_self", "base_decoder_causal"}
 
 
-def config_record(w, case, kernel_ms, launches, peaks, with_oracle):
+def config_record(w, case, kernel_ms, launches, peaks, with_oracle, kernel):
     """One sweep row: nominal and algorithmic TFLOP/s, fractions of the
     measured tensor and HBM peaks, and the oracle's rate on the host cores."""
     pairs = visible_pairs(w, case["key_lens"])
@@ -443,7 +446,7 @@ def config_record(w, case, kernel_ms, launches, peaks, with_oracle):
            "mask": inputs.MASK_NAMES[w.mask_kind],
            "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
            "us_per_step": kernel_ms * 1e3, "launches_per_step": launches,
-           "kernel": fwd_kernel_label() if w.dtype == torch.bfloat16 else "fwd_f32_kernel",
+           "kernel": kernel,
            "tflops": flops_nom / sec / 1e12,
            "tflops_algorithmic": flops_alg / sec / 1e12,
            "frac_tensor_peak": (flops_alg / sec / 1e12 / tensor_peak
@@ -486,6 +489,7 @@ def run_ours(args):
 
     kernel_ms, max_total_ms, clocks, launches_per_step, bytes_in = measure_forward(
         w, case, args, dev, stream, rank, args.steps, args.warmup)
+    kernel_label = fwd_kernel_label(w)
     n_sets = 1 if bytes_in > L2_BYTES else -(-2 * L2_BYTES // bytes_in)
     total_flops = mdist.sum_over_ranks(flops_nominal * args.steps, dev)
     total_flops_alg = mdist.sum_over_ranks(flops_alg * args.steps, dev)
@@ -557,7 +561,7 @@ def run_ours(args):
         "roofline": ({"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                       "frac": achieved / peak, "traffic": traffic,
                       "peak_source": f"{peak_src} dense bf16 (burst)",
-                      "kernel": fwd_kernel_label(),
+                      "kernel": kernel_label,
                       "kernel_ms": kernel_ms, "algorithmic_bytes": bytes_alg,
                       "achieved_gbs": bytes_alg / (kernel_ms * 1e-3) / 1e9}
                      if w.dtype == torch.bfloat16 else
@@ -583,12 +587,13 @@ def run_ours(args):
             wc = inputs.BY_NAME[name]
             if name == w.name:
                 rows.append(config_record(wc, case, kernel_ms, launches_per_step, peaks,
-                                          not args.no_cpu_baseline))
+                                          not args.no_cpu_baseline, kernel_label))
                 continue
             c = inputs.generate(wc)
             k_ms, _, _, launches, _ = measure_forward(wc, c, args, dev, stream, rank,
                                                       sweep_steps, args.warmup)
-            rows.append(config_record(wc, c, k_ms, launches, peaks, not args.no_cpu_baseline))
+            rows.append(config_record(wc, c, k_ms, launches, peaks, not args.no_cpu_baseline,
+                                      fwd_kernel_label(wc)))
             del c
         line["configs"] = rows
     print(json.dumps(line), flush=True)

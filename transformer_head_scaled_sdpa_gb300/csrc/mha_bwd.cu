@@ -16,7 +16,7 @@
 //   bwd_dkdv_kernel   units (b, h, 128-key tile); the query tiles that
 //                     see the keys stream through a two-stage ring.  Per query
 //                     tile: S^T = K Q^T and dP^T = V dO^T on the tensor cores
-//                     (keys on TMEM lanes), the eight gradient warps turn them
+//                     (keys on TMEM lanes), the sixteen gradient warps turn them
 //                     into P^T and dS^T (bf16, written over S^T and dP^T in
 //                     TMEM), and dV += P^T dO, dK += dS^T Q accumulate in TMEM
 //                     (A operands from TMEM).
@@ -36,11 +36,11 @@
 namespace mha {
 namespace {
 
-constexpr int kBwdThreads = 352;  // warps 0-7 gradient, 8 MMA, 9 TMA, 10 scheduler
-constexpr int kGradThreads = 256;
-constexpr int kMmaWarp = 8, kTmaWarp = 9, kSchedWarp = 10;
-// unit-queue readers: 8 gradient warps, the MMA warp, the TMA lane
-constexpr int kBwdUnitConsumers = 10;
+constexpr int kBwdThreads = 608;  // warps 0-15 gradient, 16 MMA, 17 TMA, 18 scheduler
+constexpr int kGradThreads = 512;
+constexpr int kMmaWarp = 16, kTmaWarp = 17, kSchedWarp = 18;
+// unit-queue readers: 16 gradient warps, the MMA warp, the TMA lane
+constexpr int kBwdUnitConsumers = 18;
 constexpr int kRoleBwdProducer = 8, kRoleBwdMma = 9, kRoleBwdGrad = 10, kRoleBwdSched = 11;
 
 template <int D>
@@ -88,9 +88,14 @@ enum { kFixFull = 0, kRingFull = 1, kRingEmpty = 3, kScores = 5, kGrads = 7, kAc
        kStgFull = 19, kStgFree = 20 };
 
 // TMEM column of the 16 rows of K16 step ks (0..3) of a half, packed as bf16
-// pairs: chunk ks / 2 (32 rows) keeps them in the first 16 of its 32 columns
-__device__ __forceinline__ constexpr uint32_t a_col(int ks) {
-  return 32u * static_cast<uint32_t>(ks >> 1) + 8u * static_cast<uint32_t>(ks & 1);
+// pairs: they are chunk ks (one gradient warp's 16 columns), kept in its
+// first 8 columns
+__device__ __forceinline__ constexpr uint32_t a_col(int ks) { return 16u * static_cast<uint32_t>(ks); }
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
 }
 
 // bf16 halves of a packed pair -> float (exact)
@@ -324,8 +329,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       umma_commit(bar(kScores + hf));
     };
     // dV += P^T dO, dK += dS^T Q over half hf.  The 16 queries of step ks are
-    // 8 packed TMEM columns: chunk ks / 2 of the half keeps its 32 queries in
-    // the first 16 columns of its own 32.
+    // 8 packed TMEM columns: chunk ks of the half (one gradient warp's 16
+    // columns) keeps them in its first 8.
     auto issue_grads = [&](int t, int hf, bool first) {
       const uint32_t rows = half_rows(t, hf);
       const uint64_t dQm = smem_desc_sw128(rows, C::CHUNK, 1024);
@@ -413,7 +418,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     mbar_wait(bar(kDrain), 0, &never, p.status, kRoleBwdMma * 64 + kDrain);
   } else {
     // ---- gradient warps: warp w owns key rows k0 + 32 (w % 4) .. (its TMEM
-    // lane quarter) and, of each half tile, the 32 queries of chunk w / 4
+    // lane quarter) and, of each half tile, the 16 queries of chunk w / 4
     const int quarter = warp & 3, cq = warp >> 2;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -422,6 +427,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     // a tile ahead into a register that is read only at the next tile
     const int vi = static_cast<int>(threadIdx.x) & 127;
     const bool v_lse = threadIdx.x < 128;
+    const bool v_thread = threadIdx.x < 256;
     const float* v_src = v_lse ? p.lse : p.dvec;
     float* v_dst = (v_lse ? lse2_s : dvec_s) + vi;
     bool ok = true;
@@ -436,6 +442,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     float vn = 0.f;
     bool vn_ready = false;   // vn holds the current unit's first value
     auto fetch_of = [&](const KvUnit& w, int t) {
+      if (!v_thread) return;
       const int qi = (w.qt_begin + t) * 128 + vi;
       vn = qi < p.Lq ? v_src[(static_cast<size_t>(w.b) * p.H + w.h) * p.Lq + qi] : -INFINITY;
     };
@@ -473,7 +480,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
           break;
         }
         // stored negated, for packed fma / add below: -lse (log2 units), -D
-        *v_dst = v_lse ? -(vn * 1.4426950408889634f) : (vn == -INFINITY ? 0.f : -vn);
+        if (v_thread) *v_dst = v_lse ? -(vn * 1.4426950408889634f) : (vn == -INFINITY ? 0.f : -vn);
         named_barrier(1, kGradThreads);
         if (*abort_flag) {
           ok = false;
@@ -505,27 +512,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             break;
           }
           tc_fence_after();
-          const uint32_t ts = tmem + C::TM_HALF * hf + lane_off + 32u * cq;
-          const int col0 = 64 * hf + 32 * cq;  // first query column of the chunk
-          uint32_t sr[32], pr[32];
-          tmem_ld32(ts, sr);
-          tmem_ld32(ts + C::TM_DP, pr);
-          float l2c[32], dvc[32];  // negated: -lse (log2 units), -D
+          const uint32_t ts = tmem + C::TM_HALF * hf + lane_off + 16u * cq;
+          const int col0 = 64 * hf + 16 * cq;  // first query column of the chunk
+          uint32_t sr[16], pr[16];
+          tmem_ld16(ts, sr);
+          tmem_ld16(ts + C::TM_DP, pr);
+          float l2c[16], dvc[16];  // negated: -lse (log2 units), -D
 #pragma unroll
-          for (int v4 = 0; v4 < 8; ++v4) {
+          for (int v4 = 0; v4 < 4; ++v4) {
             const float4 lv = reinterpret_cast<const float4*>(lse2_s + col0)[v4];
             const float4 dv = reinterpret_cast<const float4*>(dvec_s + col0)[v4];
             l2c[4 * v4] = lv.x, l2c[4 * v4 + 1] = lv.y, l2c[4 * v4 + 2] = lv.z, l2c[4 * v4 + 3] = lv.w;
             dvc[4 * v4] = dv.x, dvc[4 * v4 + 1] = dv.y, dvc[4 * v4 + 2] = dv.z, dvc[4 * v4 + 3] = dv.w;
           }
           tmem_ld_wait();
-          float pf[32];
+          float pf[16];
           // (the mask test stays outside the element loops, which then have no
-          // branches and interleave their 32 independent chains; packed f32x2
+          // branches and interleave their 16 independent chains; packed f32x2
           // arithmetic halves the issue slots of the float math)
           if (all_visible) {
 #pragma unroll
-            for (int t = 0; t < 32; t += 2) {
+            for (int t = 0; t < 16; t += 2) {
               fma2(pf[t], pf[t + 1], __uint_as_float(sr[t]), __uint_as_float(sr[t + 1]), c2, c2,
                    l2c[t], l2c[t + 1]);
               pf[t] = ex2_approx(pf[t]);
@@ -533,7 +540,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             }
           } else {
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
+            for (int t = 0; t < 16; ++t) {
               const int qi = q0 + col0 + t;
               const bool vis = key < kv_len && qi < p.Lq &&
                                !(masks_causal(p.mask_kind) && key > qi) && l2c[t] != INFINITY;
@@ -542,19 +549,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             }
           }
           // P^T in bf16 for the dV product; dS = P (dP - D) from the float32 P
-          uint32_t pk[16], dk[16];
+          uint32_t pk[8], dk[8];
 #pragma unroll
-          for (int t = 0; t < 32; t += 2) {
+          for (int t = 0; t < 16; t += 2) {
             pk[t >> 1] = pack_bf16x2(pf[t], pf[t + 1]);
             float g0, g1;
             add2(g0, g1, __uint_as_float(pr[t]), __uint_as_float(pr[t + 1]), dvc[t], dvc[t + 1]);
             mul2(g0, g1, pf[t], pf[t + 1], g0, g1);
             dk[t >> 1] = pack_bf16x2(g0, g1);
           }
-          // P^T over the first 16 of the chunk's S^T columns, dS^T over the first
-          // 16 of its dP^T columns (this thread has read them; no other has)
-          tmem_st16(ts, pk);
-          tmem_st16(ts + C::TM_DP, dk);
+          // P^T over the first 8 of the chunk's S^T columns, dS^T over the first
+          // 8 of its dP^T columns (this thread has read them; no other has)
+          tmem_st8(ts, pk);
+          tmem_st8(ts + C::TM_DP, dk);
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(bar(kGrads + hf));
@@ -562,7 +569,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       }
       if (!ok) break;
       // ---- epilogue: dV and scale * dK rows to global (rows past Lk skipped);
-      // warp w takes the 32-column chunks c with c % 2 == w / 4.  The
+      // warp w takes the 16-column chunks c with c % 4 == w / 4.  The
       // accumulators are read first, then released to the next unit.
       if (n_iter > 0) {
         ok = mbar_wait(bar(kAccDone), unit_n & 1, abort_flag, p.status,
@@ -577,11 +584,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       // thread cost this kernel about 9 % at d 128.
 #pragma unroll 1
       for (int c64 = 0; c64 < C::KCH; ++c64) {
-        const int c32 = 2 * c64 + cq;
-        uint32_t a[32], kk[32];
+        const int c16 = 4 * c64 + cq;
+        uint32_t a[16], kk[16];
         if (n_iter > 0) {
-          tmem_ld32(tmem + C::TM_ACC0 + lane_off + 32u * c32, a);
-          tmem_ld32(tmem + C::TM_ACC1 + lane_off + 32u * c32, kk);
+          tmem_ld16(tmem + C::TM_ACC0 + lane_off + 16u * c16, a);
+          tmem_ld16(tmem + C::TM_ACC1 + lane_off + 16u * c16, kk);
           tmem_ld_wait();
           if (c64 + 1 == C::KCH) {
             // this thread's last accumulator columns are read: the next unit
@@ -591,7 +598,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
           }
         } else {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) a[t] = kk[t] = 0u;
+          for (int t = 0; t < 16; ++t) a[t] = kk[t] = 0u;
         }
         // the previous chunk's stores must have read the staging buffers
         if (stg_n > 0 && !mbar_wait(bar(kStgFree), (stg_n - 1) & 1, abort_flag, p.status,
@@ -600,8 +607,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
           break;
         }
 #pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4) {
-          const uint32_t off = static_cast<uint32_t>(r * 128 + (((4 * cq + v4) ^ (r & 7)) << 4));
+        for (int v4 = 0; v4 < 2; ++v4) {
+          const uint32_t off = static_cast<uint32_t>(r * 128 + (((2 * cq + v4) ^ (r & 7)) << 4));
           st_shared_v4(stg_v + off,
                        pack_bf16x2(__uint_as_float(a[8 * v4 + 0]), __uint_as_float(a[8 * v4 + 1])),
                        pack_bf16x2(__uint_as_float(a[8 * v4 + 2]), __uint_as_float(a[8 * v4 + 3])),
@@ -921,7 +928,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     mbar_wait(bar(kDrain), 0, &never, p.status, kRoleBwdMma * 64 + 16 + kDrain);
   } else {
     // ---- gradient warps: warp w owns query rows q0 + 32 (w % 4) .. and, of
-    // each half tile, the 32 keys of chunk w / 4
+    // each half tile, the 16 keys of chunk w / 4
     const int quarter = warp & 3, cq = warp >> 2;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -945,8 +952,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       const int b = u.b, h = u.h, q0 = u.q0, n_iter = u.n_iter, kv_len = u.kv_len;
       const int qi = q0 + r;
       // D_i = dO_i . O_i of this row from the staged dO and O tiles (128-byte
-      // swizzled rows), the two warps of the lane quarter taking alternate
-      // 16-byte pieces and adding their halves in shared memory; it is also
+      // swizzled rows), the warps of chunks 0 and 1 of the lane quarter taking
+      // alternate 16-byte pieces and adding their halves in shared memory; it is also
       // written to the workspace for the dK/dV kernel, which runs next.  (A
       // unit without keys has no tiles and needs no D.)
       float l2 = -INFINITY, part = 0.f;
@@ -957,7 +964,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
                        kRoleBwdGrad * 64 + 16 + kFixFull);
         if (!ok) break;
         const int pieces = p.d / 8;  // the tiles hold zeros past d
-        for (int c = cq; c < pieces; c += 2) {
+        // (warps of chunks 0 and 1 form D; those of 2 and 3 add nothing)
+        for (int c = cq; cq < 2 && c < pieces; c += 2) {
           const uint32_t off = static_cast<uint32_t>((c >> 3) * C::CHUNK + r * 128 +
                                                      (((c & 7) ^ (r & 7)) << 4));
           const uint4 ov = ld_shared_v4(s_base + C::OFF_O + off);
@@ -968,7 +976,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         }
         mbar_arrive(bar(kOFree));
       }
-      d_part[cq * 128 + r] = part;
+      if (cq < 2) d_part[cq * 128 + r] = part;
       // (the second barrier keeps the next unit's halves from overwriting
       // this one's before both warps of the quarter have read them.  A named
       // barrier cannot time out: after each one the abort flag is checked,
@@ -999,15 +1007,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             break;
           }
           tc_fence_after();
-          const uint32_t ts = tmem + C::TM_HALF * hf + lane_off + 32u * cq;
-          uint32_t sr[32], pr[32];
-          tmem_ld32(ts, sr);
-          tmem_ld32(ts + C::TM_DP, pr);
+          const uint32_t ts = tmem + C::TM_HALF * hf + lane_off + 16u * cq;
+          uint32_t sr[16], pr[16];
+          tmem_ld16(ts, sr);
+          tmem_ld16(ts + C::TM_DP, pr);
           tmem_ld_wait();
-          float pf[32];
+          float pf[16];
           if (all_visible) {
 #pragma unroll
-            for (int t = 0; t < 32; t += 2) {
+            for (int t = 0; t < 16; t += 2) {
               fma2(pf[t], pf[t + 1], __uint_as_float(sr[t]), __uint_as_float(sr[t + 1]), c2, c2,
                    -l2, -l2);
               pf[t] = ex2_approx(pf[t]);
@@ -1015,24 +1023,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             }
           } else {
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
-              const int key = k0 + 64 * hf + 32 * cq + t;
+            for (int t = 0; t < 16; ++t) {
+              const int key = k0 + 64 * hf + 16 * cq + t;
               const bool vis = row_ok && key < kv_len && !(masks_causal(p.mask_kind) && key > qi);
               const float e = ex2_approx(fmaf(__uint_as_float(sr[t]), c2, -l2));
               pf[t] = vis ? e : 0.f;
             }
           }
           // dS = P (dP - D) from the float32 P (no product here takes P itself)
-          uint32_t dk[16];
+          uint32_t dk[8];
 #pragma unroll
-          for (int t = 0; t < 32; t += 2) {
+          for (int t = 0; t < 16; t += 2) {
             float g0, g1;
             add2(g0, g1, __uint_as_float(pr[t]), __uint_as_float(pr[t + 1]), -dvv, -dvv);
             mul2(g0, g1, pf[t], pf[t + 1], g0, g1);
             dk[t >> 1] = pack_bf16x2(g0, g1);
           }
-          // dS over the first 16 of the chunk's S columns (read by this thread only)
-          tmem_st16(ts, dk);
+          // dS over the first 8 of the chunk's S columns (read by this thread only)
+          tmem_st8(ts, dk);
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(bar(kGrads + hf));
@@ -1050,38 +1058,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       __nv_bfloat16* dq_row = reinterpret_cast<__nv_bfloat16*>(p.dq) +
                               ((static_cast<size_t>(b) * p.Lq + qi) * p.H + h) * p.d;
 #pragma unroll 1
-      for (int c32 = cq; c32 < D / 32; c32 += 2) {
-        uint32_t a[32];
+      for (int c16 = cq; c16 < D / 16; c16 += 4) {
+        uint32_t a[16];
         if (n_iter > 0) {
-          tmem_ld32(tmem + C::TM_ACC0 + lane_off + 32u * c32, a);
+          tmem_ld16(tmem + C::TM_ACC0 + lane_off + 16u * c16, a);
           tmem_ld_wait();
-          if (c32 + 2 >= D / 32) {
+          if (c16 + 4 >= D / 16) {
             // this thread's last accumulator columns are read
             tc_fence_before();
             mbar_arrive(bar(kAccFree));
           }
         } else {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) a[t] = 0u;
+          for (int t = 0; t < 16; ++t) a[t] = 0u;
         }
         if (qi < p.Lq) {
-          uint4 w[4];
+          uint4 w[2];
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
+          for (int v4 = 0; v4 < 2; ++v4) {
             w[v4].x = pack_bf16x2(__uint_as_float(a[8 * v4 + 0]) * p.scale, __uint_as_float(a[8 * v4 + 1]) * p.scale);
             w[v4].y = pack_bf16x2(__uint_as_float(a[8 * v4 + 2]) * p.scale, __uint_as_float(a[8 * v4 + 3]) * p.scale);
             w[v4].z = pack_bf16x2(__uint_as_float(a[8 * v4 + 4]) * p.scale, __uint_as_float(a[8 * v4 + 5]) * p.scale);
             w[v4].w = pack_bf16x2(__uint_as_float(a[8 * v4 + 6]) * p.scale, __uint_as_float(a[8 * v4 + 7]) * p.scale);
           }
-          if (whole_sectors && 32 * c32 + 32 <= p.d) {
-            // whole 32-byte sectors, two stores instead of four
-            st_global_v8(dq_row + 32 * c32, w[0], w[1]);
-            st_global_v8(dq_row + 32 * c32 + 16, w[2], w[3]);
+          if (whole_sectors && 16 * c16 + 16 <= p.d) {
+            // one whole 32-byte sector
+            st_global_v8(dq_row + 16 * c16, w[0], w[1]);
           } else {
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              if (32 * c32 + 8 * v4 >= p.d) break;  // columns past d are padding
-              *reinterpret_cast<uint4*>(dq_row + 32 * c32 + 8 * v4) = w[v4];
+            for (int v4 = 0; v4 < 2; ++v4) {
+              if (16 * c16 + 8 * v4 >= p.d) break;  // columns past d are padding
+              *reinterpret_cast<uint4*>(dq_row + 16 * c16 + 8 * v4) = w[v4];
             }
           }
         }
