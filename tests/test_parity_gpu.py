@@ -300,17 +300,19 @@ def test_empty_and_keyless(mha):
     assert torch.count_nonzero(out) == 0
 
 
-@pytest.mark.parametrize("Lq,Lk,d", [(300, 300, 64), (600, 300, 64), (300, 600, 64),
-                                     (300, 300, 128), (512, 512, 40)])
-def test_launch_shape(mha, Lq, Lk, d):
-    """Heads up to 64 wide over sequences of at most 512 take the light
-    one-tile kernel (one 256-thread CTA per (b, h, 128-query tile)); the rest
-    the two-tile kernel (one 384-thread CTA per (b, h, 256 query rows))."""
+@pytest.mark.parametrize("Lq,Lk,d,mask", [(300, 300, 64, NONE), (600, 300, 64, NONE),
+                                          (300, 600, 64, NONE), (300, 300, 128, NONE),
+                                          (512, 512, 40, NONE), (300, 300, 64, CAUSAL)])
+def test_launch_shape(mha, Lq, Lk, d, mask):
+    """Heads up to 64 wide over sequences of at most 512 without the causal
+    mask take the light one-tile kernel (one 256-thread CTA per (b, h,
+    128-query tile)); the rest the two-tile kernel (one 384-thread CTA per
+    (b, h, 256 query rows))."""
     case = pu.to_cuda(inputs.random_case(10, 3, 5, Lq, Lk, d))
-    mha.mha_fwd(case["q"], case["k"], case["v"])
+    mha.mha_fwd(case["q"], case["k"], case["v"], mask_kind=mask)
     info = mha.last_launch_info()
     assert mha.mha_sync_status() == 0
-    light = d <= 64 and Lq <= 512 and Lk <= 512
+    light = d <= 64 and Lq <= 512 and Lk <= 512 and mask == NONE
     expect = (3 * 5 * ((Lq + 127) // 128), 256) if light else (3 * 5 * ((Lq + 255) // 256), 384)
     assert info["kernels"] == 1 and (info["grid"], info["block"]) == expect, info
 
@@ -478,24 +480,25 @@ def test_host_entry_chunks(mha, shape):
     assert torch.equal(out, dev)
 
 
-@pytest.mark.parametrize("L,d", [(256, 64), (768, 64), (768, 128), (300, 256)])
-def test_attention_kernel_timeout_path(mha, L, d):
+@pytest.mark.parametrize("L,d,mask", [(256, 64, NONE), (256, 64, CAUSAL), (768, 128, CAUSAL),
+                                      (300, 256, CAUSAL)])
+def test_attention_kernel_timeout_path(mha, L, d, mask):
     """With one pipeline signal withheld, every CTA's bounded wait runs out
     (about a second), the kernel aborts, drains and frees its tensor memory,
     reports MHA_ERR_TIMEOUT, and the next launch computes correctly.  Covers
-    the light one-tile kernel (L 256), the two-tile kernel at both widths and
-    the wide one-tile kernel."""
+    the light one-tile kernel (L 256 unmasked), the two-tile kernel at both
+    widths and the wide one-tile kernel."""
     case = inputs.random_case(12, 1, 2, L, L, d)
     g = pu.to_cuda(case)
     mha.mha_debug_withhold_p(True)
     try:
-        mha.mha_fwd(g["q"], g["k"], g["v"], mask_kind=CAUSAL)
+        mha.mha_fwd(g["q"], g["k"], g["v"], mask_kind=mask)
         assert mha.mha_sync_status() == 7
     finally:
         mha.mha_debug_withhold_p(False)
     assert mha.mha_sync_status() == 0
-    out = pu.gpu_run(mha, case, CAUSAL)
-    pu.assert_bf16_close(out, pu.oracle_run(case, CAUSAL), "after kernel timeout")
+    out = pu.gpu_run(mha, case, mask)
+    pu.assert_bf16_close(out, pu.oracle_run(case, mask), "after kernel timeout")
 
 
 def test_attention_kernel_timeout_path_with_turns(mha):
