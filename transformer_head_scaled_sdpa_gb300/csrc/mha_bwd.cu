@@ -52,7 +52,7 @@ struct BwdCfg {
   static constexpr int OFF_A0 = 0;
   static constexpr int OFF_A1 = TILE;
   static constexpr int OFF_RING = 2 * TILE;    // stage s: pair at OFF_RING + s * 2 * TILE
-  static constexpr int OFF_VEC = OFF_RING + 4 * TILE;  // dK/dV: lse2[128], D[128]; dQ: D halves [2][128]
+  static constexpr int OFF_VEC = OFF_RING + 4 * TILE;  // dQ kernel: D halves [2][128]
   static constexpr int OFF_BAR = OFF_VEC + 2 * 128 * 4;
   static constexpr int NBAR = 21;
   // tmem slot (+0), abort flag (+4), unit queue (+8, +12), cancellation
@@ -151,8 +151,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* unit_slot = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
   const uint32_t clc_resp = s_base + C::OFF_MISC + 16;
-  float* lse2_s = reinterpret_cast<float*>(smem + C::OFF_VEC);
-  float* dvec_s = lse2_s + 128;
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
 
   const int n_kt = (p.Lk + 127) / 128;
@@ -423,29 +421,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c2 = p.scale_log2;
-    // one entry of a query tile's lse (threads 0-127) or D (128-255), loaded
-    // a tile ahead into a register that is read only at the next tile
-    const int vi = static_cast<int>(threadIdx.x) & 127;
-    const bool v_lse = threadIdx.x < 128;
-    const bool v_thread = threadIdx.x < 256;
-    const float* v_src = v_lse ? p.lse : p.dvec;
-    float* v_dst = (v_lse ? lse2_s : dvec_s) + vi;
+    // lse and D of the queries of this warp's chunk come straight from global
+    // memory (every lane loads the same 64 bytes: one broadcast), as 16-byte
+    // vectors when the rows are so aligned
+    const bool vec_ok = p.Lq % 4 == 0 && (reinterpret_cast<uintptr_t>(p.lse) & 15u) == 0 &&
+                        (reinterpret_cast<uintptr_t>(p.dvec) & 15u) == 0;
     bool ok = true;
     int ring_t = 0;  // query tiles of the units before the current one
     int unit_n = 0;  // units with work so far
     int stg_n = 0;   // epilogue chunks staged so far
     const uint32_t stg_v = s_base + C::OFF_STG, stg_k = stg_v + C::CHUNK;
-    // The next unit is taken from the queue at the current unit's last tile,
-    // and its first tile's lse / D loaded then, so that load's latency is not
-    // paid at the unit boundary.
+    // The next unit is taken from the queue at the current unit's last tile.
     int next_unit_idx = -2;  // -2: not taken early
-    float vn = 0.f;
-    bool vn_ready = false;   // vn holds the current unit's first value
-    auto fetch_of = [&](const KvUnit& w, int t) {
-      if (!v_thread) return;
-      const int qi = (w.qt_begin + t) * 128 + vi;
-      vn = qi < p.Lq ? v_src[(static_cast<size_t>(w.b) * p.H + w.h) * p.Lq + qi] : -INFINITY;
-    };
     for (int k = 0; ok; ++k) {
       int unit;
       if (next_unit_idx != -2) {
@@ -455,7 +442,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         unit = take(k, kRoleBwdGrad);
         __syncwarp();
         if (unit >= 0 && lane == 0) release(k);
-        vn_ready = false;
       }
       if (unit < 0) {
         ok = unit == -1 && !*abort_flag;
@@ -465,47 +451,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       const int b = u.b, h = u.h, k0 = u.k0, qt_begin = u.qt_begin, n_iter = u.n_iter;
       const int kv_len = u.kv_len;
       const int key = k0 + r;
-      if (n_iter > 0 && !vn_ready) fetch_of(u, 0);
-      vn_ready = false;
+      const size_t vrow = (static_cast<size_t>(b) * p.H + h) * p.Lq;
       for (int it = 0; ok && it < n_iter; ++it) {
         const int t_all = ring_t + it;  // barrier phases run over all units
         const int q0 = (qt_begin + it) * 128;
-        // the tile's lse (log2 units) and D into shared memory once the previous
-        // tile's readers are past the barrier.  (A named barrier cannot time out:
-        // after each one the abort flag is checked, and a warp that gives up
-        // arrives once on it on its way out.)
-        named_barrier(1, kGradThreads);
-        if (*abort_flag) {
-          ok = false;
-          break;
-        }
-        // stored negated, for packed fma / add below: -lse (log2 units), -D
-        if (v_thread) *v_dst = v_lse ? -(vn * 1.4426950408889634f) : (vn == -INFINITY ? 0.f : -vn);
-        named_barrier(1, kGradThreads);
-        if (*abort_flag) {
-          ok = false;
-          break;
-        }
-        if (it + 1 < n_iter) {
-          fetch_of(u, it + 1);
-        } else {
-          // last tile: the next unit and its first lse / D now
+        if (it + 1 == n_iter) {
+          // last tile: the next unit now
           next_unit_idx = take(k + 1, kRoleBwdGrad);
           __syncwarp();
-          if (next_unit_idx >= 0) {
-            if (lane == 0) release(k + 1);
-            const KvUnit w = decode(next_unit_idx);
-            if (w.n_iter > 0) {
-              fetch_of(w, 0);
-              vn_ready = true;
-            }
-          }
+          if (next_unit_idx >= 0 && lane == 0) release(k + 1);
         }
         // Every (key, query) pair of the tile is visible unless the tile holds
         // keys past the key length, queries past Lq, or the causal diagonal.
         const bool all_visible = k0 + 127 < kv_len && q0 + 127 < p.Lq &&
                                  !(masks_causal(p.mask_kind) && q0 < k0 + 127);
         for (int hf = 0; hf < 2; ++hf) {
+          const int col0 = 64 * hf + 16 * cq;  // first query column of the chunk
+          const int qb = q0 + col0;
+          // (loaded before the wait for the scores, so their latency is hidden)
+          float l2c[16], dvc[16];  // negated: -lse (log2 units), -D
+          if (vec_ok && qb + 16 <= p.Lq) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              const float4 lv = __ldg(reinterpret_cast<const float4*>(p.lse + vrow + qb) + v4);
+              const float4 dv = __ldg(reinterpret_cast<const float4*>(p.dvec + vrow + qb) + v4);
+              l2c[4 * v4] = lv.x, l2c[4 * v4 + 1] = lv.y, l2c[4 * v4 + 2] = lv.z, l2c[4 * v4 + 3] = lv.w;
+              dvc[4 * v4] = dv.x, dvc[4 * v4 + 1] = dv.y, dvc[4 * v4 + 2] = dv.z, dvc[4 * v4 + 3] = dv.w;
+            }
+          } else {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+              const bool in = qb + t < p.Lq;
+              l2c[t] = in ? __ldg(p.lse + vrow + qb + t) : -INFINITY;
+              dvc[t] = in ? __ldg(p.dvec + vrow + qb + t) : 0.f;
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < 16; t += 2) {
+            mul2(l2c[t], l2c[t + 1], l2c[t], l2c[t + 1], -1.4426950408889634f, -1.4426950408889634f);
+            dvc[t] = -dvc[t];
+            dvc[t + 1] = -dvc[t + 1];
+          }
           if (!mbar_wait(bar(kScores + hf), t_all & 1, abort_flag, p.status,
                          kRoleBwdGrad * 64 + kScores + hf)) {
             ok = false;
@@ -513,18 +499,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
           }
           tc_fence_after();
           const uint32_t ts = tmem + C::TM_HALF * hf + lane_off + 16u * cq;
-          const int col0 = 64 * hf + 16 * cq;  // first query column of the chunk
           uint32_t sr[16], pr[16];
           tmem_ld16(ts, sr);
           tmem_ld16(ts + C::TM_DP, pr);
-          float l2c[16], dvc[16];  // negated: -lse (log2 units), -D
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            const float4 lv = reinterpret_cast<const float4*>(lse2_s + col0)[v4];
-            const float4 dv = reinterpret_cast<const float4*>(dvec_s + col0)[v4];
-            l2c[4 * v4] = lv.x, l2c[4 * v4 + 1] = lv.y, l2c[4 * v4 + 2] = lv.z, l2c[4 * v4 + 3] = lv.w;
-            dvc[4 * v4] = dv.x, dvc[4 * v4 + 1] = dv.y, dvc[4 * v4 + 2] = dv.z, dvc[4 * v4 + 3] = dv.w;
-          }
           tmem_ld_wait();
           float pf[16];
           // (the mask test stays outside the element loops, which then have no
@@ -642,7 +619,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         ++unit_n;
       }
     }
-    if (!ok) named_barrier_arrive(1, kGradThreads);  // release gradient warps blocked on the barrier
   }
 
   tc_fence_before();
