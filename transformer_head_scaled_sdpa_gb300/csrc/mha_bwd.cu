@@ -486,12 +486,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
               dvc[t] = in ? __ldg(p.dvec + vrow + qb + t) : 0.f;
             }
           }
-#pragma unroll
-          for (int t = 0; t < 16; t += 2) {
-            mul2(l2c[t], l2c[t + 1], l2c[t], l2c[t + 1], -1.4426950408889634f, -1.4426950408889634f);
-            dvc[t] = -dvc[t];
-            dvc[t + 1] = -dvc[t + 1];
-          }
           if (!mbar_wait(bar(kScores + hf), t_all & 1, abort_flag, p.status,
                          kRoleBwdGrad * 64 + kScores + hf)) {
             ok = false;
@@ -503,6 +497,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
           tmem_ld16(ts, sr);
           tmem_ld16(ts + C::TM_DP, pr);
           tmem_ld_wait();
+          // the loads issued before the wait are consumed only now
+#pragma unroll
+          for (int t = 0; t < 16; t += 2) {
+            mul2(l2c[t], l2c[t + 1], l2c[t], l2c[t + 1], -1.4426950408889634f, -1.4426950408889634f);
+            dvc[t] = -dvc[t];
+            dvc[t + 1] = -dvc[t + 1];
+          }
           float pf[16];
           // (the mask test stays outside the element loops, which then have no
           // branches and interleave their 16 independent chains; packed f32x2
