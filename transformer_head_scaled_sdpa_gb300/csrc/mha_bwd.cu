@@ -54,7 +54,7 @@ struct BwdCfg {
   static constexpr int OFF_RING = 2 * TILE;    // stage s: pair at OFF_RING + s * 2 * TILE
   static constexpr int OFF_VEC = OFF_RING + 4 * TILE;  // dQ kernel: D halves [2][128]
   static constexpr int OFF_BAR = OFF_VEC + 2 * 128 * 4;
-  static constexpr int NBAR = 21;
+  static constexpr int NBAR = 22;
   // tmem slot (+0), abort flag (+4), unit queue (+8, +12), cancellation
   // response (+16, 16 bytes, 16-byte aligned)
   static constexpr int OFF_MISC = (OFF_BAR + 8 * NBAR + 15) / 16 * 16;
@@ -71,6 +71,9 @@ struct BwdCfg {
   // hf at columns 128 hf (S or S^T) and 128 hf + 64 (dP or dP^T); then the
   // d-wide accumulators
   static constexpr uint32_t TM_HALF = 128, TM_DP = 64, TM_ACC0 = 256, TM_ACC1 = 256 + D;
+  // the dQ kernel: its unit's Q and dO as bf16 pairs (A operands of the
+  // score products) after the dQ accumulator
+  static constexpr uint32_t TM_QA = 256 + D, TM_DOA = 256 + D + D / 2;
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -85,7 +88,10 @@ enum { kFixFull = 0, kRingFull = 1, kRingEmpty = 3, kScores = 5, kGrads = 7, kAc
        kOFree = 18,
        // the dK/dV epilogue: a chunk is staged (256 arrivals); its TMA stores
        // have read the staging buffers
-       kStgFull = 19, kStgFree = 20 };
+       kStgFull = 19, kStgFree = 20,
+       // the dQ kernel: the unit's Q and dO are in TMEM (copied by the
+       // gradient warps)
+       kQTmem = 21 };
 
 // TMEM column of the 16 rows of K16 step ks (0..3) of a half, packed as bf16
 // pairs: they are chunk ks (one gradient warp's 16 columns), kept in its
@@ -672,6 +678,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     mbar_init(bar(kAccFree), kGradThreads);
     mbar_init(bar(kClc), 1);
     mbar_init(bar(kOFree), kGradThreads);
+    mbar_init(bar(kQTmem), kGradThreads);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -754,12 +761,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         if (unit < 0) break;
         const QUnit u = decode(unit);
         if (u.n_iter == 0) continue;
-        // the previous unit's Q and dO (last score products) and O (the
-        // gradient warps' D) must be done with
-        if (fix_n > 0 && (!mbar_wait(bar(kFixFree), (fix_n - 1) & 1, abort_flag, p.status,
-                                     kRoleBwdProducer * 64 + 16 + kFixFree) ||
-                          !mbar_wait(bar(kOFree), (fix_n - 1) & 1, abort_flag, p.status,
-                                     kRoleBwdProducer * 64 + 16 + kOFree)))
+        // the previous unit's staged Q, dO and O must have been read (D
+        // formed, Q and dO copied into TMEM); the score products never read
+        // them from shared memory
+        if (fix_n > 0 && !mbar_wait(bar(kOFree), (fix_n - 1) & 1, abort_flag, p.status,
+                                    kRoleBwdProducer * 64 + 16 + kOFree))
           break;
         mbar_arrive_expect_tx(bar(kFixFull), 3 * C::TILE);
         for (int c = 0; c < C::KCH; ++c) {
@@ -798,8 +804,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     // ---- MMA issuer, in halves of 64 keys as in the dK/dV kernel
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
     constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
-    const uint64_t dQk = smem_desc_sw128(s_base + C::OFF_A0, 16, 1024);   // Q, K-major
-    const uint64_t dDk = smem_desc_sw128(s_base + C::OFF_A1, 16, 1024);   // dO, K-major
     // keys 64 hf .. 64 hf + 63 of ring stage (t & 1)
     auto half_rows = [&](int t, int hf) {
       return s_base + C::OFF_RING + (t & 1) * 2 * C::TILE + hf * 64 * 128;
@@ -813,12 +817,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
-        umma_ss(ts, dQk + off, dKk + off, idesc_s, ks > 0 ? 1u : 0u);
+        umma_ts(ts, tmem + C::TM_QA + 8u * ks, dKk + off, idesc_s, ks > 0 ? 1u : 0u);
       }
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         const uint64_t off = static_cast<uint64_t>((((ks >> 2) * C::CHUNK) + (ks & 3) * 32) >> 4);
-        umma_ss(ts + C::TM_DP, dDk + off, dVk + off, idesc_s, ks > 0 ? 1u : 0u);
+        umma_ts(ts + C::TM_DP, tmem + C::TM_DOA + 8u * ks, dVk + off, idesc_s, ks > 0 ? 1u : 0u);
       }
       umma_commit(bar(kScores + hf));
     };
@@ -841,8 +845,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       if (unit < 0) break;
       const QUnit u = decode(unit);
       if (u.n_iter == 0) continue;
-      ok = mbar_wait(bar(kFixFull), fix_n & 1, abort_flag, p.status,
-                     kRoleBwdMma * 64 + 16 + kFixFull) &&
+      // the unit's Q and dO in TMEM (the gradient warps copy them)
+      ok = mbar_wait(bar(kQTmem), fix_n & 1, abort_flag, p.status,
+                     kRoleBwdMma * 64 + 16 + kQTmem) &&
            mbar_wait(bar(kRingFull + (ring_t & 1)), (ring_t >> 1) & 1, abort_flag, p.status,
                      kRoleBwdMma * 64 + 16 + kRingFull);
       if (!ok) break;
@@ -850,8 +855,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       if (elect_one()) {
         issue_scores(ring_t, 0);
         issue_scores(ring_t, 1);
-        // a one-tile unit's score products are its last use of Q and dO
-        if (u.n_iter == 1) umma_commit(bar(kFixFree));
       }
       __syncwarp();
       for (int it = 0; ok && it < u.n_iter; ++it) {
@@ -888,11 +891,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
             break;
           }
           tc_fence_after();
-          if (elect_one()) {
-            issue_scores(t + 1, hf);
-            // the last tile's score products are the unit's last use of Q, dO
-            if (hf == 1 && it + 2 == u.n_iter) umma_commit(bar(kFixFree));
-          }
+          if (elect_one()) issue_scores(t + 1, hf);
           __syncwarp();
         }
       }
@@ -912,64 +911,86 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     const float c2 = p.scale_log2;
     bool ok = true;
     int ring_t = 0;  // key tiles of the units before the current one
-    int unit_n = 0;  // units with work so far
+    int unit_n = 0;  // units with work whose epilogue ran
+    int prep_n = 0;  // units with work prepared
     // dQ rows in whole 32-byte sectors: rows of a multiple of 16 elements
     // from a 32-byte aligned base
     const bool whole_sectors =
         p.d % 16 == 0 && (reinterpret_cast<uintptr_t>(p.dq) & 31u) == 0;
-    for (int k = 0; ok; ++k) {
-      const int unit = take(k, kRoleBwdGrad);
-      __syncwarp();
-      if (unit >= 0 && lane == 0) release(k);
-      if (unit < 0) {
-        ok = unit == -1 && !*abort_flag;
-        break;
-      }
-      const QUnit u = decode(unit);
-      const int b = u.b, h = u.h, q0 = u.q0, n_iter = u.n_iter, kv_len = u.kv_len;
-      const int qi = q0 + r;
-      // D_i = dO_i . O_i of this row from the staged dO and O tiles (128-byte
-      // swizzled rows), the warps of chunks 0 and 1 of the lane quarter taking
-      // alternate 16-byte pieces and adding their halves in shared memory; it is also
-      // written to the workspace for the dK/dV kernel, which runs next.  (A
-      // unit without keys has no tiles and needs no D.)
+    // Prepares a unit with key tiles once its Q, dO and O are staged: D_i =
+    // dO_i . O_i of this row (the warps of chunks 0 and 1 of the lane quarter
+    // take alternate 16-byte pieces and add their halves in shared memory; it
+    // is also written to the workspace for the dK/dV kernel, which runs next),
+    // the row's lse, and this warp's 32 columns of the unit's Q (chunks 0, 1)
+    // or dO (2, 3) copied into TMEM, where the score products read them.  The
+    // staged tiles are then free for the following unit's.
+    auto prepare = [&](const QUnit& w, float* l2_out, float* dvv_out) -> bool {
+      const int qi = w.q0 + r;
+      const size_t idx = (static_cast<size_t>(w.b) * p.H + w.h) * p.Lq + qi;
       float l2 = -INFINITY, part = 0.f;
-      const size_t idx = (static_cast<size_t>(b) * p.H + h) * p.Lq + qi;
       if (qi < p.Lq) l2 = p.lse[idx] * 1.4426950408889634f;
-      if (n_iter > 0) {
-        ok = mbar_wait(bar(kFixFull), unit_n & 1, abort_flag, p.status,
-                       kRoleBwdGrad * 64 + 16 + kFixFull);
-        if (!ok) break;
-        const int pieces = p.d / 8;  // the tiles hold zeros past d
-        // (warps of chunks 0 and 1 form D; those of 2 and 3 add nothing)
-        for (int c = cq; cq < 2 && c < pieces; c += 2) {
-          const uint32_t off = static_cast<uint32_t>((c >> 3) * C::CHUNK + r * 128 +
-                                                     (((c & 7) ^ (r & 7)) << 4));
-          const uint4 ov = ld_shared_v4(s_base + C::OFF_O + off);
-          const uint4 gv = ld_shared_v4(s_base + C::OFF_A1 + off);
-          part += bf_lo(ov.x) * bf_lo(gv.x) + bf_hi(ov.x) * bf_hi(gv.x) + bf_lo(ov.y) * bf_lo(gv.y) +
-                  bf_hi(ov.y) * bf_hi(gv.y) + bf_lo(ov.z) * bf_lo(gv.z) + bf_hi(ov.z) * bf_hi(gv.z) +
-                  bf_lo(ov.w) * bf_lo(gv.w) + bf_hi(ov.w) * bf_hi(gv.w);
-        }
-        mbar_arrive(bar(kOFree));
+      if (!mbar_wait(bar(kFixFull), prep_n & 1, abort_flag, p.status,
+                     kRoleBwdGrad * 64 + 16 + kFixFull))
+        return false;
+      const int pieces = p.d / 8;  // the tiles hold zeros past d
+      for (int c = cq; cq < 2 && c < pieces; c += 2) {
+        const uint32_t off = static_cast<uint32_t>((c >> 3) * C::CHUNK + r * 128 +
+                                                   (((c & 7) ^ (r & 7)) << 4));
+        const uint4 ov = ld_shared_v4(s_base + C::OFF_O + off);
+        const uint4 gv = ld_shared_v4(s_base + C::OFF_A1 + off);
+        part += bf_lo(ov.x) * bf_lo(gv.x) + bf_hi(ov.x) * bf_hi(gv.x) + bf_lo(ov.y) * bf_lo(gv.y) +
+                bf_hi(ov.y) * bf_hi(gv.y) + bf_lo(ov.z) * bf_lo(gv.z) + bf_hi(ov.z) * bf_hi(gv.z) +
+                bf_lo(ov.w) * bf_lo(gv.w) + bf_hi(ov.w) * bf_hi(gv.w);
       }
+      // (the previous unit's score products, the last readers of these TMEM
+      // columns, are complete: this warp waited for every one of them)
+      const int c = cq & 1;
+      if (c < C::KCH) {
+        const uint32_t src = s_base + (cq < 2 ? C::OFF_A0 : C::OFF_A1) + c * C::CHUNK + r * 128;
+        uint32_t wd[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 x = ld_shared_v4(src + (static_cast<uint32_t>(v ^ (r & 7)) << 4));
+          wd[4 * v] = x.x;
+          wd[4 * v + 1] = x.y;
+          wd[4 * v + 2] = x.z;
+          wd[4 * v + 3] = x.w;
+        }
+        tmem_st32(tmem + lane_off + (cq < 2 ? C::TM_QA : C::TM_DOA) + 32u * c, wd);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(kQTmem));
+      mbar_arrive(bar(kOFree));
+      ++prep_n;
       if (cq < 2) d_part[cq * 128 + r] = part;
       // (the second barrier keeps the next unit's halves from overwriting
       // this one's before both warps of the quarter have read them.  A named
       // barrier cannot time out: after each one the abort flag is checked,
       // and a warp that gives up arrives once on it on its way out.)
       named_barrier(1, kGradThreads);
-      if (*abort_flag) {
-        ok = false;
-        break;
-      }
+      if (*abort_flag) return false;
       const float dvv = d_part[r] + d_part[128 + r];
       named_barrier(1, kGradThreads);
-      if (*abort_flag) {
-        ok = false;
-        break;
-      }
+      if (*abort_flag) return false;
       if (cq == 0 && qi < p.Lq) p.dvec[idx] = dvv;
+      *l2_out = l2;
+      *dvv_out = dvv;
+      return true;
+    };
+    int unit = take(0, kRoleBwdGrad);
+    __syncwarp();
+    if (unit >= 0 && lane == 0) release(0);
+    QUnit u{};
+    float l2 = -INFINITY, dvv = 0.f;
+    if (unit >= 0) {
+      u = decode(unit);
+      if (u.n_iter > 0) ok = prepare(u, &l2, &dvv);
+    }
+    if (unit == -1 && *abort_flag) ok = false;
+    for (int k = 0; ok && unit >= 0; ++k) {
+      const int b = u.b, h = u.h, q0 = u.q0, n_iter = u.n_iter, kv_len = u.kv_len;
+      const int qi = q0 + r;
       const bool row_ok = qi < p.Lq && l2 != -INFINITY;
       for (int it = 0; ok && it < n_iter; ++it) {
         const int t_all = ring_t + it;  // barrier phases run over all units
@@ -1024,6 +1045,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         }
       }
       if (!ok) break;
+      // The next unit is prepared before this unit's epilogue, so the tensor
+      // cores start its first scores while the epilogue runs.
+      const int unit_next = take(k + 1, kRoleBwdGrad);
+      __syncwarp();
+      if (unit_next >= 0 && lane == 0) release(k + 1);
+      QUnit u_next{};
+      float l2_next = -INFINITY, dvv_next = 0.f;
+      if (unit_next >= 0) {
+        u_next = decode(unit_next);
+        if (u_next.n_iter > 0 && !prepare(u_next, &l2_next, &dvv_next)) {
+          ok = false;
+          break;
+        }
+      } else if (*abort_flag) {
+        ok = false;
+        break;
+      }
       // ---- epilogue: the accumulator is read first, then released to the
       // next unit
       if (n_iter > 0) {
@@ -1074,6 +1112,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         ring_t += n_iter;
         ++unit_n;
       }
+      unit = unit_next;
+      u = u_next;
+      l2 = l2_next;
+      dvv = dvv_next;
     }
     if (!ok) named_barrier_arrive(1, kGradThreads);  // release gradient warps blocked on the barrier
   }
