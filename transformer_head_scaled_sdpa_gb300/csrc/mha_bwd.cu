@@ -10,9 +10,11 @@
 //   dQ_i  = scale sum_j dS_ij k_j.
 // Two kernels, in this order on the stream:
 //   bwd_dq_kernel     units (b, h, 128-query tile); first forms D_i for
-//                     its rows (stored for the next kernel), then the key
-//                     tiles it sees stream through a two-stage ring: S = Q K^T
-//                     and dP = dO V^T, then dS (bf16, over S), then dQ += dS K.
+//                     its rows (stored for the next kernel) and copies the
+//                     unit's Q and dO into TMEM, then the key tiles it sees
+//                     stream through a two-stage ring: S = Q K^T and
+//                     dP = dO V^T (A operands from TMEM), then dS (bf16, over
+//                     S), then dQ += dS K.
 //   bwd_dkdv_kernel   units (b, h, 128-key tile); the query tiles that
 //                     see the keys stream through a two-stage ring.  Per query
 //                     tile: S^T = K Q^T and dP^T = V dO^T on the tensor cores
@@ -25,7 +27,8 @@
 // scores) while the gradient warps turn the other half's scores into P, dS.
 // Both are persistent: one CTA per SM runs unit after unit (cluster launch
 // control), loading the next unit's fixed tiles and issuing its first scores
-// while the current unit's epilogue drains.
+// while the current unit's epilogue drains (the dQ kernel loads them a unit
+// ahead: once copied into TMEM, its Q and dO are not read from shared memory).
 // Every operand reuses the forward's shared-memory layout (128-row tiles of
 // 64-feature, 128-byte swizzled chunks): K-major as an operand whose
 // reduction runs over d, MN-major where it runs over the rows.
@@ -84,9 +87,10 @@ enum { kFixFull = 0, kRingFull = 1, kRingEmpty = 3, kScores = 5, kGrads = 7, kAc
        // the persistent dK/dV kernel: the unit's last score products are done
        // with K and V; the epilogue has read the accumulators; the unit queue
        kFixFree = 11, kAccFree = 12, kUnitFull = 13, kUnitEmpty = 15, kClc = 17,
-       // the dQ kernel: the gradient warps have read the unit's O tile
+       // the dQ kernel: the gradient warps have read the unit's staged Q, dO
+       // and O tiles (D formed, Q and dO copied into TMEM)
        kOFree = 18,
-       // the dK/dV epilogue: a chunk is staged (256 arrivals); its TMA stores
+       // the dK/dV epilogue: a chunk is staged (512 arrivals); its TMA stores
        // have read the staging buffers
        kStgFull = 19, kStgFree = 20,
        // the dQ kernel: the unit's Q and dO are in TMEM (copied by the
@@ -674,7 +678,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     }
     mbar_init(bar(kAccDone), 1);
     mbar_init(bar(kDrain), 1);
-    mbar_init(bar(kFixFree), 1);
     mbar_init(bar(kAccFree), kGradThreads);
     mbar_init(bar(kClc), 1);
     mbar_init(bar(kOFree), kGradThreads);
