@@ -1,6 +1,8 @@
-"""Heads wider than 128 features (d_k, d_v up to 256: the wide kernel) and
-heads narrower than the 64- and 128-wide kernels (which issue only their own
-K steps and output columns), against the float64 oracle through the C ABI.
+"""Heads wider than 128 features (d_k, d_v up to 256: the wide kernel), the
+light 64-wide variant of the same one-tile kernel (short unmasked or
+key-padded sequences), and heads narrower than the 64- and 128-wide kernels
+(which issue only their own K steps and output columns), against the float64
+oracle through the C ABI.
 
 Covers every mask kind, ragged query and key lengths (several 64-key tiles,
 a ragged last one, sub-tile shapes), key lengths 0 and 1, d_v != d_k in both
@@ -64,6 +66,14 @@ SHAPES = [
     (2, 2, 300, 700, 32, 32, NONE, None),
     (2, 2, 200, 200, 128, 48, CAUSAL, None),
     (2, 2, 200, 200, 80, 112, NONE, None),
+    # the light one-tile kernel (heads up to 64 wide, sequences up to 512, no
+    # causal mask): d_v != d_k, key padding, ragged tiles, a one-wave grid
+    # (early trigger of the next launch) and more units than CTA slots
+    (2, 3, 300, 400, 64, 32, NONE, None),
+    (2, 2, 256, 512, 48, 64, KEYPAD, [512, 77]),
+    (1, 2, 1, 1, 64, 64, NONE, None),
+    (2, 8, 128, 128, 64, 64, NONE, None),
+    (1, 400, 128, 130, 64, 64, KEYPAD, [129]),
 ]
 
 
@@ -97,6 +107,28 @@ def test_wide_rising_rows(mha, mask):
     ref = pu.oracle_run(case, mask, scale=1.0)
     assert torch.isfinite(out.float()).all()
     pu.assert_bf16_close_rounding_aware(out, ref, f"wide rising mask={mask}")
+
+
+def test_light_launch_back_to_back(mha):
+    """Consecutive launches of the light kernel on one stream (the one-wave
+    grid triggers the next launch at its start; each launch still waits for
+    the previous one before it touches global memory): every output matches
+    the oracle, including a launch that overwrites the previous one's output
+    buffer and one that reads it as its input."""
+    host = inputs.random_case(86, 2, 8, 128, 128, 64)
+    case = pu.to_cuda(host)
+    ref = pu.oracle_run(host, NONE)
+    outs = [mha.mha_fwd(case["q"], case["k"], case["v"]) for _ in range(4)]
+    same = torch.empty_like(case["q"])
+    for _ in range(3):
+        mha.mha_fwd(case["q"], case["k"], case["v"], out=same)
+    # the next launch reads the previous launch's output as its values
+    chained = mha.mha_fwd(case["q"], case["k"], same)
+    assert mha.mha_sync_status() == 0
+    for o in outs + [same]:
+        pu.assert_bf16_close(o.cpu(), ref, "light back to back")
+    host2 = {"q": host["q"], "k": host["k"], "v": same.cpu(), "key_lens": None}
+    pu.assert_bf16_close(chained.cpu(), pu.oracle_run(host2, NONE), "light chained")
 
 
 def test_wide_causal_locality(mha):
