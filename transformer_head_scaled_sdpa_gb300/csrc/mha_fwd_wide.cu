@@ -219,6 +219,8 @@ __global__ void __launch_bounds__(kWThreads, WCfg<W>::MIN_BLOCKS)
     // launch still waits for this grid before it touches global memory.
     // (Measured, 32 x 8 heads at L 128: -4 %; a persistent grid of more units
     // than slots was 1 % slower with the trigger, so it does not trigger.)
+    // (%nsmid counts SM identifiers: at least the SMs, so the test may let a
+    // grid slightly larger than one wave trigger, which costs about 1 %)
     uint32_t nsm;
     asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));
     if (gridDim.x <= 2 * nsm) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
